@@ -1,0 +1,253 @@
+"""Seeded synthetic inputs for the routed-MoE feed-forward block.
+
+This module is the only code shared by the CPU oracle and the CUDA path.  It
+draws the tensors of a layer (activations, router, expert and dense weights,
+norm vectors) from numpy's PCG64 generator, rounds them to bf16 and, for the
+quantised workloads, encodes them in the group-64 affine format.  It holds none
+of the block's forward arithmetic: no normalisation, routing, GEMM, activation
+or dequantisation.
+
+Workloads (the shapes are the DiffusionGemma MoE layer: hidden 2816, 128
+experts, top-8, expert FFN 704, dense FFN 2112; "diffgemma — architecture &
+implemented contract", Part II §1 model constants; "DiffusionGemma port —
+plan & parity strategy", Reference dossier §1 top-level config):
+
+* ``tiny``      32 tokens, hidden 256, 16 experts top-4, expert 64, dense 128;
+                weights N(0, 0.02), router N(0, 1/16), activations N(0, 1).
+* ``canvas256`` one full-shape layer over a 256-token canvas, bf16 weights
+                N(0, 0.02) (router included), activations N(0, 1).
+* ``canvas256_q4`` the same draws as ``canvas256``, expert and dense weights
+                4-bit group-64 affine, router 8-bit group-64 affine.
+* ``batch2048_zipf`` 8 canvases (2048 tokens), bf16, and a per-expert router
+                logit bias beta*ln(p) with p Zipf(1.2) over a seeded expert
+                permutation, so that expert loads are skewed.
+* ``stack30_q4``  30 stacked layers, 64 canvases (16384 tokens), 4-bit
+                weights, 8-bit router, layer scalars U(0.5, 1.5).
+
+Seeding: ``SeedSequence(seed).spawn(1 + n_layers)``; child 0 draws the
+activations, child 1 + l draws layer l (router, then per expert gate_up and
+down, then dense gate, up, down, then the layer's extra vectors).  With
+``randvec=True`` the norm weights, router scale, per-expert scale and the
+layer scalar are drawn U(0.5, 1.5) from ``default_rng(seed + 100)`` instead of
+being ones, so that no multiply by them is dead code.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+
+__all__ = [
+    "Workload",
+    "WORKLOADS",
+    "get_workload",
+    "f32_to_bf16_bits",
+    "quantize_affine",
+    "make_layer_inputs",
+    "make_tokens",
+    "zipf_router_bias",
+]
+
+BF16_ONE = np.uint16(0x3F80)
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    tokens: int
+    hidden: int
+    n_experts: int
+    top_k: int
+    expert_inter: int
+    dense_inter: int
+    seed: int
+    weight_std: float
+    router_std: float
+    n_layers: int = 1
+    # None for bf16 weights; otherwise bits for (experts, dense, router)
+    quant: Optional[tuple] = None
+    # seed whose bf16 draws are quantised (the 4-bit canvas reuses canvas256's)
+    draw_seed: Optional[int] = None
+    zipf_beta: Optional[float] = None
+    layer_scalar_range: Optional[tuple] = None
+
+    @property
+    def quantised(self) -> bool:
+        return self.quant is not None
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 32, 256, 16, 4, 64, 128, seed=0,
+                     weight_std=0.02, router_std=1.0 / 16.0),
+    "canvas256": Workload("canvas256", 256, 2816, 128, 8, 704, 2112, seed=1,
+                          weight_std=0.02, router_std=0.02),
+    "canvas256_q4": Workload("canvas256_q4", 256, 2816, 128, 8, 704, 2112,
+                             seed=1, weight_std=0.02, router_std=0.02,
+                             quant=(4, 4, 8), draw_seed=1),
+    "batch2048_zipf": Workload("batch2048_zipf", 2048, 2816, 128, 8, 704,
+                               2112, seed=2, weight_std=0.02, router_std=0.02,
+                               zipf_beta=0.02),
+    "stack30_q4": Workload("stack30_q4", 16384, 2816, 128, 8, 704, 2112,
+                           seed=4, weight_std=0.02, router_std=0.02,
+                           n_layers=30, quant=(4, 4, 8),
+                           layer_scalar_range=(0.5, 1.5)),
+}
+
+
+def get_workload(name: str, **overrides) -> Workload:
+    w = WORKLOADS[name]
+    return dataclasses.replace(w, **overrides) if overrides else w
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (round to nearest even); returns the
+    16-bit patterns as uint16.  Inputs are finite draws, so no NaN care."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32)
+    bias = ((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF)
+    return ((u + bias) >> np.uint32(16)).astype(np.uint16)
+
+
+def _bits_to_f32(b: np.ndarray) -> np.ndarray:
+    # widening a bf16 pattern to float32 is exact; used only by the quantiser
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def quantize_affine(w_bits: np.ndarray, bits: int, group: int = 64) -> dict:
+    """Encode bf16 weights [..., K] in the group-wise affine format.
+
+    Per group of ``group`` consecutive elements along K: ``lo = min``,
+    ``hi = max``; ``scale = bf16((hi - lo) / (2**bits - 1))``;
+    ``bias = bf16(lo)``; ``q = clamp(rint((w - bias) / scale), 0, 2**bits-1)``
+    using the stored scale and bias (scale 0 gives q 0).  The decoded weight
+    is ``scale * q + bias`` ("DiffusionGemma port — plan & parity strategy",
+    Reference dossier §1: OptiQ affine quant, group_size 64, 4-bit experts,
+    8-bit router).
+
+    Storage (the MLX affine layout): 4-bit codes packed 8 per uint32 word,
+    element k at bits 4*(k % 8) of word k // 8, shape [..., K/8]; 8-bit codes
+    as uint8 [..., K]; scales and biases as bf16 bits [..., K/group].
+    """
+    if bits not in (4, 8):
+        raise ValueError("bits must be 4 or 8")
+    if w_bits.ndim == 3:   # stacked experts: one expert at a time (memory)
+        parts = [quantize_affine(w_bits[e], bits, group) for e in range(w_bits.shape[0])]
+        return {"bits": bits, "group": group,
+                **{k: np.stack([q[k] for q in parts]) for k in ("q", "scales", "biases")}}
+    K = w_bits.shape[-1]
+    if K % group:
+        raise ValueError("K must be a multiple of the group size")
+    lead = w_bits.shape[:-1]
+    w = _bits_to_f32(w_bits).reshape(*lead, K // group, group)
+    lo = w.min(axis=-1)
+    hi = w.max(axis=-1)
+    levels = np.float32(2 ** bits - 1)
+    s_bits = f32_to_bf16_bits((hi - lo) / levels)
+    b_bits = f32_to_bf16_bits(lo)
+    s = _bits_to_f32(s_bits)[..., None]
+    b = _bits_to_f32(b_bits)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(s > 0, np.rint((w - b) / np.where(s > 0, s, 1)), 0)
+    q = np.clip(q, 0, levels).astype(np.uint32).reshape(*lead, K)
+    if bits == 8:
+        packed = q.astype(np.uint8)
+    else:
+        q8 = q.reshape(*lead, K // 8, 8)
+        shifts = (np.arange(8, dtype=np.uint32) * np.uint32(4))
+        packed = np.bitwise_or.reduce(q8 << shifts, axis=-1).astype(np.uint32)
+    return {"bits": bits, "group": group, "q": packed,
+            "scales": s_bits, "biases": b_bits}
+
+
+def _normal_bf16(rng: np.random.Generator, shape, std: float) -> np.ndarray:
+    x = rng.standard_normal(shape, dtype=np.float32)
+    x *= np.float32(std)
+    return f32_to_bf16_bits(x)
+
+
+def zipf_router_bias(rng: np.random.Generator, n_experts: int, beta: float,
+                     s: float = 1.2) -> np.ndarray:
+    """Per-expert additive router-logit bias beta*ln(p[pi(e)]), with
+    p_k proportional to k^-s over k = 1..E and pi a seeded permutation."""
+    k = np.arange(1, n_experts + 1, dtype=np.float64)
+    p = k ** (-s)
+    p /= p.sum()
+    pi = rng.permutation(n_experts)
+    return (beta * np.log(p[pi])).astype(np.float32)
+
+
+def make_tokens(wl: Workload, tokens: Optional[int] = None) -> np.ndarray:
+    """Activations h [T, H] as bf16 bits, N(0, 1)."""
+    T = wl.tokens if tokens is None else tokens
+    child = np.random.SeedSequence(wl.seed).spawn(1 + wl.n_layers)[0]
+    rng = np.random.default_rng(child)
+    return _normal_bf16(rng, (T, wl.hidden), 1.0)
+
+
+def _vectors(wl: Workload, randvec: bool, layer: int) -> dict:
+    H, E = wl.hidden, wl.n_experts
+    names = ["router_scale", "w_pre_ff", "w_pre_ff2", "w_post_ff1",
+             "w_post_ff2", "w_post_ff"]
+    out = {}
+    if randvec:
+        rng = np.random.default_rng(wl.seed + 100 + 1000 * layer)
+        for n in names:
+            out[n] = f32_to_bf16_bits(rng.uniform(0.5, 1.5, H).astype(np.float32))
+        out["per_expert_scale"] = f32_to_bf16_bits(
+            rng.uniform(0.5, 1.5, E).astype(np.float32))
+        ls = float(_bits_to_f32(f32_to_bf16_bits(
+            np.float32([rng.uniform(0.5, 1.5)])))[0])
+    else:
+        for n in names:
+            out[n] = np.full(H, BF16_ONE, dtype=np.uint16)
+        out["per_expert_scale"] = np.full(E, BF16_ONE, dtype=np.uint16)
+        ls = 1.0
+    out["layer_scalar"] = ls
+    return out
+
+
+def make_layer_inputs(wl: Workload, layer: int = 0, randvec: bool = False,
+                      quantise: Optional[bool] = None) -> dict:
+    """Draw one layer's parameters.
+
+    Returns a dict of numpy arrays: bf16 tensors as uint16 bit patterns,
+    quantised tensors as the dicts of :func:`quantize_affine`.  Keys:
+    router [E, H], gate_up [E, 2I, H] (rows 0..I-1 gate, I..2I-1 up),
+    down [E, H, I], dense_gate [D, H], dense_up [D, H], dense_down [H, D],
+    router_scale [H], per_expert_scale [E], w_pre_ff, w_pre_ff2, w_post_ff1,
+    w_post_ff2, w_post_ff [H], router_bias [E] float32 or None, and the
+    python float layer_scalar.
+    """
+    H, E, I, D = wl.hidden, wl.n_experts, wl.expert_inter, wl.dense_inter
+    seed = wl.draw_seed if wl.draw_seed is not None else wl.seed
+    child = np.random.SeedSequence(seed).spawn(1 + wl.n_layers)[1 + layer]
+    rng = np.random.default_rng(child)
+    p = {}
+    p["router"] = _normal_bf16(rng, (E, H), wl.router_std)
+    gate_up = np.empty((E, 2 * I, H), dtype=np.uint16)
+    down = np.empty((E, H, I), dtype=np.uint16)
+    for e in range(E):
+        gate_up[e] = _normal_bf16(rng, (2 * I, H), wl.weight_std)
+        down[e] = _normal_bf16(rng, (H, I), wl.weight_std)
+    p["gate_up"], p["down"] = gate_up, down
+    p["dense_gate"] = _normal_bf16(rng, (D, H), wl.weight_std)
+    p["dense_up"] = _normal_bf16(rng, (D, H), wl.weight_std)
+    p["dense_down"] = _normal_bf16(rng, (H, D), wl.weight_std)
+    p["router_bias"] = (zipf_router_bias(rng, E, wl.zipf_beta)
+                        if wl.zipf_beta is not None else None)
+    p.update(_vectors(wl, randvec, layer))
+    if wl.layer_scalar_range is not None and not randvec:
+        lo, hi = wl.layer_scalar_range
+        v = np.float32([rng.uniform(lo, hi)])
+        p["layer_scalar"] = float(_bits_to_f32(f32_to_bf16_bits(v))[0])
+    do_q = wl.quantised if quantise is None else quantise
+    if do_q:
+        eb, db, rb = wl.quant if wl.quant is not None else (4, 4, 8)
+        p["router"] = quantize_affine(p["router"], rb)
+        p["gate_up"] = quantize_affine(p["gate_up"], eb)
+        p["down"] = quantize_affine(p["down"], eb)
+        for n in ("dense_gate", "dense_up", "dense_down"):
+            p[n] = quantize_affine(p[n], db)
+    return p

@@ -1,0 +1,243 @@
+"""Plain fp64 CPU oracle of the routed-MoE feed-forward block.
+
+TEST INFRASTRUCTURE.  Only the tests, the smoke check of ``__graft_entry__``
+and the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import
+this module.  The product (the CUDA library and its Python binding) never
+calls it, and it shares no code with the product: its only input is the raw
+bit patterns produced by :mod:`moe_inputs`.
+
+Every step is written the plain way, in float64, in the order the pages give:
+
+* RMSNorm ``x / sqrt(mean(x^2) + eps) * w`` with eps 1e-6, the weight
+  multiplied directly ("diffgemma — architecture & implemented contract",
+  Part II §2.1 Norms and §1 RMS eps; "DiffusionGemma port — plan & parity
+  strategy", Reference dossier §1 rms_norm_eps; "Independent GGUF Forward
+  Pass ...", §4 fact 9).
+* Router: weightless RMSNorm of the raw residual stream, times router.scale
+  and hidden^-0.5, as two literal steps (not folded into one weighted norm),
+  then a linear map to E logits, softmax over all E, top-k, renormalise the
+  k selected to sum 1, multiply by per_expert_scale ("diffgemma ...", Part II
+  §2.1 MoE order; "DiffusionGemma Explained", MOEBlock.forward; "DiffusionGemma
+  port ...", Reference dossier §2 Router and the D1 router-norm finding).
+  Ties: the higher logit wins, equal logits go to the lower expert index
+  ("diffgemma ...", §2.1 tie-break).  The selection is taken on the logits,
+  which order the experts exactly as the probabilities do.
+* Experts: ``down(gelu_tanh(gate(x)) * up(x))`` with gate_up stored fused,
+  gate rows first ("diffgemma ...", §2.1; "DiffusionGemma Explained", MLP;
+  "DiffusionGemma port ...", Reference dossier §2 MLP and Experts), input
+  ``pre_feedforward_layernorm_2(h)``; combined as the routing-weighted sum.
+* Dense always-on GEGLU MLP on ``pre_feedforward_layernorm(h)``.
+* FFN sandwich: ``h1 = post_ff_1(dense)``, ``h2 = post_ff_2(moe)``,
+  ``out = (h + post_ff(h1 + h2)) * layer_scalar`` ("DiffusionGemma port ...",
+  Reference dossier §2 DecoderLayer; "DiffusionGemma Explained",
+  MOEBlock.forward and the layer-scalar discussion).
+* Group-wise affine weights decode as ``scale * q + bias`` per group of 64
+  along K ("DiffusionGemma port ...", Reference dossier §1).
+
+Readings where the pages are silent or disagree are listed in the design
+notes; the ones that touch this file: eps inside the square root; the tanh
+form of GELU; selection on exact logits with ties to the lower index; the k
+selected experts reported in ascending expert order; the canonical
+permutation sorted by (expert, token); no rounding of intermediates.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+EPS = 1e-6
+
+__all__ = [
+    "EPS", "bf16_to_f64", "dequant_affine", "to_f64", "rms_norm", "gelu_tanh",
+    "router_logits", "select_topk", "routing_weights", "route",
+    "geglu_mlp", "experts_forward", "dense_forward", "combine",
+    "permutation", "moe_block_forward",
+]
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Decode bf16 bit patterns (uint16) to float64 exactly."""
+    b = np.asarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def dequant_affine(qt: dict) -> np.ndarray:
+    """Decode a group-wise affine tensor to float64: W = scale * q + bias.
+
+    ``qt`` holds ``bits`` (4 or 8), ``group``, ``q`` (4-bit: uint32 words with
+    element k at bits 4*(k % 8) of word k // 8; 8-bit: uint8), ``scales`` and
+    ``biases`` (bf16 bits, one per group along the last axis)."""
+    bits, group = qt["bits"], qt["group"]
+    q = np.asarray(qt["q"])
+    if bits == 4:
+        shifts = np.arange(8, dtype=np.uint32) * np.uint32(4)
+        codes = (q[..., None].astype(np.uint32) >> shifts) & np.uint32(0xF)
+        codes = codes.reshape(*q.shape[:-1], q.shape[-1] * 8)
+    elif bits == 8:
+        codes = q.astype(np.uint32)
+    else:
+        raise ValueError("bits must be 4 or 8")
+    s = bf16_to_f64(qt["scales"])
+    b = bf16_to_f64(qt["biases"])
+    K = codes.shape[-1]
+    c = codes.astype(np.float64).reshape(*codes.shape[:-1], K // group, group)
+    w = s[..., None] * c + b[..., None]
+    return w.reshape(*codes.shape[:-1], K)
+
+
+def to_f64(t) -> np.ndarray:
+    """A weight given as bf16 bits (uint16), as a group-wise affine dict, or
+    already as float64 -> float64."""
+    if isinstance(t, dict):
+        return dequant_affine(t)
+    t = np.asarray(t)
+    if t.dtype == np.float64:
+        return t
+    return bf16_to_f64(t)
+
+
+def _slice(t, e):
+    """Expert e of a stacked weight (bf16 bits or affine dict)."""
+    if isinstance(t, dict):
+        return {"bits": t["bits"], "group": t["group"], "q": t["q"][e],
+                "scales": t["scales"][e], "biases": t["biases"][e]}
+    return t[e]
+
+
+def rms_norm(x: np.ndarray, w=None, eps: float = EPS) -> np.ndarray:
+    """x / sqrt(mean(x^2, last axis) + eps), times w when given."""
+    y = x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    return y if w is None else y * w
+
+
+def gelu_tanh(x: np.ndarray) -> np.ndarray:
+    """GELU, tanh form: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))."""
+    return 0.5 * x * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (x + 0.044715 * x ** 3)))
+
+
+def router_logits(h: np.ndarray, Wr: np.ndarray, router_scale: np.ndarray,
+                  bias=None) -> np.ndarray:
+    """z = (rms_norm(h) * router_scale * H^-0.5) @ Wr^T (+ per-expert bias).
+
+    The normalisation is applied to the raw residual stream, before the
+    projection, as two literal steps."""
+    H = h.shape[-1]
+    xr = rms_norm(h)
+    xr = xr * router_scale * (H ** -0.5)
+    z = xr @ Wr.T
+    if bias is not None:
+        z = z + np.asarray(bias, dtype=np.float64)
+    return z
+
+
+def select_topk(z: np.ndarray, k: int) -> np.ndarray:
+    """Per token, the k experts with the largest logits; equal logits go to
+    the lower expert index.  Returned in ascending expert order, int32."""
+    T, E = z.shape
+    idx = np.empty((T, k), dtype=np.int32)
+    experts = np.arange(E)
+    for t in range(T):
+        order = np.lexsort((experts, -z[t]))   # by -z, then by expert id
+        idx[t] = np.sort(order[:k])
+    return idx
+
+
+def routing_weights(z: np.ndarray, idx: np.ndarray, pes: np.ndarray) -> np.ndarray:
+    """Softmax over all E logits, keep the selected, renormalise them to sum
+    1, multiply by per_expert_scale of the selected expert."""
+    zmax = z.max(axis=-1, keepdims=True)
+    p = np.exp(z - zmax)
+    p = p / p.sum(axis=-1, keepdims=True)
+    sel = np.take_along_axis(p, idx.astype(np.int64), axis=-1)
+    sel = sel / sel.sum(axis=-1, keepdims=True)
+    return sel * pes[idx]
+
+
+def route(h, Wr, router_scale, pes, k, bias=None):
+    """Router of the block: (logits [T, E], idx [T, k] int32, weights [T, k])."""
+    z = router_logits(h, Wr, router_scale, bias)
+    idx = select_topk(z, k)
+    w = routing_weights(z, idx, pes)
+    return z, idx, w
+
+
+def geglu_mlp(x: np.ndarray, W_gate: np.ndarray, W_up: np.ndarray,
+              W_down: np.ndarray) -> np.ndarray:
+    """down(gelu_tanh(x W_gate^T) * (x W_up^T)); weights stored [out, in]."""
+    return (gelu_tanh(x @ W_gate.T) * (x @ W_up.T)) @ W_down.T
+
+
+def experts_forward(xe: np.ndarray, idx: np.ndarray, w: np.ndarray,
+                    gate_up, down, inter: int) -> np.ndarray:
+    """y[t] = sum_k w[t, k] * MLP_{idx[t, k]}(xe[t]); one expert at a time,
+    over the tokens routed to it.  gate_up[e] rows 0..inter-1 are the gate,
+    rows inter..2*inter-1 the up projection."""
+    T, H = xe.shape
+    E = (gate_up["q"] if isinstance(gate_up, dict) else gate_up).shape[0]
+    y = np.zeros((T, H), dtype=np.float64)
+    for e in range(E):
+        tok, slot = np.nonzero(idx == e)
+        if tok.size == 0:
+            continue
+        gu = to_f64(_slice(gate_up, e))
+        dn = to_f64(_slice(down, e))
+        out = geglu_mlp(xe[tok], gu[:inter], gu[inter:], dn)
+        y[tok] += w[tok, slot][:, None] * out
+    return y
+
+
+def dense_forward(xd, dense_gate, dense_up, dense_down) -> np.ndarray:
+    """The always-on dense GEGLU MLP."""
+    return geglu_mlp(xd, to_f64(dense_gate), to_f64(dense_up), to_f64(dense_down))
+
+
+def combine(h, y_dense, y_moe, w_post1, w_post2, w_post, layer_scalar):
+    """out = (h + rms(rms(y_dense) w_post1 + rms(y_moe) w_post2) w_post) * s."""
+    h1 = rms_norm(y_dense, w_post1)
+    h2 = rms_norm(y_moe, w_post2)
+    o = rms_norm(h1 + h2, w_post)
+    return (h + o) * layer_scalar
+
+
+def permutation(idx: np.ndarray, n_experts: int):
+    """Canonical grouping of the T*k assignments by expert.
+
+    Assignment (t, j) has id t*k + j.  Returns ``offsets`` [E+1] (exclusive
+    prefix sum of the per-expert counts) and ``perm`` [T*k]: the assignment
+    ids sorted by (expert ascending, token ascending)."""
+    T, k = idx.shape
+    expert = idx.reshape(-1).astype(np.int64)
+    token = np.repeat(np.arange(T, dtype=np.int64), k)
+    perm = np.lexsort((token, expert)).astype(np.int32)   # by expert, then token
+    counts = np.bincount(expert, minlength=n_experts)
+    offsets = np.zeros(n_experts + 1, dtype=np.int32)
+    offsets[1:] = np.cumsum(counts)
+    return offsets, perm
+
+
+def moe_block_forward(h_bits, p: dict, top_k: int, inter: int,
+                      layer_scalar=None, with_perm: bool = True) -> dict:
+    """The whole block on one [T, H] activation, with its intermediates.
+
+    ``h_bits`` is bf16 bits (uint16) or float64; ``p`` a parameter dict as
+    produced by :func:`moe_inputs.make_layer_inputs`."""
+    h = bf16_to_f64(h_bits) if np.asarray(h_bits).dtype == np.uint16 else np.asarray(h_bits, np.float64)
+    s = p["layer_scalar"] if layer_scalar is None else layer_scalar
+    vec = {n: to_f64(p[n]) for n in ("router_scale", "per_expert_scale",
+                                          "w_pre_ff", "w_pre_ff2", "w_post_ff1",
+                                          "w_post_ff2", "w_post_ff")}
+    Wr = to_f64(p["router"])
+    z, idx, w = route(h, Wr, vec["router_scale"], vec["per_expert_scale"],
+                      top_k, p.get("router_bias"))
+    xd = rms_norm(h, vec["w_pre_ff"])
+    xe = rms_norm(h, vec["w_pre_ff2"])
+    y_moe = experts_forward(xe, idx, w, p["gate_up"], p["down"], inter)
+    y_dense = dense_forward(xd, p["dense_gate"], p["dense_up"], p["dense_down"])
+    out = combine(h, y_dense, y_moe, vec["w_post_ff1"], vec["w_post_ff2"],
+                  vec["w_post_ff"], s)
+    res = {"z": z, "idx": idx, "w": w, "xd": xd, "xe": xe, "y_moe": y_moe,
+           "y_dense": y_dense, "out": out}
+    if with_perm:
+        E = Wr.shape[0]
+        res["offsets"], res["perm"] = permutation(idx, E)
+    return res
