@@ -1,0 +1,205 @@
+/*
+ * dg_moe.h — C ABI of the GB300 (sm_103a) routed-MoE feed-forward block.
+ *
+ * The block is the FFN half of a DiffusionGemma decoder layer, run over a
+ * whole [T, H] activation (one or several 256-token canvases):
+ *
+ *   r       = 1 / sqrt(mean(h^2) + eps)                       per token
+ *   z       = (h r router_scale H^-1/2) Wr^T (+ router_bias)  E logits
+ *   S, w    = top-k of z (ties to the lower expert index); softmax over
+ *             all E, the k selected renormalised to sum 1, times
+ *             per_expert_scale
+ *   xe, xd  = h r w_pre_ff2,  h r w_pre_ff                    (bf16)
+ *   y_moe   = sum_k w_k down_e(gelu_tanh(gate_e xe) * up_e xe), e = S_k
+ *   y_dense = down_d(gelu_tanh(gate_d xd) * up_d xd)
+ *   out     = (h + rms(rms(y_dense) w_post1 + rms(y_moe) w_post2) w_post)
+ *             * layer_scalar                                   (bf16)
+ *
+ * Where this comes from:
+ *  - router order, renormalisation, per_expert_scale, tie-break, fused
+ *    gate_up [gate || up], GELU-tanh, dense MLP as the always-on path,
+ *    RMSNorm x / sqrt(mean(x^2) + eps) * w with eps 1e-6, layer_scalar:
+ *    "diffgemma — architecture & implemented contract", Part II §1 (model
+ *    constants) and §2.1 (forward-pass details);
+ *  - MOEBlock.forward, MLP, the routed combine and the layer scalar:
+ *    "DiffusionGemma Explained", sections "MLP and mixture-of-experts block"
+ *    and "Complete DiffusionGemma model";
+ *  - DecoderLayer FFN sandwich, Router (norm before the projection, two
+ *    literal steps), Experts, tensor shapes and the group-64 affine quant:
+ *    "DiffusionGemma port — plan & parity strategy", Reference dossier §1
+ *    (weight schema & quant map) and §2 (decoder architecture), and the D1
+ *    router-norm finding;
+ *  - precision policy (bf16 activations, f32 router logits and MoE scratch):
+ *    "diffgemma — architecture & implemented contract", Part III (precision
+ *    policy).
+ *
+ * Conventions
+ *  - All tensor pointers are device pointers unless a function says "host".
+ *    Weights are borrowed: the library reads them for the handle's lifetime
+ *    and never frees or writes them.  The workspace is owned by the caller;
+ *    its size comes from dg_moe_workspace_size().  The handle owns only host
+ *    memory (TMA descriptors, launch parameters).
+ *  - Layouts are row-major; [a, b] means b is contiguous.  bf16 tensors are
+ *    passed as the 16-bit patterns.  Expert weights keep the checkpoint
+ *    orientation [E, out, in]: gate_up [E, 2I, H] (rows 0..I-1 gate, I..2I-1
+ *    up), down [E, H, I]; dense gate/up [D, H], down [H, D]; router [E, H].
+ *  - Group-wise affine tensors (DG_FMT_AFFINE_U4_G64 / _U8_G64): W = s q + b
+ *    per group of 64 along the input dimension K.  q: 4-bit codes packed 8
+ *    per uint32 word, element k at bits 4 (k % 8) of word k / 8, [.., K/8];
+ *    or uint8 [.., K]; scales and biases bf16 [.., K/64].
+ *  - Every call is asynchronous on the given stream (a cudaStream_t) unless
+ *    it says otherwise; nothing synchronises the host, and routing counts
+ *    stay on the device.
+ *  - Errors: host-detectable problems return a status and launch nothing.
+ *    Kernels never trap: a bounded wait that runs out or a failed device
+ *    check records itself in a status word in the workspace, read (and
+ *    cleared) by dg_moe_last_device_status().
+ */
+#ifndef DG_MOE_H
+#define DG_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dg_stream_t; /* same type as cudaStream_t */
+typedef struct CUevent_st* dg_event_t;   /* same type as cudaEvent_t */
+
+typedef enum {
+  DG_OK = 0,
+  DG_ERR_INVALID_ARG = 1,  /* NULL pointer, negative or zero size, T > max_tokens */
+  DG_ERR_ALIGNMENT = 2,    /* a pointer below the alignment it must have */
+  DG_ERR_UNSUPPORTED = 3,  /* shape or format combination not implemented */
+  DG_ERR_CUDA = 4,         /* a CUDA runtime or driver call failed */
+  DG_ERR_TIMEOUT = 5,      /* a device-side bounded wait ran out */
+  DG_ERR_DEVICE_CHECK = 6, /* a device-side range check failed */
+  DG_ERR_WORKSPACE = 7     /* workspace NULL, too small or misaligned */
+} dg_status_t;
+
+typedef enum {
+  DG_FMT_BF16 = 0,
+  DG_FMT_AFFINE_U4_G64 = 1,
+  DG_FMT_AFFINE_U8_G64 = 2
+} dg_format_t;
+
+/* Shape and format of one layer.  Supported: hidden % 128 == 0,
+ * expert_inter % 64 == 0, dense_inter % 64 == 0, 1 <= top_k <= 16,
+ * top_k <= n_experts <= 256, hidden <= 8192, max_tokens >= 1.  gate_up and
+ * down share expert_fmt (one format per expert stack, as a step-block
+ * profile requires in "diffgemma — architecture & implemented contract",
+ * Part II §8).  rms_eps 0 means the model's 1e-6. */
+typedef struct {
+  int hidden;        /* H */
+  int n_experts;     /* E */
+  int top_k;         /* K */
+  int expert_inter;  /* I */
+  int dense_inter;   /* D */
+  int max_tokens;    /* largest T a forward may be called with */
+  dg_format_t expert_fmt;
+  dg_format_t dense_fmt;
+  dg_format_t router_fmt;
+  float rms_eps;
+  unsigned int flags; /* reserved, must be 0 */
+} dg_moe_config_t;
+
+/* A weight tensor: bf16 uses q only (the bf16 array); affine formats use all
+ * three.  All pointers 16-byte aligned. */
+typedef struct {
+  const void* q;
+  const void* scales;
+  const void* biases;
+} dg_qtensor_t;
+
+typedef struct {
+  dg_qtensor_t router;     /* [E, H] */
+  dg_qtensor_t gate_up;    /* [E, 2I, H] */
+  dg_qtensor_t down;       /* [E, H, I] */
+  dg_qtensor_t dense_gate; /* [D, H] */
+  dg_qtensor_t dense_up;   /* [D, H] */
+  dg_qtensor_t dense_down; /* [H, D] */
+  const void* router_scale;     /* bf16 [H] */
+  const void* per_expert_scale; /* bf16 [E] */
+  const void* w_pre_ff;         /* bf16 [H], dense-branch input norm */
+  const void* w_pre_ff2;        /* bf16 [H], expert input norm */
+  const void* w_post_ff1;       /* bf16 [H], dense-branch output norm */
+  const void* w_post_ff2;       /* bf16 [H], expert-sum output norm */
+  const void* w_post_ff;        /* bf16 [H], norm of the branch sum */
+  const float* router_bias;     /* f32 [E] added to the logits, or NULL
+                                   (an extension for skewed-load workloads;
+                                   the model itself has no router bias) */
+} dg_moe_weights_t;
+
+/* Optional device outputs of a forward, for stage-wise checking.  Any field
+ * may be NULL.  Filled by device-to-device copies on the forward's stream. */
+typedef struct {
+  int32_t* idx;      /* [T, K] selected experts, ascending per token */
+  float* w;          /* [T, K] routing weights, same order as idx */
+  float* logits;     /* [T, E] fp32 router logits */
+  int32_t* offsets;  /* [E + 1] exclusive prefix sum of per-expert counts */
+  int32_t* perm;     /* [T*K] assignment ids t*K + j sorted by (expert, token) */
+  uint16_t* xd;      /* bf16 [T, H] dense-branch input */
+  uint16_t* xe_perm; /* bf16 [T*K, H] expert input rows in perm order */
+  float* y_moe;      /* [T, H] routing-weighted expert sum */
+  float* y_dense;    /* [T, H] dense-branch output */
+  int32_t* n_refined;/* [1] tokens whose top-k was re-checked in fp64 */
+} dg_moe_debug_t;
+
+typedef struct dg_moe dg_moe_t;
+
+/* Bytes of device workspace a handle with this config needs.  Host only. */
+dg_status_t dg_moe_workspace_size(const dg_moe_config_t* cfg, size_t* bytes);
+
+/* Validate cfg and weights, and build the handle: TMA descriptors for the
+ * weights and for workspace buffers, launch shapes.  workspace: device
+ * memory of at least dg_moe_workspace_size() bytes, 1024-byte aligned,
+ * used only by this handle.  Allocates no device memory and launches no
+ * kernel; clears the workspace's status word with one blocking memset.
+ * Validation errors are returned before any CUDA call.  On error *out is
+ * set to NULL. */
+dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* weights,
+                          void* workspace, size_t workspace_bytes, dg_moe_t** out);
+
+/* One forward of the block.  h_in: bf16 [n_tokens, H]; h_out: bf16
+ * [n_tokens, H] (may alias h_in: h_in is last read by the final kernel,
+ * element by element before it writes).  Both 16-byte aligned.
+ * 0 <= n_tokens <= max_tokens (0 launches nothing).  dbg may be NULL. */
+dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tokens,
+                           float layer_scalar, dg_stream_t stream, const dg_moe_debug_t* dbg);
+
+/* End-to-end forward with HOST buffers: copies h_in (host, bf16
+ * [n_tokens, H]) into the workspace, runs dg_moe_forward, copies the result
+ * to h_out (host) and synchronises the stream before returning.  Page-locked
+ * host memory gives asynchronous copies; pageable memory also works. */
+dg_status_t dg_moe_forward_host(dg_moe_t* m, const void* h_in_host, void* h_out_host,
+                                int n_tokens, float layer_scalar, dg_stream_t stream);
+
+/* Release the handle (host memory only).  NULL is accepted. */
+dg_status_t dg_moe_destroy(dg_moe_t* m);
+
+/* Synchronise `stream`, read the device status word, clear it.  Returns
+ * DG_OK, DG_ERR_TIMEOUT or DG_ERR_DEVICE_CHECK; *where / *info (optional)
+ * receive the reporting site and its detail. */
+dg_status_t dg_moe_last_device_status(dg_moe_t* m, dg_stream_t stream, unsigned int* where,
+                                      unsigned int* info);
+
+/* Number of kernels one forward launches, and their names (static strings).
+ * names may be NULL; *n receives the count. */
+dg_status_t dg_moe_kernel_names(const dg_moe_t* m, const char** names, int* n);
+
+/* Profiling: when events is non-NULL, every later forward records events[i]
+ * on its stream just before kernel i and events[n_kernels] after the last
+ * one; n_events must be n_kernels + 1.  NULL switches it off.  Events are
+ * borrowed (created and destroyed by the caller). */
+dg_status_t dg_moe_set_profile_events(dg_moe_t* m, dg_event_t* events, int n_events);
+
+/* Static string for a status code. */
+const char* dg_moe_status_string(dg_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DG_MOE_H */

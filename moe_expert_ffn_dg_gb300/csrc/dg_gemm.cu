@@ -1,0 +1,318 @@
+// Grouped tcgen05 GEMMs of the MoE FFN block (sm_103a).
+//
+// One persistent kernel per projection, one CTA per SM, warp-specialised:
+//   warp 0  TMA producer: weight tile (128 rows x 64 K, bf16, 128B swizzle)
+//           and token tile (up to BN rows x 64 K) into a STAGES-deep ring;
+//   warp 1  allocates TMEM (two BN-column fp32 accumulators) and issues the
+//           tcgen05.mma (M = 128 weight rows, N = token rows rounded to 16,
+//           K = 16 per instruction) from a single thread;
+//   warps 2-5 epilogue: TMEM -> registers, fused per-mode output.
+// Weights are the M side ("swap AB"): a canvas gives ~16 tokens per expert,
+// so the 128-row side of the MMA is filled by output features and the token
+// count only sets N.
+//
+// mode 0 (gate_up): an A tile interleaves 16 gate rows and the 16 matching
+// up rows four times, so TMEM lanes 32q..32q+15 hold gate and 32q+16..32q+31
+// up of the same 16 features; the epilogue pairs them with one shuffle and
+// writes act = bf16(gelu_tanh(gate) * up) ("diffgemma — architecture &
+// implemented contract", Part II §2.1: fused [gate || up], GELU-tanh;
+// "DiffusionGemma Explained", MLP).
+// mode 1 (down): 128 output channels per tile; experts add w * y into the f32
+// per-token accumulator (the routing-weighted combine, "DiffusionGemma
+// Explained", MOEBlock.forward), the dense branch stores its f32 output.
+//
+// Tiles come from a device list {group, feature tile, first row, rows}
+// (group == E is the dense branch) and are dealt round-robin to the CTAs.
+// Every wait is bounded; a wait that runs out records itself in the status
+// word and the CTA winds down (its TMA copies and MMAs are drained before
+// TMEM is released).
+#include "dg_kernels.h"
+
+namespace dg {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kATileBytes = 128 * 128;  // 128 rows x 64 bf16
+constexpr int kBoxRows = 16;            // rows per TMA box (all maps)
+constexpr int kBoxBytes = kBoxRows * 128;
+
+template <int BN>
+struct Cfg {
+  static constexpr int kBTileBytes = BN * 128;
+  static constexpr int kStages = (192 * 1024) / (kATileBytes + kBTileBytes);
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr size_t kSmem =
+      1024 + (size_t)kStages * (kATileBytes + kBTileBytes) + 256;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ bool wait_no_abort(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+template <int MODE, int BN>
+__global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_constant__ GemmParams p) {
+  using C = Cfg<BN>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + (size_t)S * kATileBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + (size_t)S * C::kBTileBytes);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&p.wa_exp);
+    tma_prefetch_map(&p.wa_d0);
+    if (MODE == 0) tma_prefetch_map(&p.wa_d1);
+    tma_prefetch_map(&p.xb_exp);
+    tma_prefetch_map(&p.xb_d);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int ntiles = *p.ntiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const int4 td = p.tiles[tile];
+        const bool dense = td.x == p.E;
+        const int nb = (td.w + kBoxRows - 1) / kBoxRows;
+        const int kbn = dense ? p.kb_dense : p.kb_exp;
+        const uint32_t bytes = kATileBytes + nb * kBoxBytes;
+        const CUtensorMap* mb = dense ? &p.xb_d : &p.xb_exp;
+        for (int kb = 0; kb < kbn; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+            report(p.status, kDevTimeout, kSiteGemmProducer, (unsigned)tile, (unsigned)kb);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          uint8_t* a_dst = sA + (size_t)stage * kATileBytes;
+          uint8_t* b_dst = sB + (size_t)stage * C::kBTileBytes;
+          const int x = kb * 64;
+          if (MODE == 0) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              if (!dense) {
+                const int yg = td.x * 2 * p.I + td.y * 64 + 16 * c;
+                tma_load_2d(&p.wa_exp, &full[stage], a_dst + (2 * c) * kBoxBytes, x, yg);
+                tma_load_2d(&p.wa_exp, &full[stage], a_dst + (2 * c + 1) * kBoxBytes, x, yg + p.I);
+              } else {
+                const int yg = td.y * 64 + 16 * c;
+                tma_load_2d(&p.wa_d0, &full[stage], a_dst + (2 * c) * kBoxBytes, x, yg);
+                tma_load_2d(&p.wa_d1, &full[stage], a_dst + (2 * c + 1) * kBoxBytes, x, yg);
+              }
+            }
+          } else {
+            const CUtensorMap* ma = dense ? &p.wa_d0 : &p.wa_exp;
+            const int y0 = (dense ? 0 : td.x * p.H) + td.y * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              tma_load_2d(ma, &full[stage], a_dst + j * kBoxBytes, x, y0 + kBoxRows * j);
+          }
+          for (int j = 0; j < nb; ++j)
+            tma_load_2d(mb, &full[stage], b_dst + j * kBoxBytes, x, td.z + kBoxRows * j);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // no copy may still be landing in shared memory when the CTA exits
+      for (int s = 0; s < S; ++s)
+        if ((armed >> s) & 1u)
+          if (!wait_no_abort(&full[s], (armed_par >> s) & 1u))
+            report(p.status, kDevTimeout, kSiteGemmDrain, (unsigned)s, 0u);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true, issued = false;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++local) {
+        const int4 td = p.tiles[tile];
+        const bool dense = td.x == p.E;
+        const int nb = (td.w + kBoxRows - 1) / kBoxRows;
+        const int kbn = dense ? p.kb_dense : p.kb_exp;
+        const int acc = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!mbar_wait(&acc_empty[acc], (use & 1u) ^ 1u, abort_flag)) {
+          report(p.status, kDevTimeout, kSiteGemmMma, (unsigned)tile, 0xffffffffu);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        const uint32_t idesc = idesc_bf16_f32(128, nb * kBoxRows);
+        for (int kb = 0; kb < kbn; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            report(p.status, kDevTimeout, kSiteGemmMma, (unsigned)tile, (unsigned)kb);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + (size_t)stage * kATileBytes);
+          const uint32_t b0 = smem_u32(sB + (size_t)stage * C::kBTileBytes);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_bf16(d_tmem, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k),
+                      idesc, (kb | k) != 0 ? 1u : 0u);
+          umma_commit(&empty[stage]);
+          issued = true;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) umma_commit(&acc_full[acc]);
+      }
+      // every MMA issued here must have completed before TMEM is released
+      if (issued) {
+        umma_commit(drain);
+        if (!wait_no_abort(drain, 0u)) report(p.status, kDevTimeout, kSiteGemmDrain, 99u, 0u);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int local = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
+      const int4 td = p.tiles[tile];
+      const bool dense = td.x == p.E;
+      const int nb = (td.w + kBoxRows - 1) / kBoxRows;
+      const int acc = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      if (!mbar_wait(&acc_full[acc], use & 1u, abort_flag)) {
+        if (lane == 0) report(p.status, kDevTimeout, kSiteGemmEpilogue, (unsigned)tile, 0u);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
+      const int ncols = nb * kBoxRows;
+      for (int c0 = 0; c0 < ncols; c0 += 16) {
+        __syncwarp();
+        float v[16];
+        tmem_ld16(tbase + (uint32_t)c0, v);
+        if (MODE == 0) {
+          const int ld = dense ? p.D : p.I;
+          uint16_t* out = dense ? p.act_d : p.act;
+          const int feat = td.y * 64 + 16 * q + (lane & 15);
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const int j = 2 * jj;
+            const float send = lane < 16 ? v[j + 1] : v[j];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+            const float g = lane < 16 ? v[j] : recv;
+            const float u = lane < 16 ? recv : v[j + 1];
+            const int col = c0 + j + (lane >> 4);
+            if (col < td.w) {
+              const size_t row = (size_t)(td.z + col);
+              out[row * ld + feat] = f32_to_bf16_rne(gelu_tanh(g) * u);
+            }
+          }
+        } else {
+          const int feat = td.y * 128 + 32 * q + lane;
+          int tok = 0;
+          float wt = 0.f;
+          if (!dense && lane < 16 && c0 + lane < td.w) {
+            tok = p.tok_perm[td.z + c0 + lane];
+            wt = p.w_perm[td.z + c0 + lane];
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = c0 + j;
+            const int tj = __shfl_sync(0xffffffffu, tok, j);
+            const float wj = __shfl_sync(0xffffffffu, wt, j);
+            if (col < td.w) {
+              if (dense) {
+                p.y_dense[(size_t)(td.z + col) * p.H + feat] = v[j];
+              } else {
+                atomicAdd(&p.y_moe[(size_t)tj * p.H + feat], wj * v[j]);
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+template <int MODE, int BN>
+cudaError_t launch_mode_bn(const GemmParams& p, int grid, cudaStream_t s) {
+  using C = Cfg<BN>;
+  cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm<MODE, BN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+  if (err != cudaSuccess) return err;
+  k_grouped_gemm<MODE, BN><<<grid, kThreads, C::kSmem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes(int bn) { return bn == 256 ? Cfg<256>::kSmem : Cfg<128>::kSmem; }
+
+cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s) {
+  if (mode == 0) return bn == 256 ? launch_mode_bn<0, 256>(p, grid, s) : launch_mode_bn<0, 128>(p, grid, s);
+  return bn == 256 ? launch_mode_bn<1, 256>(p, grid, s) : launch_mode_bn<1, 128>(p, grid, s);
+}
+
+}  // namespace dg

@@ -48,7 +48,7 @@ import numpy as np
 EPS = 1e-6
 
 __all__ = [
-    "EPS", "bf16_to_f64", "dequant_affine", "to_f64", "rms_norm", "gelu_tanh",
+    "EPS", "bf16_to_f64", "round_bf16", "dequant_affine", "to_f64", "rms_norm", "gelu_tanh",
     "router_logits", "select_topk", "routing_weights", "route",
     "geglu_mlp", "experts_forward", "dense_forward", "combine",
     "permutation", "moe_block_forward",
@@ -59,6 +59,15 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     """Decode bf16 bit patterns (uint16) to float64 exactly."""
     b = np.asarray(bits, dtype=np.uint16)
     return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest bf16 value (8 significant bits,
+    ties to even), returned as float64.  Used only by the bf16-activation
+    variant below; finite normal-range inputs."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)                       # x = m 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(m * 256.0) / 256.0, e)
 
 
 def dequant_affine(qt: dict) -> np.ndarray:
@@ -168,12 +177,19 @@ def geglu_mlp(x: np.ndarray, W_gate: np.ndarray, W_up: np.ndarray,
 
 
 def experts_forward(xe: np.ndarray, idx: np.ndarray, w: np.ndarray,
-                    gate_up, down, inter: int) -> np.ndarray:
+                    gate_up, down, inter: int, bf16_activations: bool = False) -> np.ndarray:
     """y[t] = sum_k w[t, k] * MLP_{idx[t, k]}(xe[t]); one expert at a time,
     over the tokens routed to it.  gate_up[e] rows 0..inter-1 are the gate,
-    rows inter..2*inter-1 the up projection."""
+    rows inter..2*inter-1 the up projection.
+
+    bf16_activations: round the expert input and the GEGLU activation to bf16
+    before they are multiplied, as the activation planes are bf16 in the
+    precision policy ("diffgemma — architecture & implemented contract",
+    Part III, precision policy); everything else stays float64."""
     T, H = xe.shape
     E = (gate_up["q"] if isinstance(gate_up, dict) else gate_up).shape[0]
+    if bf16_activations:
+        xe = round_bf16(xe)
     y = np.zeros((T, H), dtype=np.float64)
     for e in range(E):
         tok, slot = np.nonzero(idx == e)
@@ -181,14 +197,22 @@ def experts_forward(xe: np.ndarray, idx: np.ndarray, w: np.ndarray,
             continue
         gu = to_f64(_slice(gate_up, e))
         dn = to_f64(_slice(down, e))
-        out = geglu_mlp(xe[tok], gu[:inter], gu[inter:], dn)
-        y[tok] += w[tok, slot][:, None] * out
+        x = xe[tok]
+        act = gelu_tanh(x @ gu[:inter].T) * (x @ gu[inter:].T)
+        if bf16_activations:
+            act = round_bf16(act)
+        y[tok] += w[tok, slot][:, None] * (act @ dn.T)
     return y
 
 
-def dense_forward(xd, dense_gate, dense_up, dense_down) -> np.ndarray:
-    """The always-on dense GEGLU MLP."""
-    return geglu_mlp(xd, to_f64(dense_gate), to_f64(dense_up), to_f64(dense_down))
+def dense_forward(xd, dense_gate, dense_up, dense_down,
+                  bf16_activations: bool = False) -> np.ndarray:
+    """The always-on dense GEGLU MLP (bf16_activations as in experts_forward)."""
+    if not bf16_activations:
+        return geglu_mlp(xd, to_f64(dense_gate), to_f64(dense_up), to_f64(dense_down))
+    x = round_bf16(xd)
+    act = round_bf16(gelu_tanh(x @ to_f64(dense_gate).T) * (x @ to_f64(dense_up).T))
+    return act @ to_f64(dense_down).T
 
 
 def combine(h, y_dense, y_moe, w_post1, w_post2, w_post, layer_scalar):

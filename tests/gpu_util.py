@@ -1,0 +1,103 @@
+"""Helpers of the GPU parity tests: run the CUDA block through the C ABI and
+compare it with the CPU oracle on the same seeded inputs."""
+
+import numpy as np
+import torch
+
+import moe_expert_ffn_dg_gb300 as pkg
+import moe_inputs as mi
+import oracle
+
+# Block output against the exact fp64 oracle: max |err| <= 2e-2 * RMS(out)
+# and cosine >= 0.9999 (the bf16 tolerance of the block's specification).
+ERR_RMS = 2e-2
+COS_MIN = 0.9999
+# Branch outputs (f32 y_moe, y_dense) against the oracle's bf16-activation
+# variant (expert/dense input and GEGLU activation rounded to bf16, the rest
+# fp64).  What remains is fp32 accumulation and activations that round to
+# the other bf16 neighbour: ~1e-4 RMS; 2e-3 RMS is ten times below the
+# bf16-rounding error itself (2.07e-2 RMS on the tiny workload).
+BRANCH_ERR_RMS = 2e-3
+BRANCH_COS_MIN = 0.99999
+W_ABS = 1e-5  # routing weights (fp32 vs fp64)
+
+
+def to_dev_bf16(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def bf16_ulp_distance(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
+    """Distance in units of the last place between bf16 patterns (ordered
+    as signed-magnitude integers)."""
+    def key(b):
+        b = b.astype(np.int32)
+        return np.where(b & 0x8000, -(b & 0x7FFF), b & 0x7FFF)
+    return np.abs(key(a_bits) - key(b_bits))
+
+
+def make_block(wl, p, max_tokens=None):
+    return pkg.MoEBlock.from_params(
+        p, hidden=wl.hidden, n_experts=wl.n_experts, top_k=wl.top_k,
+        expert_inter=wl.expert_inter, dense_inter=wl.dense_inter,
+        max_tokens=max_tokens or wl.tokens, device="cuda")
+
+
+def close_stats(got: np.ndarray, ref: np.ndarray):
+    got = got.astype(np.float64)
+    err = float(np.abs(got - ref).max()) if ref.size else 0.0
+    rms = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
+    den = np.linalg.norm(got) * np.linalg.norm(ref)
+    cos = float((got * ref).sum() / den) if den > 0 else 1.0
+    return err, rms, cos
+
+
+def assert_close(got, ref, what, err_rms=ERR_RMS, cos_min=COS_MIN):
+    err, rms, cos = close_stats(got, ref)
+    assert err <= err_rms * rms + 1e-30, f"{what}: max|err| {err:.3e} > {err_rms} * rms {rms:.3e}"
+    assert cos >= cos_min, f"{what}: cosine {cos:.7f} < {cos_min}"
+    return err / rms if rms else 0.0, cos
+
+
+def run_and_check(wl, p, h_bits, layer_scalar=None, blk=None, check_intermediates=True):
+    """Forward on the GPU and full comparison with the oracle."""
+    ls = p["layer_scalar"] if layer_scalar is None else layer_scalar
+    own = blk is None
+    if own:
+        blk = make_block(wl, p, max_tokens=max(1, h_bits.shape[0]))
+    hd = to_dev_bf16(h_bits)
+    out, dbg = blk.forward(hd, ls, debug=True)
+    torch.cuda.synchronize()
+    st = blk.device_status()
+    assert st[0] == 0, f"device status {st}"
+    ref = oracle.moe_block_forward(h_bits, p, wl.top_k, wl.expert_inter, layer_scalar=ls)
+    T, K = h_bits.shape[0], wl.top_k
+    idx = dbg["idx"].cpu().numpy()
+    assert np.array_equal(idx, ref["idx"]), \
+        f"routing differs on {int((idx != ref['idx']).any(1).sum())} of {T} tokens"
+    assert np.array_equal(dbg["offsets"].cpu().numpy(), ref["offsets"])
+    assert np.array_equal(dbg["perm"].cpu().numpy(), ref["perm"])
+    w = dbg["w"].cpu().numpy()
+    assert np.abs(w - ref["w"]).max() <= W_ABS
+    res = {"n_refined": int(dbg["n_refined"].item())}
+    if check_intermediates:
+        xd_ref = mi.f32_to_bf16_bits(ref["xd"].astype(np.float32))
+        assert bf16_ulp_distance(bf16_bits(dbg["xd"]), xd_ref).max() <= 1
+        xe_ref = mi.f32_to_bf16_bits(ref["xe"].astype(np.float32))[ref["perm"] // K]
+        assert bf16_ulp_distance(bf16_bits(dbg["xe_perm"]), xe_ref).max() <= 1
+        yd16 = oracle.dense_forward(ref["xd"], p["dense_gate"], p["dense_up"], p["dense_down"],
+                                    bf16_activations=True)
+        ym16 = oracle.experts_forward(ref["xe"], ref["idx"], ref["w"], p["gate_up"], p["down"],
+                                      wl.expert_inter, bf16_activations=True)
+        res["y_dense"] = assert_close(dbg["y_dense"].cpu().numpy(), yd16, "y_dense",
+                                      BRANCH_ERR_RMS, BRANCH_COS_MIN)
+        res["y_moe"] = assert_close(dbg["y_moe"].cpu().numpy(), ym16, "y_moe",
+                                    BRANCH_ERR_RMS, BRANCH_COS_MIN)
+    got = out.float().cpu().numpy()
+    res["out"] = assert_close(got, ref["out"], "out")
+    if own:
+        blk.close()
+    return res, out, dbg, ref

@@ -1,0 +1,184 @@
+"""GPU parity of the CUDA block (through the C ABI) against the CPU oracle.
+
+Routing (selected experts), per-expert offsets and the grouping permutation
+must be bit-exact; routing weights within 1e-5; the bf16 expert and dense
+inputs within one bf16 ulp of the rounded fp64 values; the block output and
+the f32 branch outputs within max|err| <= 2e-2 RMS and cosine >= 0.9999.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle
+from gpu_util import make_block, run_and_check, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import moe_expert_ffn_dg_gb300 as pkg
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pkg.build()
+    pkg.load_library()
+
+
+@pytest.fixture(scope="module")
+def canvas_params():
+    wl = mi.get_workload("canvas256")
+    return wl, mi.make_layer_inputs(wl), mi.make_tokens(wl)
+
+
+# ------------------------------------------------------------------ tiny
+
+@pytest.mark.parametrize("randvec", [False, True])
+def test_tiny_workload(randvec):
+    wl = mi.get_workload("tiny")
+    p = mi.make_layer_inputs(wl, randvec=randvec)
+    run_and_check(wl, p, mi.make_tokens(wl))
+
+
+@pytest.mark.parametrize("T", [1, 7, 17, 31, 300])
+def test_tiny_ragged_token_counts(T):
+    wl = mi.get_workload("tiny")
+    p = mi.make_layer_inputs(wl, randvec=True)
+    run_and_check(wl, p, mi.make_tokens(wl, tokens=T))
+
+
+def test_tiny_smaller_batch_than_max_tokens():
+    wl = mi.get_workload("tiny")
+    p = mi.make_layer_inputs(wl, randvec=True)
+    blk = make_block(wl, p, max_tokens=300)
+    for T in (300, 5, 64):
+        run_and_check(wl, p, mi.make_tokens(wl, tokens=T), blk=blk)
+    blk.close()
+
+
+def test_zero_tokens_route_to_first_experts_and_give_zero():
+    wl = mi.get_workload("tiny")
+    p = mi.make_layer_inputs(wl, randvec=True)
+    h = mi.make_tokens(wl)
+    h[3] = 0
+    h[10] = 0
+    res, out, dbg, ref = run_and_check(wl, p, h)
+    idx = dbg["idx"].cpu().numpy()
+    assert list(idx[3]) == list(range(wl.top_k))
+    assert torch.all(out[3].float() == 0)
+
+
+def test_duplicate_router_rows_tie_to_lower_index():
+    wl = mi.get_workload("tiny")
+    p = mi.make_layer_inputs(wl)
+    # experts 9 and 4 get identical router rows: a tie on every token, so
+    # whenever one of them is in the top-k boundary only expert 4 may win
+    p["router"] = p["router"].copy()
+    p["router"][9] = p["router"][4]
+    h = mi.make_tokens(wl)
+    res, out, dbg, ref = run_and_check(wl, p, h)
+    idx = dbg["idx"].cpu().numpy()
+    assert not np.any((idx == 9).any(1) & ~(idx == 4).any(1))
+
+
+def test_top_k_equal_to_expert_count():
+    wl = mi.get_workload("tiny", top_k=16)
+    p = mi.make_layer_inputs(wl, randvec=True)
+    run_and_check(wl, p, mi.make_tokens(wl))
+
+
+def test_all_tokens_to_one_expert_spans_several_token_tiles():
+    # a large bias on expert 5 sends all 600 tokens there: 600 rows in one
+    # group, several token tiles of the grouped GEMMs
+    wl = mi.get_workload("tiny")
+    p = mi.make_layer_inputs(wl, randvec=True)
+    bias = np.zeros(wl.n_experts, np.float32)
+    bias[5] = 50.0
+    p["router_bias"] = bias
+    run_and_check(wl, p, mi.make_tokens(wl, tokens=600))
+
+
+def test_routing_invariant_under_scaling_and_canvas_permutation():
+    wl = mi.get_workload("tiny")
+    p = mi.make_layer_inputs(wl, randvec=True)
+    h = mi.make_tokens(wl)
+    blk = make_block(wl, p)
+    _, d1 = blk.forward(to_dev_bf16(h), 1.0, debug=True)
+    h2 = mi.f32_to_bf16_bits(2.0 * oracle.bf16_to_f64(h).astype(np.float32))
+    _, d2 = blk.forward(to_dev_bf16(h2), 1.0, debug=True)
+    assert torch.equal(d1["idx"], d2["idx"])
+    pi = np.random.default_rng(3).permutation(wl.tokens)
+    o1, _ = blk.forward(to_dev_bf16(h), 1.0, debug=True)
+    o3, d3 = blk.forward(to_dev_bf16(np.ascontiguousarray(h[pi])), 1.0, debug=True)
+    assert torch.equal(d3["idx"], d1["idx"][torch.from_numpy(pi).cuda()])
+    diff = (o3.float() - o1.float()[torch.from_numpy(pi).cuda()]).abs().max().item()
+    assert diff <= 2e-2 * o1.float().pow(2).mean().sqrt().item()
+    blk.close()
+
+
+def test_host_buffer_forward_matches_device_forward():
+    wl = mi.get_workload("tiny")
+    p = mi.make_layer_inputs(wl, randvec=True)
+    h = mi.make_tokens(wl)
+    blk = make_block(wl, p)
+    od = blk.forward(to_dev_bf16(h), 0.75)
+    hh = torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    oh = torch.empty_like(hh).pin_memory()
+    blk.forward_host(hh, oh, 0.75)
+    torch.cuda.synchronize()
+    diff = (oh.float() - od.float().cpu()).abs().max().item()
+    assert diff <= 2e-2 * od.float().pow(2).mean().sqrt().item()
+    blk.close()
+
+
+def test_output_may_alias_input():
+    wl = mi.get_workload("tiny")
+    p = mi.make_layer_inputs(wl, randvec=True)
+    h = mi.make_tokens(wl)
+    blk = make_block(wl, p)
+    ref = blk.forward(to_dev_bf16(h), 0.9).clone()
+    x = to_dev_bf16(h)
+    blk.forward(x, 0.9, out=x)
+    torch.cuda.synchronize()
+    assert (x.float() - ref.float()).abs().max().item() <= 2e-2 * ref.float().pow(2).mean().sqrt().item()
+    blk.close()
+
+
+def test_eight_bit_router_tiny():
+    wl = mi.get_workload("tiny")
+    p = mi.make_layer_inputs(wl, randvec=True)
+    p["router"] = mi.quantize_affine(p["router"], 8)
+    run_and_check(wl, p, mi.make_tokens(wl))
+
+
+# ------------------------------------------------------------------ full shape
+
+def test_canvas256_bf16(canvas_params):
+    wl, p, h = canvas_params
+    res, *_ = run_and_check(wl, p, h)
+    print("canvas256", res)
+
+
+def test_canvas256_bf16_random_vectors():
+    wl = mi.get_workload("canvas256")
+    p = mi.make_layer_inputs(wl, randvec=True)
+    res, *_ = run_and_check(wl, p, mi.make_tokens(wl))
+    print("canvas256 randvec", res)
+
+
+def test_canvas256_eight_bit_router(canvas_params):
+    wl, p, h = canvas_params
+    q = dict(p)
+    q["router"] = mi.quantize_affine(p["router"], 8)
+    run_and_check(wl, q, h)
+
+
+def test_batch2048_zipf_skewed_loads():
+    wl = mi.get_workload("batch2048_zipf")
+    p = mi.make_layer_inputs(wl)
+    h = mi.make_tokens(wl)
+    res, out, dbg, ref = run_and_check(wl, p, h)
+    counts = np.diff(ref["offsets"])
+    print("batch2048 zipf: max load", counts.max(), "empty experts", int((counts == 0).sum()), res)
+    assert counts.max() > 4 * counts.mean()

@@ -421,3 +421,44 @@ def test_block_against_direct_formula_on_tiny_workload():
         assert list(r["idx"][t]) == sel
         np.testing.assert_allclose(r["w"][t], ww, rtol=1e-12)
         np.testing.assert_allclose(r["out"][t], out, rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------- bf16 rounding
+
+def test_round_bf16_ties_to_even_and_nearest():
+    ulp = 2.0 ** -7
+    cases = {1.0 + ulp / 2: 1.0, 1.0 + 3 * ulp / 2: 1.0 + 2 * ulp, -(1.0 + ulp / 2): -1.0,
+             1.0 + ulp / 2 + 1e-12: 1.0 + ulp, 3.0: 3.0, 0.0: 0.0}
+    for x, want in cases.items():
+        assert o.round_bf16(np.array([x]))[0] == want, x
+    # brute force: the nearest of all bf16 values of the same binade
+    rng = _rng(30)
+    x = rng.standard_normal(2000) * 10.0 ** rng.integers(-3, 3, 2000)
+    got = o.round_bf16(x)
+    for xi, gi in zip(x, got):
+        e = math.floor(math.log2(abs(xi)))
+        grid = np.sign(xi) * (1 + np.arange(0, 129) / 128.0) * 2.0 ** e
+        d = np.abs(grid - xi)
+        assert abs(gi - xi) <= d.min() + 1e-300
+        assert abs(gi) >= 2.0 ** e or gi == 0
+
+
+def test_bf16_activation_variant_rounds_only_the_activations():
+    rng = _rng(31)
+    T, H, E, I, k = 6, 16, 4, 8, 2
+    x = rng.standard_normal((T, H))
+    gu = rng.standard_normal((E, 2 * I, H)) * 0.3
+    dn = rng.standard_normal((E, H, I)) * 0.3
+    idx = np.array([sorted(rng.choice(E, k, replace=False)) for _ in range(T)], np.int32)
+    w = rng.uniform(0, 1, (T, k))
+    y = o.experts_forward(x, idx, w, gu, dn, I, bf16_activations=True)
+    xb = o.round_bf16(x)
+    ref = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            e = idx[t, j]
+            a = o.round_bf16(o.gelu_tanh(gu[e, :I] @ xb[t]) * (gu[e, I:] @ xb[t]))
+            ref[t] += w[t, j] * (dn[e] @ a)
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-14)
+    y0 = o.experts_forward(x, idx, w, gu, dn, I)
+    assert 1e-4 < np.abs(y - y0).max() / np.abs(y0).max() < 2e-2
