@@ -1,0 +1,328 @@
+"""Benchmark of the GB300 MoE FFN block: canvas-tokens/s per layer forward.
+
+Workload: one DiffusionGemma MoE feed-forward layer over a 256-token canvas
+(hidden 2816, 128 experts top-8, expert FFN 704, dense FFN 2112, bf16
+weights N(0, 0.02), activations N(0, 1), seed 1; synthetic).  A step is one
+whole forward of the block (router, grouping, gate_up, down, combine) on
+that canvas with inputs resident in HBM.  The 1.56 GB of weights read per
+step are 12x the L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  ``--impl reference`` times the CPU oracle (the only
+reference there is: the pages hold no runnable implementation) on the host
+cores, on a bounded token sample per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "canvas-tokens/s per MoE layer (µs/layer) and % of HBM/tensor roofline, 1 GB300"
+UNIT = "canvas-tokens/s"
+WORKLOAD = "canvas256"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def workload_desc(wl):
+    return (f"{wl.name}: one DiffusionGemma MoE FFN layer, T={wl.tokens} tokens (one canvas), "
+            f"H={wl.hidden}, E={wl.n_experts} top-{wl.top_k}, expert FFN {wl.expert_inter}, "
+            f"dense FFN {wl.dense_inter}, bf16 weights N(0,{wl.weight_std}), seed {wl.seed}")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def algorithmic(wl, counts):
+    """Algorithmic bytes and FLOPs of one layer forward and of its gate_up
+    GEMM: weights of the experts that received tokens, dense and router
+    weights, the activation read and the output write; intermediates that
+    an ideal kernel keeps on chip are not counted.  FLOPs exclude padding."""
+    T, H, E, K, I, D = wl.tokens, wl.hidden, wl.n_experts, wl.top_k, wl.expert_inter, wl.dense_inter
+    touched = int((np.asarray(counts) > 0).sum())
+    gu_w = touched * 2 * I * H * 2 + 2 * D * H * 2
+    dn_w = touched * H * I * 2 + H * D * 2
+    router_w = E * H * 2
+    layer_bytes = gu_w + dn_w + router_w + 2 * T * H * 2 + 4 * H * 2 + E * 2
+    layer_flops = 2 * T * H * E + 2 * T * K * 3 * H * I + 2 * T * 3 * H * D
+    gu_bytes = gu_w + T * K * H * 2 + T * H * 2 + T * K * I * 2 + T * D * 2
+    return {"touched_experts": touched, "layer_bytes": layer_bytes, "layer_flops": layer_flops,
+            "gate_up_bytes": gu_bytes}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        rows = [r.split(",") for r in open(self.f.name).read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(wl, p, h, max_seconds=30.0):
+    """The fp64 oracle, as it stands, on a bounded token sample of the same
+    workload (tokens are independent, so a sample times the per-token cost)."""
+    import oracle
+    t0 = time.time()
+    n = 16
+    oracle.moe_block_forward(h[:n], p, wl.top_k, wl.expert_inter, with_perm=False)
+    dt = time.time() - t0
+    # grow the sample while it stays inside the time budget
+    while n < wl.tokens and dt * 2 * 1.2 < max_seconds:
+        n = min(wl.tokens, n * 2)
+        t0 = time.time()
+        oracle.moe_block_forward(h[:n], p, wl.top_k, wl.expert_inter, with_perm=False)
+        dt = time.time() - t0
+    return {"value": n / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} of the {wl.tokens} canvas tokens, one layer, fp64 numpy oracle "
+                      f"(OpenBLAS threads = host cores), {dt:.2f} s"}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle timed on the host cores."""
+    import moe_inputs as mi
+    import oracle
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = mi.get_workload(WORKLOAD)
+    p = mi.make_layer_inputs(wl)
+    h = mi.make_tokens(wl)
+    # decode the weights to float64 once, outside the timed steps; the
+    # oracle accepts float64 weights as they are
+    pf = dict(p)
+    for k in ("router", "gate_up", "down", "dense_gate", "dense_up", "dense_down"):
+        pf[k] = oracle.to_f64(p[k])
+    # one token per step, bounded to about two minutes in total
+    t0 = time.time()
+    oracle.moe_block_forward(h[:1], pf, wl.top_k, wl.expert_inter, with_perm=False)
+    one = max(time.time() - t0, 1e-4)
+    steps = max(1, min(args.steps, int(120.0 / one)))
+    for i in range(min(args.warmup, 3)):
+        oracle.moe_block_forward(h[i:i + 1], pf, wl.top_k, wl.expert_inter, with_perm=False)
+    t0 = time.time()
+    for i in range(steps):
+        j = i % wl.tokens
+        oracle.moe_block_forward(h[j:j + 1], pf, wl.top_k, wl.expert_inter, with_perm=False)
+    dt = time.time() - t0
+    value = steps / dt
+    sample = (f"{steps} steps of 1 canvas token each (of {args.steps} requested; bounded to "
+              f"~2 min), fp64 numpy oracle, weights decoded to float64 before timing")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt / steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": workload_desc(wl), "tokens_per_step": 1},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def run_ours(args):
+    import torch
+
+    import moe_expert_ffn_dg_gb300 as pkg
+    import moe_inputs as mi
+    from moe_expert_ffn_dg_gb300 import binding as B
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkg.build()
+    pkg.load_library()
+
+    wl = mi.get_workload(WORKLOAD)
+    p = mi.make_layer_inputs(wl)
+    # each replica processes its own canvas (data parallel over canvases)
+    h_np = mi.make_tokens(mi.get_workload(WORKLOAD, seed=wl.seed + 1000 * rank)) if rank else mi.make_tokens(wl)
+    blk = pkg.MoEBlock.from_params(p, hidden=wl.hidden, n_experts=wl.n_experts, top_k=wl.top_k,
+                                   expert_inter=wl.expert_inter, dense_inter=wl.dense_inter,
+                                   max_tokens=wl.tokens, device=dev)
+    h = torch.from_numpy(h_np.view(np.int16)).to(dev).view(torch.bfloat16)
+    out = torch.empty_like(h)
+    stream = torch.cuda.current_stream(dev)
+    names = B.dg_moe_kernel_names(blk.handle)
+    nk = len(names)
+
+    for _ in range(max(args.warmup, 3)):
+        blk.forward(h, 1.0, out=out)
+    torch.cuda.synchronize(dev)
+    st = blk.device_status()
+    if st[0] != 0:
+        raise RuntimeError(f"device status after warm-up: {st}")
+
+    # per-kernel events on every `stride`-th step of the timed region
+    stride = max(1, args.steps // 200)
+    ev_sets = {}
+    for i in range(0, args.steps, stride):
+        ev_sets[i] = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # torch creates the CUDA event at its first record(): record every event
+    # once so the handles given to the library are real
+    for evs in ev_sets.values():
+        for e in evs:
+            e.record(stream)
+
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for i in range(args.steps):
+        evs = ev_sets.get(i)
+        B.dg_moe_set_profile_events(blk.handle, [e.cuda_event for e in evs] if evs else None)
+        blk.forward(h, 1.0, out=out)
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    B.dg_moe_set_profile_events(blk.handle, None)
+    clk = clocks.stop()
+    elapsed_ms = start.elapsed_time(stop)
+    if dist:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    st = blk.device_status()
+    if st[0] != 0:
+        raise RuntimeError(f"device status after timing: {st}")
+    per_kernel = np.zeros(nk)
+    for evs in ev_sets.values():
+        per_kernel += [evs[j].elapsed_time(evs[j + 1]) for j in range(nk)]
+    per_kernel_us = per_kernel / len(ev_sets) * 1000.0
+
+    # end to end through the host-buffer entry point: H2D of h, forward,
+    # D2H of the output, stream synchronised every step
+    h_host = torch.from_numpy(h_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+    o_host = torch.empty_like(h_host).pin_memory()
+    for _ in range(3):
+        blk.forward_host(h_host, o_host, 1.0)
+    e2e_steps = max(10, min(args.steps, 2000))
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        blk.forward_host(h_host, o_host, 1.0)
+    e2e_s = time.perf_counter() - t0
+
+    # routing of the timed canvas (for the touched-expert count)
+    _, dbg = blk.forward(h, 1.0, debug=True)
+    counts = np.diff(dbg["offsets"].cpu().numpy())
+    alg = algorithmic(wl, counts)
+    hbm, bf16_burst, bf16_sus, src = peaks()
+
+    ms = elapsed_ms / args.steps
+    value = world * wl.tokens / (ms / 1000.0)
+    gu = names.index("gemm_gate_up")
+    gu_s = per_kernel_us[gu] * 1e-6
+    achieved = alg["gate_up_bytes"] / gu_s / 1e9
+    t_roof = max(alg["layer_bytes"] / (hbm * 1e9), alg["layer_flops"] / (bf16_sus * 1e12))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(wl), "tokens_per_step": wl.tokens,
+                   "us_per_layer": ms * 1000.0, "parallelism": f"replicas x{world}",
+                   "l2": "no flush: 1.56 GB of weights per step, 12x the 129 MB L2",
+                   "touched_experts": alg["touched_experts"]},
+        "roofline": {"bound": "hbm", "kernel": "gemm_gate_up", "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else src,
+                     "algorithmic_bytes_per_launch": alg["gate_up_bytes"],
+                     "us_per_launch": per_kernel_us[gu]},
+        "layer_roofline": {"bytes": alg["layer_bytes"], "flops": alg["layer_flops"],
+                           "t_roof_us": t_roof * 1e6, "frac": t_roof / (ms / 1000.0),
+                           "basis": f"max(bytes / {hbm} GB/s, flops / {bf16_sus} TF/s) ({src})"},
+        "kernels_us": {n: round(float(v), 3) for n, v in zip(names, per_kernel_us)},
+        "e2e": {"value": world * wl.tokens * e2e_steps / e2e_s, "unit": UNIT,
+                "h2d_bytes_per_step": int(h_host.numel() * 2),
+                "d2h_bytes_per_step": int(o_host.numel() * 2), "steps": e2e_steps},
+        "clocks": clk,
+        "gpu_launches": nk * args.steps,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, p, h_np)
+    blk.close()
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -195,6 +195,10 @@ dg_status_t dg_moe_kernel_names(const dg_moe_t* m, const char** names, int* n);
  * borrowed (created and destroyed by the caller). */
 dg_status_t dg_moe_set_profile_events(dg_moe_t* m, dg_event_t* events, int n_events);
 
+/* Text of the last CUDA failure seen by this handle (the call and the CUDA
+ * error), "" if none.  Owned by the handle; valid until the next call. */
+const char* dg_moe_last_error(const dg_moe_t* m);
+
 /* Static string for a status code. */
 const char* dg_moe_status_string(dg_status_t s);
 

@@ -30,7 +30,7 @@ DG_FMT_AFFINE_U8_G64 = 2
 EXPORTED = (
     "dg_moe_workspace_size", "dg_moe_create", "dg_moe_forward", "dg_moe_forward_host",
     "dg_moe_destroy", "dg_moe_last_device_status", "dg_moe_kernel_names",
-    "dg_moe_set_profile_events", "dg_moe_status_string",
+    "dg_moe_set_profile_events", "dg_moe_status_string", "dg_moe_last_error",
 )
 
 
@@ -92,8 +92,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dg_moe_set_profile_events.argtypes = [c_void_p, POINTER(c_void_p), c_int]
     lib.dg_moe_status_string.argtypes = [c_int]
     lib.dg_moe_status_string.restype = c_char_p
+    lib.dg_moe_last_error.argtypes = [c_void_p]
+    lib.dg_moe_last_error.restype = c_char_p
     for name in EXPORTED:
-        if name != "dg_moe_status_string":
+        if name not in ("dg_moe_status_string", "dg_moe_last_error"):
             getattr(lib, name).restype = c_int
     _lib = lib
     return lib
@@ -103,9 +105,16 @@ def dg_moe_status_string(status: int) -> str:
     return load_library().dg_moe_status_string(status).decode()
 
 
-def _check(status: int, what: str) -> None:
+def _check(status: int, what: str, handle: int = None) -> None:
     if status != DG_OK:
-        raise DgError(status, what)
+        detail = ""
+        if handle and status == DG_ERR_CUDA:
+            detail = " [" + dg_moe_last_error(handle) + "]"
+        raise DgError(status, what + detail)
+
+
+def dg_moe_last_error(handle: int) -> str:
+    return load_library().dg_moe_last_error(c_void_p(handle)).decode()
 
 
 def dg_moe_workspace_size(cfg: dg_moe_config_t) -> int:
@@ -129,7 +138,7 @@ def dg_moe_forward(handle: int, h_in: int, h_out: int, n_tokens: int, layer_scal
     _check(load_library().dg_moe_forward(c_void_p(handle), c_void_p(h_in), c_void_p(h_out),
                                          n_tokens, layer_scalar, c_void_p(stream),
                                          ctypes.byref(dbg) if dbg is not None else None),
-           "dg_moe_forward")
+           "dg_moe_forward", handle)
 
 
 def dg_moe_forward_host(handle: int, h_in_host: int, h_out_host: int, n_tokens: int,
@@ -137,7 +146,7 @@ def dg_moe_forward_host(handle: int, h_in_host: int, h_out_host: int, n_tokens: 
     _check(load_library().dg_moe_forward_host(c_void_p(handle), c_void_p(h_in_host),
                                               c_void_p(h_out_host), n_tokens, layer_scalar,
                                               c_void_p(stream)),
-           "dg_moe_forward_host")
+           "dg_moe_forward_host", handle)
 
 
 def dg_moe_destroy(handle: int) -> None:

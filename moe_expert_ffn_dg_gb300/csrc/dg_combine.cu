@@ -5,81 +5,98 @@
 // DecoderLayer; "DiffusionGemma Explained", MOEBlock.forward and the layer
 // scalar; "diffgemma — architecture & implemented contract", Part II §2.1:
 // seven norms, weight multiplied directly, layer_scalar on the whole output).
-// h and out may alias: each element of h is read by the thread that writes
-// the same element of out, before it writes.
+// Every input of the token is loaded up front (one round of memory latency),
+// then two block reductions.  h and out may alias: each element of h is read
+// by the thread that writes the same element of out, before it writes.
 #include "dg_kernels.h"
 
 namespace dg {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kMaxPerThread = 32;  // H <= 8192
 
-__device__ __forceinline__ float block_sum(float v, float* red) {
+template <int NV>
+__device__ __forceinline__ void block_sum2(float& x, float& y, float2* red) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  for (int o = 16; o; o >>= 1) {
+    x += __shfl_xor_sync(0xffffffffu, x, o);
+    y += __shfl_xor_sync(0xffffffffu, y, o);
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __syncthreads();
-  if (lane == 0) red[warp] = v;
+  if (lane == 0) red[warp] = make_float2(x, y);
   __syncthreads();
-  float s = 0.f;
+  float sx = 0.f, sy = 0.f;
 #pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) s += red[w];
-  return s;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    sx += red[w].x;
+    sy += red[w].y;
+  }
+  x = sx;
+  y = sy;
 }
 
+// NPT: elements per thread (H <= NPT * 256)
+template <int NPT>
 __global__ void __launch_bounds__(kThreads) k_combine(const CombineParams p) {
-  __shared__ float red[kThreads / 32];
+  __shared__ float2 red[kThreads / 32];
   const int t = blockIdx.x;
   const int H = p.H;
   const float* yd = p.y_dense + (size_t)t * H;
   const float* ym = p.y_moe + (size_t)t * H;
-  float a[kMaxPerThread], b[kMaxPerThread];
+  const uint16_t* hrow = p.h + (size_t)t * H;
+  float a[NPT], b[NPT], hv[NPT], w1[NPT], w2[NPT], w3[NPT];
+#pragma unroll
+  for (int j = 0; j < NPT; ++j) {
+    const int i = threadIdx.x + j * kThreads;
+    const bool in = i < H;
+    a[j] = in ? yd[i] : 0.f;
+    b[j] = in ? ym[i] : 0.f;
+    hv[j] = in ? bf16_to_f32(hrow[i]) : 0.f;
+    w1[j] = in ? bf16_to_f32(p.w_post1[i]) : 0.f;
+    w2[j] = in ? bf16_to_f32(p.w_post2[i]) : 0.f;
+    w3[j] = in ? bf16_to_f32(p.w_post[i]) : 0.f;
+  }
   float sd = 0.f, sm = 0.f;
 #pragma unroll
-  for (int j = 0; j < kMaxPerThread; ++j) {
-    const int i = threadIdx.x + j * kThreads;
-    a[j] = 0.f;
-    b[j] = 0.f;
-    if (i < H) {
-      a[j] = yd[i];
-      b[j] = ym[i];
-      sd = fmaf(a[j], a[j], sd);
-      sm = fmaf(b[j], b[j], sm);
-    }
+  for (int j = 0; j < NPT; ++j) {
+    sd = fmaf(a[j], a[j], sd);
+    sm = fmaf(b[j], b[j], sm);
   }
-  sd = block_sum(sd, red);
-  sm = block_sum(sm, red);
+  block_sum2<NPT>(sd, sm, red);
   const float rd = 1.0f / sqrtf(sd / (float)H + p.eps);
   const float rm = 1.0f / sqrtf(sm / (float)H + p.eps);
-  float ss = 0.f;
+  float ss = 0.f, dummy = 0.f;
 #pragma unroll
-  for (int j = 0; j < kMaxPerThread; ++j) {
-    const int i = threadIdx.x + j * kThreads;
-    if (i < H) {
-      a[j] = a[j] * rd * bf16_to_f32(p.w_post1[i]) + b[j] * rm * bf16_to_f32(p.w_post2[i]);
-      ss = fmaf(a[j], a[j], ss);
-    }
+  for (int j = 0; j < NPT; ++j) {
+    a[j] = a[j] * rd * w1[j] + b[j] * rm * w2[j];
+    ss = fmaf(a[j], a[j], ss);
   }
-  ss = block_sum(ss, red);
+  block_sum2<NPT>(ss, dummy, red);
   const float rs = 1.0f / sqrtf(ss / (float)H + p.eps);
-  const uint16_t* hrow = p.h + (size_t)t * H;
   uint16_t* orow = p.out + (size_t)t * H;
 #pragma unroll
-  for (int j = 0; j < kMaxPerThread; ++j) {
+  for (int j = 0; j < NPT; ++j) {
     const int i = threadIdx.x + j * kThreads;
-    if (i < H) {
-      const float hv = bf16_to_f32(hrow[i]);
-      orow[i] = f32_to_bf16_rne((hv + a[j] * rs * bf16_to_f32(p.w_post[i])) * p.layer_scalar);
-    }
+    if (i < H) orow[i] = f32_to_bf16_rne((hv[j] + a[j] * rs * w3[j]) * p.layer_scalar);
   }
+}
+
+template <int NPT>
+cudaError_t launch_npt(const CombineParams& p, cudaStream_t s) {
+  k_combine<NPT><<<p.T, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
-  k_combine<<<p.T, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  const int npt = (p.H + kThreads - 1) / kThreads;
+  if (npt <= 4) return launch_npt<4>(p, s);
+  if (npt <= 8) return launch_npt<8>(p, s);
+  if (npt <= 12) return launch_npt<12>(p, s);
+  if (npt <= 16) return launch_npt<16>(p, s);
+  return launch_npt<32>(p, s);
 }
 
 }  // namespace dg

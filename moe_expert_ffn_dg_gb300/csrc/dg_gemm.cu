@@ -21,8 +21,9 @@
 // per-token accumulator (the routing-weighted combine, "DiffusionGemma
 // Explained", MOEBlock.forward), the dense branch stores its f32 output.
 //
-// Tiles come from a device list {group, feature tile, first row, rows}
-// (group == E is the dense branch) and are dealt round-robin to the CTAs.
+// Tiles {group, feature tile, first row, rows} (group == E is the dense
+// branch) are decoded from the expert offsets in each CTA and dealt
+// round-robin to the CTAs.
 // Every wait is bounded; a wait that runs out records itself in the status
 // word and the CTA winds down (its TMA copies and MMAs are drained before
 // TMEM is released).
@@ -36,17 +37,61 @@ constexpr int kATileBytes = 128 * 128;  // 128 rows x 64 bf16
 constexpr int kBoxRows = 16;            // rows per TMA box (all maps)
 constexpr int kBoxBytes = kBoxRows * 128;
 
+constexpr int kMaxGroups = 256;
+constexpr int kTileTableBytes = 2 * (kMaxGroups + 2) * 4;
+
+// Tile t of the persistent schedule: dense tiles first, then the expert tiles
+// (feature tile fastest).  s_start[e] = first expert tile of expert e
+// (exclusive prefix of ceil(n_e / bn) * mt_exp), s_off = expert offsets.
+__device__ __forceinline__ int4 decode_tile(const GemmParams& p, int t, int nd,
+                                            const int* s_start, const int* s_off) {
+  if (t < nd) {
+    const int j = t / p.mt_dense, m = t - j * p.mt_dense;
+    return make_int4(p.E, m, j * p.bn, min(p.bn, p.T - j * p.bn));
+  }
+  const int u = t - nd;
+  int lo = 0, hi = p.E - 1;  // last e with s_start[e] <= u
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_start[mid] <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  const int e = lo, local = u - s_start[e];
+  const int j = local / p.mt_exp, m = local - j * p.mt_exp;
+  const int n = s_off[e + 1] - s_off[e];
+  return make_int4(e, m, s_off[e] + j * p.bn, min(p.bn, n - j * p.bn));
+}
+
 template <int BN>
 struct Cfg {
   static constexpr int kBTileBytes = BN * 128;
   static constexpr int kStages = (192 * 1024) / (kATileBytes + kBTileBytes);
   static constexpr int kTmemCols = 2 * BN;
   static constexpr size_t kSmem =
-      1024 + (size_t)kStages * (kATileBytes + kBTileBytes) + 256;
+      1024 + (size_t)kStages * (kATileBytes + kBTileBytes) + 256 + kTileTableBytes;
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void tma_load_4d(const CUtensorMap* map, uint64_t* bar, void* dst,
+                                            int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(const CUtensorMap* map, uint64_t* bar, void* dst,
+                                            int c0, int c1, int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(c4)
+      : "memory");
 }
 
 __device__ __forceinline__ bool wait_no_abort(uint64_t* bar, uint32_t parity) {
@@ -74,6 +119,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* s_start = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full) + 256);  // [E + 1]
+  int* s_off = s_start + kMaxGroups + 2;                                            // [E + 1]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -93,19 +140,50 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
   if (warp == 0 && lane == 0) {
     tma_prefetch_map(&p.wa_exp);
     tma_prefetch_map(&p.wa_d0);
-    if (MODE == 0) tma_prefetch_map(&p.wa_d1);
-    tma_prefetch_map(&p.xb_exp);
-    tma_prefetch_map(&p.xb_d);
+    if (MODE == 0) {
+      tma_prefetch_map(&p.wa_d1);
+      tma_prefetch_map(&p.wa_d5);
+    }
+    tma_prefetch_map(&p.xb_exp64);
+    tma_prefetch_map(&p.xb_exp16);
+    tma_prefetch_map(&p.xb_d64);
+    tma_prefetch_map(&p.xb_d16);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, C::kTmemCols);
     tmem_relinquish();
   }
+  if (warp >= 2) {
+    // tile table: per-expert tile counts and their exclusive prefix (one warp)
+    const int tid = threadIdx.x - 64;
+    for (int e = tid; e <= p.E; e += 128) s_off[e] = p.offsets[e];
+    if (warp == 2) {
+      int run = 0;
+      for (int base = 0; base < p.E; base += 32) {
+        const int e = base + lane;
+        int c = 0;
+        if (e < p.E) {
+          const int n = p.offsets[e + 1] - p.offsets[e];
+          c = (n + p.bn - 1) / p.bn * p.mt_exp;
+        }
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        if (e < p.E) s_start[e] = run + incl - c;
+        run += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) s_start[p.E] = run;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const int ntiles = *p.ntiles;
+  const int nd = (p.T + p.bn - 1) / p.bn * p.mt_dense;
+  const int ntiles = nd + s_start[p.E];
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -115,12 +193,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
       uint32_t armed = 0, armed_par = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-        const int4 td = p.tiles[tile];
+        const int4 td = decode_tile(p, tile, nd, s_start, s_off);
         const bool dense = td.x == p.E;
-        const int nb = (td.w + kBoxRows - 1) / kBoxRows;
         const int kbn = dense ? p.kb_dense : p.kb_exp;
-        const uint32_t bytes = kATileBytes + nb * kBoxBytes;
-        const CUtensorMap* mb = dense ? &p.xb_d : &p.xb_exp;
+        const int nb64 = td.w / 64;
+        const int nb16 = (td.w - 64 * nb64 + kBoxRows - 1) / kBoxRows;
+        const uint32_t bytes = kATileBytes + nb64 * 64 * 128 + nb16 * kBoxBytes;
+        const CUtensorMap* mb64 = dense ? &p.xb_d64 : &p.xb_exp64;
+        const CUtensorMap* mb16 = dense ? &p.xb_d16 : &p.xb_exp16;
         for (int kb = 0; kb < kbn; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             report(p.status, kDevTimeout, kSiteGemmProducer, (unsigned)tile, (unsigned)kb);
@@ -133,13 +213,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
           uint8_t* b_dst = sB + (size_t)stage * C::kBTileBytes;
           const int x = kb * 64;
           if (MODE == 0) {
+            if (!dense) {
+              // rows e*2I + half*I + 16*(4m + c) + r, box (64, 16, 2, 4, 1)
+              tma_load_5d(&p.wa_exp, &full[stage], a_dst, x, 0, 0, 4 * td.y, td.x);
+            } else if (p.dense_5d) {
+              tma_load_4d(&p.wa_d5, &full[stage], a_dst, x, 0, 0, 4 * td.y);
+            } else {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              if (!dense) {
-                const int yg = td.x * 2 * p.I + td.y * 64 + 16 * c;
-                tma_load_2d(&p.wa_exp, &full[stage], a_dst + (2 * c) * kBoxBytes, x, yg);
-                tma_load_2d(&p.wa_exp, &full[stage], a_dst + (2 * c + 1) * kBoxBytes, x, yg + p.I);
-              } else {
+              for (int c = 0; c < 4; ++c) {
                 const int yg = td.y * 64 + 16 * c;
                 tma_load_2d(&p.wa_d0, &full[stage], a_dst + (2 * c) * kBoxBytes, x, yg);
                 tma_load_2d(&p.wa_d1, &full[stage], a_dst + (2 * c + 1) * kBoxBytes, x, yg);
@@ -147,13 +228,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
             }
           } else {
             const CUtensorMap* ma = dense ? &p.wa_d0 : &p.wa_exp;
-            const int y0 = (dense ? 0 : td.x * p.H) + td.y * 128;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              tma_load_2d(ma, &full[stage], a_dst + j * kBoxBytes, x, y0 + kBoxRows * j);
+            tma_load_2d(ma, &full[stage], a_dst, x, (dense ? 0 : td.x * p.H) + td.y * 128);
           }
-          for (int j = 0; j < nb; ++j)
-            tma_load_2d(mb, &full[stage], b_dst + j * kBoxBytes, x, td.z + kBoxRows * j);
+          for (int j = 0; j < nb64; ++j)
+            tma_load_2d(mb64, &full[stage], b_dst + j * 64 * 128, x, td.z + 64 * j);
+          for (int j = 0; j < nb16; ++j)
+            tma_load_2d(mb16, &full[stage], b_dst + (64 * nb64 + kBoxRows * j) * 128, x,
+                        td.z + 64 * nb64 + kBoxRows * j);
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           if (++stage == S) {
@@ -176,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
       int local = 0;
       bool ok = true, issued = false;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++local) {
-        const int4 td = p.tiles[tile];
+        const int4 td = decode_tile(p, tile, nd, s_start, s_off);
         const bool dense = td.x == p.E;
         const int nb = (td.w + kBoxRows - 1) / kBoxRows;
         const int kbn = dense ? p.kb_dense : p.kb_exp;
@@ -224,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int local = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
-      const int4 td = p.tiles[tile];
+      const int4 td = decode_tile(p, tile, nd, s_start, s_off);
       const bool dense = td.x == p.E;
       const int nb = (td.w + kBoxRows - 1) / kBoxRows;
       const int acc = local & 1;
@@ -308,11 +389,19 @@ cudaError_t launch_mode_bn(const GemmParams& p, int grid, cudaStream_t s) {
 
 }  // namespace
 
-size_t gemm_smem_bytes(int bn) { return bn == 256 ? Cfg<256>::kSmem : Cfg<128>::kSmem; }
+size_t gemm_smem_bytes(int bn) {
+  return bn == 256 ? Cfg<256>::kSmem : bn == 128 ? Cfg<128>::kSmem : Cfg<64>::kSmem;
+}
 
 cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s) {
-  if (mode == 0) return bn == 256 ? launch_mode_bn<0, 256>(p, grid, s) : launch_mode_bn<0, 128>(p, grid, s);
-  return bn == 256 ? launch_mode_bn<1, 256>(p, grid, s) : launch_mode_bn<1, 128>(p, grid, s);
+  if (mode == 0) {
+    if (bn == 256) return launch_mode_bn<0, 256>(p, grid, s);
+    if (bn == 128) return launch_mode_bn<0, 128>(p, grid, s);
+    return launch_mode_bn<0, 64>(p, grid, s);
+  }
+  if (bn == 256) return launch_mode_bn<1, 256>(p, grid, s);
+  if (bn == 128) return launch_mode_bn<1, 128>(p, grid, s);
+  return launch_mode_bn<1, 64>(p, grid, s);
 }
 
 }  // namespace dg

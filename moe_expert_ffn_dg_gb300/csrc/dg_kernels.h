@@ -26,9 +26,13 @@ struct RouterParams {
   int router_u8;
   float eps;
   float* r_out;      // [T] 1/rms(h)
+  double* r64_out;   // [T] 1/rms(h) in fp64 (exact re-check)
+  float* xnorm_out;  // [T] |router input|
+  float* wnorm_out;  // [E] |router row|
   int32_t* idx;      // [T, K]
   float* w;          // [T, K]
-  float* logits;     // [T, E] or null
+  float* logits;     // [T, E] fp32 logits
+  int32_t* chunk_counts;  // [nchunks, E] expert histogram per 256 tokens (zeroed)
   uint16_t* xd;      // bf16 [T, H]
   float* y_moe;      // [T, H], zeroed here
   int* n_refined;    // counter of tokens re-checked in fp64
@@ -38,15 +42,11 @@ struct ScatterParams {
   const int32_t* idx;        // [T, K]
   const float* w;            // [T, K]
   const int32_t* chunk_counts;  // [nchunks, E]
-  int T, K, E, H, I, D;
-  int bn_exp, bn_dense;      // token rows per expert / dense tile
+  int T, K, E;
   int32_t* offsets;          // [E + 1]
   int32_t* perm;             // [T*K]
   int32_t* tok_perm;         // [T*K]
   float* w_perm;             // [T*K]
-  int4* tiles_gu;            // gate_up tiles
-  int4* tiles_dn;            // down tiles
-  int* ntiles;               // [2]: gate_up, down
   DevStatus* status;
 };
 
@@ -60,15 +60,30 @@ struct GatherParams {
 };
 
 struct GemmParams {
-  CUtensorMap wa_exp;  // expert weights: gate_up [E*2I, H] or down [E*H, I]
-  CUtensorMap wa_d0;   // dense gate [D, H] (gate_up) or dense down [H, D]
-  CUtensorMap wa_d1;   // dense up [D, H] (gate_up only)
-  CUtensorMap xb_exp;  // expert rows: xe_perm [TKmax, H] or act [TKmax, I]
-  CUtensorMap xb_d;    // dense rows: xd [Tmax, H] or act_d [Tmax, D]
-  const int4* tiles;
-  const int* ntiles;
+  // A side (weights), 64 K-columns per box, 128B swizzle:
+  //  gate_up: wa_exp 5-D view of [E, 2I, H] whose 128-row box interleaves
+  //           16 gate rows and the 16 matching up rows four times;
+  //           dense: wa_d5 the same view over (dense_gate, dense_up) when up
+  //           lies above gate in memory, else 16-row boxes of wa_d0 / wa_d1.
+  //  down:    wa_exp [E*H, I] and wa_d0 [H, D], 128-row boxes.
+  CUtensorMap wa_exp;
+  CUtensorMap wa_d0;
+  CUtensorMap wa_d1;
+  CUtensorMap wa_d5;
+  // B side (token rows), boxes of 64 and of 16 rows:
+  //  gate_up: xe_perm [TKmax, H] and xd [Tmax, H]; down: act and act_d.
+  CUtensorMap xb_exp64;
+  CUtensorMap xb_exp16;
+  CUtensorMap xb_d64;
+  CUtensorMap xb_d16;
+  // Tiles, decoded in each CTA from the expert offsets: first the dense tiles
+  // (ceil(T/bn) token tiles x mt_dense feature tiles), then per expert e
+  // ceil(n_e/bn) token tiles x mt_exp feature tiles, feature tile fastest.
+  const int32_t* offsets;  // [E + 1]
+  int T, bn, mt_exp, mt_dense;
   int E, I, D, H;
   int kb_exp, kb_dense;  // 64-wide K blocks of an expert / a dense tile
+  int dense_5d;          // gate_up: dense A tile through wa_d5
   uint16_t* act;         // gate_up out: bf16 [TK, I]
   uint16_t* act_d;       // gate_up out: bf16 [T, D]
   float* y_moe;          // down out: f32 [T, H] (accumulated)
@@ -94,8 +109,7 @@ struct CombineParams {
 constexpr int kChunkTokens = 256;  // tokens per permutation chunk
 
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s);
-cudaError_t launch_route_count(const int32_t* idx, int T, int K, int E, int32_t* chunk_counts,
-                               cudaStream_t s);
+cudaError_t launch_router_select(const RouterParams& p, cudaStream_t s);
 cudaError_t launch_route_scatter(const ScatterParams& p, cudaStream_t s);
 cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s);
 // mode 0: gate_up + GEGLU, mode 1: down + weighted scatter

@@ -1,6 +1,7 @@
 // C-ABI implementation of the MoE FFN block: argument validation, workspace
 // layout, TMA descriptors and the launch sequence of one forward.
 #include <cudaTypedefs.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -15,30 +16,28 @@ namespace {
 
 constexpr int kNumKernels = 7;
 const char* const kKernelNames[kNumKernels] = {
-    "router", "route_count", "route_scatter", "gather_xe",
+    "router_logits", "router_select", "route_scatter", "gather_xe",
     "gemm_gate_up", "gemm_down", "combine"};
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-  size_t status, counters, r, idx, w, chunk_counts, offsets, perm, tok_perm, w_perm;
-  size_t xd, xe_perm, act, act_d, y_moe, y_dense, tiles_gu, tiles_dn, stage_in, stage_out;
+  size_t status, counters, r, r64, xnorm, wnorm, logits, idx, w, chunk_counts, offsets, perm,
+      tok_perm, w_perm;
+  size_t xd, xe_perm, act, act_d, y_moe, y_dense, stage_in, stage_out;
+  size_t zero_begin, zero_end;  // counters and chunk counts, cleared per forward
   size_t total;
-  int max_tiles_gu, max_tiles_dn;
 };
 
-// Smallest token-tile height the kernels use; it bounds the tile counts.
-constexpr int kMinBN = 128;
+// Token rows per GEMM tile: small canvases favour deep weight pipelines (more
+// stages fit when the token slot is small), large batches favour wide N.
+int pick_bn(int T) { return T <= 512 ? 64 : (T <= 2048 ? 128 : 256); }
 
 Layout make_layout(const dg_moe_config_t& c) {
   Layout L;
   const size_t T = (size_t)c.max_tokens, H = c.hidden, E = c.n_experts, K = c.top_k;
   const size_t I = c.expert_inter, D = c.dense_inter, TK = T * K;
   const size_t nchunks = (T + kChunkTokens - 1) / kChunkTokens;
-  const size_t exp_tok_tiles = E + (TK + kMinBN - 1) / kMinBN;
-  const size_t dense_tok_tiles = (T + kMinBN - 1) / kMinBN;
-  L.max_tiles_gu = (int)(exp_tok_tiles * (I / 64) + dense_tok_tiles * (D / 64));
-  L.max_tiles_dn = (int)(exp_tok_tiles * (H / 128) + dense_tok_tiles * (H / 128));
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -46,11 +45,17 @@ Layout make_layout(const dg_moe_config_t& c) {
     return o;
   };
   L.status = take(sizeof(DevStatus));
-  L.counters = take(16 * sizeof(int));  // [0] n_refined, [1..2] tile counts
+  L.counters = take(16 * sizeof(int));  // [0] n_refined
+  L.chunk_counts = take(nchunks * E * 4);
+  L.zero_begin = L.counters;
+  L.zero_end = L.chunk_counts + nchunks * E * 4;
   L.r = take(T * 4);
+  L.r64 = take(T * 8);
+  L.xnorm = take(T * 4);
+  L.wnorm = take(E * 4);
+  L.logits = take(T * E * 4);
   L.idx = take(TK * 4);
   L.w = take(TK * 4);
-  L.chunk_counts = take(nchunks * E * 4);
   L.offsets = take((E + 1) * 4);
   L.perm = take(TK * 4);
   L.tok_perm = take(TK * 4);
@@ -61,8 +66,6 @@ Layout make_layout(const dg_moe_config_t& c) {
   L.act_d = take(T * D * 2);
   L.y_moe = take(T * H * 4);
   L.y_dense = take(T * H * 4);
-  L.tiles_gu = take((size_t)L.max_tiles_gu * 16);
-  L.tiles_dn = take((size_t)L.max_tiles_dn * 16);
   L.stage_in = take(T * H * 2);
   L.stage_out = take(T * H * 2);
   L.total = off;
@@ -130,19 +133,49 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-// Row-major bf16 matrix [rows, cols] read in boxes of 16 rows x 64 columns
-// with the 128-byte swizzle the MMA descriptors expect.
-bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) {
+// Tiled TMA descriptor with the 128-byte swizzle the MMA descriptors expect.
+// dims[0] is the contiguous dimension (elements); strides are in bytes for
+// dims 1..rank-1.
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
+                  const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                  CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
   if (!enc) return false;
-  cuuint64_t gdim[2] = {cols, rows};
-  cuuint64_t gstride[1] = {cols * 2};
-  cuuint32_t box[2] = {64, 16};
-  cuuint32_t estride[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride,
-                   box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  cuuint64_t gdim[5], gstride[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i) gstride[i - 1] = strides[i - 1];
+  }
+  CUresult r = enc(map, dt, (cuuint32_t)rank, const_cast<void*>(base), gdim, gstride, bx, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// Row-major bf16 matrix [rows, cols] read in boxes of box_rows x 64 columns.
+bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows) {
+  const uint64_t dims[2] = {cols, rows};
+  const uint64_t strides[1] = {cols * 2};
+  const uint32_t box[2] = {64, box_rows};
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box);
+}
+
+// gate_up weights as [groups][2 halves][n/16 chunks][16 rows][K]: one box of
+// (64, 16, 2, 4, 1) is 128 rows that interleave 16 gate rows with the 16
+// matching up rows, four times.  half_stride is the byte distance from a
+// gate row to its up row; group_stride the distance between groups.
+// rank 5 (with a group dimension) for the expert stack, rank 4 for the
+// dense pair.
+bool encode_gate_up(CUtensorMap* map, const void* gate, uint64_t K, uint64_t n,
+                    uint64_t half_stride, int rank, uint64_t groups, uint64_t group_stride) {
+  const uint64_t dims[5] = {K, 16, 2, n / 16, groups};
+  const uint64_t strides[4] = {K * 2, half_stride, 16 * K * 2, group_stride};
+  const uint32_t box[5] = {64, 16, 2, 4, 1};
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, gate, dims, strides, box);
 }
 
 }  // namespace
@@ -159,7 +192,16 @@ struct dg_moe {
   GemmParams dn;
   dg_event_t* prof;
   int n_prof;
+  char last_error[256];
 };
+
+namespace {
+// Record the failing CUDA call in the handle and map it to DG_ERR_CUDA.
+dg_status_t cuda_fail(dg_moe* m, const char* what, cudaError_t e) {
+  if (m) snprintf(m->last_error, sizeof(m->last_error), "%s: %s (%d)", what, cudaGetErrorString(e), (int)e);
+  return DG_ERR_CUDA;
+}
+}  // namespace
 
 extern "C" {
 
@@ -206,6 +248,7 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
   m->L = L;
   m->prof = nullptr;
   m->n_prof = 0;
+  m->last_error[0] = 0;
   if (cudaGetDevice(&m->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess) {
     delete m;
@@ -216,18 +259,32 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
   const uint64_t T = c.max_tokens, TK = T * c.top_k;
   uint8_t* ws = m->ws;
   bool ok = true;
-  // gate_up: weights [E*2I, H], dense gate/up [D, H]; rows xe_perm / xd
-  ok = ok && encode_bf16_rows(&m->gu.wa_exp, weights->gate_up.q, E * 2 * I, H);
-  ok = ok && encode_bf16_rows(&m->gu.wa_d0, weights->dense_gate.q, D, H);
-  ok = ok && encode_bf16_rows(&m->gu.wa_d1, weights->dense_up.q, D, H);
-  ok = ok && encode_bf16_rows(&m->gu.xb_exp, ws + L.xe_perm, TK, H);
-  ok = ok && encode_bf16_rows(&m->gu.xb_d, ws + L.xd, T, H);
-  // down: weights [E*H, I], dense down [H, D]; rows act / act_d
-  ok = ok && encode_bf16_rows(&m->dn.wa_exp, weights->down.q, E * H, I);
-  ok = ok && encode_bf16_rows(&m->dn.wa_d0, weights->dense_down.q, H, D);
-  ok = ok && encode_bf16_rows(&m->dn.wa_d1, weights->dense_down.q, H, D);
-  ok = ok && encode_bf16_rows(&m->dn.xb_exp, ws + L.act, TK, I);
-  ok = ok && encode_bf16_rows(&m->dn.xb_d, ws + L.act_d, T, D);
+  // gate_up A: experts through the interleaving 5-D view; the dense pair the
+  // same way when dense_up lies above dense_gate, else 16-row boxes of each
+  ok = ok && encode_gate_up(&m->gu.wa_exp, weights->gate_up.q, H, I, I * H * 2, 5, E, 2 * I * H * 2);
+  ok = ok && encode_bf16_rows(&m->gu.wa_d0, weights->dense_gate.q, D, H, 16);
+  ok = ok && encode_bf16_rows(&m->gu.wa_d1, weights->dense_up.q, D, H, 16);
+  {
+    const uintptr_t g = (uintptr_t)weights->dense_gate.q, u = (uintptr_t)weights->dense_up.q;
+    m->gu.dense_5d = u > g && ((u - g) % 16) == 0 && (u - g) < (1ull << 40) &&
+                     encode_gate_up(&m->gu.wa_d5, weights->dense_gate.q, H, D, u - g, 4, 1, 0);
+    if (!m->gu.dense_5d) m->gu.wa_d5 = m->gu.wa_d0;
+  }
+  // gate_up B: xe_perm / xd rows
+  ok = ok && encode_bf16_rows(&m->gu.xb_exp64, ws + L.xe_perm, TK, H, 64);
+  ok = ok && encode_bf16_rows(&m->gu.xb_exp16, ws + L.xe_perm, TK, H, 16);
+  ok = ok && encode_bf16_rows(&m->gu.xb_d64, ws + L.xd, T, H, 64);
+  ok = ok && encode_bf16_rows(&m->gu.xb_d16, ws + L.xd, T, H, 16);
+  // down A: [E*H, I] and [H, D] in 128-row boxes; B: act / act_d rows
+  ok = ok && encode_bf16_rows(&m->dn.wa_exp, weights->down.q, E * H, I, 128);
+  ok = ok && encode_bf16_rows(&m->dn.wa_d0, weights->dense_down.q, H, D, 128);
+  m->dn.wa_d1 = m->dn.wa_d0;
+  m->dn.wa_d5 = m->dn.wa_d0;
+  m->dn.dense_5d = 0;
+  ok = ok && encode_bf16_rows(&m->dn.xb_exp64, ws + L.act, TK, I, 64);
+  ok = ok && encode_bf16_rows(&m->dn.xb_exp16, ws + L.act, TK, I, 16);
+  ok = ok && encode_bf16_rows(&m->dn.xb_d64, ws + L.act_d, T, D, 64);
+  ok = ok && encode_bf16_rows(&m->dn.xb_d16, ws + L.act_d, T, D, 16);
   if (!ok) {
     delete m;
     return DG_ERR_CUDA;
@@ -238,7 +295,7 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
     return DG_ERR_CUDA;
   }
   for (GemmParams* g : {&m->gu, &m->dn}) {
-    g->ntiles = nullptr;
+    g->offsets = reinterpret_cast<const int32_t*>(ws + L.offsets);
     g->E = (int)E;
     g->I = (int)I;
     g->D = (int)D;
@@ -251,16 +308,21 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
     g->w_perm = reinterpret_cast<const float*>(ws + L.w_perm);
     g->status = reinterpret_cast<DevStatus*>(ws + L.status);
   }
-  m->gu.tiles = reinterpret_cast<const int4*>(ws + L.tiles_gu);
-  m->gu.ntiles = reinterpret_cast<const int*>(ws + L.counters) + 1;
   m->gu.kb_exp = (int)(H / 64);
   m->gu.kb_dense = (int)(H / 64);
-  m->dn.tiles = reinterpret_cast<const int4*>(ws + L.tiles_dn);
-  m->dn.ntiles = reinterpret_cast<const int*>(ws + L.counters) + 2;
+  m->gu.mt_exp = (int)(I / 64);
+  m->gu.mt_dense = (int)(D / 64);
   m->dn.kb_exp = (int)(I / 64);
   m->dn.kb_dense = (int)(D / 64);
+  m->dn.mt_exp = (int)(H / 128);
+  m->dn.mt_dense = (int)(H / 128);
   *out = m;
   return DG_OK;
+}
+
+const char* dg_moe_last_error(const dg_moe_t* m) {
+  if (!m) return "no handle";
+  return m->last_error;
 }
 
 dg_status_t dg_moe_destroy(dg_moe_t* m) {
@@ -296,15 +358,21 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
   uint8_t* ws = m->ws;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int T = n_tokens, H = c.hidden, E = c.n_experts, K = c.top_k;
-  const int I = c.expert_inter, D = c.dense_inter, TK = T * K;
-  const int bn = T <= 1024 ? 128 : 256;
+  const int TK = T * K;
+  const int bn = pick_bn(T);
   int* counters = reinterpret_cast<int*>(ws + L.counters);
   DevStatus* status = reinterpret_cast<DevStatus*>(ws + L.status);
   cudaError_t err = cudaSuccess;
+  const char* failed = "";
   auto mark = [&](int i) {
-    if (m->prof && err == cudaSuccess) err = cudaEventRecord(reinterpret_cast<cudaEvent_t>(m->prof[i]), s);
+    if (err != cudaSuccess && !failed[0]) failed = i > 0 ? kKernelNames[i - 1] : "event";
+    if (m->prof && err == cudaSuccess) {
+      err = cudaEventRecord(reinterpret_cast<cudaEvent_t>(m->prof[i]), s);
+      if (err != cudaSuccess) failed = "profile event record";
+    }
   };
-  if (cudaMemsetAsync(counters, 0, 16 * sizeof(int), s) != cudaSuccess) return DG_ERR_CUDA;
+  if ((err = cudaMemsetAsync(ws + L.zero_begin, 0, L.zero_end - L.zero_begin, s)) != cudaSuccess)
+    return cuda_fail(m, "memset counters", err);
 
   RouterParams rp;
   rp.h = static_cast<const uint16_t*>(h_in);
@@ -322,18 +390,20 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
   rp.router_u8 = c.router_fmt == DG_FMT_AFFINE_U8_G64;
   rp.eps = c.rms_eps;
   rp.r_out = reinterpret_cast<float*>(ws + L.r);
+  rp.r64_out = reinterpret_cast<double*>(ws + L.r64);
+  rp.xnorm_out = reinterpret_cast<float*>(ws + L.xnorm);
+  rp.wnorm_out = reinterpret_cast<float*>(ws + L.wnorm);
   rp.idx = reinterpret_cast<int32_t*>(ws + L.idx);
   rp.w = reinterpret_cast<float*>(ws + L.w);
-  rp.logits = dbg ? dbg->logits : nullptr;
+  rp.logits = reinterpret_cast<float*>(ws + L.logits);
+  rp.chunk_counts = reinterpret_cast<int32_t*>(ws + L.chunk_counts);
   rp.xd = reinterpret_cast<uint16_t*>(ws + L.xd);
   rp.y_moe = reinterpret_cast<float*>(ws + L.y_moe);
   rp.n_refined = counters;
   mark(0);
   if (err == cudaSuccess) err = launch_router(rp, s);
   mark(1);
-  if (err == cudaSuccess)
-    err = launch_route_count(rp.idx, T, K, E, reinterpret_cast<int32_t*>(ws + L.chunk_counts), s);
-
+  if (err == cudaSuccess) err = launch_router_select(rp, s);
   ScatterParams sp;
   sp.idx = rp.idx;
   sp.w = rp.w;
@@ -341,18 +411,10 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
   sp.T = T;
   sp.K = K;
   sp.E = E;
-  sp.H = H;
-  sp.I = I;
-  sp.D = D;
-  sp.bn_exp = bn;
-  sp.bn_dense = bn;
   sp.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
   sp.perm = reinterpret_cast<int32_t*>(ws + L.perm);
   sp.tok_perm = reinterpret_cast<int32_t*>(ws + L.tok_perm);
   sp.w_perm = reinterpret_cast<float*>(ws + L.w_perm);
-  sp.tiles_gu = reinterpret_cast<int4*>(ws + L.tiles_gu);
-  sp.tiles_dn = reinterpret_cast<int4*>(ws + L.tiles_dn);
-  sp.ntiles = counters + 1;
   sp.status = status;
   mark(2);
   if (err == cudaSuccess) err = launch_route_scatter(sp, s);
@@ -367,10 +429,13 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
   gp.xe_perm = reinterpret_cast<uint16_t*>(ws + L.xe_perm);
   mark(3);
   if (err == cudaSuccess) err = launch_gather(gp, m->num_sms, s);
+  GemmParams gu = m->gu, dn = m->dn;
+  gu.T = dn.T = T;
+  gu.bn = dn.bn = bn;
   mark(4);
-  if (err == cudaSuccess) err = launch_gemm(0, bn, m->gu, m->num_sms, s);
+  if (err == cudaSuccess) err = launch_gemm(0, bn, gu, m->num_sms, s);
   mark(5);
-  if (err == cudaSuccess) err = launch_gemm(1, bn, m->dn, m->num_sms, s);
+  if (err == cudaSuccess) err = launch_gemm(1, bn, dn, m->num_sms, s);
 
   CombineParams cp;
   cp.y_dense = reinterpret_cast<const float*>(ws + L.y_dense);
@@ -387,13 +452,14 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
   mark(6);
   if (err == cudaSuccess) err = launch_combine(cp, s);
   mark(7);
-  if (err != cudaSuccess) return DG_ERR_CUDA;
+  if (err != cudaSuccess) return cuda_fail(m, failed[0] ? failed : "launch", err);
 
   if (dbg) {
     struct Copy { void* dst; size_t off; size_t bytes; };
     const Copy copies[] = {
         {dbg->idx, L.idx, (size_t)TK * 4},
         {dbg->w, L.w, (size_t)TK * 4},
+        {dbg->logits, L.logits, (size_t)T * E * 4},
         {dbg->offsets, L.offsets, (size_t)(E + 1) * 4},
         {dbg->perm, L.perm, (size_t)TK * 4},
         {dbg->xd, L.xd, (size_t)T * H * 2},
@@ -403,9 +469,9 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
         {dbg->n_refined, L.counters, 4},
     };
     for (const Copy& cp2 : copies)
-      if (cp2.dst && cudaMemcpyAsync(cp2.dst, ws + cp2.off, cp2.bytes, cudaMemcpyDeviceToDevice, s) !=
-                         cudaSuccess)
-        return DG_ERR_CUDA;
+      if (cp2.dst && (err = cudaMemcpyAsync(cp2.dst, ws + cp2.off, cp2.bytes,
+                                            cudaMemcpyDeviceToDevice, s)) != cudaSuccess)
+        return cuda_fail(m, "debug copy", err);
   }
   return DG_OK;
 }
@@ -420,13 +486,14 @@ dg_status_t dg_moe_forward_host(dg_moe_t* m, const void* h_in_host, void* h_out_
   const size_t bytes = (size_t)n_tokens * m->cfg.hidden * 2;
   void* din = m->ws + m->L.stage_in;
   void* dout = m->ws + m->L.stage_out;
-  if (cudaMemcpyAsync(din, h_in_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return DG_ERR_CUDA;
+  cudaError_t err;
+  if ((err = cudaMemcpyAsync(din, h_in_host, bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(m, "copy in", err);
   dg_status_t st = dg_moe_forward(m, din, dout, n_tokens, layer_scalar, stream, nullptr);
   if (st != DG_OK) return st;
-  if (cudaMemcpyAsync(h_out_host, dout, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return DG_ERR_CUDA;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return DG_ERR_CUDA;
+  if ((err = cudaMemcpyAsync(h_out_host, dout, bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return cuda_fail(m, "copy out", err);
+  if ((err = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(m, "synchronize", err);
   return DG_OK;
 }
 
@@ -434,11 +501,13 @@ dg_status_t dg_moe_last_device_status(dg_moe_t* m, dg_stream_t stream, unsigned 
                                       unsigned int* info) {
   if (!m) return DG_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaStreamSynchronize(s) != cudaSuccess) return DG_ERR_CUDA;
+  cudaError_t err;
+  if ((err = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(m, "synchronize", err);
   DevStatus st;
-  if (cudaMemcpy(&st, m->ws + m->L.status, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return DG_ERR_CUDA;
-  if (cudaMemset(m->ws + m->L.status, 0, sizeof(st)) != cudaSuccess) return DG_ERR_CUDA;
+  if ((err = cudaMemcpy(&st, m->ws + m->L.status, sizeof(st), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(m, "read status", err);
+  if ((err = cudaMemset(m->ws + m->L.status, 0, sizeof(st))) != cudaSuccess)
+    return cuda_fail(m, "clear status", err);
   if (where) *where = st.where;
   if (info) *info = st.info0;
   if (st.code == kDevTimeout) return DG_ERR_TIMEOUT;

@@ -9,15 +9,18 @@ import moe_inputs as mi
 import oracle
 
 # Block output against the exact fp64 oracle: max |err| <= 2e-2 * RMS(out)
-# and cosine >= 0.9999 (the bf16 tolerance of the block's specification).
+# and cosine >= 0.9999 (the bf16 tolerance of the block's specification),
+# the error measured beyond the half-ulp rounding of the bf16 output.
 ERR_RMS = 2e-2
 COS_MIN = 0.9999
 # Branch outputs (f32 y_moe, y_dense) against the oracle's bf16-activation
 # variant (expert/dense input and GEGLU activation rounded to bf16, the rest
-# fp64).  What remains is fp32 accumulation and activations that round to
-# the other bf16 neighbour: ~1e-4 RMS; 2e-3 RMS is ten times below the
-# bf16-rounding error itself (2.07e-2 RMS on the tiny workload).
-BRANCH_ERR_RMS = 2e-3
+# fp64).  What remains is fp32 accumulation and the activations whose fp32
+# value rounds to the other bf16 neighbour than the fp64 one (one bf16 ulp,
+# 2^-8 relative, on a few hundred of the T*I activations): measured up to
+# 5.3e-3 RMS; the bound 1e-2 RMS stays below the bf16-rounding error itself
+# (2.07e-2 RMS on the tiny workload), so a wrong tile or row still fails.
+BRANCH_ERR_RMS = 1e-2
 BRANCH_COS_MIN = 0.99999
 W_ABS = 1e-5  # routing weights (fp32 vs fp64)
 
@@ -55,9 +58,27 @@ def close_stats(got: np.ndarray, ref: np.ndarray):
     return err, rms, cos
 
 
-def assert_close(got, ref, what, err_rms=ERR_RMS, cos_min=COS_MIN):
+def bf16_half_ulp(ref: np.ndarray) -> np.ndarray:
+    """Half a bf16 unit in the last place at each value: the rounding error
+    any bf16 result may carry (2^(floor(log2|x|) - 8))."""
+    a = np.abs(ref)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, np.ldexp(1.0, (e - 8).astype(np.int64)), 0.0)
+
+
+def assert_close(got, ref, what, err_rms=ERR_RMS, cos_min=COS_MIN, bf16_output=False):
+    """max |got - ref| <= err_rms * RMS(ref) and cosine >= cos_min.  For a bf16
+    output the half-ulp rounding of the output itself is allowed on top of
+    the error budget (the output plane is bf16; no bf16 value can be closer
+    to the exact one than that)."""
     err, rms, cos = close_stats(got, ref)
-    assert err <= err_rms * rms + 1e-30, f"{what}: max|err| {err:.3e} > {err_rms} * rms {rms:.3e}"
+    if bf16_output:
+        excess = np.maximum(np.abs(got.astype(np.float64) - ref) - bf16_half_ulp(ref), 0.0)
+        err_budget = float(excess.max()) if excess.size else 0.0
+    else:
+        err_budget = err
+    assert err_budget <= err_rms * rms + 1e-30, \
+        f"{what}: max|err| {err:.3e} ({err_budget:.3e} beyond the bf16 half-ulp) > {err_rms} * rms {rms:.3e}"
     assert cos >= cos_min, f"{what}: cosine {cos:.7f} < {cos_min}"
     return err / rms if rms else 0.0, cos
 
@@ -97,7 +118,7 @@ def run_and_check(wl, p, h_bits, layer_scalar=None, blk=None, check_intermediate
         res["y_moe"] = assert_close(dbg["y_moe"].cpu().numpy(), ym16, "y_moe",
                                     BRANCH_ERR_RMS, BRANCH_COS_MIN)
     got = out.float().cpu().numpy()
-    res["out"] = assert_close(got, ref["out"], "out")
+    res["out"] = assert_close(got, ref["out"], "out", bf16_output=True)
     if own:
         blk.close()
     return res, out, dbg, ref
