@@ -76,21 +76,23 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 __device__ __forceinline__ void tma_load_4d(const CUtensorMap* map, uint64_t* bar, void* dst,
-                                            int c0, int c1, int c2, int c3) {
+                                            int c0, int c1, int c2, int c3, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "l"(policy)
       : "memory");
 }
 
 __device__ __forceinline__ void tma_load_5d(const CUtensorMap* map, uint64_t* bar, void* dst,
-                                            int c0, int c1, int c2, int c3, int c4) {
+                                            int c0, int c1, int c2, int c3, int c4,
+                                            uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
-      "r"(c4)
+      "r"(c4), "l"(policy)
       : "memory");
 }
 
@@ -188,6 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();  // weights: read once per forward
+      const uint64_t pol_x = l2_policy_evict_last();   // token rows: reused by feature tiles
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_par = 0;
@@ -215,26 +219,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
           if (MODE == 0) {
             if (!dense) {
               // rows e*2I + half*I + 16*(4m + c) + r, box (64, 16, 2, 4, 1)
-              tma_load_5d(&p.wa_exp, &full[stage], a_dst, x, 0, 0, 4 * td.y, td.x);
+              tma_load_5d(&p.wa_exp, &full[stage], a_dst, x, 0, 0, 4 * td.y, td.x, pol_w);
             } else if (p.dense_5d) {
-              tma_load_4d(&p.wa_d5, &full[stage], a_dst, x, 0, 0, 4 * td.y);
+              tma_load_4d(&p.wa_d5, &full[stage], a_dst, x, 0, 0, 4 * td.y, pol_w);
             } else {
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
                 const int yg = td.y * 64 + 16 * c;
-                tma_load_2d(&p.wa_d0, &full[stage], a_dst + (2 * c) * kBoxBytes, x, yg);
-                tma_load_2d(&p.wa_d1, &full[stage], a_dst + (2 * c + 1) * kBoxBytes, x, yg);
+                tma_load_2d_hint(&p.wa_d0, &full[stage], a_dst + (2 * c) * kBoxBytes, x, yg, pol_w);
+                tma_load_2d_hint(&p.wa_d1, &full[stage], a_dst + (2 * c + 1) * kBoxBytes, x, yg,
+                                 pol_w);
               }
             }
           } else {
             const CUtensorMap* ma = dense ? &p.wa_d0 : &p.wa_exp;
-            tma_load_2d(ma, &full[stage], a_dst, x, (dense ? 0 : td.x * p.H) + td.y * 128);
+            tma_load_2d_hint(ma, &full[stage], a_dst, x, (dense ? 0 : td.x * p.H) + td.y * 128,
+                             pol_w);
           }
           for (int j = 0; j < nb64; ++j)
-            tma_load_2d(mb64, &full[stage], b_dst + j * 64 * 128, x, td.z + 64 * j);
+            tma_load_2d_hint(mb64, &full[stage], b_dst + j * 64 * 128, x, td.z + 64 * j, pol_x);
           for (int j = 0; j < nb16; ++j)
-            tma_load_2d(mb16, &full[stage], b_dst + (64 * nb64 + kBoxRows * j) * 128, x,
-                        td.z + 64 * nb64 + kBoxRows * j);
+            tma_load_2d_hint(mb16, &full[stage], b_dst + (64 * nb64 + kBoxRows * j) * 128, x,
+                             td.z + 64 * nb64 + kBoxRows * j, pol_x);
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           if (++stage == S) {

@@ -26,7 +26,6 @@ struct RouterParams {
   int router_u8;
   float eps;
   float* r_out;      // [T] 1/rms(h)
-  double* r64_out;   // [T] 1/rms(h) in fp64 (exact re-check)
   float* xnorm_out;  // [T] |router input|
   float* wnorm_out;  // [E] |router row|
   int32_t* idx;      // [T, K]
@@ -35,7 +34,7 @@ struct RouterParams {
   int32_t* chunk_counts;  // [nchunks, E] expert histogram per 256 tokens (zeroed)
   uint16_t* xd;      // bf16 [T, H]
   float* y_moe;      // [T, H], zeroed here
-  int* n_refined;    // counter of tokens re-checked in fp64
+  int* n_refined;    // counter of tokens whose top-k was re-checked exactly
 };
 
 struct ScatterParams {

@@ -22,7 +22,7 @@ const char* const kKernelNames[kNumKernels] = {
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-  size_t status, counters, r, r64, xnorm, wnorm, logits, idx, w, chunk_counts, offsets, perm,
+  size_t status, counters, r, xnorm, wnorm, logits, idx, w, chunk_counts, offsets, perm,
       tok_perm, w_perm;
   size_t xd, xe_perm, act, act_d, y_moe, y_dense, stage_in, stage_out;
   size_t zero_begin, zero_end;  // counters and chunk counts, cleared per forward
@@ -50,7 +50,6 @@ Layout make_layout(const dg_moe_config_t& c) {
   L.zero_begin = L.counters;
   L.zero_end = L.chunk_counts + nchunks * E * 4;
   L.r = take(T * 4);
-  L.r64 = take(T * 8);
   L.xnorm = take(T * 4);
   L.wnorm = take(E * 4);
   L.logits = take(T * E * 4);
@@ -390,7 +389,6 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
   rp.router_u8 = c.router_fmt == DG_FMT_AFFINE_U8_G64;
   rp.eps = c.rms_eps;
   rp.r_out = reinterpret_cast<float*>(ws + L.r);
-  rp.r64_out = reinterpret_cast<double*>(ws + L.r64);
   rp.xnorm_out = reinterpret_cast<float*>(ws + L.xnorm);
   rp.wnorm_out = reinterpret_cast<float*>(ws + L.wnorm);
   rp.idx = reinterpret_cast<int32_t*>(ws + L.idx);

@@ -1,21 +1,21 @@
 // Routing of the MoE FFN block on sm_103a.
 //
-// k_router_logits / k_router_select: per token, RMS of the residual stream, router input
-//   x = h / rms(h) * router_scale * H^-1/2 (two literal steps, "DiffusionGemma
-//   port — plan & parity strategy", Reference dossier §2 Router and the D1
-//   finding), E fp32 logits, top-k with ties to the lower expert index
-//   ("diffgemma — architecture & implemented contract", Part II §2.1 MoE
-//   order), weights = softmax over the k selected logits times
+// k_router_logits / k_router_select: per token, RMS of the residual stream,
+//   router input x = h / rms(h) * router_scale * H^-1/2 (two literal steps,
+//   "DiffusionGemma port — plan & parity strategy", Reference dossier §2
+//   Router and the D1 finding), E fp32 logits, top-k with ties to the lower
+//   expert index ("diffgemma — architecture & implemented contract", Part II
+//   §2.1 MoE order), weights = softmax over the k selected logits times
 //   per_expert_scale (equal to the renormalised softmax over all E,
 //   "DiffusionGemma Explained", MOEBlock.forward).  The fp32 logits carry a
 //   rigorous error bound; a token whose top-k boundary is closer than the
-//   bound is re-checked with fp64 logits of the candidate experts, so the
-//   selected set is the one exact arithmetic gives.  Also writes the dense
+//   bound gets exact logits for its candidate experts, so the selected set is
+//   the one exact arithmetic gives.  The logits kernel also writes the dense
 //   branch input xd = bf16(h / rms(h) * w_pre_ff) and zeroes the token's row
-//   of the f32 expert-sum accumulator.
-// k_route_scatter: token -> expert grouping from the per-chunk histogram
-//   (counted by k_router_select), prefix sum and a stable scatter
-//   (assignments sorted by expert, then token).
+//   of the f32 expert-sum accumulator; the select kernel also counts the
+//   per-chunk expert histogram.
+// k_route_scatter: token -> expert grouping from the per-chunk histogram,
+//   prefix sum and a stable scatter (assignments sorted by expert, then token).
 // k_gather_xe: expert input rows xe = bf16(h / rms(h) * w_pre_ff2) in
 //   grouped order, the B operand of the gate_up GEMM.
 #include <math.h>
@@ -28,11 +28,6 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxSlots = 8;  // experts per lane: E <= 256
 
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-  return v;
-}
 __device__ __forceinline__ float warp_min_f(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v = fminf(v, __shfl_xor_sync(kFull, v, o));
@@ -71,9 +66,14 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
     f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
   }
 }
+__device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
+  return (uint32_t)f32_to_bf16_rne(a) | ((uint32_t)f32_to_bf16_rne(b) << 16);
+}
+
 // Error-free transformations in fp32 (Knuth's TwoSum; Dekker's product via
 // FMA).  A pair (hi, lo) carries a sum whose rounding error is second order
-// (~n u^2 of the magnitudes), which makes fp64 unnecessary in the loops.
+// (~n u^2 of the magnitudes), which keeps fp64 (slow on this part) out of
+// the loops.
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   s = __fadd_rn(a, b);
   const float bb = __fsub_rn(s, a);
@@ -94,85 +94,124 @@ __device__ __forceinline__ void df_add2(float& hi, float& lo, float hi2, float l
 }
 __device__ __forceinline__ double df_value(float hi, float lo) { return (double)hi + (double)lo; }
 
-__device__ __forceinline__ void unpack8p(const uint4& u, float* f) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
-}
-__device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
-  return (uint32_t)f32_to_bf16_rne(a) | ((uint32_t)f32_to_bf16_rne(b) << 16);
-}
-
-// Error bound of the fp32 logits, relative to |W_e| |x| + |bias_e|.  The
-// computed logit differs from the exact one by at most ~70 unit roundoffs
-// times sum_i |W_ei x_i| (<= |W_e| |x|): 48 from the router input (fp64
-// rms, three fp32 products), 16 from each 16-term fp32 chunk sum (chunk sums
-// are accumulated as error-free fp32 pairs), a few from the final rounding
-// and the bias add.  2^-16 = 256 unit roundoffs leaves a factor of 3.6.
-constexpr float kLogitBound = 1.52587890625e-05f;  // 2^-16
+// Error bound of the fp32 logits, relative to |W_e| |x| + |bias_e| (u is the
+// fp32 unit roundoff 2^-24).  A computed logit is (1 + d) z_e + err_e with
+// |err_e| <= ~22 u sum_i |W_ei x_i| <= 22 u |W_e| |x|: 3 u from the three
+// fp32 products of the router input, 16 u from each 16-term fp32 chunk sum
+// (chunk sums are accumulated as error-free fp32 pairs), a few u from the
+// final rounding; and d (~50 u) is the error of the fp32 1/rms, a factor
+// common to all logits of the token.  Without a router bias the common
+// factor cannot change the order, so 2^-18 = 64 u bounds err_e with a factor
+// of about 3; with a bias d acts like a per-expert error (|d| |z_e - b_e|),
+// and 2^-16 = 256 u covers 22 u + 50 u + the bias rounding.
+constexpr float kLogitBoundNoBias = 3.814697265625e-06f;  // 2^-18
+constexpr float kLogitBoundBias = 1.52587890625e-05f;     // 2^-16
 
 constexpr int kLogitExperts = 32;  // experts per block of k_router_logits
 constexpr int kLogitSlices = 8;    // K slices per expert (lanes of one warp)
 
-// Logits for TB tokens x 32 experts.  Every block recomputes the router input
-// of its tokens into shared memory, laid out [token][slice][H/8 + 4] so that
-// the eight K-slices of a warp read distinct banks; blocks of the first
-// expert column also write r, xd and zero the y_moe rows.
-template <int TB>
+// Logits for TB tokens x 32 experts.  Thread (expert, slice j) sums the
+// 16-element runs k = 16 (8 q + j) .. + 15 of the hidden dimension, so the
+// eight slices of an expert read one contiguous 256-byte run of its router
+// row.  The h rows of the block and the per-channel vectors are loaded into
+// shared memory in one round; the router input is built there, laid out
+// [token][slice][H/8 + 4] (the padding puts the eight slices of a warp on
+// distinct banks).  Blocks of the first expert column also write r, |x|,
+// xd and zero the y_moe rows.
+template <int TB, bool U8>
 __global__ void __launch_bounds__(256) k_router_logits(const RouterParams p) {
   extern __shared__ __align__(16) uint8_t sm[];
   const int H = p.H, E = p.E;
   const int L = H / kLogitSlices;   // K elements per slice (multiple of 16)
   const int LS = L + 4;             // padded slice stride (floats)
-  float* xs = reinterpret_cast<float*>(sm);  // [TB][8][LS]
+  float* xs = reinterpret_cast<float*>(sm);                                   // [TB][8][LS]
+  uint4* hs = reinterpret_cast<uint4*>(xs + (size_t)TB * kLogitSlices * LS);  // [TB][H/8]
+  uint4* rss = hs + (size_t)TB * (H >> 3);                                    // router_scale
+  uint4* wps = rss + (H >> 3);                                                // w_pre_ff
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * TB;
   const bool first_col = blockIdx.y == 0;
   const int nvec = H >> 3;
   const float cH = (float)(1.0 / sqrt((double)H));
-  const uint4* rsv = reinterpret_cast<const uint4*>(p.router_scale);
-  const uint4* wpv = reinterpret_cast<const uint4*>(p.w_pre_ff);
+  const int ngroups = H >> 6;
+
+  // thread (expert el, slice j); its first weight step is requested before
+  // the router input is built, so the latency overlaps phase 1
+  const int el = threadIdx.x >> 3, j = threadIdx.x & 7;
+  const int e_raw = blockIdx.y * kLogitExperts + el;
+  const int e = e_raw < E ? e_raw : E - 1;
+  auto load_step = [&](int c0, uint4 (&raw)[4][2]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int c = c0 + 16 * q;
+      if (c < L) {
+        const int k0 = ((c >> 4) * kLogitSlices + j) * 16;  // interleaved 16-runs
+        if constexpr (!U8) {
+          const uint4* wrow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.wr) +
+                                                              (size_t)e * H + k0);
+          raw[q][0] = __ldg(wrow);
+          raw[q][1] = __ldg(wrow + 1);
+        } else {
+          raw[q][0] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.wr) +
+                                                           (size_t)e * H + k0));
+        }
+      }
+    }
+  };
+  uint4 raw_next[4][2];
+  load_step(0, raw_next);
+
+  // ---- phase 1: h rows and vectors in one round of loads, router input, xd
+  for (int i = threadIdx.x; i < TB * nvec; i += blockDim.x) {
+    const int tl = i / nvec, v = i - tl * nvec;
+    const int t = t0 + tl;
+    hs[i] = t < p.T ? __ldg(reinterpret_cast<const uint4*>(p.h + (size_t)t * H) + v)
+                    : make_uint4(0u, 0u, 0u, 0u);
+  }
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+    rss[v] = __ldg(reinterpret_cast<const uint4*>(p.router_scale) + v);
+    if (first_col) wps[v] = __ldg(reinterpret_cast<const uint4*>(p.w_pre_ff) + v);
+  }
+  __syncthreads();
 
   for (int tl = warp; tl < TB; tl += 8) {
     const int t = t0 + tl;
     float* xrow = xs + (size_t)tl * kLogitSlices * LS;
-    if (t >= p.T) {
-      for (int i = lane; i < kLogitSlices * LS; i += 32) xrow[i] = 0.f;
-      continue;
-    }
-    const uint4* hrow = reinterpret_cast<const uint4*>(p.h + (size_t)t * H);
+    const uint4* hrow = hs + (size_t)tl * nvec;
     float ss = 0.f;
     for (int v = lane; v < nvec; v += 32) {
       float f[8];
-      unpack8(__ldg(hrow + v), f);
+      unpack8(hrow[v], f);
 #pragma unroll
       for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
     }
-    const double ssd = warp_sum_d((double)ss);
-    const double r64 = 1.0 / sqrt(ssd / (double)H + (double)p.eps);
-    const float rf = (float)r64;
+    ss = warp_sum_f(ss);
+    // 1/rms in fp32 (rsqrt and one Newton step); its error is a factor
+    // common to all logits of the token
+    const float msq = ss / (float)H + p.eps;
+    float rf = rsqrtf(msq);
+    rf = rf * (1.5f - 0.5f * msq * rf * rf);
     float xnl = 0.f;
     uint4* xdrow = reinterpret_cast<uint4*>(p.xd + (size_t)t * H);
+#pragma unroll 2
     for (int v = lane; v < nvec; v += 32) {
       float f[8], sc[8];
-      unpack8(__ldg(hrow + v), f);
-      unpack8(__ldg(rsv + v), sc);
+      unpack8(hrow[v], f);
+      unpack8(rss[v], sc);
       float x[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         x[i] = f[i] * rf * sc[i] * cH;
         xnl = fmaf(x[i], x[i], xnl);
       }
-      const int k = 8 * v, sl = k / L, off = k - sl * L;  // 8 | L: a vector never straddles
+      // element k goes to slice (k / 16) % 8 at position (k / 128) * 16 + k % 16
+      const int k = 8 * v, sl = (k >> 4) & 7, off = ((k >> 7) << 4) + (k & 15);
       float4* xo = reinterpret_cast<float4*>(xrow + sl * LS + off);
       xo[0] = make_float4(x[0], x[1], x[2], x[3]);
       xo[1] = make_float4(x[4], x[5], x[6], x[7]);
-      if (first_col) {
+      if (first_col && t < p.T) {
         float wp[8];
-        unpack8(__ldg(wpv + v), wp);
+        unpack8(wps[v], wp);
         uint4 o;
         o.x = pack2_bf16(f[0] * rf * wp[0], f[1] * rf * wp[1]);
         o.y = pack2_bf16(f[2] * rf * wp[2], f[3] * rf * wp[3]);
@@ -181,12 +220,11 @@ __global__ void __launch_bounds__(256) k_router_logits(const RouterParams p) {
         xdrow[v] = o;
       }
     }
-    if (first_col) {
-      const double xnd = warp_sum_d((double)xnl);
+    if (first_col && t < p.T) {
+      const float xnd = warp_sum_f(xnl);
       if (lane == 0) {
         p.r_out[t] = rf;
-        p.r64_out[t] = r64;
-        p.xnorm_out[t] = (float)sqrt(xnd);
+        p.xnorm_out[t] = sqrtf(xnd) * 1.001f;  // rounded up: used in a bound
       }
       float4* yr = reinterpret_cast<float4*>(p.y_moe + (size_t)t * H);
       for (int v = lane; v < (H >> 2); v += 32) yr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -194,54 +232,68 @@ __global__ void __launch_bounds__(256) k_router_logits(const RouterParams p) {
   }
   __syncthreads();
 
-  // thread (expert el, slice j): 16-term fp32 chunk sums over its K slice,
-  // added in fp64, then the 8 slices of a warp are summed with shuffles
-  const int el = threadIdx.x >> 3, j = threadIdx.x & 7;
-  const int e_raw = blockIdx.y * kLogitExperts + el;
-  const int e = e_raw < E ? e_raw : E - 1;
+  // ---- phase 2: 16-term chunk sums (two 8-term fp32x2 halves, even and odd
+  // elements), accumulated over the slice as error-free fp32 pairs; the
+  // eight slices of an expert are then summed with shuffles.  Weights of the
+  // next step are loaded while the current step computes.
   float acc_hi[TB], acc_lo[TB];
 #pragma unroll
   for (int t = 0; t < TB; ++t) {
     acc_hi[t] = 0.f;
     acc_lo[t] = 0.f;
   }
-  float wsq = 0.f;
-  const int ngroups = H >> 6;
-  for (int c = 0; c < L; c += 16) {
-    const int k0 = j * L + c;
-    float wv[16];
-    if (!p.router_u8) {
-      const uint4* wrow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.wr) +
-                                                          (size_t)e * H + k0);
-      unpack8p(__ldg(wrow), wv);
-      unpack8p(__ldg(wrow + 1), wv + 8);
-    } else {
-      // a 16-run never straddles a 64-group (16 | k0)
-      const float gs = bf16_to_f32(p.wr_scales[(size_t)e * ngroups + (k0 >> 6)]);
-      const float gb = bf16_to_f32(p.wr_biases[(size_t)e * ngroups + (k0 >> 6)]);
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.wr) +
-                                                           (size_t)e * H + k0));
-      const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+  float2 wsq2 = make_float2(0.f, 0.f);
+  const bool need_norm = blockIdx.x == 0;
+  for (int c0 = 0; c0 < L; c0 += 64) {
+    uint4 raw[4][2];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) wv[i] = fmaf(gs, (float)((wd[i >> 2] >> (8 * (i & 3))) & 0xffu), gb);
+    for (int q = 0; q < 4; ++q) {
+      raw[q][0] = raw_next[q][0];
+      raw[q][1] = raw_next[q][1];
     }
+    if (c0 + 64 < L) load_step(c0 + 64, raw_next);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) wsq = fmaf(wv[i], wv[i], wsq);
+    for (int q = 0; q < 4; ++q) {
+      const int c = c0 + 16 * q;
+      if (c >= L) break;
+      const int k0 = ((c >> 4) * kLogitSlices + j) * 16;
+      float2 w2[8];
+      if constexpr (!U8) {
+        const uint32_t wd[8] = {raw[q][0].x, raw[q][0].y, raw[q][0].z, raw[q][0].w,
+                                raw[q][1].x, raw[q][1].y, raw[q][1].z, raw[q][1].w};
 #pragma unroll
-    for (int t = 0; t < TB; ++t) {
-      const float4* xv = reinterpret_cast<const float4*>(xs + ((size_t)t * kLogitSlices + j) * LS + c);
-      float s = 0.f;
+        for (int i = 0; i < 8; ++i)
+          w2[i] = make_float2(__uint_as_float(wd[i] << 16), __uint_as_float(wd[i] & 0xffff0000u));
+      } else {
+        // a 16-run never straddles a 64-group (16 | k0)
+        const float gs = bf16_to_f32(p.wr_scales[(size_t)e * ngroups + (k0 >> 6)]);
+        const float gb = bf16_to_f32(p.wr_biases[(size_t)e * ngroups + (k0 >> 6)]);
+        const uint32_t wd[4] = {raw[q][0].x, raw[q][0].y, raw[q][0].z, raw[q][0].w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 a = xv[q];
-        s = fmaf(wv[4 * q + 0], a.x, s);
-        s = fmaf(wv[4 * q + 1], a.y, s);
-        s = fmaf(wv[4 * q + 2], a.z, s);
-        s = fmaf(wv[4 * q + 3], a.w, s);
+        for (int i = 0; i < 8; ++i)
+          w2[i] = make_float2(fmaf(gs, (float)((wd[i >> 1] >> (16 * (i & 1))) & 0xffu), gb),
+                              fmaf(gs, (float)((wd[i >> 1] >> (16 * (i & 1) + 8)) & 0xffu), gb));
       }
-      df_add(acc_hi[t], acc_lo[t], s);
+      if (need_norm) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) wsq2 = __ffma2_rn(w2[i], w2[i], wsq2);
+      }
+#pragma unroll
+      for (int t = 0; t < TB; ++t) {
+        const float4* xv =
+            reinterpret_cast<const float4*>(xs + ((size_t)t * kLogitSlices + j) * LS + c);
+        float2 a2 = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float4 a = xv[r];
+          a2 = __ffma2_rn(w2[2 * r], make_float2(a.x, a.y), a2);
+          b2 = __ffma2_rn(w2[2 * r + 1], make_float2(a.z, a.w), b2);
+        }
+        df_add(acc_hi[t], acc_lo[t], __fadd_rn(__fadd_rn(a2.x, a2.y), __fadd_rn(b2.x, b2.y)));
+      }
     }
   }
+  float wsq = wsq2.x + wsq2.y;
 #pragma unroll
   for (int o = 1; o < kLogitSlices; o <<= 1) {
     wsq += __shfl_xor_sync(kFull, wsq, o);
@@ -258,142 +310,275 @@ __global__ void __launch_bounds__(256) k_router_logits(const RouterParams p) {
     for (int t = 0; t < TB; ++t)
       if (t0 + t < p.T)
         p.logits[(size_t)(t0 + t) * E + e] = (float)(df_value(acc_hi[t], acc_lo[t]) + bias);
-    if (blockIdx.x == 0) p.wnorm_out[e] = sqrtf(wsq) * 1.001f;  // rounded up: a bound
+    if (need_norm) p.wnorm_out[e] = sqrtf(wsq) * 1.001f;  // rounded up: a bound
   }
 }
 
-// Warp per token: top-k of the fp32 logits, an fp64 re-check of the
-// candidates when the k-th / (k+1)-th boundary is closer than the error
-// bound, softmax of the k selected logits times per_expert_scale, outputs in
-// ascending expert order.
+// Exact logits: sum_i W_ei (router_scale_i h_i) with every term exact in
+// fp32 (a bf16 triple product has at most 24 significant bits; an 8-bit
+// affine weight is first split into two exact fp32 parts), summed as
+// error-free fp32 pairs; 1/rms from the exact sum of squares (bf16 squares
+// are exact).
+__device__ __forceinline__ void exact_terms_bf16(const uint4& hv, const uint4& sv, const uint4& wv,
+                                                 float& hi, float& lo) {
+  float hf[8], sf[8], wf[8];
+  unpack8(hv, hf);
+  unpack8(sv, sf);
+  unpack8(wv, wf);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) df_add(hi, lo, __fmul_rn(wf[i], __fmul_rn(sf[i], hf[i])));
+}
+__device__ __forceinline__ void exact_terms_u8(const uint4& hv, const uint4& sv, uint32_t qx,
+                                               uint32_t qy, float gs, float gb, float& hi,
+                                               float& lo) {
+  float hf[8], sf[8];
+  unpack8(hv, hf);
+  unpack8(sv, sf);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t code = ((i < 4 ? qx : qy) >> (8 * (i & 3))) & 0xffu;
+    float wh, wl;
+    two_sum(__fmul_rn(gs, (float)code), gb, wh, wl);  // W = wh + wl exactly
+    const float sh = __fmul_rn(sf[i], hf[i]);           // exact (16 bits)
+    const float p1 = __fmul_rn(wh, sh);
+    df_add(hi, lo, p1);
+    df_add(hi, lo, fmaf(wh, sh, -p1));                  // exact product error
+    df_add(hi, lo, __fmul_rn(wl, sh));
+  }
+}
+__device__ __forceinline__ void exact_squares(const uint4& hv, float& hi, float& lo) {
+  float hf[8];
+  unpack8(hv, hf);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) df_add(hi, lo, __fmul_rn(hf[i], hf[i]));
+}
+
+constexpr int kSelTokens = 8;
+constexpr int kPartJobs = 64;  // jobs whose partial sums are held at once (power of 2)
+
+// Eight tokens per block, warp per token: top-k of the fp32 logits; where
+// the k-th / (k+1)-th boundary is closer than the error bound, the candidate
+// experts get exact logits; then reselection, softmax of the k selected
+// logits times per_expert_scale, outputs in ascending expert order and the
+// per-chunk expert histogram.  For the exact logits, warp w owns the slice
+// [w H/8, (w+1) H/8) of the hidden dimension and walks every (token,
+// candidate) job of the block four at a time; the eight partial sums of a
+// job are combined in a fixed order.
+template <bool U8>
 __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
+  __shared__ int s_cand[kSelTokens][256];
+  __shared__ int s_ncand[kSelTokens];
+  __shared__ double s_zx[kSelTokens][256];
+  __shared__ double s_ss[kSelTokens];
+  __shared__ float2 s_part[kPartJobs][kSelTokens];
   const int H = p.H, E = p.E, K = p.K;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= p.T) return;
-  const float* z = p.logits + (size_t)t * E;
-  const int ngroups = H >> 6;
-  const double cHd = 1.0 / sqrt((double)H);
-  float zl[kMaxSlots], el[kMaxSlots];
-  const float xnt = p.xnorm_out[t];
-#pragma unroll
-  for (int s = 0; s < kMaxSlots; ++s) {
-    const int e = 32 * s + lane;
-    if (e < E) {
-      const float v = z[e];
-      zl[s] = isnan(v) ? -INFINITY : v;
-      const float b = p.router_bias ? fabsf(p.router_bias[e]) : 0.f;
-      el[s] = kLogitBound * (p.wnorm_out[e] * xnt + b) + 1e-30f;
-    } else {
-      zl[s] = -INFINITY;
-      el[s] = 0.f;
-    }
-  }
+  const int t = blockIdx.x * kSelTokens + warp;
+  const bool valid = t < p.T;
+
+  // ---- A: selection on the fp32 logits, candidate list if near a tie
+  float zl[kMaxSlots];
   uint32_t taken = 0;
-  for (int k = 0; k < K; ++k) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
+  int ncand = 0;
+  if (valid) {
+    const float* z = p.logits + (size_t)t * E;
+    const float xnt = p.xnorm_out[t];
+    const float bound = p.router_bias ? kLogitBoundBias : kLogitBoundNoBias;
+    float el[kMaxSlots];
 #pragma unroll
     for (int s = 0; s < kMaxSlots; ++s) {
       const int e = 32 * s + lane;
-      if (e < E && !((taken >> s) & 1u) && (zl[s] > bv || (zl[s] == bv && e < be))) {
-        bv = zl[s];
-        be = e;
+      if (e < E) {
+        const float v = z[e];
+        zl[s] = isnan(v) ? -INFINITY : v;
+        const float b = p.router_bias ? fabsf(p.router_bias[e]) : 0.f;
+        el[s] = bound * (p.wnorm_out[e] * xnt + b) + 1e-30f;
+      } else {
+        zl[s] = -INFINITY;
+        el[s] = 0.f;
       }
     }
-    warp_argmax(bv, be);
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-  }
-  float L = INFINITY, U = -INFINITY;
-#pragma unroll
-  for (int s = 0; s < kMaxSlots; ++s) {
-    if (32 * s + lane >= E) continue;
-    if ((taken >> s) & 1u) L = fminf(L, zl[s] - el[s]);
-    else U = fmaxf(U, zl[s] + el[s]);
-  }
-  L = warp_min_f(L);
-  U = warp_max_f(U);
-  if (!(L > U)) {
-    // Candidates that may belong to the exact top-k: z + bound >= L, where L
-    // is the smallest lower bound among the k chosen (at least k experts have
-    // exact logits >= L, so every exact top-k member passes).
-    uint32_t cand = 0;
-#pragma unroll
-    for (int s = 0; s < kMaxSlots; ++s)
-      if (32 * s + lane < E && zl[s] + el[s] >= L) cand |= 1u << s;
-    const double r64 = p.r64_out[t];
-    const uint16_t* hrow = p.h + (size_t)t * H;
-    double zx[kMaxSlots];
-#pragma unroll
-    for (int s = 0; s < kMaxSlots; ++s) {
-      zx[s] = -INFINITY;
-      uint32_t m = __ballot_sync(kFull, (cand >> s) & 1u);
-      while (m) {
-        const int src = __ffs(m) - 1;
-        m &= m - 1;
-        const int e = 32 * s + src;
-        // exact terms W_ei * (router_scale_i * h_i) summed as an fp32 pair:
-        // a bf16 triple product has at most 24 significant bits, and an
-        // 8-bit affine weight is split into two exact fp32 parts first
-        float hi = 0.f, lo = 0.f;
-        const uint4* hv = reinterpret_cast<const uint4*>(hrow);
-        const uint4* sv = reinterpret_cast<const uint4*>(p.router_scale);
-        for (int v = lane; v < (H >> 3); v += 32) {
-          float hf[8], sf[8], wf[8];
-          unpack8p(__ldg(hv + v), hf);
-          unpack8p(__ldg(sv + v), sf);
-          if (!p.router_u8) {
-            unpack8p(__ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.wr) +
-                                                          (size_t)e * H) + v), wf);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) df_add(hi, lo, __fmul_rn(wf[i], __fmul_rn(sf[i], hf[i])));
-          } else {
-            const int g = (8 * v) >> 6;
-            const float gs = bf16_to_f32(p.wr_scales[(size_t)e * ngroups + g]);
-            const float gb = bf16_to_f32(p.wr_biases[(size_t)e * ngroups + g]);
-            const uint2 q = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(p.wr) +
-                                                                 (size_t)e * H) + v);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint32_t code = ((i < 4 ? q.x : q.y) >> (8 * (i & 3))) & 0xffu;
-              float wh, wl;
-              two_sum(__fmul_rn(gs, (float)code), gb, wh, wl);   // W = wh + wl exactly
-              const float sh = __fmul_rn(sf[i], hf[i]);           // exact (16 bits)
-              const float p1 = __fmul_rn(wh, sh);
-              const float p1e = fmaf(wh, sh, -p1);                // exact product error
-              df_add(hi, lo, p1);
-              df_add(hi, lo, p1e);
-              df_add(hi, lo, __fmul_rn(wl, sh));
-            }
-          }
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-          const float h2 = __shfl_xor_sync(kFull, hi, o);
-          const float l2 = __shfl_xor_sync(kFull, lo, o);
-          df_add2(hi, lo, h2, l2);
-        }
-        const double part = df_value(hi, lo);
-        const double zz = part * r64 * cHd + (p.router_bias ? (double)p.router_bias[e] : 0.0);
-        if (lane == src) zx[s] = zz;
-      }
-    }
-    taken = 0;
     for (int k = 0; k < K; ++k) {
-      double bv = -INFINITY;
+      float bv = -INFINITY;
       int be = 0x7fffffff;
 #pragma unroll
       for (int s = 0; s < kMaxSlots; ++s) {
         const int e = 32 * s + lane;
-        if (((cand >> s) & 1u) && !((taken >> s) & 1u) && (zx[s] > bv || (zx[s] == bv && e < be))) {
-          bv = zx[s];
+        if (e < E && !((taken >> s) & 1u) && (zl[s] > bv || (zl[s] == bv && e < be))) {
+          bv = zl[s];
           be = e;
         }
       }
       warp_argmax(bv, be);
-      if (be != 0x7fffffff && (be & 31) == lane) taken |= 1u << (be >> 5);
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
     }
+    float L = INFINITY, U = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kMaxSlots; ++s) {
+      if (32 * s + lane >= E) continue;
+      if ((taken >> s) & 1u) L = fminf(L, zl[s] - el[s]);
+      else U = fmaxf(U, zl[s] + el[s]);
+    }
+    L = warp_min_f(L);
+    U = warp_max_f(U);
+    if (!(L > U)) {
+      // candidates that may belong to the exact top-k: z + bound >= L (at
+      // least k experts have exact logits >= L, so every exact top-k member
+      // passes); listed in ascending expert order
+      const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+      for (int s = 0; s < kMaxSlots; ++s) {
+        const bool c = 32 * s + lane < E && zl[s] + el[s] >= L;
+        const unsigned ms = __ballot_sync(kFull, c);
+        if (c) s_cand[warp][ncand + __popc(ms & lt)] = 32 * s + lane;
+        ncand += __popc(ms);
+      }
+    }
+  }
+  if (lane == 0) s_ncand[warp] = ncand;
+  __syncthreads();
+
+  // ---- B: exact logits.  Jobs of a near-tie token: its sum of squares
+  // (c = -1), then its candidates (c = 0 .. ncand-1).
+  int njobs = 0, first[kSelTokens + 1];
+#pragma unroll
+  for (int w = 0; w < kSelTokens; ++w) {
+    first[w] = njobs;
+    njobs += s_ncand[w] > 0 ? s_ncand[w] + 1 : 0;
+  }
+  first[kSelTokens] = njobs;
+  if (njobs > 0) {
+    const int vs = H >> 6;  // 8-element vectors per warp slice
+    const int vbase = warp * vs;
+    const int ngroups = H >> 6;
+    const uint4* sv = reinterpret_cast<const uint4*>(p.router_scale);
+    for (int j0 = 0; j0 < njobs; j0 += 4) {
+      int jt[4], je[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int job = j0 + u;
+        int w = 0;
+#pragma unroll
+        for (int q = 1; q < kSelTokens; ++q)
+          if (job >= first[q]) w = q;
+        const int c = job - first[w] - 1;
+        jt[u] = job < njobs ? w : -1;
+        je[u] = (job < njobs && c >= 0) ? s_cand[w][c] : -1;
+      }
+      float hi[4], lo[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        hi[u] = 0.f;
+        lo[u] = 0.f;
+      }
+      for (int vv = lane; vv < vs; vv += 32) {
+        const int v = vbase + vv;
+        const uint4 rs = __ldg(sv + v);
+        uint4 rh[4], rw[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (jt[u] < 0) continue;
+          const int tt = blockIdx.x * kSelTokens + jt[u];
+          rh[u] = __ldg(reinterpret_cast<const uint4*>(p.h + (size_t)tt * H) + v);
+          if (je[u] >= 0) {
+            if constexpr (!U8) {
+              rw[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.wr) +
+                                                           (size_t)je[u] * H) + v);
+            } else {
+              const uint2 q2 = __ldg(reinterpret_cast<const uint2*>(
+                                         static_cast<const uint8_t*>(p.wr) + (size_t)je[u] * H) + v);
+              rw[u] = make_uint4(q2.x, q2.y, 0u, 0u);
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (jt[u] < 0) continue;
+          if (je[u] < 0) {
+            exact_squares(rh[u], hi[u], lo[u]);
+          } else if constexpr (!U8) {
+            exact_terms_bf16(rh[u], rs, rw[u], hi[u], lo[u]);
+          } else {
+            const int gi = (8 * v) >> 6;
+            exact_terms_u8(rh[u], rs, rw[u].x, rw[u].y,
+                           bf16_to_f32(p.wr_scales[(size_t)je[u] * ngroups + gi]),
+                           bf16_to_f32(p.wr_biases[(size_t)je[u] * ngroups + gi]), hi[u], lo[u]);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+          df_add2(hi[u], lo[u], __shfl_xor_sync(kFull, hi[u], o), __shfl_xor_sync(kFull, lo[u], o));
+        if (lane == 0 && jt[u] >= 0)
+          s_part[(j0 + u) & (kPartJobs - 1)][warp] = make_float2(hi[u], lo[u]);
+      }
+      // every kPartJobs jobs (and at the end) the partials are combined
+      if (((j0 + 4) & (kPartJobs - 1)) == 0 || j0 + 4 >= njobs) {
+        __syncthreads();
+        const int jb = j0 & ~(kPartJobs - 1);
+        if ((int)threadIdx.x < kPartJobs && jb + (int)threadIdx.x < njobs) {
+          const int job = jb + threadIdx.x;
+          float sh = 0.f, sl = 0.f;
+#pragma unroll
+          for (int q = 0; q < kSelTokens; ++q)
+            df_add2(sh, sl, s_part[threadIdx.x][q].x, s_part[threadIdx.x][q].y);
+          int w = 0;
+#pragma unroll
+          for (int q = 1; q < kSelTokens; ++q)
+            if (job >= first[q]) w = q;
+          const int c = job - first[w] - 1;
+          if (c < 0) s_ss[w] = df_value(sh, sl);
+          else s_zx[w][c] = df_value(sh, sl);
+        }
+        __syncthreads();
+      }
+    }
+    // exact logit = dot * (1/rms) * H^-1/2 + bias
+    const double cHd = 1.0 / sqrt((double)H);
+    for (int i = threadIdx.x; i < kSelTokens * 256; i += blockDim.x) {
+      const int w = i >> 8, c = i & 255;
+      if (c < s_ncand[w]) {
+        const double r64 = 1.0 / sqrt(s_ss[w] / (double)H + (double)p.eps);
+        const int e = s_cand[w][c];
+        s_zx[w][c] = s_zx[w][c] * r64 * cHd + (p.router_bias ? (double)p.router_bias[e] : 0.0);
+      }
+    }
+  }
+  __syncthreads();
+  if (!valid) return;
+
+  // ---- C: reselection among the candidates, weights, outputs
+  if (ncand > 0) {
     if (lane == 0) atomicAdd(p.n_refined, 1);
+    // candidate c = lane + 32 q is held by this lane; bit q of usedc marks it taken
+    taken = 0;
+    uint32_t usedc = 0;
+    for (int k = 0; k < K; ++k) {
+      double bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int q = 0; q < kMaxSlots; ++q) {
+        const int c = lane + 32 * q;
+        if (c < ncand && !((usedc >> q) & 1u)) {
+          const int e = s_cand[warp][c];
+          const double v = s_zx[warp][c];
+          if (v > bv || (v == bv && e < be)) {
+            bv = v;
+            be = e;
+          }
+        }
+      }
+      warp_argmax(bv, be);
+      if (be == 0x7fffffff) break;
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+#pragma unroll
+      for (int q = 0; q < kMaxSlots; ++q) {
+        const int c = lane + 32 * q;
+        if (c < ncand && s_cand[warp][c] == be) usedc |= 1u << q;
+      }
+    }
   }
   float zmax = -INFINITY;
 #pragma unroll
@@ -442,16 +627,20 @@ __device__ int block_excl_scan256(int v, int* tmp, int* total) {
   return incl - v;
 }
 
-__global__ void __launch_bounds__(256) k_route_scatter(const ScatterParams p) {
+// One block per 256-token chunk.  Stable position of assignment (t, j) with
+// expert e: all assignments to lower experts, then to e from earlier chunks,
+// earlier warps of this chunk and earlier lanes of this warp (per-warp
+// expert masks built with shared-memory atomics).
+__global__ void __launch_bounds__(256, 1) k_route_scatter(const ScatterParams p) {
   __shared__ int s_tmp[256];
   __shared__ int s_base[256];
-  __shared__ int s_before[256];
-  __shared__ unsigned s_wmask[8][256];
+  __shared__ unsigned s_wmask[8][256];  // per warp and expert: lanes (tokens) that chose it
   __shared__ int s_wbase[8][256];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int chunk = blockIdx.x, nchunks = gridDim.x;
   const int E = p.E, K = p.K, T = p.T;
 
+  for (int i = tid; i < 8 * 256; i += 256) (&s_wmask[0][0])[i] = 0u;
   int tot = 0, bef = 0;
   if (tid < E) {
     for (int c = 0; c < nchunks; ++c) {
@@ -460,72 +649,46 @@ __global__ void __launch_bounds__(256) k_route_scatter(const ScatterParams p) {
       if (c < chunk) bef += v;
     }
   }
+  const int t = chunk * kChunkTokens + tid;
+  const bool valid = t < T;
+  int ex[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) ex[j] = (j < K && valid) ? p.idx[(size_t)t * K + j] : -1;
   int total;
-  const int base = block_excl_scan256(tot, s_tmp, &total);
-  s_base[tid] = base;
-  s_before[tid] = bef;
-
+  const int base = block_excl_scan256(tot, s_tmp, &total);  // synchronises: masks are clear
+  s_base[tid] = base + bef;
   if (chunk == 0) {
     if (tid < E) p.offsets[tid] = base;
     if (tid == 0) p.offsets[E] = total;
   }
-
-  // stable ranks inside the chunk: per warp, one ballot per expert
-  const int t = chunk * kChunkTokens + tid;
-  const bool valid = t < T;
-  int ex[16];
-  unsigned bits[8];
-#pragma unroll
-  for (int w = 0; w < 8; ++w) bits[w] = 0u;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    ex[j] = -1;
-    if (j < K && valid) {
-      const int e = p.idx[(size_t)t * K + j];
-      if ((unsigned)e < (unsigned)E) {
-        ex[j] = e;
-#pragma unroll
-        for (int w = 0; w < 8; ++w)
-          if ((e >> 5) == w) bits[w] |= 1u << (e & 31);
-      } else {
-        report(p.status, kDevBounds, kSiteScatter, (unsigned)t, (unsigned)e);
-      }
-    }
-  }
-#pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    if (32 * w >= E) break;
-    for (int b = 0; b < 32; ++b) {
-      const int e = 32 * w + b;
-      if (e >= E) break;
-      const unsigned m = __ballot_sync(kFull, (bits[w] >> b) & 1u);
-      if (lane == 0) s_wmask[warp][e] = m;
-    }
+    if ((unsigned)ex[j] < (unsigned)E) atomicOr(&s_wmask[warp][ex[j]], 1u << lane);
+    else if (ex[j] >= 0) report(p.status, kDevBounds, kSiteScatter, (unsigned)t, (unsigned)ex[j]);
   }
   __syncthreads();
   if (tid < E) {
     int run = 0;
+#pragma unroll
     for (int w = 0; w < 8; ++w) {
       s_wbase[w][tid] = run;
       run += __popc(s_wmask[w][tid]);
     }
   }
   __syncthreads();
-  if (valid) {
-    const unsigned lt = (1u << lane) - 1u;
+  const unsigned lt = (1u << lane) - 1u;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (j >= K) break;
-      const int e = ex[j];
-      if (e < 0) continue;
-      const int pos = s_base[e] + s_before[e] + s_wbase[warp][e] + __popc(s_wmask[warp][e] & lt);
-      p.perm[pos] = t * K + j;
-      p.tok_perm[pos] = t;
-      p.w_perm[pos] = p.w[(size_t)t * K + j];
-    }
+  for (int j = 0; j < 16; ++j) {
+    const int e = ex[j];
+    if ((unsigned)e >= (unsigned)E) continue;
+    const int pos = s_base[e] + s_wbase[warp][e] + __popc(s_wmask[warp][e] & lt);
+    p.perm[pos] = t * K + j;
+    p.tok_perm[pos] = t;
+    p.w_perm[pos] = p.w[(size_t)t * K + j];
   }
 }
 
+// Warp per grouped row; loads of four vectors per round.
 __global__ void __launch_bounds__(256) k_gather_xe(const GatherParams p) {
   const int lane = threadIdx.x & 31;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -536,47 +699,65 @@ __global__ void __launch_bounds__(256) k_gather_xe(const GatherParams p) {
     const float r = p.r[t];
     const uint4* hrow = reinterpret_cast<const uint4*>(p.h + (size_t)t * p.H);
     uint4* orow = reinterpret_cast<uint4*>(p.xe_perm + (size_t)row * p.H);
-    for (int v = lane; v < nvec; v += 32) {
-      float f[8], w[8];
-      unpack8(__ldg(hrow + v), f);
-      unpack8(__ldg(wv + v), w);
-      uint4 o;
-      o.x = pack2_bf16(f[0] * r * w[0], f[1] * r * w[1]);
-      o.y = pack2_bf16(f[2] * r * w[2], f[3] * r * w[3]);
-      o.z = pack2_bf16(f[4] * r * w[4], f[5] * r * w[5]);
-      o.w = pack2_bf16(f[6] * r * w[6], f[7] * r * w[7]);
-      orow[v] = o;
+    for (int v0 = lane; v0 < nvec; v0 += 128) {
+      uint4 rh[4], rw[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = v0 + 32 * u;
+        if (v < nvec) {
+          rh[u] = __ldg(hrow + v);
+          rw[u] = __ldg(wv + v);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = v0 + 32 * u;
+        if (v >= nvec) break;
+        float f[8], w[8];
+        unpack8(rh[u], f);
+        unpack8(rw[u], w);
+        uint4 o;
+        o.x = pack2_bf16(f[0] * r * w[0], f[1] * r * w[1]);
+        o.y = pack2_bf16(f[2] * r * w[2], f[3] * r * w[3]);
+        o.z = pack2_bf16(f[4] * r * w[4], f[5] * r * w[5]);
+        o.w = pack2_bf16(f[6] * r * w[6], f[7] * r * w[7]);
+        orow[v] = o;
+      }
     }
   }
 }
 
 template <int TB>
 size_t router_smem(int H) {
-  return sizeof(float) * (size_t)TB * kLogitSlices * (H / kLogitSlices + 4);
+  return sizeof(float) * (size_t)TB * kLogitSlices * (H / kLogitSlices + 4) +
+         (size_t)(TB + 2) * H * 2;
 }
 
-template <int TB>
+template <int TB, bool U8>
 cudaError_t launch_router_tb(const RouterParams& p, cudaStream_t s) {
   const size_t smem = router_smem<TB>(p.H);
-  cudaError_t err = cudaFuncSetAttribute(k_router_logits<TB>,
+  cudaError_t err = cudaFuncSetAttribute(k_router_logits<TB, U8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const dim3 grid((p.T + TB - 1) / TB, (p.E + kLogitExperts - 1) / kLogitExperts);
-  k_router_logits<TB><<<grid, 256, smem, s>>>(p);
+  k_router_logits<TB, U8><<<grid, 256, smem, s>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s) {
-  // eight tokens per block amortise the router-weight reads; four when the
-  // staged router input of eight would not fit
-  if (router_smem<8>(p.H) <= 160 * 1024) return launch_router_tb<8>(p, s);
-  return launch_router_tb<4>(p, s);
+  // four tokens per block give a single canvas enough blocks; eight halve
+  // the router-weight reads of large batches (when the staged input fits)
+  const bool big = p.T > 2048 && router_smem<8>(p.H) <= 160 * 1024;
+  if (p.router_u8) return big ? launch_router_tb<8, true>(p, s) : launch_router_tb<4, true>(p, s);
+  return big ? launch_router_tb<8, false>(p, s) : launch_router_tb<4, false>(p, s);
 }
 
 cudaError_t launch_router_select(const RouterParams& p, cudaStream_t s) {
-  k_router_select<<<(p.T + 7) / 8, 256, 0, s>>>(p);
+  const int grid = (p.T + kSelTokens - 1) / kSelTokens;
+  if (p.router_u8) k_router_select<true><<<grid, 256, 0, s>>>(p);
+  else k_router_select<false><<<grid, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 
