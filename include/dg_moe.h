@@ -199,6 +199,29 @@ dg_status_t dg_moe_set_profile_events(dg_moe_t* m, dg_event_t* events, int n_eve
  * error), "" if none.  Owned by the handle; valid until the next call. */
 const char* dg_moe_last_error(const dg_moe_t* m);
 
+/* Routing only, for callers that may not allocate device memory.  The
+ * pages have no counterpart: this is a library convenience.  Some callers
+ * cannot call cudaMalloc (an allocator hook or arena that owns all device
+ * memory, a host framework that forbids allocation on its hot path); this
+ * entry point needs no handle and no workspace.  It runs the same routing
+ * kernels as dg_moe_forward on h_in (bf16 [n_tokens, H]) with the router
+ * weights of `weights` (router, router_scale, per_expert_scale, w_pre_ff,
+ * router_bias; cfg gives H, E, K, router_fmt and rms_eps) and writes
+ * idx_out (int32 [n_tokens, K], ascending experts per token) and w_out
+ * (f32 [n_tokens, K]), asynchronously on `stream`.
+ * Scratch: a fixed 8 MiB array in the library's device memory, held on
+ * every GPU that loads the library until the process exits.  It needs
+ * about n_tokens * (6 H + 4 E + 8) bytes; larger calls return
+ * DG_ERR_UNSUPPORTED (a 256-token canvas at H 2816 needs 4.5 MB).  The first
+ * call on a device looks up the array's device address (a CUDA runtime
+ * query, no allocation), so make that first call before any stream
+ * capture.  Every call on a device shares the one array: calls that can
+ * overlap on the GPU (different streams without ordering) race.  Allocates
+ * nothing. */
+dg_status_t dg_moe_route_noalloc(const dg_moe_config_t* cfg, const dg_moe_weights_t* weights,
+                                 const void* h_in, int n_tokens, int32_t* idx_out, float* w_out,
+                                 dg_stream_t stream);
+
 /* Static string for a status code. */
 const char* dg_moe_status_string(dg_status_t s);
 

@@ -31,6 +31,7 @@ EXPORTED = (
     "dg_moe_workspace_size", "dg_moe_create", "dg_moe_forward", "dg_moe_forward_host",
     "dg_moe_destroy", "dg_moe_last_device_status", "dg_moe_kernel_names",
     "dg_moe_set_profile_events", "dg_moe_status_string", "dg_moe_last_error",
+    "dg_moe_route_noalloc",
 )
 
 
@@ -90,6 +91,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dg_moe_last_device_status.argtypes = [c_void_p, c_void_p, POINTER(c_uint), POINTER(c_uint)]
     lib.dg_moe_kernel_names.argtypes = [c_void_p, POINTER(c_char_p), POINTER(c_int)]
     lib.dg_moe_set_profile_events.argtypes = [c_void_p, POINTER(c_void_p), c_int]
+    lib.dg_moe_route_noalloc.argtypes = [POINTER(dg_moe_config_t), POINTER(dg_moe_weights_t),
+                                         c_void_p, c_int, c_void_p, c_void_p, c_void_p]
     lib.dg_moe_status_string.argtypes = [c_int]
     lib.dg_moe_status_string.restype = c_char_p
     lib.dg_moe_last_error.argtypes = [c_void_p]
@@ -185,3 +188,13 @@ def dg_moe_set_profile_events(handle: int, events) -> None:
 
 
 _EVENT_ARRAYS: dict = {}
+
+
+def dg_moe_route_noalloc(cfg: dg_moe_config_t, weights: dg_moe_weights_t, h_in: int,
+                         n_tokens: int, idx_out: int, w_out: int, stream: int) -> None:
+    """Routing only, with the library's fixed device scratch (no allocation);
+    see include/dg_moe.h."""
+    _check(load_library().dg_moe_route_noalloc(ctypes.byref(cfg), ctypes.byref(weights),
+                                               c_void_p(h_in), n_tokens, c_void_p(idx_out),
+                                               c_void_p(w_out), c_void_p(stream)),
+           "dg_moe_route_noalloc")
