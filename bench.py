@@ -51,6 +51,21 @@ def peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
+def gate_up_traffic():
+    """DRAM bytes per gate_up launch from the committed ncu capture, while the
+    GEMM sources are the ones it was taken on (None otherwise)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "gemm_gate_up_canvas256.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    csrc = os.path.join(ROOT, "moe_expert_ffn_dg_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("dg_gemm.cu", "dg_common.cuh", "dg_kernels.h"):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return rec["dram_bytes_per_launch"] if h.hexdigest()[:16] == rec["gemm_source_sha256_16"] else None
+
+
 def algorithmic(wl, counts):
     """Algorithmic bytes and FLOPs of one layer forward and of its gate_up
     GEMM: weights of the experts that received tokens, dense and router
@@ -284,7 +299,7 @@ def run_ours(args):
                    "l2": "no flush: 1.56 GB of weights per step, 12x the 129 MB L2",
                    "touched_experts": alg["touched_experts"]},
         "roofline": {"bound": "hbm", "kernel": "gemm_gate_up", "achieved": achieved, "peak": hbm,
-                     "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": gate_up_traffic(),
                      "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else src,
                      "algorithmic_bytes_per_launch": alg["gate_up_bytes"],
                      "us_per_launch": per_kernel_us[gu]},
