@@ -8,6 +8,7 @@ that canvas with inputs resident in HBM.  The 1.56 GB of weights read per
 step are 12x the L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload canvas256|canvas256_q4|batch2048_zipf]
 
 Prints one JSON line.  ``--impl reference`` times the CPU oracle (the only
 reference there is: the pages hold no runnable implementation) on the host
@@ -38,9 +39,22 @@ FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def workload_desc(wl):
-    return (f"{wl.name}: one DiffusionGemma MoE FFN layer, T={wl.tokens} tokens (one canvas), "
+    if wl.quant:
+        wdesc = (f"N(0,{wl.weight_std}) draws in group-64 affine {wl.quant[0]}-bit (experts), "
+                 f"{wl.quant[1]}-bit (dense), {wl.quant[2]}-bit (router)")
+    else:
+        wdesc = f"bf16 weights N(0,{wl.weight_std})"
+    extra = f", Zipf router bias beta {wl.zipf_beta}" if wl.zipf_beta else ""
+    return (f"{wl.name}: one DiffusionGemma MoE FFN layer, T={wl.tokens} tokens "
+            f"({wl.tokens // 256} canvas{'es' if wl.tokens > 256 else ''}), "
             f"H={wl.hidden}, E={wl.n_experts} top-{wl.top_k}, expert FFN {wl.expert_inter}, "
-            f"dense FFN {wl.dense_inter}, bf16 weights N(0,{wl.weight_std}), seed {wl.seed}")
+            f"dense FFN {wl.dense_inter}, {wdesc}{extra}, seed {wl.seed}")
+
+
+def weight_bytes(n, bits):
+    """Bytes of n weights: bf16, or group-64 affine codes plus a bf16 scale
+    and bias per 64 weights."""
+    return 2 * n if bits is None else n * bits // 8 + n // 64 * 4
 
 
 def peaks():
@@ -66,16 +80,21 @@ def gate_up_traffic():
     return rec["dram_bytes_per_launch"] if h.hexdigest()[:16] == rec["gemm_source_sha256_16"] else None
 
 
+def traffic_for(wl):
+    return gate_up_traffic() if wl.name == WORKLOAD else None
+
+
 def algorithmic(wl, counts):
     """Algorithmic bytes and FLOPs of one layer forward and of its gate_up
     GEMM: weights of the experts that received tokens, dense and router
     weights, the activation read and the output write; intermediates that
     an ideal kernel keeps on chip are not counted.  FLOPs exclude padding."""
     T, H, E, K, I, D = wl.tokens, wl.hidden, wl.n_experts, wl.top_k, wl.expert_inter, wl.dense_inter
+    eb, db, rb = wl.quant if wl.quant else (None, None, None)
     touched = int((np.asarray(counts) > 0).sum())
-    gu_w = touched * 2 * I * H * 2 + 2 * D * H * 2
-    dn_w = touched * H * I * 2 + H * D * 2
-    router_w = E * H * 2
+    gu_w = touched * weight_bytes(2 * I * H, eb) + weight_bytes(2 * D * H, db)
+    dn_w = touched * weight_bytes(H * I, eb) + weight_bytes(H * D, db)
+    router_w = weight_bytes(E * H, rb)
     layer_bytes = gu_w + dn_w + router_w + 2 * T * H * 2 + 4 * H * 2 + E * 2
     layer_flops = 2 * T * H * E + 2 * T * K * 3 * H * I + 2 * T * 3 * H * D
     gu_bytes = gu_w + T * K * H * 2 + T * H * 2 + T * K * I * 2 + T * D * 2
@@ -154,7 +173,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    wl = mi.get_workload(WORKLOAD)
+    wl = mi.get_workload(args.workload)
     p = mi.make_layer_inputs(wl)
     h = mi.make_tokens(wl)
     # decode the weights to float64 once, outside the timed steps; the
@@ -206,10 +225,10 @@ def run_ours(args):
     pkg.build()
     pkg.load_library()
 
-    wl = mi.get_workload(WORKLOAD)
+    wl = mi.get_workload(args.workload)
     p = mi.make_layer_inputs(wl)
     # each replica processes its own canvas (data parallel over canvases)
-    h_np = mi.make_tokens(mi.get_workload(WORKLOAD, seed=wl.seed + 1000 * rank)) if rank else mi.make_tokens(wl)
+    h_np = mi.make_tokens(mi.get_workload(args.workload, seed=wl.seed + 1000 * rank)) if rank else mi.make_tokens(wl)
     blk = pkg.MoEBlock.from_params(p, hidden=wl.hidden, n_experts=wl.n_experts, top_k=wl.top_k,
                                    expert_inter=wl.expert_inter, dense_inter=wl.dense_inter,
                                    max_tokens=wl.tokens, device=dev)
@@ -296,10 +315,12 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(wl), "tokens_per_step": wl.tokens,
                    "us_per_layer": ms * 1000.0, "parallelism": f"replicas x{world}",
-                   "l2": "no flush: 1.56 GB of weights per step, 12x the 129 MB L2",
+                   "weights": "bf16" if not wl.quant else f"u{wl.quant[0]} g64 affine experts and dense, u{wl.quant[2]} router, dequantised to bf16 on chip",
+                   "l2": f"no flush: {alg['layer_bytes'] / 1e9:.3f} GB of weights per step, "
+                         f"{alg['layer_bytes'] / 129e6:.1f}x the 129 MB L2",
                    "touched_experts": alg["touched_experts"]},
         "roofline": {"bound": "hbm", "kernel": "gemm_gate_up", "achieved": achieved, "peak": hbm,
-                     "unit": "GB/s", "frac": achieved / hbm, "traffic": gate_up_traffic(),
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic_for(wl),
                      "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else src,
                      "algorithmic_bytes_per_launch": alg["gate_up_bytes"],
                      "us_per_launch": per_kernel_us[gu]},
@@ -330,6 +351,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=["canvas256", "canvas256_q4", "batch2048_zipf"])
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

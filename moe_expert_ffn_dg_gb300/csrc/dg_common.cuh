@@ -27,6 +27,7 @@ enum : unsigned int { kDevOk = 0, kDevTimeout = 1, kDevBounds = 2 };
 enum : unsigned int {
   kSiteGemmProducer = 1, kSiteGemmMma = 2, kSiteGemmEpilogue = 3,
   kSiteGemmDrain = 4, kSiteScatter = 5, kSiteGather = 6,
+  kSiteGemmDequant = 7, kSiteGemmTokens = 8,
 };
 
 __device__ __forceinline__ void report(DevStatus* st, unsigned code, unsigned where,

@@ -27,40 +27,15 @@
 // Every wait is bounded; a wait that runs out records itself in the status
 // word and the CTA winds down (its TMA copies and MMAs are drained before
 // TMEM is released).
-#include "dg_kernels.h"
+#include "dg_gemm_common.cuh"
 
 namespace dg {
 namespace {
 
+using namespace gemm;
+
 constexpr int kThreads = 192;
 constexpr int kATileBytes = 128 * 128;  // 128 rows x 64 bf16
-constexpr int kBoxRows = 16;            // rows per TMA box (all maps)
-constexpr int kBoxBytes = kBoxRows * 128;
-
-constexpr int kMaxGroups = 256;
-constexpr int kTileTableBytes = 2 * (kMaxGroups + 2) * 4;
-
-// Tile t of the persistent schedule: dense tiles first, then the expert tiles
-// (feature tile fastest).  s_start[e] = first expert tile of expert e
-// (exclusive prefix of ceil(n_e / bn) * mt_exp), s_off = expert offsets.
-__device__ __forceinline__ int4 decode_tile(const GemmParams& p, int t, int nd,
-                                            const int* s_start, const int* s_off) {
-  if (t < nd) {
-    const int j = t / p.mt_dense, m = t - j * p.mt_dense;
-    return make_int4(p.E, m, j * p.bn, min(p.bn, p.T - j * p.bn));
-  }
-  const int u = t - nd;
-  int lo = 0, hi = p.E - 1;  // last e with s_start[e] <= u
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_start[mid] <= u) lo = mid;
-    else hi = mid - 1;
-  }
-  const int e = lo, local = u - s_start[e];
-  const int j = local / p.mt_exp, m = local - j * p.mt_exp;
-  const int n = s_off[e + 1] - s_off[e];
-  return make_int4(e, m, s_off[e] + j * p.bn, min(p.bn, n - j * p.bn));
-}
 
 template <int BN>
 struct Cfg {
@@ -70,41 +45,6 @@ struct Cfg {
   static constexpr size_t kSmem =
       1024 + (size_t)kStages * (kATileBytes + kBTileBytes) + 256 + kTileTableBytes;
 };
-
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
-__device__ __forceinline__ void tma_load_4d(const CUtensorMap* map, uint64_t* bar, void* dst,
-                                            int c0, int c1, int c2, int c3, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
-      "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_5d(const CUtensorMap* map, uint64_t* bar, void* dst,
-                                            int c0, int c1, int c2, int c3, int c4,
-                                            uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
-      "r"(c4), "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ bool wait_no_abort(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  while (true) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
 
 template <int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_constant__ GemmParams p) {
@@ -155,31 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
     tmem_alloc(tmem_holder, C::kTmemCols);
     tmem_relinquish();
   }
-  if (warp >= 2) {
-    // tile table: per-expert tile counts and their exclusive prefix (one warp)
-    const int tid = threadIdx.x - 64;
-    for (int e = tid; e <= p.E; e += 128) s_off[e] = p.offsets[e];
-    if (warp == 2) {
-      int run = 0;
-      for (int base = 0; base < p.E; base += 32) {
-        const int e = base + lane;
-        int c = 0;
-        if (e < p.E) {
-          const int n = p.offsets[e + 1] - p.offsets[e];
-          c = (n + p.bn - 1) / p.bn * p.mt_exp;
-        }
-        int incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += v;
-        }
-        if (e < p.E) s_start[e] = run + incl - c;
-        run += __shfl_sync(0xffffffffu, incl, 31);
-      }
-      if (lane == 0) s_start[p.E] = run;
-    }
-  }
+  if (warp >= 2) build_tile_table(p, threadIdx.x - 64, s_start, s_off);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -312,7 +228,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
     int local = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
       const int4 td = decode_tile(p, tile, nd, s_start, s_off);
-      const bool dense = td.x == p.E;
       const int nb = (td.w + kBoxRows - 1) / kBoxRows;
       const int acc = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
@@ -323,51 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
-      const int ncols = nb * kBoxRows;
-      for (int c0 = 0; c0 < ncols; c0 += 16) {
-        __syncwarp();
-        float v[16];
-        tmem_ld16(tbase + (uint32_t)c0, v);
-        if (MODE == 0) {
-          const int ld = dense ? p.D : p.I;
-          uint16_t* out = dense ? p.act_d : p.act;
-          const int feat = td.y * 64 + 16 * q + (lane & 15);
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const int j = 2 * jj;
-            const float send = lane < 16 ? v[j + 1] : v[j];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-            const float g = lane < 16 ? v[j] : recv;
-            const float u = lane < 16 ? recv : v[j + 1];
-            const int col = c0 + j + (lane >> 4);
-            if (col < td.w) {
-              const size_t row = (size_t)(td.z + col);
-              out[row * ld + feat] = f32_to_bf16_rne(gelu_tanh(g) * u);
-            }
-          }
-        } else {
-          const int feat = td.y * 128 + 32 * q + lane;
-          int tok = 0;
-          float wt = 0.f;
-          if (!dense && lane < 16 && c0 + lane < td.w) {
-            tok = p.tok_perm[td.z + c0 + lane];
-            wt = p.w_perm[td.z + c0 + lane];
-          }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = c0 + j;
-            const int tj = __shfl_sync(0xffffffffu, tok, j);
-            const float wj = __shfl_sync(0xffffffffu, wt, j);
-            if (col < td.w) {
-              if (dense) {
-                p.y_dense[(size_t)(td.z + col) * p.H + feat] = v[j];
-              } else {
-                atomicAdd(&p.y_moe[(size_t)tj * p.H + feat], wj * v[j]);
-              }
-            }
-          }
-        }
-      }
+      epilogue_tile<MODE>(p, td, tbase, nb * kBoxRows, q, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);

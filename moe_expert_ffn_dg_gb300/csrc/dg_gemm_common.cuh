@@ -1,0 +1,164 @@
+// Pieces shared by the grouped GEMM kernels (bf16 weights through shared
+// memory, 4-bit weights dequantised into TMEM): the persistent tile schedule,
+// TMA loads of rank 4 and 5, the drain wait and the per-mode epilogue.
+#pragma once
+
+#include "dg_kernels.h"
+
+namespace dg {
+namespace gemm {
+
+constexpr int kBoxRows = 16;  // token rows per small TMA box
+constexpr int kBoxBytes = kBoxRows * 128;
+constexpr int kMaxGroups = 256;
+constexpr int kTileTableBytes = 2 * (kMaxGroups + 2) * 4;
+
+// Tile t of the persistent schedule: dense tiles first, then the expert tiles
+// (feature tile fastest).  s_start[e] = first expert tile of expert e
+// (exclusive prefix of ceil(n_e / bn) * mt_exp), s_off = expert offsets.
+// Returns {group, feature tile, first row, rows}; group == E is the dense
+// branch.
+__device__ __forceinline__ int4 decode_tile(const GemmParams& p, int t, int nd,
+                                            const int* s_start, const int* s_off) {
+  if (t < nd) {
+    const int j = t / p.mt_dense, m = t - j * p.mt_dense;
+    return make_int4(p.E, m, j * p.bn, min(p.bn, p.T - j * p.bn));
+  }
+  const int u = t - nd;
+  int lo = 0, hi = p.E - 1;  // last e with s_start[e] <= u
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_start[mid] <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  const int e = lo, local = u - s_start[e];
+  const int j = local / p.mt_exp, m = local - j * p.mt_exp;
+  const int n = s_off[e + 1] - s_off[e];
+  return make_int4(e, m, s_off[e] + j * p.bn, min(p.bn, n - j * p.bn));
+}
+
+// Fill the tile table from the expert offsets: s_off = offsets, s_start =
+// exclusive prefix of the per-expert tile counts.  Called by 4 consecutive
+// warps (tid 0..127); the prefix is taken by the first of them.
+__device__ __forceinline__ void build_tile_table(const GemmParams& p, int tid, int* s_start,
+                                                 int* s_off) {
+  const int lane = tid & 31;
+  for (int e = tid; e <= p.E; e += 128) s_off[e] = p.offsets[e];
+  if (tid < 32) {
+    int run = 0;
+    for (int base = 0; base < p.E; base += 32) {
+      const int e = base + lane;
+      int c = 0;
+      if (e < p.E) {
+        const int n = p.offsets[e + 1] - p.offsets[e];
+        c = (n + p.bn - 1) / p.bn * p.mt_exp;
+      }
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (e < p.E) s_start[e] = run + incl - c;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) s_start[p.E] = run;
+  }
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void tma_load_4d(const CUtensorMap* map, uint64_t* bar, void* dst,
+                                            int c0, int c1, int c2, int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(const CUtensorMap* map, uint64_t* bar, void* dst,
+                                            int c0, int c1, int c2, int c3, int c4,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(c4), "l"(policy)
+      : "memory");
+}
+
+// Wait that ignores the abort flag (used to drain in-flight copies and MMAs
+// before the CTA exits); bounded by kWaitLimitNs.
+__device__ __forceinline__ bool wait_no_abort(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// Epilogue of one tile from TMEM: warp quarter q reads its 32 lanes (the
+// tile's 128 weight rows are the lanes), ncols token columns.
+// MODE 0 (gate_up): lanes 32q..32q+15 hold gate and 32q+16..32q+31 up of the
+// same 16 features; pair them with one shuffle and write
+// act = bf16(gelu_tanh(gate) * up).
+// MODE 1 (down): 128 output channels; experts add w * y into the f32
+// per-token accumulator, the dense branch stores its f32 output.
+template <int MODE>
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, int4 td, uint32_t tbase,
+                                              int ncols, int q, int lane) {
+  const bool dense = td.x == p.E;
+  for (int c0 = 0; c0 < ncols; c0 += 16) {
+    __syncwarp();
+    float v[16];
+    tmem_ld16(tbase + (uint32_t)c0, v);
+    if (MODE == 0) {
+      const int ld = dense ? p.D : p.I;
+      uint16_t* out = dense ? p.act_d : p.act;
+      const int feat = td.y * 64 + 16 * q + (lane & 15);
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int j = 2 * jj;
+        const float send = lane < 16 ? v[j + 1] : v[j];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+        const float g = lane < 16 ? v[j] : recv;
+        const float u = lane < 16 ? recv : v[j + 1];
+        const int col = c0 + j + (lane >> 4);
+        if (col < td.w) {
+          const size_t row = (size_t)(td.z + col);
+          out[row * ld + feat] = f32_to_bf16_rne(gelu_tanh(g) * u);
+        }
+      }
+    } else {
+      const int feat = td.y * 128 + 32 * q + lane;
+      int tok = 0;
+      float wt = 0.f;
+      if (!dense && lane < 16 && c0 + lane < td.w) {
+        tok = p.tok_perm[td.z + c0 + lane];
+        wt = p.w_perm[td.z + c0 + lane];
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int col = c0 + j;
+        const int tj = __shfl_sync(0xffffffffu, tok, j);
+        const float wj = __shfl_sync(0xffffffffu, wt, j);
+        if (col < td.w) {
+          if (dense) {
+            p.y_dense[(size_t)(td.z + col) * p.H + feat] = v[j];
+          } else {
+            atomicAdd(&p.y_moe[(size_t)tj * p.H + feat], wj * v[j]);
+          }
+        }
+      }
+    }
+  }
+}
+
+}  // namespace gemm
+}  // namespace dg

@@ -1,0 +1,601 @@
+// Grouped tcgen05 GEMMs over 4-bit group-64 affine weights (sm_103a).
+//
+// The weight format is the one of "DiffusionGemma port — plan & parity
+// strategy", Reference dossier §1 (OptiQ affine quantisation, group size 64,
+// 4-bit experts): per row, code words of 8 four-bit codes (code k of a word at
+// bits 4k), and per group of 64 codes a bf16 scale s and bias b; the weight is
+// s * q + b.  "diffgemma — architecture & implemented contract" (Part IV,
+// measurements) names the dequantisation as the cost that dominates 4-bit
+// expert layers; here it runs beside the tensor core instead of in front of it.
+//
+// Dataflow of one tile (128 weight rows x up to BN token rows):
+//   warp 0   TMA: code slabs (128 rows x 256 codes = 16 KB, 128B swizzle) into
+//            a ring, and per tile the rows' scales and biases (bulk copies);
+//   warp 1   TMA: token sub-blocks (BN rows x 64 bf16) into a second ring;
+//   warp 2   TMEM owner and MMA issuer: tcgen05.mma with A read from TMEM
+//            (the dequantised weights) and B from shared memory (tokens),
+//            one slab (16 MMAs of K = 16) per round;
+//   warp 3   waits, for the issuer, until a slab's operands are ready and
+//            hands it over through a named barrier (see below);
+//   warps 4-11  dequantise: each thread expands one weight row of a slab to
+//            bf16 (exact s * q + b, one rounding) and stores it into TMEM with
+//            tcgen05.st, two warps per 32-lane quarter;
+//   warps 12-15 epilogue, as for bf16 weights (GEGLU or weighted combine).
+// The bf16 weights never pass through shared memory: shared-memory traffic
+// per weight is the half byte of its code plus its share of the token tile.
+//
+// TMEM columns: two fp32 accumulators of BN columns, then NA slots of 128
+// columns, each holding one dequantised slab (128 lanes x 256 bf16, two codes
+// per 32-bit column, K-major: the layout the MMA reads A from TMEM).
+//
+// Why the issuer does not wait on mbarriers itself: on sm_103a, a shared-
+// memory access (an mbarrier poll or a plain load) by a thread that has
+// tcgen05.mma in flight stalls until those MMAs complete, so one poll per
+// slab costs the MMA pipeline latency (measured ~700 cycles against ~55
+// cycles per M=128, K=16 MMA).  Another warp's polls are not affected, and a
+// named CTA barrier is not a memory access.  So warp 3 does the bounded
+// mbarrier waits and meets the issuer at a barrier.red.or once per slab; the
+// reduced predicate carries "stop" (a wait that ran out), so both warps leave
+// on the same round and the barrier can never be left half-arrived.
+//
+// Every wait is bounded; a wait that runs out records itself in the status
+// word and the CTA winds down (copies, stores and MMAs in flight are drained
+// before TMEM is released).
+#include "dg_gemm_common.cuh"
+
+namespace dg {
+namespace {
+
+using namespace gemm;
+
+constexpr int kThreadsQ = 512;
+constexpr int kSlabK = 256;                  // codes per row of a slab
+constexpr int kQSlabBytes = 128 * kSlabK / 2;  // 16 KB
+constexpr int kDequantWarp0 = 4;
+constexpr int kNumDequantWarps = 8;
+constexpr int kEpilogueWarp0 = 12;
+
+template <int BN>
+struct CfgQ {
+  static constexpr int kSQ = BN == 64 ? 6 : 5;  // code slabs in flight
+  static constexpr int kSB = BN == 64 ? 6 : 4;  // token sub-blocks in flight
+  static constexpr int kBBytes = BN * 128;
+  static constexpr int kNA = (512 - 2 * BN) / 128;  // dequantised slabs in TMEM
+  static constexpr int kBarBytes = 512;
+  static constexpr size_t kFixed = 1024 + (size_t)kSQ * kQSlabBytes + (size_t)kSB * kBBytes +
+                                   kBarBytes + kTileTableBytes;
+};
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs, fp32 accumulate, one CTA.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Store 32 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+// Named barrier 1 between the MMA issuer warp and its waiter warp (64
+// threads, both block), OR-reducing one predicate: returns true if either
+// side passed true.
+constexpr int kHandoffBarrier = 1;
+__device__ __forceinline__ bool handoff(bool stop) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "barrier.cta.red.or.pred p, %2, 64, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)stop), "n"(kHandoffBarrier)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void lds_u32x4(const uint8_t* p, uint32_t (&w)[4]) {
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+               : "r"(smem_u32(p))
+               : "memory");
+}
+
+__device__ __forceinline__ __nv_bfloat162 as_bf162(uint32_t u) {
+  __nv_bfloat162 r;
+  memcpy(&r, &u, 4);
+  return r;
+}
+__device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 v) {
+  uint32_t r;
+  memcpy(&r, &v, 4);
+  return r;
+}
+
+// 32 codes (four words) -> 16 bf16 pairs in K order, w = s * q + b rounded
+// once to bf16.  A code q sits in the low mantissa bits of the bf16 128 + q
+// (0x4300 | q, exact); subtracting 128 leaves q exactly, then one fused
+// multiply-add applies the group's scale and bias.
+__device__ __forceinline__ void dequant32(const uint32_t (&w)[4], uint32_t s2, uint32_t b2,
+                                          uint32_t (&o)[16]) {
+  const __nv_bfloat162 s = as_bf162(s2), b = as_bf162(b2), m = as_bf162(0x43004300u);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t u = w[j] >> 4;
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) {
+      // bytes: [w.byte pp, -, u.byte pp, -] -> codes 2pp (low) and 2pp+1 (high)
+      uint32_t t = __byte_perm(w[j], u, 0x4400u + 0x1111u * pp);
+      t = (t & 0x000F000Fu) | 0x43004300u;
+      const __nv_bfloat162 qv = __hsub2(as_bf162(t), m);
+      o[4 * j + pp] = as_u32(__hfma2(qv, s, b));
+    }
+  }
+}
+
+template <int MODE, int BN>
+__global__ void __launch_bounds__(kThreadsQ, 1)
+    k_grouped_gemm_q4(const __grid_constant__ GemmParams p) {
+  using C = CfgQ<BN>;
+  constexpr int SQ = C::kSQ, SB = C::kSB, NA = C::kNA;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sQ = smem;
+  uint8_t* sB = sQ + (size_t)SQ * kQSlabBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (size_t)SB * C::kBBytes);
+  uint64_t* qfull = bars;
+  uint64_t* qempty = qfull + SQ;
+  uint64_t* bfull = qempty + SQ;
+  uint64_t* bempty = bfull + SB;
+  uint64_t* afull = bempty + SB;
+  uint64_t* aempty = afull + NA;
+  uint64_t* sfull = aempty + NA;
+  uint64_t* sempty = sfull + 2;
+  uint64_t* acc_full = sempty + 2;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* s_start = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + C::kBarBytes);
+  int* s_off = s_start + kMaxGroups + 2;
+  uint8_t* sScale = reinterpret_cast<uint8_t*>(bars) + C::kBarBytes + kTileTableBytes;
+  const int slot_bytes = p.sc_slot_bytes;  // scales of one tile; biases follow
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SQ; ++s) {
+      mbar_init(&qfull[s], 1);
+      mbar_init(&qempty[s], kNumDequantWarps);
+    }
+    for (int s = 0; s < SB; ++s) {
+      mbar_init(&bfull[s], 1);
+      mbar_init(&bempty[s], 1);
+    }
+    for (int a = 0; a < NA; ++a) {
+      mbar_init(&afull[a], kNumDequantWarps);
+      mbar_init(&aempty[a], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&sfull[a], 1);
+      mbar_init(&sempty[a], kNumDequantWarps);
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&p.wa_exp);
+    tma_prefetch_map(&p.wa_d0);
+    if (MODE == 0) {
+      tma_prefetch_map(&p.wa_d1);
+      tma_prefetch_map(&p.wa_d5);
+    }
+  }
+  if (warp == 1 && lane == 0) {
+    tma_prefetch_map(&p.xb_exp64);
+    tma_prefetch_map(&p.xb_exp16);
+    tma_prefetch_map(&p.xb_d64);
+    tma_prefetch_map(&p.xb_d16);
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  if (warp >= kEpilogueWarp0) build_tile_table(p, threadIdx.x - 32 * kEpilogueWarp0, s_start, s_off);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const uint32_t a_col0 = 2 * BN;  // first TMEM column of the dequantised slabs
+  const int nd = (p.T + p.bn - 1) / p.bn * p.mt_dense;
+  const int ntiles = nd + s_start[p.E];
+
+  if (warp == 0) {
+    // ------------------------------------------------- weight codes + scales
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();
+      int qs = 0;
+      uint32_t qph = 0, qarmed = 0, qarmed_par = 0, sarmed = 0, sarmed_par = 0;
+      bool ok = true;
+      int local = 0;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++local) {
+        const int4 td = decode_tile(p, tile, nd, s_start, s_off);
+        const bool dense = td.x == p.E;
+        const int ng = dense ? p.kb_dense : p.kb_exp;  // groups of 64 per row
+        const uint32_t rowb = 2u * (uint32_t)ng;        // scale bytes per row
+        const int ss = local & 1;
+        const uint32_t sph = (uint32_t)(local >> 1) & 1u;
+        if (!mbar_wait(&sempty[ss], sph ^ 1u, abort_flag)) {
+          report(p.status, kDevTimeout, kSiteGemmProducer, (unsigned)tile, 0xfffffffeu);
+          *abort_flag = 1;
+          break;
+        }
+        uint8_t* dsc = sScale + (size_t)ss * 2 * slot_bytes;
+        uint8_t* dbi = dsc + slot_bytes;
+        mbar_arrive_expect_tx(&sfull[ss], 2u * 128u * rowb);
+        if (MODE == 0) {
+          // 16-row blocks in the order of the interleaved slab: block 2c+h
+          // holds gate (h = 0) or up (h = 1) rows 16c..16c+15 of the tile
+#pragma unroll 1
+          for (int blk = 0; blk < 8; ++blk) {
+            const int c4 = blk >> 1, h = blk & 1;
+            size_t src_row;
+            const uint16_t *sc, *bi;
+            if (dense) {
+              src_row = (size_t)(64 * td.y + 16 * c4);
+              sc = h ? p.sc_d1 : p.sc_d0;
+              bi = h ? p.bi_d1 : p.bi_d0;
+            } else {
+              src_row = (size_t)td.x * 2 * p.I + (size_t)h * p.I + 64 * td.y + 16 * c4;
+              sc = p.sc_exp;
+              bi = p.bi_exp;
+            }
+            bulk_g2s(dsc + (size_t)16 * blk * rowb, sc + src_row * ng, 16 * rowb, &sfull[ss], pol_w);
+            bulk_g2s(dbi + (size_t)16 * blk * rowb, bi + src_row * ng, 16 * rowb, &sfull[ss], pol_w);
+          }
+        } else {
+          const size_t src_row = (dense ? (size_t)0 : (size_t)td.x * p.H) + 128 * (size_t)td.y;
+          const uint16_t* sc = dense ? p.sc_d0 : p.sc_exp;
+          const uint16_t* bi = dense ? p.bi_d0 : p.bi_exp;
+          bulk_g2s(dsc, sc + src_row * ng, 128 * rowb, &sfull[ss], pol_w);
+          bulk_g2s(dbi, bi + src_row * ng, 128 * rowb, &sfull[ss], pol_w);
+        }
+        sarmed |= 1u << ss;
+        sarmed_par = (sarmed_par & ~(1u << ss)) | (sph << ss);
+
+        const int nsl = (ng + 3) / 4;
+        for (int sl = 0; sl < nsl; ++sl) {
+          if (!mbar_wait(&qempty[qs], qph ^ 1u, abort_flag)) {
+            report(p.status, kDevTimeout, kSiteGemmProducer, (unsigned)tile, (unsigned)sl);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&qfull[qs], kQSlabBytes);
+          uint8_t* dst = sQ + (size_t)qs * kQSlabBytes;
+          const int x = sl * (kSlabK / 8);  // u32 words
+          if (MODE == 0) {
+            if (!dense) {
+              tma_load_5d(&p.wa_exp, &qfull[qs], dst, x, 0, 0, 4 * td.y, td.x, pol_w);
+            } else if (p.dense_5d) {
+              tma_load_4d(&p.wa_d5, &qfull[qs], dst, x, 0, 0, 4 * td.y, pol_w);
+            } else {
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const int yg = td.y * 64 + 16 * c;
+                tma_load_2d_hint(&p.wa_d0, &qfull[qs], dst + (2 * c) * kBoxBytes, x, yg, pol_w);
+                tma_load_2d_hint(&p.wa_d1, &qfull[qs], dst + (2 * c + 1) * kBoxBytes, x, yg, pol_w);
+              }
+            }
+          } else {
+            const CUtensorMap* ma = dense ? &p.wa_d0 : &p.wa_exp;
+            tma_load_2d_hint(ma, &qfull[qs], dst, x, (dense ? 0 : td.x * p.H) + td.y * 128, pol_w);
+          }
+          qarmed |= 1u << qs;
+          qarmed_par = (qarmed_par & ~(1u << qs)) | (qph << qs);
+          if (++qs == SQ) {
+            qs = 0;
+            qph ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < SQ; ++s)
+        if ((qarmed >> s) & 1u)
+          if (!wait_no_abort(&qfull[s], (qarmed_par >> s) & 1u))
+            report(p.status, kDevTimeout, kSiteGemmDrain, (unsigned)s, 1u);
+      for (int s = 0; s < 2; ++s)
+        if ((sarmed >> s) & 1u)
+          if (!wait_no_abort(&sfull[s], (sarmed_par >> s) & 1u))
+            report(p.status, kDevTimeout, kSiteGemmDrain, (unsigned)s, 2u);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------- token sub-blocks
+    if (lane == 0) {
+      const uint64_t pol_x = l2_policy_evict_last();
+      int bs = 0;
+      uint32_t bph = 0, armed = 0, armed_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const int4 td = decode_tile(p, tile, nd, s_start, s_off);
+        const bool dense = td.x == p.E;
+        const int kbn = dense ? p.kb_dense : p.kb_exp;
+        const int nb64 = td.w / 64;
+        const int nb16 = (td.w - 64 * nb64 + kBoxRows - 1) / kBoxRows;
+        const uint32_t bytes = nb64 * 64 * 128 + nb16 * kBoxBytes;
+        const CUtensorMap* mb64 = dense ? &p.xb_d64 : &p.xb_exp64;
+        const CUtensorMap* mb16 = dense ? &p.xb_d16 : &p.xb_exp16;
+        for (int kb = 0; kb < kbn; ++kb) {
+          if (!mbar_wait(&bempty[bs], bph ^ 1u, abort_flag)) {
+            report(p.status, kDevTimeout, kSiteGemmTokens, (unsigned)tile, (unsigned)kb);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bfull[bs], bytes);
+          uint8_t* b_dst = sB + (size_t)bs * C::kBBytes;
+          const int x = kb * 64;
+          for (int j = 0; j < nb64; ++j)
+            tma_load_2d_hint(mb64, &bfull[bs], b_dst + j * 64 * 128, x, td.z + 64 * j, pol_x);
+          for (int j = 0; j < nb16; ++j)
+            tma_load_2d_hint(mb16, &bfull[bs], b_dst + (64 * nb64 + kBoxRows * j) * 128, x,
+                             td.z + 64 * nb64 + kBoxRows * j, pol_x);
+          armed |= 1u << bs;
+          armed_par = (armed_par & ~(1u << bs)) | (bph << bs);
+          if (++bs == SB) {
+            bs = 0;
+            bph ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < SB; ++s)
+        if ((armed >> s) & 1u)
+          if (!wait_no_abort(&bfull[s], (armed_par >> s) & 1u))
+            report(p.status, kDevTimeout, kSiteGemmDrain, (unsigned)s, 3u);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------- MMA issuer
+    // Learns that a slab's operands are ready only through handoff(): it
+    // touches no mbarrier while its MMAs are in flight.
+    int bs = 0, as = 0, local = 0;
+    bool stop = false, issued = false;
+    for (int tile = blockIdx.x; tile < ntiles && !stop; tile += gridDim.x, ++local) {
+      const int4 td = decode_tile(p, tile, nd, s_start, s_off);
+      const bool dense = td.x == p.E;
+      const int kbn = dense ? p.kb_dense : p.kb_exp;
+      const int nsl = (kbn + 3) / 4;
+      const int nb = (td.w + kBoxRows - 1) / kBoxRows;
+      const int acc = local & 1;
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+      const uint32_t idesc = idesc_bf16_f32(128, nb * kBoxRows);
+      for (int sl = 0; sl < nsl; ++sl) {
+        if (handoff(false)) {
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        const int nsub = min(4, kbn - 4 * sl);
+        if (lane == 0) {
+          const uint32_t a_tmem = tmem_base + a_col0 + (uint32_t)(as * 128);
+          for (int j = 0; j < nsub; ++j) {
+            const uint32_t b0 = smem_u32(sB + (size_t)((bs + j) % SB) * C::kBBytes);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              umma_bf16_ts(d_tmem, a_tmem + (uint32_t)(32 * j + 8 * k),
+                           sw128_kmajor_desc(b0 + 32 * k), idesc, (sl | j | k) != 0 ? 1u : 0u);
+            umma_commit(&bempty[(bs + j) % SB]);
+          }
+          umma_commit(&aempty[as]);
+          if (sl == nsl - 1) umma_commit(&acc_full[acc]);
+        }
+        issued = true;
+        bs = (bs + nsub) % SB;
+        if (++as == NA) as = 0;
+        __syncwarp();
+      }
+    }
+    // every MMA issued here must have completed before TMEM is released
+    if (lane == 0 && issued) {
+      umma_commit(drain);
+      if (!wait_no_abort(drain, 0u)) report(p.status, kDevTimeout, kSiteGemmDrain, 99u, 0u);
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------- waiter for the issuer
+    int bs = 0, as = 0, local = 0;
+    uint32_t bph = 0, aph = 0;
+    bool stop = false;
+    for (int tile = blockIdx.x; tile < ntiles && !stop; tile += gridDim.x, ++local) {
+      const int4 td = decode_tile(p, tile, nd, s_start, s_off);
+      const bool dense = td.x == p.E;
+      const int kbn = dense ? p.kb_dense : p.kb_exp;
+      const int nsl = (kbn + 3) / 4;
+      const int acc = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      for (int sl = 0; sl < nsl; ++sl) {
+        bool ok = true;
+        unsigned what = 0;
+        if (sl == 0 && !mbar_wait(&acc_empty[acc], (use & 1u) ^ 1u, abort_flag)) {
+          ok = false;
+          what = 0xffffffffu;
+        }
+        if (ok && !mbar_wait(&afull[as], aph, abort_flag)) {
+          ok = false;
+          what = 0x10000u + sl;
+        }
+        const int nsub = min(4, kbn - 4 * sl);
+        for (int j = 0; j < nsub && ok; ++j) {
+          if (!mbar_wait(&bfull[bs], bph, abort_flag)) {
+            ok = false;
+            what = (unsigned)(4 * sl + j);
+          }
+          if (++bs == SB) {
+            bs = 0;
+            bph ^= 1u;
+          }
+        }
+        if (++as == NA) {
+          as = 0;
+          aph ^= 1u;
+        }
+        if (!ok) {
+          if (lane == 0) report(p.status, kDevTimeout, kSiteGemmMma, (unsigned)tile, what);
+          *abort_flag = 1;
+        }
+        if (handoff(!ok)) {
+          stop = true;
+          break;
+        }
+      }
+    }
+  } else if (warp >= kDequantWarp0 && warp < kDequantWarp0 + kNumDequantWarps) {
+    // ------------------------------------------------- dequantise into TMEM
+    const int q = warp & 3;                        // TMEM lane quarter
+    const int half = (warp - kDequantWarp0) >> 2;  // chunks 4*half .. 4*half+3 of a slab
+    const int row = 32 * q + lane;                 // weight row of the tile = TMEM lane
+    const uint32_t lane_base = tmem_base + ((uint32_t)(32 * q) << 16) + a_col0;
+    int qs = 0, as = 0, local = 0;
+    uint32_t qph = 0, aph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++local) {
+      const int4 td = decode_tile(p, tile, nd, s_start, s_off);
+      const bool dense = td.x == p.E;
+      const int ng = dense ? p.kb_dense : p.kb_exp;
+      const int ss = local & 1;
+      const uint32_t sph = (uint32_t)(local >> 1) & 1u;
+      if (!mbar_wait(&sfull[ss], sph, abort_flag)) {
+        if (lane == 0) report(p.status, kDevTimeout, kSiteGemmDequant, (unsigned)tile, 0xffffu);
+        *abort_flag = 1;
+        break;
+      }
+      const uint16_t* sc_row =
+          reinterpret_cast<const uint16_t*>(sScale + (size_t)ss * 2 * slot_bytes) + row * ng;
+      const uint16_t* bi_row = sc_row + slot_bytes / 2;
+      const int nsl = (ng + 3) / 4;
+      for (int sl = 0; sl < nsl; ++sl) {
+        if (!mbar_wait(&qfull[qs], qph, abort_flag) ||
+            !mbar_wait(&aempty[as], aph ^ 1u, abort_flag)) {
+          if (lane == 0) report(p.status, kDevTimeout, kSiteGemmDequant, (unsigned)tile, (unsigned)sl);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint8_t* qrow = sQ + (size_t)qs * kQSlabBytes + row * 128;
+#pragma unroll
+        for (int gg = 0; gg < 2; ++gg) {
+          // one group of 64 codes: chunks c and c + 1 of the slab
+          const int c = 4 * half + 2 * gg;
+          const int g = (sl * 8 + c) >> 1;
+          if (g < ng) {
+            uint32_t w0[4], w1[4];
+            lds_u32x4(qrow + ((c ^ (row & 7)) << 4), w0);
+            lds_u32x4(qrow + (((c + 1) ^ (row & 7)) << 4), w1);
+            const uint32_t s = sc_row[g], b = bi_row[g];
+            const uint32_t s2 = s | (s << 16), b2 = b | (b << 16);
+            uint32_t o[32];
+            dequant32(w0, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
+            dequant32(w1, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[16]));
+            tmem_st32(lane_base + (uint32_t)(as * 128 + 16 * c), o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&afull[as]);
+          mbar_arrive(&qempty[qs]);
+        }
+        if (++qs == SQ) {
+          qs = 0;
+          qph ^= 1u;
+        }
+        if (++as == NA) {
+          as = 0;
+          aph ^= 1u;
+        }
+      }
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(&sempty[ss]);
+    }
+    tmem_st_wait();
+  } else if (warp >= kEpilogueWarp0) {
+    // ------------------------------------------------- epilogue
+    const int q = warp & 3;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
+      const int4 td = decode_tile(p, tile, nd, s_start, s_off);
+      const int nb = (td.w + kBoxRows - 1) / kBoxRows;
+      const int acc = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      if (!mbar_wait(&acc_full[acc], use & 1u, abort_flag)) {
+        if (lane == 0) report(p.status, kDevTimeout, kSiteGemmEpilogue, (unsigned)tile, 0u);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
+      epilogue_tile<MODE>(p, td, tbase, nb * kBoxRows, q, lane);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+template <int MODE, int BN>
+cudaError_t launch_q4(const GemmParams& p, int grid, cudaStream_t s) {
+  const size_t smem = CfgQ<BN>::kFixed + 4 * (size_t)p.sc_slot_bytes;
+  cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm_q4<MODE, BN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  k_grouped_gemm_q4<MODE, BN><<<grid, kThreadsQ, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_q4_smem_bytes(int bn, int sc_slot_bytes) {
+  return (bn == 128 ? CfgQ<128>::kFixed : CfgQ<64>::kFixed) + 4 * (size_t)sc_slot_bytes;
+}
+
+cudaError_t launch_gemm_q4(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s) {
+  if (mode == 0) return bn == 128 ? launch_q4<0, 128>(p, grid, s) : launch_q4<0, 64>(p, grid, s);
+  return bn == 128 ? launch_q4<1, 128>(p, grid, s) : launch_q4<1, 64>(p, grid, s);
+}
+
+}  // namespace dg

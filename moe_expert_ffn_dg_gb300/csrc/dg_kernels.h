@@ -90,6 +90,17 @@ struct GemmParams {
   const int32_t* tok_perm;
   const float* w_perm;
   DevStatus* status;
+  // 4-bit group-64 affine weights (the wa_* maps then hold the u32 code words,
+  // 8 codes a word, 128B swizzle, boxes of 32 words = 256 codes): bf16 scale
+  // and bias rows [rows, K/64] of the expert stack and of the dense matrices
+  // (gate_up: d0 = dense gate, d1 = dense up; down: d0 = dense down).
+  const uint16_t* sc_exp;
+  const uint16_t* bi_exp;
+  const uint16_t* sc_d0;
+  const uint16_t* bi_d0;
+  const uint16_t* sc_d1;
+  const uint16_t* bi_d1;
+  int sc_slot_bytes;  // shared-memory bytes of one tile's scale (or bias) rows
 };
 
 struct CombineParams {
@@ -114,6 +125,9 @@ cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s);
 // mode 0: gate_up + GEGLU, mode 1: down + weighted scatter
 cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s);
 size_t gemm_smem_bytes(int bn);
+// 4-bit weights, dequantised into TMEM; same modes.  bn is 64 or 128.
+cudaError_t launch_gemm_q4(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s);
+size_t gemm_q4_smem_bytes(int bn, int sc_slot_bytes);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 
 }  // namespace dg

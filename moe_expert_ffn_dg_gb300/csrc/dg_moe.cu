@@ -82,7 +82,14 @@ dg_status_t check_config(const dg_moe_config_t* c) {
   if (c->hidden % 128 || c->expert_inter % 64 || c->dense_inter % 64) return DG_ERR_UNSUPPORTED;
   if (c->hidden > 8192 || c->n_experts > 256 || c->top_k > 16) return DG_ERR_UNSUPPORTED;
   if (c->max_tokens > (1 << 20)) return DG_ERR_UNSUPPORTED;
-  if (c->expert_fmt != DG_FMT_BF16 || c->dense_fmt != DG_FMT_BF16) return DG_ERR_UNSUPPORTED;
+  // expert and dense weights: both bf16, or both 4-bit group-64 affine
+  const bool bf16w = c->expert_fmt == DG_FMT_BF16 && c->dense_fmt == DG_FMT_BF16;
+  const bool q4w = c->expert_fmt == DG_FMT_AFFINE_U4_G64 && c->dense_fmt == DG_FMT_AFFINE_U4_G64;
+  if (!bf16w && !q4w) return DG_ERR_UNSUPPORTED;
+  // 4-bit: one tile's scale and bias rows (128 x K/64 each, twice) must fit
+  // in shared memory beside the pipelines
+  if (q4w && (c->hidden > 4096 || c->expert_inter > 4096 || c->dense_inter > 4096))
+    return DG_ERR_UNSUPPORTED;
   if (c->router_fmt != DG_FMT_BF16 && c->router_fmt != DG_FMT_AFFINE_U8_G64)
     return DG_ERR_UNSUPPORTED;
   return DG_OK;
@@ -93,7 +100,9 @@ dg_status_t check_qtensor(const dg_qtensor_t& t, dg_format_t fmt) {
   if (!aligned(t.q, 16)) return DG_ERR_ALIGNMENT;
   if (fmt != DG_FMT_BF16) {
     if (!t.scales || !t.biases) return DG_ERR_INVALID_ARG;
-    if (!aligned(t.scales, 2) || !aligned(t.biases, 2)) return DG_ERR_ALIGNMENT;
+    // 4-bit scale rows are fetched with bulk copies (16-byte granules)
+    const size_t a = fmt == DG_FMT_AFFINE_U4_G64 ? 16 : 2;
+    if (!aligned(t.scales, a) || !aligned(t.biases, a)) return DG_ERR_ALIGNMENT;
   }
   return DG_OK;
 }
@@ -163,18 +172,31 @@ bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box);
 }
 
+// Row-major 4-bit code matrix [rows, K] (u32 words of 8 codes) read in boxes
+// of box_rows x 32 words (256 codes, 128 bytes).
+bool encode_q4_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K,
+                    uint32_t box_rows) {
+  const uint64_t dims[2] = {K / 8, rows};
+  const uint64_t strides[1] = {K / 2};
+  const uint32_t box[2] = {32, box_rows};
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, base, dims, strides, box);
+}
+
 // gate_up weights as [groups][2 halves][n/16 chunks][16 rows][K]: one box of
-// (64, 16, 2, 4, 1) is 128 rows that interleave 16 gate rows with the 16
-// matching up rows, four times.  half_stride is the byte distance from a
-// gate row to its up row; group_stride the distance between groups.
+// (128 bytes of K, 16, 2, 4, 1) is 128 rows that interleave 16 gate rows with
+// the 16 matching up rows, four times.  half_stride is the byte distance from
+// a gate row to its up row; group_stride the distance between groups.
 // rank 5 (with a group dimension) for the expert stack, rank 4 for the
-// dense pair.
+// dense pair.  q4: 4-bit code words instead of bf16.
 bool encode_gate_up(CUtensorMap* map, const void* gate, uint64_t K, uint64_t n,
-                    uint64_t half_stride, int rank, uint64_t groups, uint64_t group_stride) {
-  const uint64_t dims[5] = {K, 16, 2, n / 16, groups};
-  const uint64_t strides[4] = {K * 2, half_stride, 16 * K * 2, group_stride};
-  const uint32_t box[5] = {64, 16, 2, 4, 1};
-  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, gate, dims, strides, box);
+                    uint64_t half_stride, int rank, uint64_t groups, uint64_t group_stride,
+                    bool q4 = false) {
+  const uint64_t row_bytes = q4 ? K / 2 : K * 2;
+  const uint64_t dims[5] = {q4 ? K / 8 : K, 16, 2, n / 16, groups};
+  const uint64_t strides[4] = {row_bytes, half_stride, 16 * row_bytes, group_stride};
+  const uint32_t box[5] = {q4 ? 32u : 64u, 16, 2, 4, 1};
+  return encode_tiled(map, q4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      rank, gate, dims, strides, box);
 }
 
 }  // namespace
@@ -189,6 +211,7 @@ struct dg_moe {
   int num_sms;
   GemmParams gu;
   GemmParams dn;
+  bool q4;  // 4-bit expert and dense weights
   dg_event_t* prof;
   int n_prof;
   char last_error[256];
@@ -260,13 +283,22 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
   bool ok = true;
   // gate_up A: experts through the interleaving 5-D view; the dense pair the
   // same way when dense_up lies above dense_gate, else 16-row boxes of each
-  ok = ok && encode_gate_up(&m->gu.wa_exp, weights->gate_up.q, H, I, I * H * 2, 5, E, 2 * I * H * 2);
-  ok = ok && encode_bf16_rows(&m->gu.wa_d0, weights->dense_gate.q, D, H, 16);
-  ok = ok && encode_bf16_rows(&m->gu.wa_d1, weights->dense_up.q, D, H, 16);
+  const bool q4 = c.expert_fmt == DG_FMT_AFFINE_U4_G64;
+  m->q4 = q4;
+  const uint64_t wb2 = q4 ? 1 : 4;  // bytes of two weights
+  ok = ok && encode_gate_up(&m->gu.wa_exp, weights->gate_up.q, H, I, I * H * wb2 / 2, 5, E,
+                            2 * I * H * wb2 / 2, q4);
+  if (q4) {
+    ok = ok && encode_q4_rows(&m->gu.wa_d0, weights->dense_gate.q, D, H, 16);
+    ok = ok && encode_q4_rows(&m->gu.wa_d1, weights->dense_up.q, D, H, 16);
+  } else {
+    ok = ok && encode_bf16_rows(&m->gu.wa_d0, weights->dense_gate.q, D, H, 16);
+    ok = ok && encode_bf16_rows(&m->gu.wa_d1, weights->dense_up.q, D, H, 16);
+  }
   {
     const uintptr_t g = (uintptr_t)weights->dense_gate.q, u = (uintptr_t)weights->dense_up.q;
     m->gu.dense_5d = u > g && ((u - g) % 16) == 0 && (u - g) < (1ull << 40) &&
-                     encode_gate_up(&m->gu.wa_d5, weights->dense_gate.q, H, D, u - g, 4, 1, 0);
+                     encode_gate_up(&m->gu.wa_d5, weights->dense_gate.q, H, D, u - g, 4, 1, 0, q4);
     if (!m->gu.dense_5d) m->gu.wa_d5 = m->gu.wa_d0;
   }
   // gate_up B: xe_perm / xd rows
@@ -275,8 +307,13 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
   ok = ok && encode_bf16_rows(&m->gu.xb_d64, ws + L.xd, T, H, 64);
   ok = ok && encode_bf16_rows(&m->gu.xb_d16, ws + L.xd, T, H, 16);
   // down A: [E*H, I] and [H, D] in 128-row boxes; B: act / act_d rows
-  ok = ok && encode_bf16_rows(&m->dn.wa_exp, weights->down.q, E * H, I, 128);
-  ok = ok && encode_bf16_rows(&m->dn.wa_d0, weights->dense_down.q, H, D, 128);
+  if (q4) {
+    ok = ok && encode_q4_rows(&m->dn.wa_exp, weights->down.q, E * H, I, 128);
+    ok = ok && encode_q4_rows(&m->dn.wa_d0, weights->dense_down.q, H, D, 128);
+  } else {
+    ok = ok && encode_bf16_rows(&m->dn.wa_exp, weights->down.q, E * H, I, 128);
+    ok = ok && encode_bf16_rows(&m->dn.wa_d0, weights->dense_down.q, H, D, 128);
+  }
   m->dn.wa_d1 = m->dn.wa_d0;
   m->dn.wa_d5 = m->dn.wa_d0;
   m->dn.dense_5d = 0;
@@ -315,6 +352,20 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
   m->dn.kb_dense = (int)(D / 64);
   m->dn.mt_exp = (int)(H / 128);
   m->dn.mt_dense = (int)(H / 128);
+  // scale and bias rows of the 4-bit weights (unused for bf16)
+  auto u16 = [](const void* v) { return static_cast<const uint16_t*>(v); };
+  m->gu.sc_exp = u16(weights->gate_up.scales);
+  m->gu.bi_exp = u16(weights->gate_up.biases);
+  m->gu.sc_d0 = u16(weights->dense_gate.scales);
+  m->gu.bi_d0 = u16(weights->dense_gate.biases);
+  m->gu.sc_d1 = u16(weights->dense_up.scales);
+  m->gu.bi_d1 = u16(weights->dense_up.biases);
+  m->dn.sc_exp = u16(weights->down.scales);
+  m->dn.bi_exp = u16(weights->down.biases);
+  m->dn.sc_d0 = m->dn.sc_d1 = u16(weights->dense_down.scales);
+  m->dn.bi_d0 = m->dn.bi_d1 = u16(weights->dense_down.biases);
+  m->gu.sc_slot_bytes = (int)round_up(128 * (H / 64) * 2, 128);
+  m->dn.sc_slot_bytes = (int)round_up(128 * (I > D ? I : D) / 64 * 2, 128);
   *out = m;
   return DG_OK;
 }
@@ -358,7 +409,7 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int T = n_tokens, H = c.hidden, E = c.n_experts, K = c.top_k;
   const int TK = T * K;
-  const int bn = pick_bn(T);
+  const int bn = m->q4 ? (pick_bn(T) < 128 ? pick_bn(T) : 128) : pick_bn(T);
   int* counters = reinterpret_cast<int*>(ws + L.counters);
   DevStatus* status = reinterpret_cast<DevStatus*>(ws + L.status);
   cudaError_t err = cudaSuccess;
@@ -431,9 +482,11 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
   gu.T = dn.T = T;
   gu.bn = dn.bn = bn;
   mark(4);
-  if (err == cudaSuccess) err = launch_gemm(0, bn, gu, m->num_sms, s);
+  if (err == cudaSuccess)
+    err = m->q4 ? launch_gemm_q4(0, bn, gu, m->num_sms, s) : launch_gemm(0, bn, gu, m->num_sms, s);
   mark(5);
-  if (err == cudaSuccess) err = launch_gemm(1, bn, dn, m->num_sms, s);
+  if (err == cudaSuccess)
+    err = m->q4 ? launch_gemm_q4(1, bn, dn, m->num_sms, s) : launch_gemm(1, bn, dn, m->num_sms, s);
 
   CombineParams cp;
   cp.y_dense = reinterpret_cast<const float*>(ws + L.y_dense);

@@ -39,6 +39,11 @@ notes; the ones that touch this file: eps inside the square root; the tanh
 form of GELU; selection on exact logits with ties to the lower index; the k
 selected experts reported in ascending expert order; the canonical
 permutation sorted by (expert, token); no rounding of intermediates.
+
+Two variants serve the intermediate checks of the tensor-core path, not the
+block's definition: ``bf16_activations`` rounds the activation planes to bf16,
+and ``bf16_weights`` rounds each group-wise affine weight, once decoded
+exactly, to bf16 (the operand type of the bf16 tensor-core product).
 """
 
 from __future__ import annotations
@@ -48,7 +53,8 @@ import numpy as np
 EPS = 1e-6
 
 __all__ = [
-    "EPS", "bf16_to_f64", "round_bf16", "dequant_affine", "to_f64", "rms_norm", "gelu_tanh",
+    "EPS", "bf16_to_f64", "round_bf16", "dequant_affine", "to_f64", "decoded", "rms_norm",
+    "gelu_tanh",
     "router_logits", "select_topk", "routing_weights", "route",
     "geglu_mlp", "experts_forward", "dense_forward", "combine",
     "permutation", "moe_block_forward",
@@ -170,6 +176,13 @@ def route(h, Wr, router_scale, pes, k, bias=None):
     return z, idx, w
 
 
+def decoded(t, bf16_weights: bool = False) -> np.ndarray:
+    """A weight as float64; with bf16_weights, a group-wise affine weight is
+    rounded to bf16 after its exact decode (bf16 weights are unchanged)."""
+    w = to_f64(t)
+    return round_bf16(w) if (bf16_weights and isinstance(t, dict)) else w
+
+
 def geglu_mlp(x: np.ndarray, W_gate: np.ndarray, W_up: np.ndarray,
               W_down: np.ndarray) -> np.ndarray:
     """down(gelu_tanh(x W_gate^T) * (x W_up^T)); weights stored [out, in]."""
@@ -177,7 +190,8 @@ def geglu_mlp(x: np.ndarray, W_gate: np.ndarray, W_up: np.ndarray,
 
 
 def experts_forward(xe: np.ndarray, idx: np.ndarray, w: np.ndarray,
-                    gate_up, down, inter: int, bf16_activations: bool = False) -> np.ndarray:
+                    gate_up, down, inter: int, bf16_activations: bool = False,
+                    bf16_weights: bool = False) -> np.ndarray:
     """y[t] = sum_k w[t, k] * MLP_{idx[t, k]}(xe[t]); one expert at a time,
     over the tokens routed to it.  gate_up[e] rows 0..inter-1 are the gate,
     rows inter..2*inter-1 the up projection.
@@ -185,7 +199,8 @@ def experts_forward(xe: np.ndarray, idx: np.ndarray, w: np.ndarray,
     bf16_activations: round the expert input and the GEGLU activation to bf16
     before they are multiplied, as the activation planes are bf16 in the
     precision policy ("diffgemma — architecture & implemented contract",
-    Part III, precision policy); everything else stays float64."""
+    Part III, precision policy); everything else stays float64.
+    bf16_weights: decode affine weights exactly, then round them to bf16."""
     T, H = xe.shape
     E = (gate_up["q"] if isinstance(gate_up, dict) else gate_up).shape[0]
     if bf16_activations:
@@ -195,8 +210,8 @@ def experts_forward(xe: np.ndarray, idx: np.ndarray, w: np.ndarray,
         tok, slot = np.nonzero(idx == e)
         if tok.size == 0:
             continue
-        gu = to_f64(_slice(gate_up, e))
-        dn = to_f64(_slice(down, e))
+        gu = decoded(_slice(gate_up, e), bf16_weights)
+        dn = decoded(_slice(down, e), bf16_weights)
         x = xe[tok]
         act = gelu_tanh(x @ gu[:inter].T) * (x @ gu[inter:].T)
         if bf16_activations:
@@ -206,13 +221,15 @@ def experts_forward(xe: np.ndarray, idx: np.ndarray, w: np.ndarray,
 
 
 def dense_forward(xd, dense_gate, dense_up, dense_down,
-                  bf16_activations: bool = False) -> np.ndarray:
-    """The always-on dense GEGLU MLP (bf16_activations as in experts_forward)."""
+                  bf16_activations: bool = False, bf16_weights: bool = False) -> np.ndarray:
+    """The always-on dense GEGLU MLP (bf16_activations, bf16_weights as in
+    experts_forward)."""
+    Wg, Wu, Wd = (decoded(t, bf16_weights) for t in (dense_gate, dense_up, dense_down))
     if not bf16_activations:
-        return geglu_mlp(xd, to_f64(dense_gate), to_f64(dense_up), to_f64(dense_down))
+        return geglu_mlp(xd, Wg, Wu, Wd)
     x = round_bf16(xd)
-    act = round_bf16(gelu_tanh(x @ to_f64(dense_gate).T) * (x @ to_f64(dense_up).T))
-    return act @ to_f64(dense_down).T
+    act = round_bf16(gelu_tanh(x @ Wg.T) * (x @ Wu.T))
+    return act @ Wd.T
 
 
 def combine(h, y_dense, y_moe, w_post1, w_post2, w_post, layer_scalar):
@@ -240,11 +257,14 @@ def permutation(idx: np.ndarray, n_experts: int):
 
 
 def moe_block_forward(h_bits, p: dict, top_k: int, inter: int,
-                      layer_scalar=None, with_perm: bool = True) -> dict:
+                      layer_scalar=None, with_perm: bool = True,
+                      bf16_weights: bool = False) -> dict:
     """The whole block on one [T, H] activation, with its intermediates.
 
     ``h_bits`` is bf16 bits (uint16) or float64; ``p`` a parameter dict as
-    produced by :func:`moe_inputs.make_layer_inputs`."""
+    produced by :func:`moe_inputs.make_layer_inputs`.  bf16_weights: the
+    expert and dense affine weights rounded to bf16 after their exact decode
+    (the block on bf16-decoded weights; the router is left exact)."""
     h = bf16_to_f64(h_bits) if np.asarray(h_bits).dtype == np.uint16 else np.asarray(h_bits, np.float64)
     s = p["layer_scalar"] if layer_scalar is None else layer_scalar
     vec = {n: to_f64(p[n]) for n in ("router_scale", "per_expert_scale",
@@ -255,8 +275,10 @@ def moe_block_forward(h_bits, p: dict, top_k: int, inter: int,
                       top_k, p.get("router_bias"))
     xd = rms_norm(h, vec["w_pre_ff"])
     xe = rms_norm(h, vec["w_pre_ff2"])
-    y_moe = experts_forward(xe, idx, w, p["gate_up"], p["down"], inter)
-    y_dense = dense_forward(xd, p["dense_gate"], p["dense_up"], p["dense_down"])
+    y_moe = experts_forward(xe, idx, w, p["gate_up"], p["down"], inter,
+                            bf16_weights=bf16_weights)
+    y_dense = dense_forward(xd, p["dense_gate"], p["dense_up"], p["dense_down"],
+                            bf16_weights=bf16_weights)
     out = combine(h, y_dense, y_moe, vec["w_post_ff1"], vec["w_post_ff2"],
                   vec["w_post_ff"], s)
     res = {"z": z, "idx": idx, "w": w, "xd": xd, "xe": xe, "y_moe": y_moe,

@@ -83,8 +83,16 @@ def assert_close(got, ref, what, err_rms=ERR_RMS, cos_min=COS_MIN, bf16_output=F
     return err / rms if rms else 0.0, cos
 
 
-def run_and_check(wl, p, h_bits, layer_scalar=None, blk=None, check_intermediates=True):
-    """Forward on the GPU and full comparison with the oracle."""
+def run_and_check(wl, p, h_bits, layer_scalar=None, blk=None, check_intermediates=True,
+                  ref_bf16_weights=False):
+    """Forward on the GPU and full comparison with the oracle.
+
+    Group-wise affine expert and dense weights reach the tensor cores decoded
+    to bf16, so the branch outputs are compared with the oracle variant that
+    rounds the exact decode to bf16 as well.  The block output is compared
+    with the exact oracle, or, with ref_bf16_weights, with the exact block on
+    the bf16-decoded weights (for shapes with no 4-bit configuration of their
+    own, as the fp32 draws of the small workload are cast to bf16 first)."""
     ls = p["layer_scalar"] if layer_scalar is None else layer_scalar
     own = blk is None
     if own:
@@ -94,7 +102,9 @@ def run_and_check(wl, p, h_bits, layer_scalar=None, blk=None, check_intermediate
     torch.cuda.synchronize()
     st = blk.device_status()
     assert st[0] == 0, f"device status {st}"
-    ref = oracle.moe_block_forward(h_bits, p, wl.top_k, wl.expert_inter, layer_scalar=ls)
+    ref = oracle.moe_block_forward(h_bits, p, wl.top_k, wl.expert_inter, layer_scalar=ls,
+                                   bf16_weights=ref_bf16_weights)
+    q_w = isinstance(p["gate_up"], dict)
     T, K = h_bits.shape[0], wl.top_k
     idx = dbg["idx"].cpu().numpy()
     assert np.array_equal(idx, ref["idx"]), \
@@ -110,9 +120,9 @@ def run_and_check(wl, p, h_bits, layer_scalar=None, blk=None, check_intermediate
         xe_ref = mi.f32_to_bf16_bits(ref["xe"].astype(np.float32))[ref["perm"] // K]
         assert bf16_ulp_distance(bf16_bits(dbg["xe_perm"]), xe_ref).max() <= 1
         yd16 = oracle.dense_forward(ref["xd"], p["dense_gate"], p["dense_up"], p["dense_down"],
-                                    bf16_activations=True)
+                                    bf16_activations=True, bf16_weights=q_w)
         ym16 = oracle.experts_forward(ref["xe"], ref["idx"], ref["w"], p["gate_up"], p["down"],
-                                      wl.expert_inter, bf16_activations=True)
+                                      wl.expert_inter, bf16_activations=True, bf16_weights=q_w)
         res["y_dense"] = assert_close(dbg["y_dense"].cpu().numpy(), yd16, "y_dense",
                                       BRANCH_ERR_RMS, BRANCH_COS_MIN)
         res["y_moe"] = assert_close(dbg["y_moe"].cpu().numpy(), ym16, "y_moe",

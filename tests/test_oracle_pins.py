@@ -376,6 +376,41 @@ def test_quantised_block_equals_dequant_then_bf16_block():
     np.testing.assert_allclose(rq["out"], rd["out"], rtol=1e-12, atol=1e-12)
 
 
+def test_bf16_decoded_weights_are_the_rounded_exact_decode():
+    # the bf16_weights variant: exact decode by hand, then round to nearest
+    # even bf16 through the input module's independent rounding (the decode
+    # s*q + b of bf16 s, b and a 4-bit q is exact in float32)
+    rng = _rng(31)
+    w = mi.f32_to_bf16_bits(rng.standard_normal((4, 256)).astype(np.float32) * 0.02)
+    qt = mi.quantize_affine(w, 4)
+    exact = _dequant_by_hand(qt)
+    want = o.bf16_to_f64(mi.f32_to_bf16_bits(exact.astype(np.float32)))
+    assert np.array_equal(exact.astype(np.float32).astype(np.float64), exact)
+    got = o.decoded(qt, bf16_weights=True)
+    np.testing.assert_array_equal(got, want)
+    # within half a bf16 ulp of the exact decode, and not all equal to it
+    ulp = np.ldexp(1.0, np.floor(np.log2(np.abs(np.where(exact == 0, 1, exact)))).astype(int) - 7)
+    assert np.all(np.abs(got - exact) <= ulp / 2)
+    assert np.any(got != exact)
+    # bf16 weights and float64 weights pass through unchanged
+    assert np.array_equal(o.decoded(w, True), o.bf16_to_f64(w))
+
+
+def test_bf16_weights_variant_leaves_bf16_block_unchanged_and_changes_q4_block():
+    wl = mi.get_workload("tiny")
+    h = mi.make_tokens(wl)[:8]
+    pb = mi.make_layer_inputs(wl, randvec=True)
+    r0 = o.moe_block_forward(h, pb, wl.top_k, wl.expert_inter)
+    r1 = o.moe_block_forward(h, pb, wl.top_k, wl.expert_inter, bf16_weights=True)
+    assert np.array_equal(r0["out"], r1["out"])
+    pq = mi.make_layer_inputs(wl, randvec=True, quantise=True)
+    q0 = o.moe_block_forward(h, pq, wl.top_k, wl.expert_inter)
+    q1 = o.moe_block_forward(h, pq, wl.top_k, wl.expert_inter, bf16_weights=True)
+    assert np.array_equal(q0["idx"], q1["idx"])         # the router stays exact
+    d = np.abs(q1["out"] - q0["out"]).max()
+    assert 0 < d < 0.05 * np.sqrt(np.mean(q0["out"] ** 2))
+
+
 # ---------------------------------------------------------------- whole block
 
 def test_canvas_permutation_permutes_outputs():
