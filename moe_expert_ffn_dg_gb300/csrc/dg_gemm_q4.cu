@@ -11,16 +11,18 @@
 // Dataflow of one tile (128 weight rows x up to BN token rows):
 //   warp 0   TMA: code slabs (128 rows x 256 codes = 16 KB, 128B swizzle) into
 //            a ring, and per tile the rows' scales and biases (bulk copies);
-//   warp 1   TMA: token sub-blocks (BN rows x 64 bf16) into a second ring;
+//   warp 1   TMA: token slabs (BN rows x 256 bf16, as four 64-column
+//            sub-blocks) into a second ring;
 //   warp 2   TMEM owner and MMA issuer: tcgen05.mma with A read from TMEM
 //            (the dequantised weights) and B from shared memory (tokens),
 //            one slab (16 MMAs of K = 16) per round;
 //   warp 3   waits, for the issuer, until a slab's operands are ready and
 //            hands it over through a named barrier (see below);
-//   warps 4-11  dequantise: each thread expands one weight row of a slab to
-//            bf16 (exact s * q + b, one rounding) and stores it into TMEM with
-//            tcgen05.st, two warps per 32-lane quarter;
-//   warps 12-15 epilogue, as for bf16 weights (GEGLU or weighted combine).
+//   warps 4-19  dequantise: each thread expands one group of 64 codes of one
+//            weight row of a slab to bf16 (exact s * q + b, one rounding) and
+//            stores it into TMEM with tcgen05.st; four warps per 32-lane
+//            quarter, one group each;
+//   warps 20-23 epilogue, as for bf16 weights (GEGLU or weighted combine).
 // The bf16 weights never pass through shared memory: shared-memory traffic
 // per weight is the half byte of its code plus its share of the token tile.
 //
@@ -48,21 +50,26 @@ namespace {
 
 using namespace gemm;
 
-constexpr int kThreadsQ = 512;
-constexpr int kSlabK = 256;                  // codes per row of a slab
+constexpr int kSlabK = 256;                    // codes per row of a slab
 constexpr int kQSlabBytes = 128 * kSlabK / 2;  // 16 KB
 constexpr int kDequantWarp0 = 4;
-constexpr int kNumDequantWarps = 8;
-constexpr int kEpilogueWarp0 = 12;
+constexpr int kNumDequantWarps = 16;           // 4 per TMEM lane quarter, one group of 64 each
+constexpr int kEpilogueWarp0 = kDequantWarp0 + kNumDequantWarps;
+constexpr int kThreadsQ = 32 * (kEpilogueWarp0 + 4);  // 768
 
+// Per token-tile width: code slabs in flight (SQ), token slabs in flight
+// (SB; a token slab is the four 64-column sub-blocks of one code slab) and
+// dequantised slabs held in TMEM (NA) beside the two BN-column accumulators.
+// Narrow tiles keep more token slabs in flight: the ring must cover the
+// TMA latency plus the time an MMA batch takes to complete.
 template <int BN>
 struct CfgQ {
-  static constexpr int kSQ = BN == 64 ? 6 : 5;  // code slabs in flight
-  static constexpr int kSB = BN == 64 ? 6 : 4;  // token sub-blocks in flight
-  static constexpr int kBBytes = BN * 128;
-  static constexpr int kNA = (512 - 2 * BN) / 128;  // dequantised slabs in TMEM
+  static constexpr int kSQ = BN == 128 ? 3 : 4;
+  static constexpr int kSB = BN == 32 ? 6 : BN == 64 ? 3 : 2;
+  static constexpr int kBSlabBytes = 4 * BN * 128;
+  static constexpr int kNA = (512 - 2 * BN) / 128 < 3 ? (512 - 2 * BN) / 128 : 3;
   static constexpr int kBarBytes = 512;
-  static constexpr size_t kFixed = 1024 + (size_t)kSQ * kQSlabBytes + (size_t)kSB * kBBytes +
+  static constexpr size_t kFixed = 1024 + (size_t)kSQ * kQSlabBytes + (size_t)kSB * kBSlabBytes +
                                    kBarBytes + kTileTableBytes;
 };
 
@@ -167,7 +174,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sQ = smem;
   uint8_t* sB = sQ + (size_t)SQ * kQSlabBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (size_t)SB * C::kBBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (size_t)SB * C::kBSlabBytes);
   uint64_t* qfull = bars;
   uint64_t* qempty = qfull + SQ;
   uint64_t* bfull = qempty + SQ;
@@ -337,7 +344,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
             report(p.status, kDevTimeout, kSiteGemmDrain, (unsigned)s, 2u);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------- token sub-blocks
+    // ------------------------------------------------- token slabs
     if (lane == 0) {
       const uint64_t pol_x = l2_policy_evict_last();
       int bs = 0;
@@ -347,26 +354,30 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         const int4 td = decode_tile(p, tile, nd, s_start, s_off);
         const bool dense = td.x == p.E;
         const int kbn = dense ? p.kb_dense : p.kb_exp;
+        const int nsl = (kbn + 3) / 4;
         const int nb64 = td.w / 64;
         const int nb16 = (td.w - 64 * nb64 + kBoxRows - 1) / kBoxRows;
-        const uint32_t bytes = nb64 * 64 * 128 + nb16 * kBoxBytes;
+        const uint32_t sub_bytes = nb64 * 64 * 128 + nb16 * kBoxBytes;
         const CUtensorMap* mb64 = dense ? &p.xb_d64 : &p.xb_exp64;
         const CUtensorMap* mb16 = dense ? &p.xb_d16 : &p.xb_exp16;
-        for (int kb = 0; kb < kbn; ++kb) {
+        for (int sl = 0; sl < nsl; ++sl) {
           if (!mbar_wait(&bempty[bs], bph ^ 1u, abort_flag)) {
-            report(p.status, kDevTimeout, kSiteGemmTokens, (unsigned)tile, (unsigned)kb);
+            report(p.status, kDevTimeout, kSiteGemmTokens, (unsigned)tile, (unsigned)sl);
             *abort_flag = 1;
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&bfull[bs], bytes);
-          uint8_t* b_dst = sB + (size_t)bs * C::kBBytes;
-          const int x = kb * 64;
-          for (int j = 0; j < nb64; ++j)
-            tma_load_2d_hint(mb64, &bfull[bs], b_dst + j * 64 * 128, x, td.z + 64 * j, pol_x);
-          for (int j = 0; j < nb16; ++j)
-            tma_load_2d_hint(mb16, &bfull[bs], b_dst + (64 * nb64 + kBoxRows * j) * 128, x,
-                             td.z + 64 * nb64 + kBoxRows * j, pol_x);
+          const int nsub = min(4, kbn - 4 * sl);
+          mbar_arrive_expect_tx(&bfull[bs], sub_bytes * (uint32_t)nsub);
+          for (int j = 0; j < nsub; ++j) {
+            uint8_t* b_dst = sB + (size_t)bs * C::kBSlabBytes + (size_t)j * BN * 128;
+            const int x = (4 * sl + j) * 64;
+            for (int r = 0; r < nb64; ++r)
+              tma_load_2d_hint(mb64, &bfull[bs], b_dst + r * 64 * 128, x, td.z + 64 * r, pol_x);
+            for (int r = 0; r < nb16; ++r)
+              tma_load_2d_hint(mb16, &bfull[bs], b_dst + (64 * nb64 + kBoxRows * r) * 128, x,
+                               td.z + 64 * nb64 + kBoxRows * r, pol_x);
+          }
           armed |= 1u << bs;
           armed_par = (armed_par & ~(1u << bs)) | (bph << bs);
           if (++bs == SB) {
@@ -404,19 +415,20 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         const int nsub = min(4, kbn - 4 * sl);
         if (lane == 0) {
           const uint32_t a_tmem = tmem_base + a_col0 + (uint32_t)(as * 128);
+          const uint32_t b_slab = smem_u32(sB + (size_t)bs * C::kBSlabBytes);
           for (int j = 0; j < nsub; ++j) {
-            const uint32_t b0 = smem_u32(sB + (size_t)((bs + j) % SB) * C::kBBytes);
+            const uint32_t b0 = b_slab + (uint32_t)(j * BN * 128);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               umma_bf16_ts(d_tmem, a_tmem + (uint32_t)(32 * j + 8 * k),
                            sw128_kmajor_desc(b0 + 32 * k), idesc, (sl | j | k) != 0 ? 1u : 0u);
-            umma_commit(&bempty[(bs + j) % SB]);
           }
+          umma_commit(&bempty[bs]);
           umma_commit(&aempty[as]);
           if (sl == nsl - 1) umma_commit(&acc_full[acc]);
         }
         issued = true;
-        bs = (bs + nsub) % SB;
+        if (++bs == SB) bs = 0;
         if (++as == NA) as = 0;
         __syncwarp();
       }
@@ -449,16 +461,13 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
           ok = false;
           what = 0x10000u + sl;
         }
-        const int nsub = min(4, kbn - 4 * sl);
-        for (int j = 0; j < nsub && ok; ++j) {
-          if (!mbar_wait(&bfull[bs], bph, abort_flag)) {
-            ok = false;
-            what = (unsigned)(4 * sl + j);
-          }
-          if (++bs == SB) {
-            bs = 0;
-            bph ^= 1u;
-          }
+        if (ok && !mbar_wait(&bfull[bs], bph, abort_flag)) {
+          ok = false;
+          what = 0x20000u + sl;
+        }
+        if (++bs == SB) {
+          bs = 0;
+          bph ^= 1u;
         }
         if (++as == NA) {
           as = 0;
@@ -474,11 +483,11 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         }
       }
     }
-  } else if (warp >= kDequantWarp0 && warp < kDequantWarp0 + kNumDequantWarps) {
+  } else if (warp >= kDequantWarp0 && warp < kEpilogueWarp0) {
     // ------------------------------------------------- dequantise into TMEM
-    const int q = warp & 3;                        // TMEM lane quarter
-    const int half = (warp - kDequantWarp0) >> 2;  // chunks 4*half .. 4*half+3 of a slab
-    const int row = 32 * q + lane;                 // weight row of the tile = TMEM lane
+    const int q = warp & 3;                          // TMEM lane quarter
+    const int gg = (warp - kDequantWarp0) >> 2;      // group of 64 codes within a slab
+    const int row = 32 * q + lane;                   // weight row of the tile = TMEM lane
     const uint32_t lane_base = tmem_base + ((uint32_t)(32 * q) << 16) + a_col0;
     int qs = 0, as = 0, local = 0;
     uint32_t qph = 0, aph = 0;
@@ -507,23 +516,19 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
           break;
         }
         tc_fence_after();
-        const uint8_t* qrow = sQ + (size_t)qs * kQSlabBytes + row * 128;
-#pragma unroll
-        for (int gg = 0; gg < 2; ++gg) {
-          // one group of 64 codes: chunks c and c + 1 of the slab
-          const int c = 4 * half + 2 * gg;
-          const int g = (sl * 8 + c) >> 1;
-          if (g < ng) {
-            uint32_t w0[4], w1[4];
-            lds_u32x4(qrow + ((c ^ (row & 7)) << 4), w0);
-            lds_u32x4(qrow + (((c + 1) ^ (row & 7)) << 4), w1);
-            const uint32_t s = sc_row[g], b = bi_row[g];
-            const uint32_t s2 = s | (s << 16), b2 = b | (b << 16);
-            uint32_t o[32];
-            dequant32(w0, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
-            dequant32(w1, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[16]));
-            tmem_st32(lane_base + (uint32_t)(as * 128 + 16 * c), o);
-          }
+        const int g = 4 * sl + gg;  // this warp's group of 64 codes
+        if (g < ng) {
+          const uint8_t* qrow = sQ + (size_t)qs * kQSlabBytes + row * 128;
+          const int c = 2 * gg;  // its two 32-code chunks: c and c + 1
+          uint32_t w0[4], w1[4];
+          lds_u32x4(qrow + ((c ^ (row & 7)) << 4), w0);
+          lds_u32x4(qrow + (((c + 1) ^ (row & 7)) << 4), w1);
+          const uint32_t s = sc_row[g], b = bi_row[g];
+          const uint32_t s2 = s | (s << 16), b2 = b | (b << 16);
+          uint32_t o[32];
+          dequant32(w0, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
+          dequant32(w1, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[16]));
+          tmem_st32(lane_base + (uint32_t)(as * 128 + 16 * c), o);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -545,7 +550,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       if (ok && lane == 0) mbar_arrive(&sempty[ss]);
     }
     tmem_st_wait();
-  } else if (warp >= kEpilogueWarp0) {
+  } else {
     // ------------------------------------------------- epilogue
     const int q = warp & 3;
     int local = 0;
@@ -590,12 +595,19 @@ cudaError_t launch_q4(const GemmParams& p, int grid, cudaStream_t s) {
 }  // namespace
 
 size_t gemm_q4_smem_bytes(int bn, int sc_slot_bytes) {
-  return (bn == 128 ? CfgQ<128>::kFixed : CfgQ<64>::kFixed) + 4 * (size_t)sc_slot_bytes;
+  const size_t fixed = bn == 128 ? CfgQ<128>::kFixed : bn == 64 ? CfgQ<64>::kFixed : CfgQ<32>::kFixed;
+  return fixed + 4 * (size_t)sc_slot_bytes;
 }
 
 cudaError_t launch_gemm_q4(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s) {
-  if (mode == 0) return bn == 128 ? launch_q4<0, 128>(p, grid, s) : launch_q4<0, 64>(p, grid, s);
-  return bn == 128 ? launch_q4<1, 128>(p, grid, s) : launch_q4<1, 64>(p, grid, s);
+  if (mode == 0) {
+    if (bn == 128) return launch_q4<0, 128>(p, grid, s);
+    if (bn == 64) return launch_q4<0, 64>(p, grid, s);
+    return launch_q4<0, 32>(p, grid, s);
+  }
+  if (bn == 128) return launch_q4<1, 128>(p, grid, s);
+  if (bn == 64) return launch_q4<1, 64>(p, grid, s);
+  return launch_q4<1, 32>(p, grid, s);
 }
 
 }  // namespace dg

@@ -33,6 +33,17 @@ struct Layout {
 // stages fit when the token slot is small), large batches favour wide N.
 int pick_bn(int T) { return T <= 512 ? 64 : (T <= 2048 ? 128 : 256); }
 
+// The same for the 4-bit GEMM (its TMEM holds two accumulators and the
+// dequantised slabs, so 128 is the widest): narrow tiles for one canvas keep
+// six token slabs in flight; the widest one whose shared memory fits.
+int pick_bn_q4(int T, size_t slot_gu, size_t slot_dn, size_t smem_max) {
+  int bn = T <= 256 ? 32 : (T <= 512 ? 64 : 128);
+  while (bn > 32 && (gemm_q4_smem_bytes(bn, (int)slot_gu) > smem_max ||
+                     gemm_q4_smem_bytes(bn, (int)slot_dn) > smem_max))
+    bn /= 2;
+  return bn;
+}
+
 Layout make_layout(const dg_moe_config_t& c) {
   Layout L;
   const size_t T = (size_t)c.max_tokens, H = c.hidden, E = c.n_experts, K = c.top_k;
@@ -212,6 +223,7 @@ struct dg_moe {
   GemmParams gu;
   GemmParams dn;
   bool q4;  // 4-bit expert and dense weights
+  size_t smem_optin;  // largest dynamic shared memory a block may opt into
   dg_event_t* prof;
   int n_prof;
   char last_error[256];
@@ -271,11 +283,15 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
   m->prof = nullptr;
   m->n_prof = 0;
   m->last_error[0] = 0;
+  int optin = 0;
   if (cudaGetDevice(&m->device) != cudaSuccess ||
-      cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess) {
+      cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, m->device) !=
+          cudaSuccess) {
     delete m;
     return DG_ERR_CUDA;
   }
+  m->smem_optin = (size_t)optin;
   const dg_moe_config_t& c = m->cfg;
   const uint64_t H = c.hidden, E = c.n_experts, I = c.expert_inter, D = c.dense_inter;
   const uint64_t T = c.max_tokens, TK = T * c.top_k;
@@ -366,6 +382,10 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
   m->dn.bi_d0 = m->dn.bi_d1 = u16(weights->dense_down.biases);
   m->gu.sc_slot_bytes = (int)round_up(128 * (H / 64) * 2, 128);
   m->dn.sc_slot_bytes = (int)round_up(128 * (I > D ? I : D) / 64 * 2, 128);
+  if (q4 && gemm_q4_smem_bytes(32, m->gu.sc_slot_bytes) > m->smem_optin) {
+    delete m;
+    return DG_ERR_UNSUPPORTED;
+  }
   *out = m;
   return DG_OK;
 }
@@ -409,7 +429,8 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int T = n_tokens, H = c.hidden, E = c.n_experts, K = c.top_k;
   const int TK = T * K;
-  const int bn = m->q4 ? (pick_bn(T) < 128 ? pick_bn(T) : 128) : pick_bn(T);
+  const int bn = m->q4 ? pick_bn_q4(T, m->gu.sc_slot_bytes, m->dn.sc_slot_bytes, m->smem_optin)
+                      : pick_bn(T);
   int* counters = reinterpret_cast<int*>(ws + L.counters);
   DevStatus* status = reinterpret_cast<DevStatus*>(ws + L.status);
   cudaError_t err = cudaSuccess;
