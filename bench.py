@@ -8,7 +8,7 @@ that canvas with inputs resident in HBM.  The 1.56 GB of weights read per
 step are 12x the L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload canvas256|canvas256_q4|batch2048_zipf]
+                  [--workload canvas256|canvas256_q4|batch2048_zipf|stack30_q4]
 
 Prints one JSON line.  ``--impl reference`` times the CPU oracle (the only
 reference there is: the pages hold no runnable implementation) on the host
@@ -206,6 +206,152 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def _gen_layer(job):
+    """Worker of the weight-generation pool: one layer's seeded draws."""
+    import moe_inputs as mi
+    name, layer = job
+    return layer, mi.make_layer_inputs(mi.get_workload(name), layer=layer)
+
+
+def run_stack(args):
+    """The 30-layer 4-bit stack over 64 canvases (16384 tokens): a step is one
+    forward through all layers (each with its own seeded weights), timed as a
+    whole and reported per layer."""
+    import multiprocessing as mp
+
+    import moe_inputs as mi
+    wl = mi.get_workload(args.workload)
+    L = wl.n_layers
+    # generate the layers' weights on the host cores before any CUDA call
+    t_gen = time.time()
+    ctx = mp.get_context("spawn")
+    pool = ctx.Pool(processes=max(1, min(16, (os.cpu_count() or 2) - 1)))
+    gen = pool.imap(_gen_layer, [(wl.name, l) for l in range(L)])
+
+    import torch
+
+    import moe_expert_ffn_dg_gb300 as pkg
+    from moe_expert_ffn_dg_gb300 import binding as B
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    pkg.build()
+    pkg.load_library()
+    eb, db, rb = wl.quant
+    fmt = {4: B.DG_FMT_AFFINE_U4_G64, 8: B.DG_FMT_AFFINE_U8_G64}
+    shape = dict(hidden=wl.hidden, n_experts=wl.n_experts, top_k=wl.top_k,
+                 expert_inter=wl.expert_inter, dense_inter=wl.dense_inter, max_tokens=wl.tokens)
+    ws = torch.empty(pkg.MoEBlock.workspace_bytes(**shape, expert_fmt=fmt[eb], dense_fmt=fmt[db],
+                                                  router_fmt=fmt[rb]), dtype=torch.uint8, device=dev)
+    blocks, scalars, p0 = [None] * L, [None] * L, None
+    for layer, p in gen:
+        blocks[layer] = pkg.MoEBlock.from_params(p, **shape, device=dev, workspace=ws)
+        scalars[layer] = p["layer_scalar"]
+        if layer == 0:
+            p0 = p
+    pool.close()
+    pool.join()
+    t_gen = time.time() - t_gen
+    h_np = mi.make_tokens(wl)
+    h = torch.from_numpy(h_np.view(np.int16)).to(dev).view(torch.bfloat16)
+    bufs = [torch.empty_like(h), torch.empty_like(h)]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(x):
+        for l in range(L):
+            out = bufs[l % 2]
+            blocks[l].forward(x, scalars[l], out=out)
+            x = out
+        return x
+
+    for _ in range(max(args.warmup, 3)):
+        step(h)
+    torch.cuda.synchronize(dev)
+    st = blocks[0].device_status()
+    if st[0] != 0:
+        raise RuntimeError(f"device status after warm-up: {st}")
+    names = B.dg_moe_kernel_names(blocks[0].handle)
+    nk = len(names)
+    prof_layer = L // 2
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+               for _ in range(args.steps)]
+    for evs in ev_sets:
+        for e in evs:
+            e.record(stream)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(0)
+    time.sleep(0.3)
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for i in range(args.steps):
+        B.dg_moe_set_profile_events(blocks[prof_layer].handle, [e.cuda_event for e in ev_sets[i]])
+        step(h)
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    B.dg_moe_set_profile_events(blocks[prof_layer].handle, None)
+    clk = clocks.stop()
+    st = blocks[0].device_status()
+    if st[0] != 0:
+        raise RuntimeError(f"device status after timing: {st}")
+    ms_step = start.elapsed_time(stop) / args.steps
+    per_kernel = np.zeros(nk)
+    for evs in ev_sets:
+        per_kernel += [evs[j].elapsed_time(evs[j + 1]) for j in range(nk)]
+    per_kernel_us = per_kernel / len(ev_sets) * 1000.0
+
+    # end to end: pinned host input -> device, all layers, output -> host
+    h_host = torch.from_numpy(h_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+    o_host = torch.empty_like(h_host).pin_memory()
+    e2e_steps = max(3, min(args.steps, 10))
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        x = h_host.to(dev, non_blocking=True)
+        o_host.copy_(step(x), non_blocking=True)
+        torch.cuda.synchronize(dev)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+
+    _, dbg = blocks[0].forward(h, scalars[0], debug=True)
+    counts = np.diff(dbg["offsets"].cpu().numpy())
+    alg = algorithmic(wl, counts)
+    hbm, bf16_burst, bf16_sus, src = peaks()
+    T, H, K, I, D = wl.tokens, wl.hidden, wl.top_k, wl.expert_inter, wl.dense_inter
+    gu_flops = 2 * T * K * H * 2 * I + 2 * T * H * 2 * D
+    gu = names.index("gemm_gate_up")
+    gu_tf = gu_flops / (per_kernel_us[gu] * 1e-6) / 1e12
+    t_layer = ms_step / L / 1000.0
+    line = {
+        "metric": METRIC, "value": T / t_layer, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(wl) + f", {L} layers each with its own weights",
+                   "tokens_per_step": T, "layers_per_step": L, "us_per_layer": t_layer * 1e6,
+                   "weights": f"u{eb} g64 affine experts and dense, u{rb} router, dequantised "
+                              f"to bf16 on chip", "weight_generation_s": round(t_gen, 1),
+                   "l2": f"no flush: {alg['layer_bytes'] / 1e9:.3f} GB of weights per layer, "
+                         f"{alg['layer_bytes'] / 129e6:.1f}x the 129 MB L2"},
+        "roofline": {"bound": "tensor", "kernel": "gemm_gate_up", "achieved": gu_tf,
+                     "peak": bf16_sus, "unit": "TFLOP/s", "frac": gu_tf / bf16_sus, "traffic": None,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json bf16_tflops_sustained)",
+                     "algorithmic_flops_per_launch": gu_flops, "us_per_launch": per_kernel_us[gu],
+                     "kernel_of_layer": prof_layer},
+        "layer_roofline": {"bytes": alg["layer_bytes"], "flops": alg["layer_flops"],
+                           "achieved_tflops": alg["layer_flops"] / t_layer / 1e12,
+                           "frac_of_bf16_peak": alg["layer_flops"] / t_layer / 1e12 / bf16_sus,
+                           "basis": f"flops / {bf16_sus} TF/s ({src}, sustained)"},
+        "kernels_us": {n: round(float(v), 3) for n, v in zip(names, per_kernel_us)},
+        "e2e": {"value": T * L / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h_host.numel() * 2),
+                "d2h_bytes_per_step": int(o_host.numel() * 2), "steps": e2e_steps,
+                "note": "per layer: tokens / (end-to-end step time / layers)"},
+        "clocks": clk,
+        "gpu_launches": nk * L * args.steps,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, p0, h_np, max_seconds=20.0)
+    for b in blocks:
+        b.close()
+    print(json.dumps(line))
+
+
 def run_ours(args):
     import torch
 
@@ -352,12 +498,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=["canvas256", "canvas256_q4", "batch2048_zipf"])
+                    choices=["canvas256", "canvas256_q4", "batch2048_zipf", "stack30_q4"])
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "stack30_q4":
+        run_stack(args)
     else:
         run_ours(args)
 

@@ -66,7 +66,12 @@ class MoEBlock:
     the handle.  ``forward`` runs the block on a bf16 [T, H] device tensor."""
 
     def __init__(self, weights: dict, *, hidden: int, n_experts: int, top_k: int,
-                 expert_inter: int, dense_inter: int, max_tokens: int, rms_eps: float = 1e-6):
+                 expert_inter: int, dense_inter: int, max_tokens: int, rms_eps: float = 1e-6,
+                 workspace: torch.Tensor = None):
+        """workspace: optional uint8 device tensor to use instead of a private
+        one (at least workspace_bytes(...) + 1024 bytes).  Layers that run
+        one after another on one stream may share a workspace; the handle
+        keeps only its device status word there between forwards."""
         self.weights = weights  # keeps the device tensors alive
         self.hidden, self.n_experts, self.top_k = hidden, n_experts, top_k
         self.expert_inter, self.dense_inter, self.max_tokens = expert_inter, dense_inter, max_tokens
@@ -76,7 +81,11 @@ class MoEBlock:
                                      rms_eps, 0)
         self.device = weights["router_scale"].device
         ws_bytes = B.dg_moe_workspace_size(self.cfg)
-        self.workspace = torch.empty(ws_bytes + 1024, dtype=torch.uint8, device=self.device)
+        if workspace is None:
+            workspace = torch.empty(ws_bytes + 1024, dtype=torch.uint8, device=self.device)
+        elif workspace.numel() < ws_bytes + 1024 or workspace.device != self.device:
+            raise ValueError("shared workspace too small or on another device")
+        self.workspace = workspace
         base = self.workspace.data_ptr()
         self._ws_ptr = (base + 1023) // 1024 * 1024
         self._ws_bytes = ws_bytes
@@ -92,9 +101,20 @@ class MoEBlock:
 
     @classmethod
     def from_params(cls, p: dict, *, hidden, n_experts, top_k, expert_inter, dense_inter,
-                    max_tokens, device="cuda"):
+                    max_tokens, device="cuda", workspace=None):
         return cls(params_to_device(p, device), hidden=hidden, n_experts=n_experts, top_k=top_k,
-                   expert_inter=expert_inter, dense_inter=dense_inter, max_tokens=max_tokens)
+                   expert_inter=expert_inter, dense_inter=dense_inter, max_tokens=max_tokens,
+                   workspace=workspace)
+
+    @staticmethod
+    def workspace_bytes(*, hidden, n_experts, top_k, expert_inter, dense_inter, max_tokens,
+                        expert_fmt=B.DG_FMT_BF16, dense_fmt=B.DG_FMT_BF16,
+                        router_fmt=B.DG_FMT_BF16, rms_eps=1e-6) -> int:
+        """Bytes to allocate for a workspace shared by layers of this shape
+        (the C library's requirement plus 1024 bytes of alignment slack)."""
+        cfg = B.dg_moe_config_t(hidden, n_experts, top_k, expert_inter, dense_inter, max_tokens,
+                                expert_fmt, dense_fmt, router_fmt, rms_eps, 0)
+        return B.dg_moe_workspace_size(cfg) + 1024
 
     def _stream(self, stream=None) -> int:
         s = stream if stream is not None else torch.cuda.current_stream(self.device)

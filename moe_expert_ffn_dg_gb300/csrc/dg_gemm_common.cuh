@@ -135,25 +135,48 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int4 td, uint
           out[row * ld + feat] = f32_to_bf16_rne(gelu_tanh(g) * u);
         }
       }
-    } else {
+    } else if (dense) {
       const int feat = td.y * 128 + 32 * q + lane;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (c0 + j < td.w) p.y_dense[(size_t)(td.z + c0 + j) * p.H + feat] = v[j];
+    } else {
+      // Routing-weighted add into the f32 per-token accumulator, four
+      // features per vector reduction: transpose each 4 x 4 block of
+      // (lane in quad) x (token) values across the quad, so lane 4i + r ends
+      // up with features 4i..4i+3 of token 4m + r.
       int tok = 0;
       float wt = 0.f;
-      if (!dense && lane < 16 && c0 + lane < td.w) {
+      if (lane < 16 && c0 + lane < td.w) {
         tok = p.tok_perm[td.z + c0 + lane];
         wt = p.w_perm[td.z + c0 + lane];
       }
+      const int r = lane & 3;
+      float* ybase = p.y_moe + td.y * 128 + 32 * q + (lane & ~3);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int col = c0 + j;
-        const int tj = __shfl_sync(0xffffffffu, tok, j);
-        const float wj = __shfl_sync(0xffffffffu, wt, j);
-        if (col < td.w) {
-          if (dense) {
-            p.y_dense[(size_t)(td.z + col) * p.H + feat] = v[j];
-          } else {
-            atomicAdd(&p.y_moe[(size_t)tj * p.H + feat], wj * v[j]);
-          }
+      for (int m = 0; m < 4; ++m) {
+        float a[4] = {v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]};
+#pragma unroll
+        for (int j2 = 0; j2 < 2; ++j2) {  // swap the off-diagonal 2 x 2 blocks
+          const float send = (r & 2) ? a[j2] : a[j2 + 2];
+          const float recv = __shfl_xor_sync(0xffffffffu, send, 2);
+          if (r & 2) a[j2] = recv;
+          else a[j2 + 2] = recv;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; j += 2) {  // transpose inside each 2 x 2 block
+          const float send = (r & 1) ? a[j] : a[j + 1];
+          const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+          if (r & 1) a[j] = recv;
+          else a[j + 1] = recv;
+        }
+        const int tj = __shfl_sync(0xffffffffu, tok, 4 * m + r);
+        const float wj = __shfl_sync(0xffffffffu, wt, 4 * m + r);
+        if (c0 + 4 * m + r < td.w) {
+          float* dst = ybase + (size_t)tj * p.H;
+          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(wj * a[0]),
+                       "f"(wj * a[1]), "f"(wj * a[2]), "f"(wj * a[3])
+                       : "memory");
         }
       }
     }

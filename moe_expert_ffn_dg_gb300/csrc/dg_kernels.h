@@ -117,6 +117,9 @@ struct CombineParams {
 };
 
 constexpr int kChunkTokens = 256;  // tokens per permutation chunk
+// From this many tokens on, the logits come from the register-tiled kernel
+// (64 tokens x 128 experts per block) instead of the 4-token one.
+constexpr int kRouterTileMinTokens = 1024;
 
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s);
 cudaError_t launch_router_select(const RouterParams& p, cudaStream_t s);

@@ -314,6 +314,224 @@ __global__ void __launch_bounds__(256) k_router_logits(const RouterParams p) {
   }
 }
 
+// Logits for large batches: a register-tiled product of 64 tokens x 128
+// experts per block, K in chunks of 32 staged in shared memory (router input
+// and decoded weights as fp32, K-major).  Thread (ty, tx) accumulates the
+// 4 x 8 tile tokens 4ty.., experts 8tx..; each 32-term chunk sum (sequential
+// fp32 FMAs, error <= 32 u of the chunk's sum of |terms|) is folded into an
+// error-free fp32 pair, so the logits carry the same bound as the
+// small-batch kernel.  The router weights are read once per 64 tokens and
+// the per-token work (1/rms, |x|, xd, the y_moe zeroing) once per token.
+constexpr int kRT = 64;   // tokens per block
+constexpr int kRE = 128;  // experts per block
+constexpr int kRK = 32;   // K per staged chunk
+constexpr int kXS = kRT + 4;
+constexpr int kWS = kRE + 4;
+
+template <bool U8>
+__global__ void __launch_bounds__(256, 2) k_router_logits_tile(const RouterParams p) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  float* xT = reinterpret_cast<float*>(sm);           // [2][kRK][kXS]
+  float* wT = xT + 2 * kRK * kXS;                     // [2][kRK][kWS]
+  float* rs = wT + 2 * kRK * kWS;                     // [kRT] 1/rms
+  uint16_t* sc_s = reinterpret_cast<uint16_t*>(rs + kRT);  // [H] router_scale
+  const int H = p.H, E = p.E;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int t0 = blockIdx.x * kRT, e0 = blockIdx.y * kRE;
+  const bool first_col = blockIdx.y == 0;
+  const float cH = (float)(1.0 / sqrt((double)H));
+  const int nvec = H >> 3;
+
+  for (int v = tid; v < nvec; v += 256)
+    reinterpret_cast<uint4*>(sc_s)[v] = __ldg(reinterpret_cast<const uint4*>(p.router_scale) + v);
+  __syncthreads();
+
+  // ---- per token: 1/rms (and, in the first expert column, |x|, xd, y_moe = 0)
+  for (int tl = warp; tl < kRT; tl += 8) {
+    const int t = t0 + tl;
+    if (t >= p.T) {
+      if (lane == 0) rs[tl] = 0.f;
+      continue;
+    }
+    const uint4* hrow = reinterpret_cast<const uint4*>(p.h + (size_t)t * H);
+    float ss = 0.f;
+    for (int v = lane; v < nvec; v += 32) {
+      float f[8];
+      unpack8(__ldg(hrow + v), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+    }
+    ss = warp_sum_f(ss);
+    const float msq = ss / (float)H + p.eps;
+    float rf = rsqrtf(msq);
+    rf = rf * (1.5f - 0.5f * msq * rf * rf);
+    if (lane == 0) rs[tl] = rf;
+    if (first_col) {
+      float xnl = 0.f;
+      uint4* xdrow = reinterpret_cast<uint4*>(p.xd + (size_t)t * H);
+      for (int v = lane; v < nvec; v += 32) {
+        float f[8], sc[8], wp[8];
+        unpack8(__ldg(hrow + v), f);
+        unpack8(reinterpret_cast<const uint4*>(sc_s)[v], sc);
+        unpack8(__ldg(reinterpret_cast<const uint4*>(p.w_pre_ff) + v), wp);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float x = f[i] * rf * sc[i] * cH;
+          xnl = fmaf(x, x, xnl);
+        }
+        uint4 o;
+        o.x = pack2_bf16(f[0] * rf * wp[0], f[1] * rf * wp[1]);
+        o.y = pack2_bf16(f[2] * rf * wp[2], f[3] * rf * wp[3]);
+        o.z = pack2_bf16(f[4] * rf * wp[4], f[5] * rf * wp[5]);
+        o.w = pack2_bf16(f[6] * rf * wp[6], f[7] * rf * wp[7]);
+        xdrow[v] = o;
+      }
+      const float xnd = warp_sum_f(xnl);
+      if (lane == 0) {
+        p.r_out[t] = rf;
+        p.xnorm_out[t] = sqrtf(xnd) * 1.001f;  // rounded up: used in a bound
+      }
+      float4* yr = reinterpret_cast<float4*>(p.y_moe + (size_t)t * H);
+      for (int v = lane; v < (H >> 2); v += 32) yr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  __syncthreads();
+
+  // ---- staging of one K chunk: x^ (64 tokens x 32) and decoded W (128 x 32)
+  const int xt = tid & 63, xo = tid >> 6;           // token, octet of the chunk
+  const int we = tid & 127, wh = tid >> 7;          // expert, 16-run of the chunk
+  const int e_load = e0 + we < E ? e0 + we : E - 1;
+  const bool need_norm = blockIdx.x == 0;
+  float wsq = 0.f;
+  const float rx = rs[xt];
+  const bool tok_ok = t0 + xt < p.T;
+  auto stage = [&](int buf, int k0) {
+    float* xb = xT + buf * kRK * kXS;
+    float* wb = wT + buf * kRK * kWS;
+    {
+      const int k = k0 + 8 * xo;
+      float f[8], sc[8];
+      const uint4 hv = tok_ok ? __ldg(reinterpret_cast<const uint4*>(p.h + (size_t)(t0 + xt) * H + k))
+                              : make_uint4(0u, 0u, 0u, 0u);
+      unpack8(hv, f);
+      unpack8(reinterpret_cast<const uint4*>(sc_s)[k >> 3], sc);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xb[(8 * xo + i) * kXS + xt] = f[i] * rx * sc[i] * cH;
+    }
+    {
+      const int k = k0 + 16 * wh;
+      float* wcol = wb + (16 * wh) * kWS + we;
+      if constexpr (!U8) {
+        const uint4* wrow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.wr) +
+                                                            (size_t)e_load * H + k);
+#pragma unroll
+        for (int h8 = 0; h8 < 2; ++h8) {
+          float a[8];
+          unpack8(__ldg(wrow + h8), a);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            wcol[(8 * h8 + i) * kWS] = a[i];
+            if (need_norm) wsq = fmaf(a[i], a[i], wsq);
+          }
+        }
+      } else {
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.wr) +
+                                                             (size_t)e_load * H + k));
+        const int g = k >> 6;
+        const float gs = bf16_to_f32(p.wr_scales[(size_t)e_load * (H >> 6) + g]);
+        const float gb = bf16_to_f32(p.wr_biases[(size_t)e_load * (H >> 6) + g]);
+        const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float w = fmaf(gs, (float)((wd[i >> 2] >> (8 * (i & 3))) & 0xffu), gb);
+          wcol[i * kWS] = w;
+          if (need_norm) wsq = fmaf(w, w, wsq);
+        }
+      }
+    }
+  };
+
+  // ---- tiled product
+  const int ty = tid >> 4, tx = tid & 15;
+  float hi[4][8], lo[4][8];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      hi[a][b] = 0.f;
+      lo[a][b] = 0.f;
+    }
+  const int nch = H / kRK;
+  stage(0, 0);
+  __syncthreads();
+  for (int c = 0; c < nch; ++c) {
+    const int cur = c & 1;
+    if (c + 1 < nch) stage(cur ^ 1, (c + 1) * kRK);
+    const float* xb = xT + cur * kRK * kXS;
+    const float* wb = wT + cur * kRK * kWS;
+    float2 acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[a][b] = make_float2(0.f, 0.f);
+#pragma unroll 8
+    for (int kk = 0; kk < kRK; ++kk) {
+      const float4 xa = *reinterpret_cast<const float4*>(xb + kk * kXS + 4 * ty);
+      const float4 w0 = *reinterpret_cast<const float4*>(wb + kk * kWS + 8 * tx);
+      const float4 w1 = *reinterpret_cast<const float4*>(wb + kk * kWS + 8 * tx + 4);
+      const float xs[4] = {xa.x, xa.y, xa.z, xa.w};
+      const float2 w2[4] = {make_float2(w0.x, w0.y), make_float2(w0.z, w0.w),
+                            make_float2(w1.x, w1.y), make_float2(w1.z, w1.w)};
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = __ffma2_rn(make_float2(xs[a], xs[a]), w2[b], acc[a][b]);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        df_add(hi[a][2 * b], lo[a][2 * b], acc[a][b].x);
+        df_add(hi[a][2 * b + 1], lo[a][2 * b + 1], acc[a][b].y);
+      }
+    __syncthreads();
+  }
+
+  // ---- |W_e| from the first token block; logits
+  if (need_norm) {
+    float* red = xT;  // staging buffers are free now
+    red[tid] = wsq;
+    __syncthreads();
+    if (tid < kRE && e0 + tid < E) p.wnorm_out[e0 + tid] = sqrtf(red[tid] + red[tid + kRE]) * 1.001f;
+  }
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    const int e = e0 + 8 * tx + b;
+    if (e >= E) continue;
+    const double bias = p.router_bias ? (double)p.router_bias[e] : 0.0;
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int t = t0 + 4 * ty + a;
+      if (t < p.T) p.logits[(size_t)t * E + e] = (float)(df_value(hi[a][b], lo[a][b]) + bias);
+    }
+  }
+}
+
+size_t router_tile_smem(int H) {
+  return sizeof(float) * (2 * kRK * kXS + 2 * kRK * kWS + kRT) + (size_t)H * 2;
+}
+
+template <bool U8>
+cudaError_t launch_router_tile(const RouterParams& p, cudaStream_t s) {
+  const size_t smem = router_tile_smem(p.H);
+  cudaError_t err = cudaFuncSetAttribute(k_router_logits_tile<U8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  const dim3 grid((p.T + kRT - 1) / kRT, (p.E + kRE - 1) / kRE);
+  k_router_logits_tile<U8><<<grid, 256, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
 // Exact logits: sum_i W_ei (router_scale_i h_i) with every term exact in
 // fp32 (a bf16 triple product has at most 24 significant bits; an 8-bit
 // affine weight is first split into two exact fp32 parts), summed as
@@ -747,11 +965,13 @@ cudaError_t launch_router_tb(const RouterParams& p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s) {
-  // four tokens per block give a single canvas enough blocks; eight halve
-  // the router-weight reads of large batches (when the staged input fits)
-  const bool big = p.T > 2048 && router_smem<8>(p.H) <= 160 * 1024;
-  if (p.router_u8) return big ? launch_router_tb<8, true>(p, s) : launch_router_tb<4, true>(p, s);
-  return big ? launch_router_tb<8, false>(p, s) : launch_router_tb<4, false>(p, s);
+  // four tokens per block give a single canvas enough blocks; from a few
+  // canvases on, the register-tiled kernel reads the router weights once per
+  // 64 tokens and does the per-token work once
+  if (p.T >= kRouterTileMinTokens) {
+    return p.router_u8 ? launch_router_tile<true>(p, s) : launch_router_tile<false>(p, s);
+  }
+  return p.router_u8 ? launch_router_tb<4, true>(p, s) : launch_router_tb<4, false>(p, s);
 }
 
 cudaError_t launch_router_select(const RouterParams& p, cudaStream_t s) {
