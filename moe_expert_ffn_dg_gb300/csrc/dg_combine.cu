@@ -40,6 +40,8 @@ __device__ __forceinline__ void block_sum2(float& x, float& y, float2* red) {
 template <int NPT>
 __global__ void __launch_bounds__(kThreads) k_combine(const CombineParams p) {
   __shared__ float2 red[kThreads / 32];
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x;
   const int H = p.H;
   const float* yd = p.y_dense + (size_t)t * H;
@@ -84,8 +86,7 @@ __global__ void __launch_bounds__(kThreads) k_combine(const CombineParams p) {
 
 template <int NPT>
 cudaError_t launch_npt(const CombineParams& p, cudaStream_t s) {
-  k_combine<NPT><<<p.T, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k_combine<NPT>, dim3(p.T), dim3(kThreads), 0, s, p);
 }
 
 }  // namespace

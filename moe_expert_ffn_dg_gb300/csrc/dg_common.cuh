@@ -96,6 +96,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// ------------------------------------------------------------------ PDL
+
+// Programmatic dependent launch.  Every kernel of the block lets the next one
+// in the stream launch as soon as all of its own blocks have started
+// (pdl_trigger), and waits, before it reads anything an earlier kernel wrote,
+// until its predecessor grid has completed (pdl_wait).  Because every kernel
+// waits before it can complete, completion is transitive down the chain.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {

@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
   int* s_off = s_start + kMaxGroups + 2;                                            // [E + 1]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -95,6 +96,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
     tmem_alloc(tmem_holder, C::kTmemCols);
     tmem_relinquish();
   }
+  // everything above touches only this CTA's resources; from here on the
+  // kernel reads what earlier kernels wrote
+  pdl_wait();
   if (warp >= 2) build_tile_table(p, threadIdx.x - 64, s_start, s_off);
   tc_fence_before();
   __syncthreads();
@@ -260,8 +264,7 @@ cudaError_t launch_mode_bn(const GemmParams& p, int grid, cudaStream_t s) {
   cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm<MODE, BN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
   if (err != cudaSuccess) return err;
-  k_grouped_gemm<MODE, BN><<<grid, kThreads, C::kSmem, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k_grouped_gemm<MODE, BN>, dim3(grid), dim3(kThreads), C::kSmem, s, p);
 }
 
 }  // namespace

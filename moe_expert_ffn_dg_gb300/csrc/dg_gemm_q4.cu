@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   const int slot_bytes = p.sc_slot_bytes;  // scales of one tile; biases follow
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SQ; ++s) {
@@ -236,6 +237,9 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     tmem_alloc(tmem_holder, 512);
     tmem_relinquish();
   }
+  // everything above touches only this CTA's resources; from here on the
+  // kernel reads what earlier kernels wrote
+  pdl_wait();
   if (warp >= kEpilogueWarp0) build_tile_table(p, threadIdx.x - 32 * kEpilogueWarp0, s_start, s_off);
   tc_fence_before();
   __syncthreads();
@@ -588,8 +592,7 @@ cudaError_t launch_q4(const GemmParams& p, int grid, cudaStream_t s) {
   cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm_q4<MODE, BN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  k_grouped_gemm_q4<MODE, BN><<<grid, kThreadsQ, smem, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k_grouped_gemm_q4<MODE, BN>, dim3(grid), dim3(kThreadsQ), smem, s, p);
 }
 
 }  // namespace

@@ -121,6 +121,24 @@ constexpr int kChunkTokens = 256;  // tokens per permutation chunk
 // (64 tokens x 128 experts per block) instead of the 4-token one.
 constexpr int kRouterTileMinTokens = 1024;
 
+// Launch with programmatic stream serialization (the kernel pairs
+// pdl_trigger / pdl_wait, see dg_common.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s);
 cudaError_t launch_router_select(const RouterParams& p, cudaStream_t s);
 cudaError_t launch_route_scatter(const ScatterParams& p, cudaStream_t s);

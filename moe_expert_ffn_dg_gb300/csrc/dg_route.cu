@@ -137,6 +137,8 @@ __global__ void __launch_bounds__(256) k_router_logits(const RouterParams p) {
 
   // thread (expert el, slice j); its first weight step is requested before
   // the router input is built, so the latency overlaps phase 1
+  pdl_trigger();
+  pdl_wait();
   const int el = threadIdx.x >> 3, j = threadIdx.x & 7;
   const int e_raw = blockIdx.y * kLogitExperts + el;
   const int e = e_raw < E ? e_raw : E - 1;
@@ -341,6 +343,8 @@ __global__ void __launch_bounds__(256, 2) k_router_logits_tile(const RouterParam
   const bool first_col = blockIdx.y == 0;
   const float cH = (float)(1.0 / sqrt((double)H));
   const int nvec = H >> 3;
+  pdl_trigger();
+  pdl_wait();
 
   for (int v = tid; v < nvec; v += 256)
     reinterpret_cast<uint4*>(sc_s)[v] = __ldg(reinterpret_cast<const uint4*>(p.router_scale) + v);
@@ -528,8 +532,7 @@ cudaError_t launch_router_tile(const RouterParams& p, cudaStream_t s) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const dim3 grid((p.T + kRT - 1) / kRT, (p.E + kRE - 1) / kRE);
-  k_router_logits_tile<U8><<<grid, 256, smem, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k_router_logits_tile<U8>, grid, dim3(256), smem, s, p);
 }
 
 // Exact logits: sum_i W_ei (router_scale_i h_i) with every term exact in
@@ -593,6 +596,8 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kSelTokens + warp;
   const bool valid = t < p.T;
+  pdl_trigger();
+  pdl_wait();
 
   // ---- A: selection on the fp32 logits, candidate list if near a tie
   float zl[kMaxSlots];
@@ -854,6 +859,8 @@ __global__ void __launch_bounds__(256, 1) k_route_scatter(const ScatterParams p)
   __shared__ int s_base[256];
   __shared__ unsigned s_wmask[8][256];  // per warp and expert: lanes (tokens) that chose it
   __shared__ int s_wbase[8][256];
+  pdl_trigger();
+  pdl_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int chunk = blockIdx.x, nchunks = gridDim.x;
   const int E = p.E, K = p.K, T = p.T;
@@ -908,6 +915,8 @@ __global__ void __launch_bounds__(256, 1) k_route_scatter(const ScatterParams p)
 
 // Warp per grouped row; loads of four vectors per round.
 __global__ void __launch_bounds__(256) k_gather_xe(const GatherParams p) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
   const int nvec = p.H >> 3;
@@ -958,8 +967,7 @@ cudaError_t launch_router_tb(const RouterParams& p, cudaStream_t s) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const dim3 grid((p.T + TB - 1) / TB, (p.E + kLogitExperts - 1) / kLogitExperts);
-  k_router_logits<TB, U8><<<grid, 256, smem, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k_router_logits<TB, U8>, grid, dim3(256), smem, s, p);
 }
 
 }  // namespace
@@ -976,15 +984,13 @@ cudaError_t launch_router(const RouterParams& p, cudaStream_t s) {
 
 cudaError_t launch_router_select(const RouterParams& p, cudaStream_t s) {
   const int grid = (p.T + kSelTokens - 1) / kSelTokens;
-  if (p.router_u8) k_router_select<true><<<grid, 256, 0, s>>>(p);
-  else k_router_select<false><<<grid, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return p.router_u8 ? launch_pdl(k_router_select<true>, dim3(grid), dim3(256), 0, s, p)
+                     : launch_pdl(k_router_select<false>, dim3(grid), dim3(256), 0, s, p);
 }
 
 cudaError_t launch_route_scatter(const ScatterParams& p, cudaStream_t s) {
   const int grid = (p.T + kChunkTokens - 1) / kChunkTokens;
-  k_route_scatter<<<grid, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k_route_scatter, dim3(grid), dim3(256), 0, s, p);
 }
 
 cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s) {
@@ -992,8 +998,7 @@ cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s) {
   int grid = (p.TK + rows_per_block - 1) / rows_per_block;
   grid = grid < num_sms * 8 ? grid : num_sms * 8;
   if (grid < 1) grid = 1;
-  k_gather_xe<<<grid, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k_gather_xe, dim3(grid), dim3(256), 0, s, p);
 }
 
 }  // namespace dg
