@@ -28,11 +28,6 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxSlots = 8;  // experts per lane: E <= 256
 
-__device__ __forceinline__ float warp_min_f(float v) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v = fminf(v, __shfl_xor_sync(kFull, v, o));
-  return v;
-}
 __device__ __forceinline__ float warp_max_f(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
@@ -575,7 +570,17 @@ __device__ __forceinline__ void exact_squares(const uint4& hv, float& hi, float&
 }
 
 constexpr int kSelTokens = 8;
-constexpr int kPartJobs = 64;  // jobs whose partial sums are held at once (power of 2)
+
+// Order-preserving map of a float (no NaN) to an unsigned key, and back; -0
+// and +0 compare equal as floats, so -0 is first made +0.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t b = __float_as_uint(__fadd_rn(v, 0.0f));
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 
 // Eight tokens per block, warp per token: top-k of the fp32 logits; where
 // the k-th / (k+1)-th boundary is closer than the error bound, the candidate
@@ -591,7 +596,6 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
   __shared__ int s_ncand[kSelTokens];
   __shared__ double s_zx[kSelTokens][256];
   __shared__ double s_ss[kSelTokens];
-  __shared__ float2 s_part[kPartJobs][kSelTokens];
   const int H = p.H, E = p.E, K = p.K;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kSelTokens + warp;
@@ -601,7 +605,7 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
 
   // ---- A: selection on the fp32 logits, candidate list if near a tie
   float zl[kMaxSlots];
-  uint32_t taken = 0;
+  uint32_t taken = 0, certain = 0;  // slot masks of this lane
   int ncand = 0;
   if (valid) {
     const float* z = p.logits + (size_t)t * E;
@@ -621,37 +625,58 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
         el[s] = 0.f;
       }
     }
+    // k rounds: each lane's best untaken slot (ties to the lower expert),
+    // then the warp's largest key and, among lanes holding it, the lowest
+    // expert index (two integer reductions per round)
+    uint32_t zk[kMaxSlots];
+#pragma unroll
+    for (int s = 0; s < kMaxSlots; ++s) zk[s] = order_key(zl[s]);
     for (int k = 0; k < K; ++k) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
+      uint32_t bk = 0;
+      uint32_t be = 0xffffffffu;
 #pragma unroll
       for (int s = 0; s < kMaxSlots; ++s) {
         const int e = 32 * s + lane;
-        if (e < E && !((taken >> s) & 1u) && (zl[s] > bv || (zl[s] == bv && e < be))) {
-          bv = zl[s];
-          be = e;
+        if (e < E && !((taken >> s) & 1u) && zk[s] > bk) {  // slots ascend in e
+          bk = zk[s];
+          be = (uint32_t)e;
         }
       }
-      warp_argmax(bv, be);
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      const uint32_t wk = __reduce_max_sync(kFull, bk);
+      const uint32_t we = __reduce_min_sync(kFull, bk == wk ? be : 0xffffffffu);
+      if ((int)(we & 31) == lane) taken |= 1u << (we >> 5);
     }
-    float L = INFINITY, U = -INFINITY;
+    uint32_t lk = 0xffffffffu, uk = 0u;
 #pragma unroll
     for (int s = 0; s < kMaxSlots; ++s) {
       if (32 * s + lane >= E) continue;
-      if ((taken >> s) & 1u) L = fminf(L, zl[s] - el[s]);
-      else U = fmaxf(U, zl[s] + el[s]);
+      if ((taken >> s) & 1u) lk = min(lk, order_key(zl[s] - el[s]));
+      else uk = max(uk, order_key(zl[s] + el[s]));
     }
-    L = warp_min_f(L);
-    U = warp_max_f(U);
+    const float L = key_value(__reduce_min_sync(kFull, lk));
+    const uint32_t ukw = __reduce_max_sync(kFull, uk);
+    const float U = ukw == 0u ? -INFINITY : key_value(ukw);  // 0: every expert taken
     if (!(L > U)) {
-      // candidates that may belong to the exact top-k: z + bound >= L (at
-      // least k experts have exact logits >= L, so every exact top-k member
-      // passes); listed in ascending expert order
+      // A selected expert whose lower bound is above every unselected upper
+      // bound beats every unselected expert exactly, so at most k - 1 others
+      // can beat it: it is certainly in the exact top-k.  The other m' = k - m
+      // places go to the exact top-m' of the rest.  Let L2 be the smallest
+      // lower bound of the uncertain selected experts: the m' of them have
+      // exact logits >= L2, so every member of that exact top-m' has an upper
+      // bound >= L2.  Those are the candidates (ascending expert order); they
+      // get exact logits.
+#pragma unroll
+      for (int s = 0; s < kMaxSlots; ++s)
+        if (((taken >> s) & 1u) && zl[s] - el[s] > U) certain |= 1u << s;
+      uint32_t l2k = 0xffffffffu;
+#pragma unroll
+      for (int s = 0; s < kMaxSlots; ++s)
+        if (((taken & ~certain) >> s) & 1u) l2k = min(l2k, order_key(zl[s] - el[s]));
+      const float L2 = key_value(__reduce_min_sync(kFull, l2k));
       const unsigned lt = (1u << lane) - 1u;
 #pragma unroll
       for (int s = 0; s < kMaxSlots; ++s) {
-        const bool c = 32 * s + lane < E && zl[s] + el[s] >= L;
+        const bool c = 32 * s + lane < E && !((certain >> s) & 1u) && zl[s] + el[s] >= L2;
         const unsigned ms = __ballot_sync(kFull, c);
         if (c) s_cand[warp][ncand + __popc(ms & lt)] = 32 * s + lane;
         ncand += __popc(ms);
@@ -662,7 +687,9 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
   __syncthreads();
 
   // ---- B: exact logits.  Jobs of a near-tie token: its sum of squares
-  // (c = -1), then its candidates (c = 0 .. ncand-1).
+  // (c = -1), then its candidates (c = 0 .. ncand-1).  One warp per job: the
+  // whole dot product over H, its loads issued in batches, lanes strided over
+  // the 8-element vectors, then a fixed shuffle tree.
   int njobs = 0, first[kSelTokens + 1];
 #pragma unroll
   for (int w = 0; w < kSelTokens; ++w) {
@@ -671,93 +698,74 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
   }
   first[kSelTokens] = njobs;
   if (njobs > 0) {
-    const int vs = H >> 6;  // 8-element vectors per warp slice
-    const int vbase = warp * vs;
+    const int nvec = H >> 3;
     const int ngroups = H >> 6;
     const uint4* sv = reinterpret_cast<const uint4*>(p.router_scale);
-    for (int j0 = 0; j0 < njobs; j0 += 4) {
-      int jt[4], je[4];
+    for (int job = warp; job < njobs; job += kSelTokens) {
+      int w = 0;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int job = j0 + u;
-        int w = 0;
+      for (int q = 1; q < kSelTokens; ++q)
+        if (job >= first[q]) w = q;
+      const int c = job - first[w] - 1;
+      const int e = c >= 0 ? s_cand[w][c] : -1;
+      const int tt = blockIdx.x * kSelTokens + w;
+      const uint4* hrow = reinterpret_cast<const uint4*>(p.h + (size_t)tt * H);
+      // kB independent (hi, lo) chains, one per vector of a batch
+      constexpr int kB = 4;  // vectors per lane in flight
+      float hi4[kB], lo4[kB];
 #pragma unroll
-        for (int q = 1; q < kSelTokens; ++q)
-          if (job >= first[q]) w = q;
-        const int c = job - first[w] - 1;
-        jt[u] = job < njobs ? w : -1;
-        je[u] = (job < njobs && c >= 0) ? s_cand[w][c] : -1;
+      for (int u = 0; u < kB; ++u) {
+        hi4[u] = 0.f;
+        lo4[u] = 0.f;
       }
-      float hi[4], lo[4];
+      for (int v0 = lane; v0 < nvec; v0 += 32 * kB) {
+        uint4 rh[kB], rs[kB], rw[kB];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        hi[u] = 0.f;
-        lo[u] = 0.f;
-      }
-      for (int vv = lane; vv < vs; vv += 32) {
-        const int v = vbase + vv;
-        const uint4 rs = __ldg(sv + v);
-        uint4 rh[4], rw[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (jt[u] < 0) continue;
-          const int tt = blockIdx.x * kSelTokens + jt[u];
-          rh[u] = __ldg(reinterpret_cast<const uint4*>(p.h + (size_t)tt * H) + v);
-          if (je[u] >= 0) {
-            if constexpr (!U8) {
-              rw[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.wr) +
-                                                           (size_t)je[u] * H) + v);
-            } else {
-              const uint2 q2 = __ldg(reinterpret_cast<const uint2*>(
-                                         static_cast<const uint8_t*>(p.wr) + (size_t)je[u] * H) + v);
-              rw[u] = make_uint4(q2.x, q2.y, 0u, 0u);
+        for (int u = 0; u < kB; ++u) {
+          const int v = v0 + 32 * u;
+          if (v < nvec) {
+            rh[u] = __ldg(hrow + v);
+            if (e >= 0) {
+              rs[u] = __ldg(sv + v);
+              if constexpr (!U8) {
+                rw[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.wr) +
+                                                             (size_t)e * H) + v);
+              } else {
+                const uint2 q2 = __ldg(reinterpret_cast<const uint2*>(
+                                           static_cast<const uint8_t*>(p.wr) + (size_t)e * H) + v);
+                rw[u] = make_uint4(q2.x, q2.y, 0u, 0u);
+              }
             }
           }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (jt[u] < 0) continue;
-          if (je[u] < 0) {
-            exact_squares(rh[u], hi[u], lo[u]);
+        for (int u = 0; u < kB; ++u) {
+          const int v = v0 + 32 * u;
+          if (v >= nvec) continue;
+          if (e < 0) {
+            exact_squares(rh[u], hi4[u], lo4[u]);
           } else if constexpr (!U8) {
-            exact_terms_bf16(rh[u], rs, rw[u], hi[u], lo[u]);
+            exact_terms_bf16(rh[u], rs[u], rw[u], hi4[u], lo4[u]);
           } else {
             const int gi = (8 * v) >> 6;
-            exact_terms_u8(rh[u], rs, rw[u].x, rw[u].y,
-                           bf16_to_f32(p.wr_scales[(size_t)je[u] * ngroups + gi]),
-                           bf16_to_f32(p.wr_biases[(size_t)je[u] * ngroups + gi]), hi[u], lo[u]);
+            exact_terms_u8(rh[u], rs[u], rw[u].x, rw[u].y,
+                           bf16_to_f32(p.wr_scales[(size_t)e * ngroups + gi]),
+                           bf16_to_f32(p.wr_biases[(size_t)e * ngroups + gi]), hi4[u], lo4[u]);
           }
         }
       }
+      float hi = hi4[0], lo = lo4[0];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 1; u < kB; ++u) df_add2(hi, lo, hi4[u], lo4[u]);
 #pragma unroll
-        for (int o = 16; o; o >>= 1)
-          df_add2(hi[u], lo[u], __shfl_xor_sync(kFull, hi[u], o), __shfl_xor_sync(kFull, lo[u], o));
-        if (lane == 0 && jt[u] >= 0)
-          s_part[(j0 + u) & (kPartJobs - 1)][warp] = make_float2(hi[u], lo[u]);
-      }
-      // every kPartJobs jobs (and at the end) the partials are combined
-      if (((j0 + 4) & (kPartJobs - 1)) == 0 || j0 + 4 >= njobs) {
-        __syncthreads();
-        const int jb = j0 & ~(kPartJobs - 1);
-        if ((int)threadIdx.x < kPartJobs && jb + (int)threadIdx.x < njobs) {
-          const int job = jb + threadIdx.x;
-          float sh = 0.f, sl = 0.f;
-#pragma unroll
-          for (int q = 0; q < kSelTokens; ++q)
-            df_add2(sh, sl, s_part[threadIdx.x][q].x, s_part[threadIdx.x][q].y);
-          int w = 0;
-#pragma unroll
-          for (int q = 1; q < kSelTokens; ++q)
-            if (job >= first[q]) w = q;
-          const int c = job - first[w] - 1;
-          if (c < 0) s_ss[w] = df_value(sh, sl);
-          else s_zx[w][c] = df_value(sh, sl);
-        }
-        __syncthreads();
+      for (int o = 16; o; o >>= 1)
+        df_add2(hi, lo, __shfl_xor_sync(kFull, hi, o), __shfl_xor_sync(kFull, lo, o));
+      if (lane == 0) {
+        if (c < 0) s_ss[w] = df_value(hi, lo);
+        else s_zx[w][c] = df_value(hi, lo);
       }
     }
+    __syncthreads();
     // exact logit = dot * (1/rms) * H^-1/2 + bias
     const double cHd = 1.0 / sqrt((double)H);
     for (int i = threadIdx.x; i < kSelTokens * 256; i += blockDim.x) {
@@ -775,10 +783,15 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
   // ---- C: reselection among the candidates, weights, outputs
   if (ncand > 0) {
     if (lane == 0) atomicAdd(p.n_refined, 1);
-    // candidate c = lane + 32 q is held by this lane; bit q of usedc marks it taken
-    taken = 0;
+    // candidate c = lane + 32 q is held by this lane; bit q of usedc marks it
+    // taken.  The certain experts stay; the rest of the k come from the
+    // candidates by exact logit (ties to the lower index).
+    int ncert = 0;
+#pragma unroll
+    for (int s = 0; s < kMaxSlots; ++s) ncert += __popc(__ballot_sync(kFull, (certain >> s) & 1u));
+    taken = certain;
     uint32_t usedc = 0;
-    for (int k = 0; k < K; ++k) {
+    for (int k = ncert; k < K; ++k) {
       double bv = -INFINITY;
       int be = 0x7fffffff;
 #pragma unroll
