@@ -102,13 +102,15 @@ __device__ __forceinline__ double df_value(float hi, float lo) { return (double)
 constexpr float kLogitBoundNoBias = 3.814697265625e-06f;  // 2^-18
 constexpr float kLogitBoundBias = 1.52587890625e-05f;     // 2^-16
 
-constexpr int kLogitExperts = 32;  // experts per block of k_router_logits
+constexpr int kLogitEPT = 2;                    // experts per thread of k_router_logits
+constexpr int kLogitExperts = 32 * kLogitEPT;  // experts per block of k_router_logits
 constexpr int kLogitSlices = 8;    // K slices per expert (lanes of one warp)
 
-// Logits for TB tokens x 32 experts.  Thread (expert, slice j) sums the
-// 16-element runs k = 16 (8 q + j) .. + 15 of the hidden dimension, so the
-// eight slices of an expert read one contiguous 256-byte run of its router
-// row.  The h rows of the block and the per-channel vectors are loaded into
+// Logits for TB tokens x 64 experts.  Thread (el, slice j) handles experts
+// el and el + 32 of the block's column and sums the 16-element runs
+// k = 16 (8 q + j) .. + 15 of the hidden dimension, so the eight slices of an
+// expert read one contiguous 256-byte run of its router row; every router
+// input value read from shared memory serves both experts.  The h rows of the block and the per-channel vectors are loaded into
 // shared memory in one round; the router input is built there, laid out
 // [token][slice][H/8 + 4] (the padding puts the eight slices of a warp on
 // distinct banks).  Blocks of the first expert column also write r, |x|,
@@ -134,29 +136,38 @@ __global__ void __launch_bounds__(256) k_router_logits(const RouterParams p) {
   // the router input is built, so the latency overlaps phase 1
   pdl_trigger();
   pdl_wait();
+  constexpr int EPT = kLogitEPT;
   const int el = threadIdx.x >> 3, j = threadIdx.x & 7;
-  const int e_raw = blockIdx.y * kLogitExperts + el;
-  const int e = e_raw < E ? e_raw : E - 1;
-  auto load_step = [&](int c0, uint4 (&raw)[4][2]) {
+  int ee[EPT];
+  bool evalid[EPT];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int c = c0 + 16 * q;
-      if (c < L) {
-        const int k0 = ((c >> 4) * kLogitSlices + j) * 16;  // interleaved 16-runs
+  for (int q = 0; q < EPT; ++q) {
+    const int er = blockIdx.y * kLogitExperts + el + 32 * q;
+    evalid[q] = er < E;
+    ee[q] = er < E ? er : E - 1;
+  }
+  // router weights of one 16-run for this thread's experts
+  auto load_run = [&](int c, uint4 (&raw)[EPT][2]) {
+    if (c < L) {
+      const int k0 = ((c >> 4) * kLogitSlices + j) * 16;  // interleaved 16-runs
+#pragma unroll
+      for (int q = 0; q < EPT; ++q) {
         if constexpr (!U8) {
           const uint4* wrow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.wr) +
-                                                              (size_t)e * H + k0);
+                                                              (size_t)ee[q] * H + k0);
           raw[q][0] = __ldg(wrow);
           raw[q][1] = __ldg(wrow + 1);
         } else {
           raw[q][0] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.wr) +
-                                                           (size_t)e * H + k0));
+                                                           (size_t)ee[q] * H + k0));
         }
       }
     }
   };
-  uint4 raw_next[4][2];
-  load_step(0, raw_next);
+  // two runs in flight, requested before the router input is built
+  uint4 raw_a[EPT][2], raw_b[EPT][2];
+  load_run(0, raw_a);
+  load_run(16, raw_b);
 
   // ---- phase 1: h rows and vectors in one round of loads, router input, xd
   for (int i = threadIdx.x; i < TB * nvec; i += blockDim.x) {
@@ -231,83 +242,94 @@ __global__ void __launch_bounds__(256) k_router_logits(const RouterParams p) {
 
   // ---- phase 2: 16-term chunk sums (two 8-term fp32x2 halves, even and odd
   // elements), accumulated over the slice as error-free fp32 pairs; the
-  // eight slices of an expert are then summed with shuffles.  Weights of the
-  // next step are loaded while the current step computes.
-  float acc_hi[TB], acc_lo[TB];
+  // eight slices of an expert are then summed with shuffles.  Weights two
+  // runs ahead are loaded while the current run computes.
+  float acc_hi[EPT][TB], acc_lo[EPT][TB];
+  float2 wsq2[EPT];
 #pragma unroll
-  for (int t = 0; t < TB; ++t) {
-    acc_hi[t] = 0.f;
-    acc_lo[t] = 0.f;
-  }
-  float2 wsq2 = make_float2(0.f, 0.f);
-  const bool need_norm = blockIdx.x == 0;
-  for (int c0 = 0; c0 < L; c0 += 64) {
-    uint4 raw[4][2];
+  for (int q = 0; q < EPT; ++q) {
+    wsq2[q] = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      raw[q][0] = raw_next[q][0];
-      raw[q][1] = raw_next[q][1];
+    for (int t = 0; t < TB; ++t) {
+      acc_hi[q][t] = 0.f;
+      acc_lo[q][t] = 0.f;
     }
-    if (c0 + 64 < L) load_step(c0 + 64, raw_next);
+  }
+  const bool need_norm = blockIdx.x == 0;
+  for (int c = 0; c < L; c += 16) {
+    const int k0 = ((c >> 4) * kLogitSlices + j) * 16;
+    float2 w2[EPT][8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int c = c0 + 16 * q;
-      if (c >= L) break;
-      const int k0 = ((c >> 4) * kLogitSlices + j) * 16;
-      float2 w2[8];
+    for (int q = 0; q < EPT; ++q) {
       if constexpr (!U8) {
-        const uint32_t wd[8] = {raw[q][0].x, raw[q][0].y, raw[q][0].z, raw[q][0].w,
-                                raw[q][1].x, raw[q][1].y, raw[q][1].z, raw[q][1].w};
+        const uint32_t wd[8] = {raw_a[q][0].x, raw_a[q][0].y, raw_a[q][0].z, raw_a[q][0].w,
+                                raw_a[q][1].x, raw_a[q][1].y, raw_a[q][1].z, raw_a[q][1].w};
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          w2[i] = make_float2(__uint_as_float(wd[i] << 16), __uint_as_float(wd[i] & 0xffff0000u));
+          w2[q][i] = make_float2(__uint_as_float(wd[i] << 16), __uint_as_float(wd[i] & 0xffff0000u));
       } else {
         // a 16-run never straddles a 64-group (16 | k0)
-        const float gs = bf16_to_f32(p.wr_scales[(size_t)e * ngroups + (k0 >> 6)]);
-        const float gb = bf16_to_f32(p.wr_biases[(size_t)e * ngroups + (k0 >> 6)]);
-        const uint32_t wd[4] = {raw[q][0].x, raw[q][0].y, raw[q][0].z, raw[q][0].w};
+        const float gs = bf16_to_f32(p.wr_scales[(size_t)ee[q] * ngroups + (k0 >> 6)]);
+        const float gb = bf16_to_f32(p.wr_biases[(size_t)ee[q] * ngroups + (k0 >> 6)]);
+        const uint32_t wd[4] = {raw_a[q][0].x, raw_a[q][0].y, raw_a[q][0].z, raw_a[q][0].w};
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          w2[i] = make_float2(fmaf(gs, (float)((wd[i >> 1] >> (16 * (i & 1))) & 0xffu), gb),
-                              fmaf(gs, (float)((wd[i >> 1] >> (16 * (i & 1) + 8)) & 0xffu), gb));
+          w2[q][i] = make_float2(fmaf(gs, (float)((wd[i >> 1] >> (16 * (i & 1))) & 0xffu), gb),
+                                 fmaf(gs, (float)((wd[i >> 1] >> (16 * (i & 1) + 8)) & 0xffu), gb));
       }
       if (need_norm) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) wsq2 = __ffma2_rn(w2[i], w2[i], wsq2);
+        for (int i = 0; i < 8; ++i) wsq2[q] = __ffma2_rn(w2[q][i], w2[q][i], wsq2[q]);
       }
+    }
 #pragma unroll
-      for (int t = 0; t < TB; ++t) {
-        const float4* xv =
-            reinterpret_cast<const float4*>(xs + ((size_t)t * kLogitSlices + j) * LS + c);
+    for (int q = 0; q < EPT; ++q) {
+      raw_a[q][0] = raw_b[q][0];
+      raw_a[q][1] = raw_b[q][1];
+    }
+    load_run(c + 32, raw_b);
+#pragma unroll
+    for (int t = 0; t < TB; ++t) {
+      const float4* xv =
+          reinterpret_cast<const float4*>(xs + ((size_t)t * kLogitSlices + j) * LS + c);
+      float4 xa[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) xa[r] = xv[r];
+#pragma unroll
+      for (int q = 0; q < EPT; ++q) {
         float2 a2 = make_float2(0.f, 0.f), b2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          const float4 a = xv[r];
-          a2 = __ffma2_rn(w2[2 * r], make_float2(a.x, a.y), a2);
-          b2 = __ffma2_rn(w2[2 * r + 1], make_float2(a.z, a.w), b2);
+          a2 = __ffma2_rn(w2[q][2 * r], make_float2(xa[r].x, xa[r].y), a2);
+          b2 = __ffma2_rn(w2[q][2 * r + 1], make_float2(xa[r].z, xa[r].w), b2);
         }
-        df_add(acc_hi[t], acc_lo[t], __fadd_rn(__fadd_rn(a2.x, a2.y), __fadd_rn(b2.x, b2.y)));
+        df_add(acc_hi[q][t], acc_lo[q][t],
+               __fadd_rn(__fadd_rn(a2.x, a2.y), __fadd_rn(b2.x, b2.y)));
       }
     }
   }
-  float wsq = wsq2.x + wsq2.y;
 #pragma unroll
-  for (int o = 1; o < kLogitSlices; o <<= 1) {
-    wsq += __shfl_xor_sync(kFull, wsq, o);
+  for (int q = 0; q < EPT; ++q) {
+    float wsq = wsq2[q].x + wsq2[q].y;
 #pragma unroll
-    for (int t = 0; t < TB; ++t) {
-      const float h2 = __shfl_xor_sync(kFull, acc_hi[t], o);
-      const float l2 = __shfl_xor_sync(kFull, acc_lo[t], o);
-      df_add2(acc_hi[t], acc_lo[t], h2, l2);
+    for (int o = 1; o < kLogitSlices; o <<= 1) {
+      wsq += __shfl_xor_sync(kFull, wsq, o);
+#pragma unroll
+      for (int t = 0; t < TB; ++t) {
+        const float h2 = __shfl_xor_sync(kFull, acc_hi[q][t], o);
+        const float l2 = __shfl_xor_sync(kFull, acc_lo[q][t], o);
+        df_add2(acc_hi[q][t], acc_lo[q][t], h2, l2);
+      }
     }
-  }
-  if (j == 0 && e_raw < E) {
-    const double bias = p.router_bias ? (double)p.router_bias[e] : 0.0;
+    if (j == 0 && evalid[q]) {
+      const int e = ee[q];
+      const double bias = p.router_bias ? (double)p.router_bias[e] : 0.0;
 #pragma unroll
-    for (int t = 0; t < TB; ++t)
-      if (t0 + t < p.T)
-        p.logits[(size_t)(t0 + t) * E + e] = (float)(df_value(acc_hi[t], acc_lo[t]) + bias);
-    if (need_norm) p.wnorm_out[e] = sqrtf(wsq) * 1.001f;  // rounded up: a bound
+      for (int t = 0; t < TB; ++t)
+        if (t0 + t < p.T)
+          p.logits[(size_t)(t0 + t) * E + e] = (float)(df_value(acc_hi[q][t], acc_lo[q][t]) + bias);
+      if (need_norm) p.wnorm_out[e] = sqrtf(wsq) * 1.001f;  // rounded up: a bound
+    }
   }
 }
 
