@@ -358,6 +358,7 @@ def run_ours(args):
     import moe_expert_ffn_dg_gb300 as pkg
     import moe_inputs as mi
     from moe_expert_ffn_dg_gb300 import binding as B
+    from moe_expert_ffn_dg_gb300 import replicas
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -374,7 +375,7 @@ def run_ours(args):
     wl = mi.get_workload(args.workload)
     p = mi.make_layer_inputs(wl)
     # each replica processes its own canvas (data parallel over canvases)
-    h_np = mi.make_tokens(mi.get_workload(args.workload, seed=wl.seed + 1000 * rank)) if rank else mi.make_tokens(wl)
+    h_np = mi.make_tokens(mi.get_workload(args.workload, seed=replicas.replica_seed(wl.seed, rank)))
     blk = pkg.MoEBlock.from_params(p, hidden=wl.hidden, n_experts=wl.n_experts, top_k=wl.top_k,
                                    expert_inter=wl.expert_inter, dense_inter=wl.dense_inter,
                                    max_tokens=wl.tokens, device=dev)
@@ -417,11 +418,7 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     B.dg_moe_set_profile_events(blk.handle, None)
     clk = clocks.stop()
-    elapsed_ms = start.elapsed_time(stop)
-    if dist:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = replicas.max_over_ranks(start.elapsed_time(stop), dist, dev)
     st = blk.device_status()
     if st[0] != 0:
         raise RuntimeError(f"device status after timing: {st}")
@@ -450,7 +447,7 @@ def run_ours(args):
     hbm, bf16_burst, bf16_sus, src = peaks()
 
     ms = elapsed_ms / args.steps
-    value = world * wl.tokens / (ms / 1000.0)
+    value = replicas.aggregate_throughput(world, wl.tokens, ms / 1000.0)
     gu = names.index("gemm_gate_up")
     gu_s = per_kernel_us[gu] * 1e-6
     achieved = alg["gate_up_bytes"] / gu_s / 1e9
