@@ -373,9 +373,12 @@ def run_ours(args):
     pkg.load_library()
 
     wl = mi.get_workload(args.workload)
+    if args.tokens:
+        wl = mi.get_workload(args.workload, tokens=args.tokens)
     p = mi.make_layer_inputs(wl)
     # each replica processes its own canvas (data parallel over canvases)
-    h_np = mi.make_tokens(mi.get_workload(args.workload, seed=replicas.replica_seed(wl.seed, rank)))
+    h_np = mi.make_tokens(mi.get_workload(args.workload, seed=replicas.replica_seed(wl.seed, rank),
+                                          tokens=wl.tokens))
     blk = pkg.MoEBlock.from_params(p, hidden=wl.hidden, n_experts=wl.n_experts, top_k=wl.top_k,
                                    expert_inter=wl.expert_inter, dense_inter=wl.dense_inter,
                                    max_tokens=wl.tokens, device=dev)
@@ -494,6 +497,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="token count of a one-layer workload (default: the workload's own)")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["canvas256", "canvas256_q4", "batch2048_zipf", "stack30_q4"])
     args = ap.parse_args()

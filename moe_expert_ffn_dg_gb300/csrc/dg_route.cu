@@ -333,22 +333,24 @@ __global__ void __launch_bounds__(256) k_router_logits(const RouterParams p) {
   }
 }
 
-// Logits for large batches: a register-tiled product of 64 tokens x 128
+// Logits for large batches: a register-tiled product of 64 tokens x 64
 // experts per block, K in chunks of 32 staged in shared memory (router input
 // and decoded weights as fp32, K-major).  Thread (ty, tx) accumulates the
-// 4 x 8 tile tokens 4ty.., experts 8tx..; each 32-term chunk sum (sequential
+// 4 x 4 tile tokens 4ty.., experts 4tx..; each 32-term chunk sum (sequential
 // fp32 FMAs, error <= 32 u of the chunk's sum of |terms|) is folded into an
 // error-free fp32 pair, so the logits carry the same bound as the
-// small-batch kernel.  The router weights are read once per 64 tokens and
-// the per-token work (1/rms, |x|, xd, the y_moe zeroing) once per token.
+// small-batch kernel.  The raw inputs of the next chunk are loaded into
+// registers while the current chunk computes.  The router weights are read
+// once per 64 tokens; the per-token work (1/rms, and in the first expert
+// column |x|, xd and the y_moe zeroing) once per token and column.
 constexpr int kRT = 64;   // tokens per block
-constexpr int kRE = 128;  // experts per block
+constexpr int kRE = 64;   // experts per block
 constexpr int kRK = 32;   // K per staged chunk
 constexpr int kXS = kRT + 4;
 constexpr int kWS = kRE + 4;
 
 template <bool U8>
-__global__ void __launch_bounds__(256, 2) k_router_logits_tile(const RouterParams p) {
+__global__ void __launch_bounds__(256, 3) k_router_logits_tile(const RouterParams p) {
   extern __shared__ __align__(16) uint8_t sm[];
   float* xT = reinterpret_cast<float*>(sm);           // [2][kRK][kXS]
   float* wT = xT + 2 * kRK * kXS;                     // [2][kRK][kWS]
@@ -418,103 +420,102 @@ __global__ void __launch_bounds__(256, 2) k_router_logits_tile(const RouterParam
   }
   __syncthreads();
 
-  // ---- staging of one K chunk: x^ (64 tokens x 32) and decoded W (128 x 32)
-  const int xt = tid & 63, xo = tid >> 6;           // token, octet of the chunk
-  const int we = tid & 127, wh = tid >> 7;          // expert, 16-run of the chunk
+  // ---- staging: thread (row, octet) moves 8 K values of token row xt and of
+  // expert row we; the raw values of the next chunk wait in registers
+  const int xt = tid & 63, oc = tid >> 6;
+  const int we = tid & 63;
   const int e_load = e0 + we < E ? e0 + we : E - 1;
   const bool need_norm = blockIdx.x == 0;
-  float wsq = 0.f;
-  const float rx = rs[xt];
   const bool tok_ok = t0 + xt < p.T;
-  auto stage = [&](int buf, int k0) {
-    float* xb = xT + buf * kRK * kXS;
-    float* wb = wT + buf * kRK * kWS;
-    {
-      const int k = k0 + 8 * xo;
-      float f[8], sc[8];
-      const uint4 hv = tok_ok ? __ldg(reinterpret_cast<const uint4*>(p.h + (size_t)(t0 + xt) * H + k))
-                              : make_uint4(0u, 0u, 0u, 0u);
-      unpack8(hv, f);
-      unpack8(reinterpret_cast<const uint4*>(sc_s)[k >> 3], sc);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) xb[(8 * xo + i) * kXS + xt] = f[i] * rx * sc[i] * cH;
+  const float rx = rs[xt];
+  float wsq = 0.f;
+  uint4 hv;   // next chunk: 8 h values of token xt
+  uint4 wv;   // next chunk: 8 router weights of expert we (bf16, or 8 codes in .x/.y)
+  auto fetch = [&](int k0) {
+    const int k = k0 + 8 * oc;
+    hv = tok_ok ? __ldg(reinterpret_cast<const uint4*>(p.h + (size_t)(t0 + xt) * H + k))
+                : make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (!U8) {
+      wv = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.wr) +
+                                                (size_t)e_load * H + k));
+    } else {
+      const uint2 q2 = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(p.wr) +
+                                                            (size_t)e_load * H + k));
+      wv = make_uint4(q2.x, q2.y, 0u, 0u);
     }
-    {
-      const int k = k0 + 16 * wh;
-      float* wcol = wb + (16 * wh) * kWS + we;
-      if constexpr (!U8) {
-        const uint4* wrow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.wr) +
-                                                            (size_t)e_load * H + k);
+  };
+  auto store = [&](int buf, int k0) {
+    const int k = k0 + 8 * oc;
+    float* xb = xT + buf * kRK * kXS + (8 * oc) * kXS + xt;
+    float* wb = wT + buf * kRK * kWS + (8 * oc) * kWS + we;
+    float f[8], sc[8];
+    unpack8(hv, f);
+    unpack8(reinterpret_cast<const uint4*>(sc_s)[k >> 3], sc);
 #pragma unroll
-        for (int h8 = 0; h8 < 2; ++h8) {
-          float a[8];
-          unpack8(__ldg(wrow + h8), a);
+    for (int i = 0; i < 8; ++i) xb[i * kXS] = f[i] * rx * sc[i] * cH;
+    float w[8];
+    if constexpr (!U8) {
+      unpack8(wv, w);
+    } else {
+      const int g = k >> 6;
+      const float gs = bf16_to_f32(p.wr_scales[(size_t)e_load * (H >> 6) + g]);
+      const float gb = bf16_to_f32(p.wr_biases[(size_t)e_load * (H >> 6) + g]);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            wcol[(8 * h8 + i) * kWS] = a[i];
-            if (need_norm) wsq = fmaf(a[i], a[i], wsq);
-          }
-        }
-      } else {
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.wr) +
-                                                             (size_t)e_load * H + k));
-        const int g = k >> 6;
-        const float gs = bf16_to_f32(p.wr_scales[(size_t)e_load * (H >> 6) + g]);
-        const float gb = bf16_to_f32(p.wr_biases[(size_t)e_load * (H >> 6) + g]);
-        const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+      for (int i = 0; i < 8; ++i)
+        w[i] = fmaf(gs, (float)((((i < 4) ? wv.x : wv.y) >> (8 * (i & 3))) & 0xffu), gb);
+    }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float w = fmaf(gs, (float)((wd[i >> 2] >> (8 * (i & 3))) & 0xffu), gb);
-          wcol[i * kWS] = w;
-          if (need_norm) wsq = fmaf(w, w, wsq);
-        }
-      }
+    for (int i = 0; i < 8; ++i) {
+      wb[i * kWS] = w[i];
+      if (need_norm) wsq = fmaf(w[i], w[i], wsq);
     }
   };
 
   // ---- tiled product
   const int ty = tid >> 4, tx = tid & 15;
-  float hi[4][8], lo[4][8];
+  float hi[4][4], lo[4][4];
 #pragma unroll
   for (int a = 0; a < 4; ++a)
 #pragma unroll
-    for (int b = 0; b < 8; ++b) {
+    for (int b = 0; b < 4; ++b) {
       hi[a][b] = 0.f;
       lo[a][b] = 0.f;
     }
   const int nch = H / kRK;
-  stage(0, 0);
+  fetch(0);
+  store(0, 0);
   __syncthreads();
   for (int c = 0; c < nch; ++c) {
     const int cur = c & 1;
-    if (c + 1 < nch) stage(cur ^ 1, (c + 1) * kRK);
-    const float* xb = xT + cur * kRK * kXS;
-    const float* wb = wT + cur * kRK * kWS;
-    float2 acc[4][4];
+    if (c + 1 < nch) fetch((c + 1) * kRK);
+    const float* xb = xT + cur * kRK * kXS + 4 * ty;
+    const float* wb = wT + cur * kRK * kWS + 4 * tx;
+    float2 acc[4][2];
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) acc[a][b] = make_float2(0.f, 0.f);
+    for (int a = 0; a < 4; ++a) {
+      acc[a][0] = make_float2(0.f, 0.f);
+      acc[a][1] = make_float2(0.f, 0.f);
+    }
 #pragma unroll 8
     for (int kk = 0; kk < kRK; ++kk) {
-      const float4 xa = *reinterpret_cast<const float4*>(xb + kk * kXS + 4 * ty);
-      const float4 w0 = *reinterpret_cast<const float4*>(wb + kk * kWS + 8 * tx);
-      const float4 w1 = *reinterpret_cast<const float4*>(wb + kk * kWS + 8 * tx + 4);
+      const float4 xa = *reinterpret_cast<const float4*>(xb + kk * kXS);
+      const float4 w4 = *reinterpret_cast<const float4*>(wb + kk * kWS);
       const float xs[4] = {xa.x, xa.y, xa.z, xa.w};
-      const float2 w2[4] = {make_float2(w0.x, w0.y), make_float2(w0.z, w0.w),
-                            make_float2(w1.x, w1.y), make_float2(w1.z, w1.w)};
+      const float2 w01 = make_float2(w4.x, w4.y), w23 = make_float2(w4.z, w4.w);
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) acc[a][b] = __ffma2_rn(make_float2(xs[a], xs[a]), w2[b], acc[a][b]);
+      for (int a = 0; a < 4; ++a) {
+        acc[a][0] = __ffma2_rn(make_float2(xs[a], xs[a]), w01, acc[a][0]);
+        acc[a][1] = __ffma2_rn(make_float2(xs[a], xs[a]), w23, acc[a][1]);
+      }
     }
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        df_add(hi[a][2 * b], lo[a][2 * b], acc[a][b].x);
-        df_add(hi[a][2 * b + 1], lo[a][2 * b + 1], acc[a][b].y);
-      }
+    for (int a = 0; a < 4; ++a) {
+      df_add(hi[a][0], lo[a][0], acc[a][0].x);
+      df_add(hi[a][1], lo[a][1], acc[a][0].y);
+      df_add(hi[a][2], lo[a][2], acc[a][1].x);
+      df_add(hi[a][3], lo[a][3], acc[a][1].y);
+    }
+    if (c + 1 < nch) store(cur ^ 1, (c + 1) * kRK);
     __syncthreads();
   }
 
@@ -523,11 +524,13 @@ __global__ void __launch_bounds__(256, 2) k_router_logits_tile(const RouterParam
     float* red = xT;  // staging buffers are free now
     red[tid] = wsq;
     __syncthreads();
-    if (tid < kRE && e0 + tid < E) p.wnorm_out[e0 + tid] = sqrtf(red[tid] + red[tid + kRE]) * 1.001f;
+    if (tid < kRE && e0 + tid < E)
+      p.wnorm_out[e0 + tid] =
+          sqrtf(red[tid] + red[tid + 64] + red[tid + 128] + red[tid + 192]) * 1.001f;
   }
 #pragma unroll
-  for (int b = 0; b < 8; ++b) {
-    const int e = e0 + 8 * tx + b;
+  for (int b = 0; b < 4; ++b) {
+    const int e = e0 + 4 * tx + b;
     if (e >= E) continue;
     const double bias = p.router_bias ? (double)p.router_bias[e] : 0.0;
 #pragma unroll

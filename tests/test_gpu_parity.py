@@ -41,7 +41,7 @@ def test_tiny_workload(randvec):
     run_and_check(wl, p, mi.make_tokens(wl))
 
 
-@pytest.mark.parametrize("T", [1, 7, 17, 31, 300, 1100])
+@pytest.mark.parametrize("T", [1, 7, 17, 31, 300, 1100, 4100])
 def test_tiny_ragged_token_counts(T):
     wl = mi.get_workload("tiny")
     p = mi.make_layer_inputs(wl, randvec=True)
