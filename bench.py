@@ -75,7 +75,7 @@ def gate_up_traffic():
     rec = json.load(open(path))
     csrc = os.path.join(ROOT, "moe_expert_ffn_dg_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("dg_gemm.cu", "dg_common.cuh", "dg_kernels.h"):
+    for f in rec.get("hashed_sources", ["dg_gemm.cu", "dg_common.cuh", "dg_kernels.h"]):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return rec["dram_bytes_per_launch"] if h.hexdigest()[:16] == rec["gemm_source_sha256_16"] else None
 
