@@ -48,6 +48,8 @@ __all__ = [
     "make_layer_inputs",
     "make_tokens",
     "zipf_router_bias",
+    "SC_WORKLOADS",
+    "make_sc_inputs",
 ]
 
 BF16_ONE = np.uint16(0x3F80)
@@ -96,8 +98,20 @@ WORKLOADS = {
 }
 
 
+# The self-conditioning MLP (dense-FFN shapes, before layer 0) over one
+# canvas: the soft signal and the token embeddings drawn N(0, 1).
+SC_WORKLOADS = {
+    "sc_tiny": Workload("sc_tiny", 32, 256, 1, 1, 64, 128, seed=6,
+                        weight_std=0.02, router_std=0.02),
+    "sc_canvas256": Workload("sc_canvas256", 256, 2816, 1, 1, 704, 2112, seed=5,
+                             weight_std=0.02, router_std=0.02),
+    "sc_canvas256_q4": Workload("sc_canvas256_q4", 256, 2816, 1, 1, 704, 2112, seed=5,
+                                weight_std=0.02, router_std=0.02, quant=(4, 4, 8)),
+}
+
+
 def get_workload(name: str, **overrides) -> Workload:
-    w = WORKLOADS[name]
+    w = WORKLOADS[name] if name in WORKLOADS else SC_WORKLOADS[name]
     return dataclasses.replace(w, **overrides) if overrides else w
 
 
@@ -251,3 +265,33 @@ def make_layer_inputs(wl: Workload, layer: int = 0, randvec: bool = False,
         for n in ("dense_gate", "dense_up", "dense_down"):
             p[n] = quantize_affine(p[n], db)
     return p
+
+
+def make_sc_inputs(wl: Workload, randvec: bool = False, quantise: Optional[bool] = None,
+                   tokens: Optional[int] = None) -> dict:
+    """Draws of the self-conditioning MLP: token embeddings and soft signal
+    [T, H] (N(0, 1), bf16 bits), gate and up [D, H], down [H, D] (N(0, std)),
+    and the pre_norm vector (ones, or U(0.5, 1.5) with randvec).  Seeding:
+    SeedSequence(seed).spawn(2): child 0 the activations (embeddings, then
+    signal), child 1 the weights (gate, up, down).  With quantise (default: the
+    workload's own), gate/up/down in the group-64 affine format at the
+    workload's dense bits."""
+    T = wl.tokens if tokens is None else tokens
+    H, D = wl.hidden, wl.dense_inter
+    ca, cw = np.random.SeedSequence(wl.seed).spawn(2)
+    ra, rw = np.random.default_rng(ca), np.random.default_rng(cw)
+    out = {"embeds": _normal_bf16(ra, (T, H), 1.0), "signal": _normal_bf16(ra, (T, H), 1.0)}
+    out["gate"] = _normal_bf16(rw, (D, H), wl.weight_std)
+    out["up"] = _normal_bf16(rw, (D, H), wl.weight_std)
+    out["down"] = _normal_bf16(rw, (H, D), wl.weight_std)
+    if randvec:
+        r = np.random.default_rng(wl.seed + 100)
+        out["pre_norm"] = f32_to_bf16_bits(r.uniform(0.5, 1.5, H).astype(np.float32))
+    else:
+        out["pre_norm"] = np.full(H, BF16_ONE, dtype=np.uint16)
+    do_q = wl.quantised if quantise is None else quantise
+    if do_q:
+        bits = wl.quant[1] if wl.quant is not None else 4
+        for n in ("gate", "up", "down"):
+            out[n] = quantize_affine(out[n], bits)
+    return out

@@ -57,7 +57,7 @@ __all__ = [
     "gelu_tanh",
     "router_logits", "select_topk", "routing_weights", "route",
     "geglu_mlp", "experts_forward", "dense_forward", "combine",
-    "permutation", "moe_block_forward",
+    "permutation", "moe_block_forward", "sc_mlp_forward",
 ]
 
 
@@ -287,3 +287,20 @@ def moe_block_forward(h_bits, p: dict, top_k: int, inter: int,
         E = Wr.shape[0]
         res["offsets"], res["perm"] = permutation(idx, E)
     return res
+
+
+def sc_mlp_forward(embeds_bits, signal_bits, p: dict, bf16_weights: bool = False) -> np.ndarray:
+    """The self-conditioning MLP on a canvas: the soft signal (previous-step
+    probabilities times the embedding table) through a pre-normed GEGLU MLP of
+    the dense FFN's shape, added to the token embeddings, then RMS-normalised
+    without a weight ("DiffusionGemma port — plan & parity strategy",
+    Reference dossier §3 Self-conditioning; "diffgemma — architecture &
+    implemented contract", Part II §2.1 SC injection; "DiffusionGemma
+    Explained", MLP with conditioning_mlp).  p: gate, up, down weights and the
+    pre_norm vector; inputs bf16 bits [T, H]."""
+    x = bf16_to_f64(embeds_bits)
+    sig = bf16_to_f64(signal_bits)
+    normed = rms_norm(sig, to_f64(p["pre_norm"]))
+    sc = geglu_mlp(normed, decoded(p["gate"], bf16_weights), decoded(p["up"], bf16_weights),
+                   decoded(p["down"], bf16_weights))
+    return rms_norm(x + sc)

@@ -497,3 +497,46 @@ def test_bf16_activation_variant_rounds_only_the_activations():
     np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-14)
     y0 = o.experts_forward(x, idx, w, gu, dn, I)
     assert 1e-4 < np.abs(y - y0).max() / np.abs(y0).max() < 2e-2
+
+
+# ---------------------------------------------------------------- self-conditioning MLP
+
+def test_sc_zero_signal_is_the_weightless_norm_of_the_embeddings():
+    # the MLP maps 0 to 0 ("DiffusionGemma Explained": relevant for the
+    # self-conditioning MLP on the first decode step), so only the post-norm
+    # of the embeddings remains; checked against torch's RMSNorm routine
+    import torch
+    wl = mi.get_workload("sc_tiny")
+    p = mi.make_sc_inputs(wl, randvec=True)
+    zero = np.zeros_like(p["signal"])
+    got = o.sc_mlp_forward(p["embeds"], zero, p)
+    x = torch.from_numpy(o.bf16_to_f64(p["embeds"]))
+    want = torch.nn.functional.rms_norm(x, (x.shape[-1],), eps=1e-6).numpy()
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_sc_composition_prenorm_signal_residual_then_weightless_postnorm():
+    # structure of the pages' listing: RMSNorm_w on the signal, GEGLU MLP,
+    # add to the embeddings, RMSNorm without weight; torch ops as the reference
+    import torch
+    wl = mi.get_workload("sc_tiny")
+    p = mi.make_sc_inputs(wl, randvec=True)
+    got = o.sc_mlp_forward(p["embeds"], p["signal"], p)
+    t = lambda a: torch.from_numpy(o.bf16_to_f64(a))
+    H = wl.hidden
+    n = torch.nn.functional.rms_norm(t(p["signal"]), (H,), weight=t(p["pre_norm"]), eps=1e-6)
+    g = torch.nn.functional.gelu(n @ t(p["gate"]).T, approximate="tanh")
+    s = (g * (n @ t(p["up"]).T)) @ t(p["down"]).T
+    want = torch.nn.functional.rms_norm(t(p["embeds"]) + s, (H,), eps=1e-6).numpy()
+    np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-10)
+    # every output row has unit RMS up to eps
+    assert np.all(np.abs(np.sqrt((got ** 2).mean(1)) - 1) < 1e-5)
+
+
+def test_sc_permuting_tokens_permutes_outputs():
+    wl = mi.get_workload("sc_tiny")
+    p = mi.make_sc_inputs(wl)
+    pi = np.random.default_rng(9).permutation(wl.tokens)
+    a = o.sc_mlp_forward(p["embeds"], p["signal"], p)
+    b = o.sc_mlp_forward(p["embeds"][pi], p["signal"][pi], p)
+    np.testing.assert_array_equal(a[pi], b)
