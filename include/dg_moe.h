@@ -222,6 +222,65 @@ dg_status_t dg_moe_route_noalloc(const dg_moe_config_t* cfg, const dg_moe_weight
                                  const void* h_in, int n_tokens, int32_t* idx_out, float* w_out,
                                  dg_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Self-conditioning MLP (before layer 0 of a decode step):
+ *
+ *   x   = rms(signal) * pre_norm                        (bf16)
+ *   s   = down(gelu_tanh(gate x) * up x)                dense-FFN shapes
+ *   out = (embeds + s) / sqrt(mean((embeds + s)^2) + eps)   (bf16, no weight)
+ *
+ * "DiffusionGemma port — plan & parity strategy", Reference dossier §3
+ * (SelfConditioning: pre_norm, gate/up/down, post_norm = RMSNormNoScale);
+ * "diffgemma — architecture & implemented contract", Part II §2.1 (SC
+ * injection) and Part I §4 (SC MLP, q8/4-bit gate/up/down);
+ * "DiffusionGemma Explained", MLP (conditioning_mlp) and the note that the
+ * MLP maps 0 to 0 on the first decode step.  The signal is the soft
+ * embedding of the previous step (probabilities times the embedding table
+ * times sqrt(hidden)), computed by the caller.
+ * Runs on the same grouped GEMM kernels as the dense branch of the block.
+ * ------------------------------------------------------------------------ */
+typedef struct dg_sc_mlp dg_sc_mlp_t;
+
+typedef struct {
+  int hidden;         /* H, multiple of 128 */
+  int inter;          /* gate/up rows, multiple of 64 */
+  int max_tokens;     /* largest n_tokens of a forward */
+  dg_format_t fmt;    /* gate, up, down: DG_FMT_BF16 or DG_FMT_AFFINE_U4_G64 */
+  float rms_eps;      /* 0 means 1e-6 */
+  unsigned flags;     /* must be 0 */
+} dg_sc_mlp_config_t;
+
+typedef struct {
+  dg_qtensor_t gate;     /* [inter, H] */
+  dg_qtensor_t up;       /* [inter, H] */
+  dg_qtensor_t down;     /* [H, inter] */
+  const void* pre_norm;  /* bf16 [H] */
+} dg_sc_mlp_weights_t;
+
+/* Bytes of workspace a handle of this configuration needs. */
+dg_status_t dg_sc_mlp_workspace_size(const dg_sc_mlp_config_t* cfg, size_t* bytes);
+
+/* Create a handle: validates the configuration and the weights (device
+ * pointers, 16-byte aligned; borrowed), lays out the caller's workspace
+ * (1024-byte aligned, at least dg_sc_mlp_workspace_size bytes) and builds
+ * the TMA descriptors.  Allocates no device memory. */
+dg_status_t dg_sc_mlp_create(const dg_sc_mlp_config_t* cfg, const dg_sc_mlp_weights_t* weights,
+                             void* workspace, size_t workspace_bytes, dg_sc_mlp_t** out);
+
+/* out = the self-conditioning MLP of (embeds, signal), all bf16 [n_tokens, H]
+ * device tensors, 16-byte aligned; out may alias embeds or signal.  n_tokens
+ * in [0, max_tokens]; asynchronous on `stream`.  Device-side failures are
+ * read with dg_sc_mlp_last_device_status. */
+dg_status_t dg_sc_mlp_forward(dg_sc_mlp_t* m, const void* embeds, const void* signal, void* out,
+                              int n_tokens, dg_stream_t stream);
+
+/* Synchronise `stream`, read and clear the handle's device status word
+ * (DG_OK, DG_ERR_TIMEOUT or DG_ERR_DEVICE_CHECK). */
+dg_status_t dg_sc_mlp_last_device_status(dg_sc_mlp_t* m, dg_stream_t stream);
+
+/* Free the handle (NULL is accepted). */
+dg_status_t dg_sc_mlp_destroy(dg_sc_mlp_t* m);
+
 /* Static string for a status code. */
 const char* dg_moe_status_string(dg_status_t s);
 

@@ -13,7 +13,7 @@ from .binding import DgError, load_library  # noqa: F401
 
 def __getattr__(name):
     # the torch-level holder imports torch lazily
-    if name in ("MoEBlock", "params_to_device"):
+    if name in ("MoEBlock", "ScMlp", "params_to_device"):
         from . import block
         return getattr(block, name)
     raise AttributeError(name)

@@ -32,6 +32,8 @@ EXPORTED = (
     "dg_moe_destroy", "dg_moe_last_device_status", "dg_moe_kernel_names",
     "dg_moe_set_profile_events", "dg_moe_status_string", "dg_moe_last_error",
     "dg_moe_route_noalloc",
+    "dg_sc_mlp_workspace_size", "dg_sc_mlp_create", "dg_sc_mlp_forward",
+    "dg_sc_mlp_last_device_status", "dg_sc_mlp_destroy",
 )
 
 
@@ -60,6 +62,16 @@ class dg_moe_debug_t(ctypes.Structure):
                 ("offsets", c_void_p), ("perm", c_void_p), ("xd", c_void_p),
                 ("xe_perm", c_void_p), ("y_moe", c_void_p), ("y_dense", c_void_p),
                 ("n_refined", c_void_p)]
+
+
+class dg_sc_mlp_config_t(ctypes.Structure):
+    _fields_ = [("hidden", c_int), ("inter", c_int), ("max_tokens", c_int), ("fmt", c_int),
+                ("rms_eps", c_float), ("flags", c_uint)]
+
+
+class dg_sc_mlp_weights_t(ctypes.Structure):
+    _fields_ = [("gate", dg_qtensor_t), ("up", dg_qtensor_t), ("down", dg_qtensor_t),
+                ("pre_norm", c_void_p)]
 
 
 class DgError(RuntimeError):
@@ -93,6 +105,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dg_moe_set_profile_events.argtypes = [c_void_p, POINTER(c_void_p), c_int]
     lib.dg_moe_route_noalloc.argtypes = [POINTER(dg_moe_config_t), POINTER(dg_moe_weights_t),
                                          c_void_p, c_int, c_void_p, c_void_p, c_void_p]
+    lib.dg_sc_mlp_workspace_size.argtypes = [POINTER(dg_sc_mlp_config_t), POINTER(c_size_t)]
+    lib.dg_sc_mlp_create.argtypes = [POINTER(dg_sc_mlp_config_t), POINTER(dg_sc_mlp_weights_t),
+                                     c_void_p, c_size_t, POINTER(c_void_p)]
+    lib.dg_sc_mlp_forward.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p]
+    lib.dg_sc_mlp_last_device_status.argtypes = [c_void_p, c_void_p]
+    lib.dg_sc_mlp_destroy.argtypes = [c_void_p]
     lib.dg_moe_status_string.argtypes = [c_int]
     lib.dg_moe_status_string.restype = c_char_p
     lib.dg_moe_last_error.argtypes = [c_void_p]
@@ -198,3 +216,34 @@ def dg_moe_route_noalloc(cfg: dg_moe_config_t, weights: dg_moe_weights_t, h_in: 
                                                c_void_p(h_in), n_tokens, c_void_p(idx_out),
                                                c_void_p(w_out), c_void_p(stream)),
            "dg_moe_route_noalloc")
+
+
+def dg_sc_mlp_workspace_size(cfg: dg_sc_mlp_config_t) -> int:
+    n = c_size_t(0)
+    _check(load_library().dg_sc_mlp_workspace_size(ctypes.byref(cfg), ctypes.byref(n)),
+           "dg_sc_mlp_workspace_size")
+    return n.value
+
+
+def dg_sc_mlp_create(cfg: dg_sc_mlp_config_t, weights: dg_sc_mlp_weights_t, workspace: int,
+                     workspace_bytes: int) -> int:
+    h = c_void_p(0)
+    _check(load_library().dg_sc_mlp_create(ctypes.byref(cfg), ctypes.byref(weights),
+                                           c_void_p(workspace), workspace_bytes, ctypes.byref(h)),
+           "dg_sc_mlp_create")
+    return h.value
+
+
+def dg_sc_mlp_forward(handle: int, embeds: int, signal: int, out: int, n_tokens: int,
+                      stream: int) -> None:
+    _check(load_library().dg_sc_mlp_forward(c_void_p(handle), c_void_p(embeds), c_void_p(signal),
+                                            c_void_p(out), n_tokens, c_void_p(stream)),
+           "dg_sc_mlp_forward")
+
+
+def dg_sc_mlp_last_device_status(handle: int, stream: int) -> int:
+    return load_library().dg_sc_mlp_last_device_status(c_void_p(handle), c_void_p(stream))
+
+
+def dg_sc_mlp_destroy(handle: int) -> None:
+    _check(load_library().dg_sc_mlp_destroy(c_void_p(handle)), "dg_sc_mlp_destroy")

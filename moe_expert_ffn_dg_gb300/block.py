@@ -172,3 +172,65 @@ class MoEBlock:
             self.close()
         except Exception:
             pass
+
+
+class ScMlp:
+    """The self-conditioning MLP (before layer 0 of a decode step): device
+    weights (borrowed by the C handle), a workspace and the handle.
+    ``forward(embeds, signal)`` returns the bf16 [T, H] result."""
+
+    def __init__(self, weights: dict, *, hidden: int, inter: int, max_tokens: int,
+                 rms_eps: float = 1e-6):
+        self.weights = weights
+        self.hidden, self.inter, self.max_tokens = hidden, inter, max_tokens
+        self.cfg = B.dg_sc_mlp_config_t(hidden, inter, max_tokens, _fmt(weights["gate"]),
+                                        rms_eps, 0)
+        self.device = weights["pre_norm"].device
+        ws_bytes = B.dg_sc_mlp_workspace_size(self.cfg)
+        self.workspace = torch.empty(ws_bytes + 1024, dtype=torch.uint8, device=self.device)
+        ptr = (self.workspace.data_ptr() + 1023) // 1024 * 1024
+        self.cw = B.dg_sc_mlp_weights_t(_qt(weights["gate"]), _qt(weights["up"]),
+                                        _qt(weights["down"]), weights["pre_norm"].data_ptr())
+        self.handle = B.dg_sc_mlp_create(self.cfg, self.cw, ptr, ws_bytes)
+
+    @classmethod
+    def from_params(cls, p: dict, *, hidden, inter, max_tokens, device="cuda"):
+        w = {}
+        for k in ("gate", "up", "down"):
+            v = p[k]
+            if isinstance(v, dict):
+                w[k] = {"bits": v["bits"], "group": v["group"],
+                        "q": _to_device(v["q"], device),
+                        "scales": _to_device(v["scales"], device),
+                        "biases": _to_device(v["biases"], device)}
+            else:
+                w[k] = _to_device(v, device)
+        w["pre_norm"] = _to_device(p["pre_norm"], device)
+        return cls(w, hidden=hidden, inter=inter, max_tokens=max_tokens)
+
+    def forward(self, embeds: torch.Tensor, signal: torch.Tensor, out: torch.Tensor = None,
+                stream=None) -> torch.Tensor:
+        for t in (embeds, signal):
+            assert t.dtype == torch.bfloat16 and t.is_contiguous() and t.shape[1] == self.hidden
+        assert embeds.shape == signal.shape
+        if out is None:
+            out = torch.empty_like(embeds)
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        B.dg_sc_mlp_forward(self.handle, embeds.data_ptr(), signal.data_ptr(), out.data_ptr(),
+                            embeds.shape[0], s.cuda_stream)
+        return out
+
+    def device_status(self, stream=None) -> int:
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        return B.dg_sc_mlp_last_device_status(self.handle, s.cuda_stream)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            B.dg_sc_mlp_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

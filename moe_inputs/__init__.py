@@ -101,8 +101,10 @@ WORKLOADS = {
 # The self-conditioning MLP (dense-FFN shapes, before layer 0) over one
 # canvas: the soft signal and the token embeddings drawn N(0, 1).
 SC_WORKLOADS = {
+    # weight std 0.1 so that the MLP's share of the output (about the
+    # embeddings' RMS, as on the full shape) is not hidden by the embeddings
     "sc_tiny": Workload("sc_tiny", 32, 256, 1, 1, 64, 128, seed=6,
-                        weight_std=0.02, router_std=0.02),
+                        weight_std=0.1, router_std=0.02),
     "sc_canvas256": Workload("sc_canvas256", 256, 2816, 1, 1, 704, 2112, seed=5,
                              weight_std=0.02, router_std=0.02),
     "sc_canvas256_q4": Workload("sc_canvas256_q4", 256, 2816, 1, 1, 704, 2112, seed=5,

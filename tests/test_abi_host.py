@@ -28,7 +28,7 @@ def _cfg(**kw):
 
 
 def test_library_exports_every_declared_function(lib):
-    decl = set(re.findall(r"\b(dg_moe_\w+)\s*\(", open(HEADER).read()))
+    decl = set(re.findall(r"\b(dg_(?:moe|sc_mlp)_\w+)\s*\(", open(HEADER).read()))
     assert decl == set(B.EXPORTED)
     for name in decl:
         assert hasattr(lib, name)
@@ -97,3 +97,23 @@ def test_null_handle_is_rejected_and_destroy_accepts_null(lib):
     n = ctypes.c_int(0)
     assert lib.dg_moe_kernel_names(None, None, ctypes.byref(n)) == B.DG_ERR_INVALID_ARG
     assert lib.dg_moe_set_profile_events(None, None, 0) == B.DG_ERR_INVALID_ARG
+
+
+def _sc_cfg(**kw):
+    c = dict(hidden=2816, inter=2112, max_tokens=256, fmt=0, rms_eps=1e-6, flags=0)
+    c.update(kw)
+    return B.dg_sc_mlp_config_t(**c)
+
+
+def test_sc_mlp_workspace_and_create_validation(lib):
+    assert B.dg_sc_mlp_workspace_size(_sc_cfg()) > 256 * 2816 * 4
+    for bad in (dict(hidden=100), dict(inter=100), dict(fmt=2), dict(flags=1)):
+        with pytest.raises(B.DgError):
+            B.dg_sc_mlp_workspace_size(_sc_cfg(**bad))
+    w = B.dg_sc_mlp_weights_t()
+    h = ctypes.c_void_p(0)
+    # null weights and a null workspace are refused before any CUDA call
+    assert lib.dg_sc_mlp_create(ctypes.byref(_sc_cfg()), ctypes.byref(w), None, 0,
+                                ctypes.byref(h)) == B.DG_ERR_INVALID_ARG
+    assert lib.dg_sc_mlp_forward(None, None, None, None, 1, None) == B.DG_ERR_INVALID_ARG
+    assert lib.dg_sc_mlp_destroy(None) == B.DG_OK
