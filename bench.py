@@ -8,7 +8,8 @@ that canvas with inputs resident in HBM.  The 1.56 GB of weights read per
 step are 12x the L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload canvas256|canvas256_q4|batch2048_zipf|stack30_q4]
+                  [--workload canvas256|canvas256_q4|batch2048_zipf|stack30_q4|
+                              sc_canvas256|sc_canvas256_q4]
 
 Prints one JSON line.  ``--impl reference`` times the CPU oracle (the only
 reference there is: the pages hold no runnable implementation) on the host
@@ -174,6 +175,19 @@ def run_reference(args):
     if rank != 0:
         return
     wl = mi.get_workload(args.workload)
+    if wl.name.startswith("sc_"):
+        p = mi.make_sc_inputs(wl, randvec=True)
+        n, dt = sc_cpu_sample(wl, p, 120.0)
+        line = {"impl": "reference", "metric": SC_METRIC, "value": n / dt, "unit": UNIT,
+                "n_gpus": args.gpus, "steps": 1, "warmup": 0, "ms_per_step": 1000.0 * dt,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": sc_desc(wl), "tokens_per_step": n},
+                "cpu_baseline": {"value": n / dt, "unit": UNIT, "cores": os.cpu_count(),
+                                 "kind": "oracle", "sample": f"{n} canvas tokens, fp64 oracle"},
+                "e2e": {"value": n / dt, "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
     p = mi.make_layer_inputs(wl)
     h = mi.make_tokens(wl)
     # decode the weights to float64 once, outside the timed steps; the
@@ -352,6 +366,155 @@ def run_stack(args):
     print(json.dumps(line))
 
 
+SC_METRIC = "canvas-tokens/s of the self-conditioning MLP (µs/call) and % of HBM roofline, 1 GB300"
+
+
+def sc_desc(wl):
+    w = (f"gate/up/down N(0,{wl.weight_std}) draws in group-64 affine {wl.quant[1]}-bit"
+         if wl.quant else f"bf16 gate/up/down N(0,{wl.weight_std})")
+    return (f"{wl.name}: the self-conditioning MLP of DiffusionGemma (pre-normed GEGLU of the "
+            f"dense FFN's shape on the soft signal, added to the embeddings, weightless "
+            f"RMSNorm), T={wl.tokens} tokens, H={wl.hidden}, FFN {wl.dense_inter}, {w}, "
+            f"embeddings and signal N(0,1), pre_norm U(0.5,1.5), seed {wl.seed}")
+
+
+def sc_algorithmic(wl):
+    """Bytes and FLOPs of one self-conditioning forward and of its gate_up
+    GEMM: the three weight matrices, the embeddings and signal read, the
+    output write; x, act and the f32 MLP output stay on chip in an ideal
+    kernel."""
+    T, H, D = wl.tokens, wl.hidden, wl.dense_inter
+    db = wl.quant[1] if wl.quant else None
+    w = weight_bytes(3 * D * H, db)
+    return {"bytes": w + 3 * T * H * 2 + H * 2, "flops": 2 * T * 3 * H * D,
+            "gate_up_bytes": weight_bytes(2 * D * H, db) + T * H * 2 + T * D * 2,
+            "gate_up_flops": 2 * T * 2 * H * D}
+
+
+def sc_cpu_sample(wl, p, max_seconds):
+    import oracle
+    n, dt = 1, 0.0
+    while True:
+        t0 = time.time()
+        oracle.sc_mlp_forward(p["embeds"][:n], p["signal"][:n], p)
+        dt = time.time() - t0
+        if n >= wl.tokens or dt * 2 * 1.2 > max_seconds:
+            return n, dt
+        n = min(wl.tokens, n * 2)
+
+
+def run_sc(args):
+    """The self-conditioning MLP over one canvas: a step is one forward
+    (pre-norm, gate_up + GEGLU, down, residual + RMSNorm) with the inputs
+    resident in HBM."""
+    import torch
+
+    import moe_expert_ffn_dg_gb300 as pkg
+    import moe_inputs as mi
+    from moe_expert_ffn_dg_gb300 import binding as B
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    pkg.build()
+    pkg.load_library()
+    wl = mi.get_workload(args.workload, **({"tokens": args.tokens} if args.tokens else {}))
+    p = mi.make_sc_inputs(wl, randvec=True)
+    sc = pkg.ScMlp.from_params(p, hidden=wl.hidden, inter=wl.dense_inter, max_tokens=wl.tokens,
+                               device=dev)
+
+    def dev16(a):
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    e, sig = dev16(p["embeds"]), dev16(p["signal"])
+    out = torch.empty_like(e)
+    stream = torch.cuda.current_stream(dev)
+    names = B.dg_sc_mlp_kernel_names(sc.handle)
+    nk = len(names)
+    for _ in range(max(args.warmup, 3)):
+        sc.forward(e, sig, out=out)
+    torch.cuda.synchronize(dev)
+    if sc.device_status() != 0:
+        raise RuntimeError("device status after warm-up")
+    stride = max(1, args.steps // 200)
+    ev_sets = {i: [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+               for i in range(0, args.steps, stride)}
+    for evs in ev_sets.values():
+        for ev in evs:
+            ev.record(stream)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(0)
+    time.sleep(0.3)
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for i in range(args.steps):
+        evs = ev_sets.get(i)
+        B.dg_sc_mlp_set_profile_events(sc.handle, [x.cuda_event for x in evs] if evs else None)
+        sc.forward(e, sig, out=out)
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    B.dg_sc_mlp_set_profile_events(sc.handle, None)
+    clk = clocks.stop()
+    if sc.device_status() != 0:
+        raise RuntimeError("device status after timing")
+    ms = start.elapsed_time(stop) / args.steps
+    per_kernel = np.zeros(nk)
+    for evs in ev_sets.values():
+        per_kernel += [evs[j].elapsed_time(evs[j + 1]) for j in range(nk)]
+    per_kernel_us = per_kernel / len(ev_sets) * 1000.0
+
+    # end to end: pinned host embeddings and signal in, output back, synchronised
+    e_host = torch.from_numpy(p["embeds"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    s_host = torch.from_numpy(p["signal"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    o_host = torch.empty_like(e_host).pin_memory()
+    e_dev, s_dev = torch.empty_like(e), torch.empty_like(sig)
+    e2e_steps = max(10, min(args.steps, 2000))
+    for i in range(3 + e2e_steps):
+        if i == 3:
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+        e_dev.copy_(e_host, non_blocking=True)
+        s_dev.copy_(s_host, non_blocking=True)
+        sc.forward(e_dev, s_dev, out=e_dev)
+        o_host.copy_(e_dev, non_blocking=True)
+        torch.cuda.synchronize(dev)
+    e2e_s = time.perf_counter() - t0
+
+    alg = sc_algorithmic(wl)
+    hbm, bf16_burst, bf16_sus, src = peaks()
+    gu = names.index("gemm_gate_up")
+    achieved = alg["gate_up_bytes"] / (per_kernel_us[gu] * 1e-6) / 1e9
+    t_roof = max(alg["bytes"] / (hbm * 1e9), alg["flops"] / (bf16_burst * 1e12))
+    line = {
+        "metric": SC_METRIC, "value": wl.tokens / (ms / 1000.0), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": sc_desc(wl), "tokens_per_step": wl.tokens, "us_per_call": ms * 1e3,
+                   "l2": f"no flush: inputs and weights resident; {alg['bytes'] / 1e6:.1f} MB per "
+                         f"step fit the 129 MB L2, so the HBM fraction is an upper bound"},
+        "roofline": {"bound": "hbm", "kernel": "gemm_gate_up", "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes_per_launch": alg["gate_up_bytes"],
+                     "us_per_launch": per_kernel_us[gu]},
+        "step_roofline": {"bytes": alg["bytes"], "flops": alg["flops"], "t_roof_us": t_roof * 1e6,
+                          "frac": t_roof / (ms / 1000.0),
+                          "basis": f"max(bytes / {hbm} GB/s, flops / {bf16_burst} TF/s) ({src})"},
+        "kernels_us": {n: round(float(v), 3) for n, v in zip(names, per_kernel_us)},
+        "e2e": {"value": wl.tokens * e2e_steps / e2e_s, "unit": UNIT,
+                "h2d_bytes_per_step": int(e_host.numel() * 2 + s_host.numel() * 2),
+                "d2h_bytes_per_step": int(o_host.numel() * 2), "steps": e2e_steps},
+        "clocks": clk,
+        "gpu_launches": nk * args.steps,
+    }
+    if not args.no_cpu_baseline:
+        n, dt = sc_cpu_sample(wl, p, 20.0)
+        line["cpu_baseline"] = {"value": n / dt, "unit": UNIT, "cores": os.cpu_count(),
+                                "kind": "oracle",
+                                "sample": f"{n} of the {wl.tokens} canvas tokens, fp64 numpy "
+                                          f"oracle, {dt:.2f} s"}
+    sc.close()
+    print(json.dumps(line))
+
+
 def run_ours(args):
     import torch
 
@@ -500,7 +663,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=0,
                     help="token count of a one-layer workload (default: the workload's own)")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=["canvas256", "canvas256_q4", "batch2048_zipf", "stack30_q4"])
+                    choices=["canvas256", "canvas256_q4", "batch2048_zipf", "stack30_q4",
+                             "sc_canvas256", "sc_canvas256_q4"])
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -508,6 +672,8 @@ def main():
         run_reference(args)
     elif args.workload == "stack30_q4":
         run_stack(args)
+    elif args.workload.startswith("sc_"):
+        run_sc(args)
     else:
         run_ours(args)
 

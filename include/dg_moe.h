@@ -278,6 +278,14 @@ dg_status_t dg_sc_mlp_forward(dg_sc_mlp_t* m, const void* embeds, const void* si
  * (DG_OK, DG_ERR_TIMEOUT or DG_ERR_DEVICE_CHECK). */
 dg_status_t dg_sc_mlp_last_device_status(dg_sc_mlp_t* m, dg_stream_t stream);
 
+/* Number of kernels one forward launches and their names, as
+ * dg_moe_kernel_names. */
+dg_status_t dg_sc_mlp_kernel_names(const dg_sc_mlp_t* m, const char** names, int* n);
+
+/* Profiling events around each kernel of later forwards, as
+ * dg_moe_set_profile_events (n_events = number of kernels + 1, NULL off). */
+dg_status_t dg_sc_mlp_set_profile_events(dg_sc_mlp_t* m, dg_event_t* events, int n_events);
+
 /* Free the handle (NULL is accepted). */
 dg_status_t dg_sc_mlp_destroy(dg_sc_mlp_t* m);
 

@@ -33,7 +33,8 @@ EXPORTED = (
     "dg_moe_set_profile_events", "dg_moe_status_string", "dg_moe_last_error",
     "dg_moe_route_noalloc",
     "dg_sc_mlp_workspace_size", "dg_sc_mlp_create", "dg_sc_mlp_forward",
-    "dg_sc_mlp_last_device_status", "dg_sc_mlp_destroy",
+    "dg_sc_mlp_last_device_status", "dg_sc_mlp_destroy", "dg_sc_mlp_kernel_names",
+    "dg_sc_mlp_set_profile_events",
 )
 
 
@@ -111,6 +112,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dg_sc_mlp_forward.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p]
     lib.dg_sc_mlp_last_device_status.argtypes = [c_void_p, c_void_p]
     lib.dg_sc_mlp_destroy.argtypes = [c_void_p]
+    lib.dg_sc_mlp_kernel_names.argtypes = [c_void_p, POINTER(c_char_p), POINTER(c_int)]
+    lib.dg_sc_mlp_set_profile_events.argtypes = [c_void_p, POINTER(c_void_p), c_int]
     lib.dg_moe_status_string.argtypes = [c_int]
     lib.dg_moe_status_string.restype = c_char_p
     lib.dg_moe_last_error.argtypes = [c_void_p]
@@ -182,27 +185,40 @@ def dg_moe_last_device_status(handle: int, stream: int):
     return s, where.value, info.value
 
 
-def dg_moe_kernel_names(handle: int) -> list:
+def _kernel_names(fn, handle: int) -> list:
     n = c_int(0)
-    lib = load_library()
-    _check(lib.dg_moe_kernel_names(c_void_p(handle), None, ctypes.byref(n)), "dg_moe_kernel_names")
+    _check(fn(c_void_p(handle), None, ctypes.byref(n)), fn.__name__)
     arr = (c_char_p * n.value)()
-    _check(lib.dg_moe_kernel_names(c_void_p(handle), arr, ctypes.byref(n)), "dg_moe_kernel_names")
+    _check(fn(c_void_p(handle), arr, ctypes.byref(n)), fn.__name__)
     return [a.decode() for a in arr]
+
+
+def _set_profile_events(fn, handle: int, events) -> None:
+    if events is None:
+        _check(fn(c_void_p(handle), None, 0), fn.__name__)
+        _EVENT_ARRAYS.pop(handle, None)
+        return
+    arr = (c_void_p * len(events))(*events)
+    _check(fn(c_void_p(handle), arr, len(events)), fn.__name__)
+    # keep the array alive as long as the handle may use it
+    _EVENT_ARRAYS[handle] = arr
+
+
+def dg_moe_kernel_names(handle: int) -> list:
+    return _kernel_names(load_library().dg_moe_kernel_names, handle)
 
 
 def dg_moe_set_profile_events(handle: int, events) -> None:
     """events: list of cudaEvent_t handles (ints), or None to switch off."""
-    lib = load_library()
-    if events is None:
-        _check(lib.dg_moe_set_profile_events(c_void_p(handle), None, 0),
-               "dg_moe_set_profile_events")
-        return
-    arr = (c_void_p * len(events))(*events)
-    _check(lib.dg_moe_set_profile_events(c_void_p(handle), arr, len(events)),
-           "dg_moe_set_profile_events")
-    # keep the array alive as long as the handle may use it
-    _EVENT_ARRAYS[handle] = arr
+    _set_profile_events(load_library().dg_moe_set_profile_events, handle, events)
+
+
+def dg_sc_mlp_kernel_names(handle: int) -> list:
+    return _kernel_names(load_library().dg_sc_mlp_kernel_names, handle)
+
+
+def dg_sc_mlp_set_profile_events(handle: int, events) -> None:
+    _set_profile_events(load_library().dg_sc_mlp_set_profile_events, handle, events)
 
 
 _EVENT_ARRAYS: dict = {}

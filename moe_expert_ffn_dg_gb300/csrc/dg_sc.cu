@@ -125,6 +125,10 @@ __global__ void __launch_bounds__(kScThreads) k_sc_post(const uint16_t* embeds,
   }
 }
 
+constexpr int kScKernels = 4;
+const char* const kScKernelNames[kScKernels] = {"sc_prenorm", "gemm_gate_up", "gemm_down",
+                                                 "sc_post"};
+
 struct ScLayout {
   size_t status, zero, x, act, y, total;
 };
@@ -171,6 +175,7 @@ struct dg_sc_mlp {
   size_t smem_optin;
   bool q4;
   GemmParams gu, dn;
+  dg_event_t* prof = nullptr;
 };
 
 extern "C" {
@@ -309,10 +314,18 @@ dg_status_t dg_sc_mlp_forward(dg_sc_mlp_t* m, const void* embeds, const void* si
   const float eps = m->cfg.rms_eps;
   uint8_t* ws = m->ws;
   const ScLayout& L = m->L;
-  cudaError_t err = launch_pdl(k_sc_prenorm, dim3(T), dim3(kScThreads), 0, s,
-                               static_cast<const uint16_t*>(signal),
-                               static_cast<const uint16_t*>(m->w.pre_norm), H, eps,
-                               reinterpret_cast<uint16_t*>(ws + L.x));
+  cudaError_t err = cudaSuccess;
+  auto mark = [&](int i) {
+    if (m->prof && err == cudaSuccess)
+      err = cudaEventRecord(reinterpret_cast<cudaEvent_t>(m->prof[i]), s);
+  };
+  mark(0);
+  if (err == cudaSuccess)
+    err = launch_pdl(k_sc_prenorm, dim3(T), dim3(kScThreads), 0, s,
+                     static_cast<const uint16_t*>(signal),
+                     static_cast<const uint16_t*>(m->w.pre_norm), H, eps,
+                     reinterpret_cast<uint16_t*>(ws + L.x));
+  mark(1);
   GemmParams gu = m->gu, dn = m->dn;
   gu.T = dn.T = T;
   const int bn = m->q4 ? pick_bn_q4(T, gu.sc_slot_bytes, dn.sc_slot_bytes, m->smem_optin)
@@ -320,13 +333,16 @@ dg_status_t dg_sc_mlp_forward(dg_sc_mlp_t* m, const void* embeds, const void* si
   gu.bn = dn.bn = bn;
   if (err == cudaSuccess)
     err = m->q4 ? launch_gemm_q4(0, bn, gu, m->num_sms, s) : launch_gemm(0, bn, gu, m->num_sms, s);
+  mark(2);
   if (err == cudaSuccess)
     err = m->q4 ? launch_gemm_q4(1, bn, dn, m->num_sms, s) : launch_gemm(1, bn, dn, m->num_sms, s);
+  mark(3);
   if (err == cudaSuccess)
     err = launch_pdl(k_sc_post, dim3(T), dim3(kScThreads), 0, s,
                      static_cast<const uint16_t*>(embeds),
                      reinterpret_cast<const float*>(ws + L.y), H, eps,
                      static_cast<uint16_t*>(out));
+  mark(4);
   return err == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }
 
@@ -340,6 +356,21 @@ dg_status_t dg_sc_mlp_last_device_status(dg_sc_mlp_t* m, dg_stream_t stream) {
   if (cudaMemset(m->ws + m->L.status, 0, sizeof(st)) != cudaSuccess) return DG_ERR_CUDA;
   if (st.code == kDevTimeout) return DG_ERR_TIMEOUT;
   if (st.code == kDevBounds) return DG_ERR_DEVICE_CHECK;
+  return DG_OK;
+}
+
+dg_status_t dg_sc_mlp_kernel_names(const dg_sc_mlp_t* m, const char** names, int* n) {
+  if (!m || !n) return DG_ERR_INVALID_ARG;
+  *n = kScKernels;
+  if (names)
+    for (int i = 0; i < kScKernels; ++i) names[i] = kScKernelNames[i];
+  return DG_OK;
+}
+
+dg_status_t dg_sc_mlp_set_profile_events(dg_sc_mlp_t* m, dg_event_t* events, int n_events) {
+  if (!m) return DG_ERR_INVALID_ARG;
+  if (events && n_events != kScKernels + 1) return DG_ERR_INVALID_ARG;
+  m->prof = events;
   return DG_OK;
 }
 
