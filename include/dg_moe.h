@@ -211,8 +211,8 @@ const char* dg_moe_last_error(const dg_moe_t* m);
  * (f32 [n_tokens, K]), asynchronously on `stream`.
  * Scratch: a fixed 8 MiB array in the library's device memory, held on
  * every GPU that loads the library until the process exits.  It needs
- * about n_tokens * (6 H + 4 E + 8) bytes; larger calls return
- * DG_ERR_UNSUPPORTED (a 256-token canvas at H 2816 needs 4.5 MB).  The first
+ * about n_tokens * (2 H + 4 E + 8) bytes; larger calls return
+ * DG_ERR_UNSUPPORTED (a 256-token canvas at H 2816 needs 1.6 MB).  The first
  * call on a device looks up the array's device address (a CUDA runtime
  * query, no allocation), so make that first call before any stream
  * capture.  Every call on a device shares the one array: calls that can

@@ -108,8 +108,10 @@ __device__ __forceinline__ bool wait_no_abort(uint64_t* bar, uint32_t parity) {
 // MODE 0 (gate_up): lanes 32q..32q+15 hold gate and 32q+16..32q+31 up of the
 // same 16 features; pair them with one shuffle and write
 // act = bf16(gelu_tanh(gate) * up).
-// MODE 1 (down): 128 output channels; experts add w * y into the f32
-// per-token accumulator, the dense branch stores its f32 output.
+// MODE 1 (down): 128 output channels; the dense branch stores its f32
+// output; experts either store w * y as the f32 row of the assignment
+// (y_perm, summed per token later) or add it into the f32 per-token
+// accumulator (y_moe).
 template <int MODE>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int4 td, uint32_t tbase,
                                               int ncols, int q, int lane) {
@@ -140,6 +142,16 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int4 td, uint
 #pragma unroll
       for (int j = 0; j < 16; ++j)
         if (c0 + j < td.w) p.y_dense[(size_t)(td.z + c0 + j) * p.H + feat] = v[j];
+    } else if (p.y_perm) {
+      // lane l holds channel 32q + l of 16 grouped rows: each store writes
+      // 128 contiguous bytes of one row
+      const int feat = td.y * 128 + 32 * q + lane;
+      const float wl = (lane < 16 && c0 + lane < td.w) ? p.w_perm[td.z + c0 + lane] : 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, wl, j);
+        if (c0 + j < td.w) p.y_perm[(size_t)(td.z + c0 + j) * p.H + feat] = wj * v[j];
+      }
     } else {
       // Routing-weighted add into the f32 per-token accumulator, four
       // features per vector reduction: transpose each 4 x 4 block of

@@ -8,41 +8,41 @@
 // measurements) names the dequantisation as the cost that dominates 4-bit
 // expert layers; here it runs beside the tensor core instead of in front of it.
 //
-// Dataflow of one tile (128 weight rows x up to BN token rows):
-//   warp 0   TMA: code slabs (128 rows x 256 codes = 16 KB, 128B swizzle) into
-//            a ring, and per tile the rows' scales and biases (bulk copies);
-//   warp 1   TMA: token slabs (BN rows x 256 bf16, as four 64-column
-//            sub-blocks) into a second ring;
-//   warp 2   TMEM owner and MMA issuer: tcgen05.mma with A read from TMEM
-//            (the dequantised weights) and B from shared memory (tokens),
-//            one slab (16 MMAs of K = 16) per round;
-//   warp 3   waits, for the issuer, until a slab's operands are ready and
+// Dataflow of one tile (128 weight rows x up to BN token rows), in stages of
+// one group (64 along K):
+//   warp 0   TMA: code slabs (128 rows x 128 codes = 8 KB, 64B swizzle,
+//            two stages each) into a ring, and per tile the rows' scales and
+//            biases (bulk copies);
+//   warp 1   TMA: the tokens of each stage (BN rows x 64 bf16) into a ring;
+//   warp 2   TMEM owner and MMA issuer: four tcgen05.mma (K = 16) per stage,
+//            both operands in shared memory;
+//   warp 3   waits, for the issuer, until a stage's operands are ready and
 //            hands it over through a named barrier (see below);
-//   warps 4-19  dequantise: each thread expands one group of 64 codes of one
-//            weight row of a slab to bf16 (exact s * q + b, one rounding) and
-//            stores it into TMEM with tcgen05.st; four warps per 32-lane
-//            quarter, one group each;
+//   warps 4-19  dequantise, in four teams of four warps (one warp per 32
+//            weight rows): stage s of the sequence belongs to team s mod 4,
+//            whose threads expand one row's 64 codes each to bf16 (exact
+//            s * q + b, one rounding) into one of the team's own A stages, in
+//            the 128B-swizzled K-major layout the MMA reads;
 //   warps 20-23 epilogue, as for bf16 weights (GEGLU or weighted combine).
-// The bf16 weights never pass through shared memory: shared-memory traffic
-// per weight is the half byte of its code plus its share of the token tile.
-//
-// TMEM columns: two fp32 accumulators of BN columns, then NA slots of 128
-// columns, each holding one dequantised slab (128 lanes x 256 bf16, two codes
-// per 32-bit column, K-major: the layout the MMA reads A from TMEM).
+// Dequantised weights go to shared memory rather than TMEM: concurrent
+// tcgen05.st traffic slows A-from-TMEM MMAs about threefold on this part,
+// while shared-memory stores at the full store rate leave shared-memory MMAs
+// at their unloaded cost (55 cycles for N <= 128, 128 for N = 256).  TMEM
+// then holds only the two fp32 accumulators, so token tiles go up to 256.
 //
 // Why the issuer does not wait on mbarriers itself: on sm_103a, a shared-
 // memory access (an mbarrier poll or a plain load) by a thread that has
 // tcgen05.mma in flight stalls until those MMAs complete, so one poll per
-// slab costs the MMA pipeline latency (measured ~700 cycles against ~55
+// stage costs the MMA pipeline latency (measured ~700 cycles against ~55
 // cycles per M=128, K=16 MMA).  Another warp's polls are not affected, and a
 // named CTA barrier is not a memory access.  So warp 3 does the bounded
-// mbarrier waits and meets the issuer at a barrier.red.or once per slab; the
+// mbarrier waits and meets the issuer at a barrier.red.or once per stage; the
 // reduced predicate carries "stop" (a wait that ran out), so both warps leave
 // on the same round and the barrier can never be left half-arrived.
 //
 // Every wait is bounded; a wait that runs out records itself in the status
-// word and the CTA winds down (copies, stores and MMAs in flight are drained
-// before TMEM is released).
+// word and the CTA winds down (copies and MMAs in flight are drained before
+// TMEM is released).
 #include "dg_gemm_common.cuh"
 
 namespace dg {
@@ -50,28 +50,50 @@ namespace {
 
 using namespace gemm;
 
-constexpr int kSlabK = 256;                    // codes per row of a slab
-constexpr int kQSlabBytes = 128 * kSlabK / 2;  // 16 KB
+constexpr int kSlabK = 128;                    // codes per row of a slab (two stages)
+constexpr int kQSlabBytes = 128 * kSlabK / 2;  // 8 KB
+constexpr int kQBoxBytes = 16 * kSlabK / 2;    // one 16-row box of a slab
+constexpr int kAStageBytes = 128 * 128;        // 128 rows x 64 bf16
 constexpr int kDequantWarp0 = 4;
-constexpr int kNumDequantWarps = 16;           // 4 per TMEM lane quarter, one group of 64 each
+constexpr int kNumDequantWarps = 16;           // 4 teams x 4 lane quarters
 constexpr int kEpilogueWarp0 = kDequantWarp0 + kNumDequantWarps;
 constexpr int kThreadsQ = 32 * (kEpilogueWarp0 + 4);  // 768
 
-// Per token-tile width: code slabs in flight (SQ), token slabs in flight
-// (SB; a token slab is the four 64-column sub-blocks of one code slab) and
-// dequantised slabs held in TMEM (NA) beside the two BN-column accumulators.
-// Narrow tiles keep more token slabs in flight: the ring must cover the
-// TMA latency plus the time an MMA batch takes to complete.
+// Per token-tile width: code slabs in flight (SQ, even: slots of even slabs
+// feed teams 0 and 1, odd ones teams 2 and 3), token stages in flight (NB,
+// BN x 128 bytes each) and A stages per team (M; 16 KB each).  Every ring
+// slot has one consumer group that takes its uses in order, so an mbarrier
+// parity wait can never be two phases ahead of the slot.  The token ring
+// covers the L2 latency plus the MMA time of a stage (4 MMAs: ~220 cycles
+// for BN <= 128, 512 for BN = 256); a team refills its A stage while the
+// other three teams' stages are multiplied (two stages each for the
+// narrowest tiles, whose stages are shortest).  All fit beside
+// double-buffered per-tile scales of up to 47 groups (K = 3008).
 template <int BN>
 struct CfgQ {
-  static constexpr int kSQ = BN == 128 ? 3 : 4;
-  static constexpr int kSB = BN == 32 ? 6 : BN == 64 ? 3 : 2;
-  static constexpr int kBSlabBytes = 4 * BN * 128;
-  static constexpr int kNA = (512 - 2 * BN) / 128 < 3 ? (512 - 2 * BN) / 128 : 3;
+  static constexpr int kSQ = BN == 64 ? 4 : 2;
+  static constexpr int kNB = BN == 256 ? 3 : BN == 128 ? 6 : BN == 64 ? 10 : 8;
+  static constexpr int kM = BN == 32 ? 2 : 1;
+  static constexpr int kNA = 4 * kM;
+  static constexpr int kBStageBytes = BN * 128;
   static constexpr int kBarBytes = 512;
-  static constexpr size_t kFixed = 1024 + (size_t)kSQ * kQSlabBytes + (size_t)kSB * kBSlabBytes +
+  static constexpr size_t kFixed = 1024 + (size_t)kSQ * kQSlabBytes +
+                                   (size_t)kNB * kBStageBytes + (size_t)kNA * kAStageBytes +
                                    kBarBytes + kTileTableBytes;
 };
+
+// Team that owns stage g of a tile whose first code slab has the global
+// index slab0: slabs alternate between teams {0, 1} and {2, 3}.
+__device__ __forceinline__ int stage_team(uint32_t slab0, int g) {
+  return 2 * (int)((slab0 + (uint32_t)(g >> 1)) & 1u) + (g & 1);
+}
+
+// Four per-team stage counters in one register (16 bits each; only their
+// low bits matter, for the slot and the parity): the issuer must not touch
+// local memory while its MMAs are in flight.
+__device__ __forceinline__ uint32_t team_count(uint64_t packed, int team) {
+  return (uint32_t)(packed >> (16 * team)) & 0xFFFFu;
+}
 
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
                                          uint64_t* bar, uint64_t policy) {
@@ -82,30 +104,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs, fp32 accumulate, one CTA.
-__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Store 32 consecutive 32-bit columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
 // Named barrier 1 between the MMA issuer warp and its waiter warp (64
 // threads, both block), OR-reducing one predicate: returns true if either
 // side passed true.
@@ -122,8 +120,12 @@ __device__ __forceinline__ bool handoff(bool stop) {
       : "memory");
   return r != 0;
 }
-__device__ __forceinline__ void tmem_st_wait() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+// Store 16 bytes at a shared-memory address.
+__device__ __forceinline__ void sts_u32x4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                          uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
 }
 
 __device__ __forceinline__ void lds_u32x4(const uint8_t* p, uint32_t (&w)[4]) {
@@ -169,17 +171,18 @@ template <int MODE, int BN>
 __global__ void __launch_bounds__(kThreadsQ, 1)
     k_grouped_gemm_q4(const __grid_constant__ GemmParams p) {
   using C = CfgQ<BN>;
-  constexpr int SQ = C::kSQ, SB = C::kSB, NA = C::kNA;
+  constexpr int SQ = C::kSQ, NB = C::kNB, NA = C::kNA;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sQ = smem;
   uint8_t* sB = sQ + (size_t)SQ * kQSlabBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (size_t)SB * C::kBSlabBytes);
+  uint8_t* sA = sB + (size_t)NB * C::kBStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sA + (size_t)NA * kAStageBytes);
   uint64_t* qfull = bars;
   uint64_t* qempty = qfull + SQ;
   uint64_t* bfull = qempty + SQ;
-  uint64_t* bempty = bfull + SB;
-  uint64_t* afull = bempty + SB;
+  uint64_t* bempty = bfull + NB;
+  uint64_t* afull = bempty + NB;
   uint64_t* aempty = afull + NA;
   uint64_t* sfull = aempty + NA;
   uint64_t* sempty = sfull + 2;
@@ -199,14 +202,14 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < SQ; ++s) {
       mbar_init(&qfull[s], 1);
-      mbar_init(&qempty[s], kNumDequantWarps);
+      mbar_init(&qempty[s], 8);  // the two teams of the slot
     }
-    for (int s = 0; s < SB; ++s) {
+    for (int s = 0; s < NB; ++s) {
       mbar_init(&bfull[s], 1);
       mbar_init(&bempty[s], 1);
     }
     for (int a = 0; a < NA; ++a) {
-      mbar_init(&afull[a], kNumDequantWarps);
+      mbar_init(&afull[a], 4);  // the four warps of one team
       mbar_init(&aempty[a], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -245,7 +248,6 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const uint32_t a_col0 = 2 * BN;  // first TMEM column of the dequantised slabs
   const int nd = (p.T + p.bn - 1) / p.bn * p.mt_dense;
   const int ntiles = nd + s_start[p.E];
 
@@ -302,7 +304,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         sarmed |= 1u << ss;
         sarmed_par = (sarmed_par & ~(1u << ss)) | (sph << ss);
 
-        const int nsl = (ng + 3) / 4;
+        const int nsl = (ng + 1) / 2;
         for (int sl = 0; sl < nsl; ++sl) {
           if (!mbar_wait(&qempty[qs], qph ^ 1u, abort_flag)) {
             report(p.status, kDevTimeout, kSiteGemmProducer, (unsigned)tile, (unsigned)sl);
@@ -322,8 +324,8 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
                 const int yg = td.y * 64 + 16 * c;
-                tma_load_2d_hint(&p.wa_d0, &qfull[qs], dst + (2 * c) * kBoxBytes, x, yg, pol_w);
-                tma_load_2d_hint(&p.wa_d1, &qfull[qs], dst + (2 * c + 1) * kBoxBytes, x, yg, pol_w);
+                tma_load_2d_hint(&p.wa_d0, &qfull[qs], dst + (2 * c) * kQBoxBytes, x, yg, pol_w);
+                tma_load_2d_hint(&p.wa_d1, &qfull[qs], dst + (2 * c + 1) * kQBoxBytes, x, yg, pol_w);
               }
             }
           } else {
@@ -348,7 +350,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
             report(p.status, kDevTimeout, kSiteGemmDrain, (unsigned)s, 2u);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------- token slabs
+    // ------------------------------------------------- token stages
     if (lane == 0) {
       const uint64_t pol_x = l2_policy_evict_last();
       int bs = 0;
@@ -357,85 +359,81 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
         const int4 td = decode_tile(p, tile, nd, s_start, s_off);
         const bool dense = td.x == p.E;
-        const int kbn = dense ? p.kb_dense : p.kb_exp;
-        const int nsl = (kbn + 3) / 4;
+        const int ng = dense ? p.kb_dense : p.kb_exp;
         const int nb64 = td.w / 64;
         const int nb16 = (td.w - 64 * nb64 + kBoxRows - 1) / kBoxRows;
-        const uint32_t sub_bytes = nb64 * 64 * 128 + nb16 * kBoxBytes;
+        const uint32_t stage_bytes = nb64 * 64 * 128 + nb16 * kBoxBytes;
         const CUtensorMap* mb64 = dense ? &p.xb_d64 : &p.xb_exp64;
         const CUtensorMap* mb16 = dense ? &p.xb_d16 : &p.xb_exp16;
-        for (int sl = 0; sl < nsl; ++sl) {
+        for (int g = 0; g < ng; ++g) {
           if (!mbar_wait(&bempty[bs], bph ^ 1u, abort_flag)) {
-            report(p.status, kDevTimeout, kSiteGemmTokens, (unsigned)tile, (unsigned)sl);
+            report(p.status, kDevTimeout, kSiteGemmTokens, (unsigned)tile, (unsigned)g);
             *abort_flag = 1;
             ok = false;
             break;
           }
-          const int nsub = min(4, kbn - 4 * sl);
-          mbar_arrive_expect_tx(&bfull[bs], sub_bytes * (uint32_t)nsub);
-          for (int j = 0; j < nsub; ++j) {
-            uint8_t* b_dst = sB + (size_t)bs * C::kBSlabBytes + (size_t)j * BN * 128;
-            const int x = (4 * sl + j) * 64;
-            for (int r = 0; r < nb64; ++r)
-              tma_load_2d_hint(mb64, &bfull[bs], b_dst + r * 64 * 128, x, td.z + 64 * r, pol_x);
-            for (int r = 0; r < nb16; ++r)
-              tma_load_2d_hint(mb16, &bfull[bs], b_dst + (64 * nb64 + kBoxRows * r) * 128, x,
-                               td.z + 64 * nb64 + kBoxRows * r, pol_x);
-          }
+          mbar_arrive_expect_tx(&bfull[bs], stage_bytes);
+          uint8_t* b_dst = sB + (size_t)bs * C::kBStageBytes;
+          const int x = 64 * g;
+          for (int r = 0; r < nb64; ++r)
+            tma_load_2d_hint(mb64, &bfull[bs], b_dst + r * 64 * 128, x, td.z + 64 * r, pol_x);
+          for (int r = 0; r < nb16; ++r)
+            tma_load_2d_hint(mb16, &bfull[bs], b_dst + (64 * nb64 + kBoxRows * r) * 128, x,
+                             td.z + 64 * nb64 + kBoxRows * r, pol_x);
           armed |= 1u << bs;
           armed_par = (armed_par & ~(1u << bs)) | (bph << bs);
-          if (++bs == SB) {
+          if (++bs == NB) {
             bs = 0;
             bph ^= 1u;
           }
         }
       }
-      for (int s = 0; s < SB; ++s)
+      for (int s = 0; s < NB; ++s)
         if ((armed >> s) & 1u)
           if (!wait_no_abort(&bfull[s], (armed_par >> s) & 1u))
             report(p.status, kDevTimeout, kSiteGemmDrain, (unsigned)s, 3u);
     }
   } else if (warp == 2) {
     // ------------------------------------------------- MMA issuer
-    // Learns that a slab's operands are ready only through handoff(): it
+    // Learns that a stage's operands are ready only through handoff(): it
     // touches no mbarrier while its MMAs are in flight.
-    int bs = 0, as = 0, local = 0;
+    int bs = 0, local = 0;
+    uint32_t slab0 = 0;
+    uint64_t cnt = 0;
     bool stop = false, issued = false;
     for (int tile = blockIdx.x; tile < ntiles && !stop; tile += gridDim.x, ++local) {
       const int4 td = decode_tile(p, tile, nd, s_start, s_off);
       const bool dense = td.x == p.E;
-      const int kbn = dense ? p.kb_dense : p.kb_exp;
-      const int nsl = (kbn + 3) / 4;
+      const int ng = dense ? p.kb_dense : p.kb_exp;
       const int nb = (td.w + kBoxRows - 1) / kBoxRows;
       const int acc = local & 1;
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
       const uint32_t idesc = idesc_bf16_f32(128, nb * kBoxRows);
-      for (int sl = 0; sl < nsl; ++sl) {
+      for (int g = 0; g < ng; ++g) {
         if (handoff(false)) {
           stop = true;
           break;
         }
         tc_fence_after();
-        const int nsub = min(4, kbn - 4 * sl);
+        const int team = stage_team(slab0, g);
+        const uint32_t as = (uint32_t)team + 4u * (team_count(cnt, team) % C::kM);
+        cnt += 1ull << (16 * team);
         if (lane == 0) {
-          const uint32_t a_tmem = tmem_base + a_col0 + (uint32_t)(as * 128);
-          const uint32_t b_slab = smem_u32(sB + (size_t)bs * C::kBSlabBytes);
-          for (int j = 0; j < nsub; ++j) {
-            const uint32_t b0 = b_slab + (uint32_t)(j * BN * 128);
+          const uint32_t a0 = smem_u32(sA + (size_t)as * kAStageBytes);
+          const uint32_t b0 = smem_u32(sB + (size_t)bs * C::kBStageBytes);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              umma_bf16_ts(d_tmem, a_tmem + (uint32_t)(32 * j + 8 * k),
-                           sw128_kmajor_desc(b0 + 32 * k), idesc, (sl | j | k) != 0 ? 1u : 0u);
-          }
+          for (int k = 0; k < 4; ++k)
+            umma_bf16(d_tmem, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k),
+                      idesc, (g | k) != 0 ? 1u : 0u);
           umma_commit(&bempty[bs]);
           umma_commit(&aempty[as]);
-          if (sl == nsl - 1) umma_commit(&acc_full[acc]);
+          if (g == ng - 1) umma_commit(&acc_full[acc]);
         }
         issued = true;
-        if (++bs == SB) bs = 0;
-        if (++as == NA) as = 0;
+        if (++bs == NB) bs = 0;
         __syncwarp();
       }
+      slab0 += (uint32_t)(ng + 1) / 2;
     }
     // every MMA issued here must have completed before TMEM is released
     if (lane == 0 && issued) {
@@ -444,38 +442,39 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     }
   } else if (warp == 3) {
     // ------------------------------------------------- waiter for the issuer
-    int bs = 0, as = 0, local = 0;
-    uint32_t bph = 0, aph = 0;
+    int bs = 0, local = 0;
+    uint32_t bph = 0, slab0 = 0;
+    uint64_t cnt = 0;
     bool stop = false;
     for (int tile = blockIdx.x; tile < ntiles && !stop; tile += gridDim.x, ++local) {
       const int4 td = decode_tile(p, tile, nd, s_start, s_off);
       const bool dense = td.x == p.E;
-      const int kbn = dense ? p.kb_dense : p.kb_exp;
-      const int nsl = (kbn + 3) / 4;
+      const int ng = dense ? p.kb_dense : p.kb_exp;
       const int acc = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
-      for (int sl = 0; sl < nsl; ++sl) {
+      for (int g = 0; g < ng; ++g) {
         bool ok = true;
         unsigned what = 0;
-        if (sl == 0 && !mbar_wait(&acc_empty[acc], (use & 1u) ^ 1u, abort_flag)) {
+        const int team = stage_team(slab0, g);
+        const uint32_t n = team_count(cnt, team);
+        const uint32_t as = (uint32_t)team + 4u * (n % C::kM);
+        const uint32_t aph = (n / C::kM) & 1u;
+        cnt += 1ull << (16 * team);
+        if (g == 0 && !mbar_wait(&acc_empty[acc], (use & 1u) ^ 1u, abort_flag)) {
           ok = false;
           what = 0xffffffffu;
         }
         if (ok && !mbar_wait(&afull[as], aph, abort_flag)) {
           ok = false;
-          what = 0x10000u + sl;
+          what = 0x10000u + g;
         }
         if (ok && !mbar_wait(&bfull[bs], bph, abort_flag)) {
           ok = false;
-          what = 0x20000u + sl;
+          what = 0x20000u + g;
         }
-        if (++bs == SB) {
+        if (++bs == NB) {
           bs = 0;
           bph ^= 1u;
-        }
-        if (++as == NA) {
-          as = 0;
-          aph ^= 1u;
         }
         if (!ok) {
           if (lane == 0) report(p.status, kDevTimeout, kSiteGemmMma, (unsigned)tile, what);
@@ -486,15 +485,23 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
           break;
         }
       }
+      slab0 += (uint32_t)(ng + 1) / 2;
     }
   } else if (warp >= kDequantWarp0 && warp < kEpilogueWarp0) {
-    // ------------------------------------------------- dequantise into TMEM
-    const int q = warp & 3;                          // TMEM lane quarter
-    const int gg = (warp - kDequantWarp0) >> 2;      // group of 64 codes within a slab
-    const int row = 32 * q + lane;                   // weight row of the tile = TMEM lane
-    const uint32_t lane_base = tmem_base + ((uint32_t)(32 * q) << 16) + a_col0;
-    int qs = 0, as = 0, local = 0;
-    uint32_t qph = 0, aph = 0;
+    // ------------------------------------------------- dequantise into A stages
+    const int q = warp & 3;                          // 32-row quarter of the tile
+    const int team = (warp - kDequantWarp0) >> 2;
+    const int row = 32 * q + lane;                   // weight row of the tile
+    // this thread's row in an A stage (128B-swizzled K-major: 8-row atoms of
+    // 1024 bytes, 16-byte chunk c of row r at chunk c ^ (r & 7))
+    const uint32_t a_row = smem_u32(sA) + (uint32_t)((row >> 3) * 1024 + (row & 7) * 128);
+    const int rsw = row & 7;
+    // its row in a code slab (64B swizzle: 16-byte chunk c of row r at chunk
+    // c ^ ((r >> 1) & 3))
+    const int qsw = (row >> 1) & 3;
+    const int half = team & 1;  // which group of a slab this team expands
+    int local = 0;
+    uint32_t slab0 = 0, j = 0;  // global index of the tile's first slab; own stages
     bool ok = true;
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++local) {
       const int4 td = decode_tile(p, tile, nd, s_start, s_off);
@@ -510,50 +517,57 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       const uint16_t* sc_row =
           reinterpret_cast<const uint16_t*>(sScale + (size_t)ss * 2 * slot_bytes) + row * ng;
       const uint16_t* bi_row = sc_row + slot_bytes / 2;
-      const int nsl = (ng + 3) / 4;
+      const int nsl = (ng + 1) / 2;
       for (int sl = 0; sl < nsl; ++sl) {
-        if (!mbar_wait(&qfull[qs], qph, abort_flag) ||
-            !mbar_wait(&aempty[as], aph ^ 1u, abort_flag)) {
+        const uint32_t X = slab0 + (uint32_t)sl;  // global slab index
+        if ((int)(X & 1u) != (team >> 1)) continue;  // the other pair of teams' slab
+        const uint32_t qs = X % SQ, qph = (X / SQ) & 1u;
+        if (!mbar_wait(&qfull[qs], qph, abort_flag)) {
           if (lane == 0) report(p.status, kDevTimeout, kSiteGemmDequant, (unsigned)tile, (unsigned)sl);
           *abort_flag = 1;
           ok = false;
           break;
         }
-        tc_fence_after();
-        const int g = 4 * sl + gg;  // this warp's group of 64 codes
+        const int g = 2 * sl + half;  // this team's group of 64 codes
         if (g < ng) {
-          const uint8_t* qrow = sQ + (size_t)qs * kQSlabBytes + row * 128;
-          const int c = 2 * gg;  // its two 32-code chunks: c and c + 1
-          uint32_t w0[4], w1[4];
-          lds_u32x4(qrow + ((c ^ (row & 7)) << 4), w0);
-          lds_u32x4(qrow + (((c + 1) ^ (row & 7)) << 4), w1);
-          const uint32_t s = sc_row[g], b = bi_row[g];
-          const uint32_t s2 = s | (s << 16), b2 = b | (b << 16);
-          uint32_t o[32];
-          dequant32(w0, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
-          dequant32(w1, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[16]));
-          tmem_st32(lane_base + (uint32_t)(as * 128 + 16 * c), o);
+          const uint32_t as = (uint32_t)team + 4u * (j % C::kM), use = j / C::kM;
+          ++j;
+          if (!mbar_wait(&aempty[as], (use & 1u) ^ 1u, abort_flag)) {
+            if (lane == 0)
+              report(p.status, kDevTimeout, kSiteGemmDequant, (unsigned)tile, 0x10000u + sl);
+            *abort_flag = 1;
+            ok = false;
+            // the code slab is still released below so the producer drains
+          } else {
+            const uint8_t* qrow = sQ + (size_t)qs * kQSlabBytes + row * (kSlabK / 2);
+            const int c = 2 * half;  // the group's two 32-code chunks: c and c + 1
+            uint32_t w0[4], w1[4];
+            lds_u32x4(qrow + ((c ^ qsw) << 4), w0);
+            lds_u32x4(qrow + (((c + 1) ^ qsw) << 4), w1);
+            const uint32_t s = sc_row[g], b = bi_row[g];
+            const uint32_t s2 = s | (s << 16), b2 = b | (b << 16);
+            uint32_t o[32];
+            dequant32(w0, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
+            dequant32(w1, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[16]));
+            const uint32_t dst = a_row + as * (uint32_t)kAStageBytes;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+              sts_u32x4(dst + (uint32_t)((ch ^ rsw) << 4), o[4 * ch], o[4 * ch + 1],
+                        o[4 * ch + 2], o[4 * ch + 3]);
+            // make the generic-proxy stores visible to the tensor core
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&afull[as]);
+          }
         }
-        tmem_st_wait();
-        tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&afull[as]);
-          mbar_arrive(&qempty[qs]);
-        }
-        if (++qs == SQ) {
-          qs = 0;
-          qph ^= 1u;
-        }
-        if (++as == NA) {
-          as = 0;
-          aph ^= 1u;
-        }
+        if (lane == 0) mbar_arrive(&qempty[qs]);
+        if (!ok) break;
       }
+      slab0 += (uint32_t)nsl;
       __syncwarp();
       if (ok && lane == 0) mbar_arrive(&sempty[ss]);
     }
-    tmem_st_wait();
   } else {
     // ------------------------------------------------- epilogue
     const int q = warp & 3;
@@ -598,16 +612,21 @@ cudaError_t launch_q4(const GemmParams& p, int grid, cudaStream_t s) {
 }  // namespace
 
 size_t gemm_q4_smem_bytes(int bn, int sc_slot_bytes) {
-  const size_t fixed = bn == 128 ? CfgQ<128>::kFixed : bn == 64 ? CfgQ<64>::kFixed : CfgQ<32>::kFixed;
+  const size_t fixed = bn == 256   ? CfgQ<256>::kFixed
+                       : bn == 128 ? CfgQ<128>::kFixed
+                       : bn == 64  ? CfgQ<64>::kFixed
+                                   : CfgQ<32>::kFixed;
   return fixed + 4 * (size_t)sc_slot_bytes;
 }
 
 cudaError_t launch_gemm_q4(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s) {
   if (mode == 0) {
+    if (bn == 256) return launch_q4<0, 256>(p, grid, s);
     if (bn == 128) return launch_q4<0, 128>(p, grid, s);
     if (bn == 64) return launch_q4<0, 64>(p, grid, s);
     return launch_q4<0, 32>(p, grid, s);
   }
+  if (bn == 256) return launch_q4<1, 256>(p, grid, s);
   if (bn == 128) return launch_q4<1, 128>(p, grid, s);
   if (bn == 64) return launch_q4<1, 64>(p, grid, s);
   return launch_q4<1, 32>(p, grid, s);

@@ -33,7 +33,7 @@ struct RouterParams {
   float* logits;     // [T, E] fp32 logits
   int32_t* chunk_counts;  // [nchunks, E] expert histogram per 256 tokens (zeroed)
   uint16_t* xd;      // bf16 [T, H]
-  float* y_moe;      // [T, H], zeroed here
+  float* y_moe;      // [T, H], zeroed here (null: not zeroed)
   int* n_refined;    // counter of tokens whose top-k was re-checked exactly
 };
 
@@ -46,6 +46,7 @@ struct ScatterParams {
   int32_t* perm;             // [T*K]
   int32_t* tok_perm;         // [T*K]
   float* w_perm;             // [T*K]
+  int32_t* inv;              // [T*K] grouped row of assignment t*K + k, or null
   DevStatus* status;
 };
 
@@ -85,7 +86,8 @@ struct GemmParams {
   int dense_5d;          // gate_up: dense A tile through wa_d5
   uint16_t* act;         // gate_up out: bf16 [TK, I]
   uint16_t* act_d;       // gate_up out: bf16 [T, D]
-  float* y_moe;          // down out: f32 [T, H] (accumulated)
+  float* y_moe;          // down out: f32 [T, H] (accumulated), when y_perm is null
+  float* y_perm;         // down out: f32 [T*K, H], w * expert output per grouped row, or null
   float* y_dense;        // down out: f32 [T, H]
   const int32_t* tok_perm;
   const float* w_perm;
@@ -105,7 +107,11 @@ struct GemmParams {
 
 struct CombineParams {
   const float* y_dense;
-  const float* y_moe;
+  const float* y_moe;   // [T, H], read when y_perm is null
+  const float* y_perm;  // [T*K, H] weighted expert rows, or null
+  const int32_t* inv;   // [T*K] grouped row of each assignment (with y_perm)
+  int K;
+  float* y_moe_out;     // with y_perm: the summed [T, H] rows written here, or null
   const uint16_t* h;
   const uint16_t* w_post1;
   const uint16_t* w_post2;
@@ -117,6 +123,11 @@ struct CombineParams {
 };
 
 constexpr int kChunkTokens = 256;  // tokens per permutation chunk
+// From this many tokens on, the down GEMM stores each assignment's weighted
+// f32 row and the combine sums a token's K rows, instead of reducing into
+// the per-token accumulator with global atomics (whose throughput, ~1.7 TB/s
+// of payload on this part, bounds the down GEMM of large batches).
+constexpr int kPartialRowsMinTokens = 1024;
 // From this many tokens on, the logits come from the register-tiled kernel
 // (64 tokens x 64 experts per block) instead of the 4-token one (measured:
 // 4-token blocks are faster at 2048 tokens, 117 vs 195 us; the tiled kernel

@@ -25,8 +25,8 @@ const char* const kKernelNames[kNumKernels] = {
 
 struct Layout {
   size_t status, counters, r, xnorm, wnorm, logits, idx, w, chunk_counts, offsets, perm,
-      tok_perm, w_perm;
-  size_t xd, xe_perm, act, act_d, y_moe, y_dense, stage_in, stage_out;
+      tok_perm, w_perm, inv;
+  size_t xd, xe_perm, act, act_d, y_moe, y_dense, y_perm, stage_in, stage_out;
   size_t zero_begin, zero_end;  // counters and chunk counts, cleared per forward
   size_t total;
 };
@@ -58,12 +58,15 @@ Layout make_layout(const dg_moe_config_t& c) {
   L.perm = take(TK * 4);
   L.tok_perm = take(TK * 4);
   L.w_perm = take(TK * 4);
+  L.inv = take(TK * 4);
   L.xd = take(T * H * 2);
   L.xe_perm = take(TK * H * 2);
   L.act = take(TK * I * 2);
   L.act_d = take(T * D * 2);
   L.y_moe = take(T * H * 4);
   L.y_dense = take(T * H * 4);
+  // weighted expert rows, for batches that avoid the atomic reduction
+  L.y_perm = T >= (size_t)kPartialRowsMinTokens ? take(TK * H * 4) : 0;
   L.stage_in = take(T * H * 2);
   L.stage_out = take(T * H * 2);
   L.total = off;
@@ -86,7 +89,7 @@ dg_status_t check_config(const dg_moe_config_t* c) {
   if (!bf16w && !q4w) return DG_ERR_UNSUPPORTED;
   // 4-bit: one tile's scale and bias rows (128 x K/64 each, twice) must fit
   // in shared memory beside the pipelines
-  if (q4w && (c->hidden > 4096 || c->expert_inter > 4096 || c->dense_inter > 4096))
+  if (q4w && (c->hidden > 3008 || c->expert_inter > 3008 || c->dense_inter > 3008))
     return DG_ERR_UNSUPPORTED;
   if (c->router_fmt != DG_FMT_BF16 && c->router_fmt != DG_FMT_AFFINE_U8_G64)
     return DG_ERR_UNSUPPORTED;
@@ -287,7 +290,8 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
   m->dn.bi_d0 = m->dn.bi_d1 = u16(weights->dense_down.biases);
   m->gu.sc_slot_bytes = (int)round_up(128 * (H / 64) * 2, 128);
   m->dn.sc_slot_bytes = (int)round_up(128 * (I > D ? I : D) / 64 * 2, 128);
-  if (q4 && gemm_q4_smem_bytes(32, m->gu.sc_slot_bytes) > m->smem_optin) {
+  if (q4 && (gemm_q4_smem_bytes(32, m->gu.sc_slot_bytes) > m->smem_optin ||
+             gemm_q4_smem_bytes(32, m->dn.sc_slot_bytes) > m->smem_optin)) {
     delete m;
     return DG_ERR_UNSUPPORTED;
   }
@@ -373,7 +377,10 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
   rp.logits = reinterpret_cast<float*>(ws + L.logits);
   rp.chunk_counts = reinterpret_cast<int32_t*>(ws + L.chunk_counts);
   rp.xd = reinterpret_cast<uint16_t*>(ws + L.xd);
-  rp.y_moe = reinterpret_cast<float*>(ws + L.y_moe);
+  // large batches: weighted expert rows summed by the combine, no
+  // accumulator to clear; small ones: atomic adds into the cleared y_moe
+  const bool partials = T >= kPartialRowsMinTokens;
+  rp.y_moe = partials ? nullptr : reinterpret_cast<float*>(ws + L.y_moe);
   rp.n_refined = counters;
   mark(0);
   if (err == cudaSuccess) err = launch_router(rp, s);
@@ -390,6 +397,7 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
   sp.perm = reinterpret_cast<int32_t*>(ws + L.perm);
   sp.tok_perm = reinterpret_cast<int32_t*>(ws + L.tok_perm);
   sp.w_perm = reinterpret_cast<float*>(ws + L.w_perm);
+  sp.inv = partials ? reinterpret_cast<int32_t*>(ws + L.inv) : nullptr;
   sp.status = status;
   mark(2);
   if (err == cudaSuccess) err = launch_route_scatter(sp, s);
@@ -407,6 +415,7 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
   GemmParams gu = m->gu, dn = m->dn;
   gu.T = dn.T = T;
   gu.bn = dn.bn = bn;
+  dn.y_perm = partials ? reinterpret_cast<float*>(ws + L.y_perm) : nullptr;
   mark(4);
   if (err == cudaSuccess)
     err = m->q4 ? launch_gemm_q4(0, bn, gu, m->num_sms, s) : launch_gemm(0, bn, gu, m->num_sms, s);
@@ -417,6 +426,10 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
   CombineParams cp;
   cp.y_dense = reinterpret_cast<const float*>(ws + L.y_dense);
   cp.y_moe = reinterpret_cast<const float*>(ws + L.y_moe);
+  cp.y_perm = dn.y_perm;
+  cp.inv = sp.inv;
+  cp.K = K;
+  cp.y_moe_out = partials && dbg && dbg->y_moe ? reinterpret_cast<float*>(ws + L.y_moe) : nullptr;
   cp.h = rp.h;
   cp.w_post1 = static_cast<const uint16_t*>(m->w.w_post_ff1);
   cp.w_post2 = static_cast<const uint16_t*>(m->w.w_post_ff2);

@@ -30,7 +30,7 @@ size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Offsets inside the scratch array for T tokens, hidden H, E experts.
 struct RouteScratch {
-  size_t r, xnorm, wnorm, logits, counts, nref, xd, ymoe, total;
+  size_t r, xnorm, wnorm, logits, counts, nref, xd, total;
 };
 RouteScratch route_scratch_layout(size_t T, size_t H, size_t E) {
   RouteScratch s;
@@ -47,7 +47,6 @@ RouteScratch route_scratch_layout(size_t T, size_t H, size_t E) {
   s.wnorm = take(E * 4);
   s.logits = take(T * E * 4);
   s.xd = take(T * H * 2);
-  s.ymoe = take(T * H * 4);
   s.total = off;
   return s;
 }
@@ -126,7 +125,7 @@ extern "C" dg_status_t dg_moe_route_noalloc(const dg_moe_config_t* cfg,
   rp.logits = reinterpret_cast<float*>(sc + L.logits);
   rp.chunk_counts = reinterpret_cast<int32_t*>(sc + L.counts);
   rp.xd = reinterpret_cast<uint16_t*>(sc + L.xd);
-  rp.y_moe = reinterpret_cast<float*>(sc + L.ymoe);
+  rp.y_moe = nullptr;  // no accumulator to clear: routing only
   rp.n_refined = reinterpret_cast<int*>(sc + L.nref);
   if (launch_router(rp, s) != cudaSuccess) return DG_ERR_CUDA;
   if (launch_router_select(rp, s) != cudaSuccess) return DG_ERR_CUDA;

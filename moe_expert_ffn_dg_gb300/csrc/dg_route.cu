@@ -234,8 +234,10 @@ __global__ void __launch_bounds__(256) k_router_logits(const RouterParams p) {
         p.r_out[t] = rf;
         p.xnorm_out[t] = sqrtf(xnd) * 1.001f;  // rounded up: used in a bound
       }
-      float4* yr = reinterpret_cast<float4*>(p.y_moe + (size_t)t * H);
-      for (int v = lane; v < (H >> 2); v += 32) yr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (p.y_moe) {
+        float4* yr = reinterpret_cast<float4*>(p.y_moe + (size_t)t * H);
+        for (int v = lane; v < (H >> 2); v += 32) yr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
   }
   __syncthreads();
@@ -414,8 +416,10 @@ __global__ void __launch_bounds__(256, 3) k_router_logits_tile(const RouterParam
         p.r_out[t] = rf;
         p.xnorm_out[t] = sqrtf(xnd) * 1.001f;  // rounded up: used in a bound
       }
-      float4* yr = reinterpret_cast<float4*>(p.y_moe + (size_t)t * H);
-      for (int v = lane; v < (H >> 2); v += 32) yr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (p.y_moe) {
+        float4* yr = reinterpret_cast<float4*>(p.y_moe + (size_t)t * H);
+        for (int v = lane; v < (H >> 2); v += 32) yr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
   }
   __syncthreads();
@@ -948,6 +952,7 @@ __global__ void __launch_bounds__(256, 1) k_route_scatter(const ScatterParams p)
     p.perm[pos] = t * K + j;
     p.tok_perm[pos] = t;
     p.w_perm[pos] = p.w[(size_t)t * K + j];
+    if (p.inv) p.inv[t * K + j] = pos;
   }
 }
 

@@ -159,7 +159,7 @@ dg_status_t sc_check_config(const dg_sc_mlp_config_t* c) {
     return DG_ERR_UNSUPPORTED;
   if (c->max_tokens > (1 << 20)) return DG_ERR_UNSUPPORTED;
   if (c->fmt != DG_FMT_BF16 && c->fmt != DG_FMT_AFFINE_U4_G64) return DG_ERR_UNSUPPORTED;
-  if (c->fmt == DG_FMT_AFFINE_U4_G64 && (c->hidden > 4096 || c->inter > 4096))
+  if (c->fmt == DG_FMT_AFFINE_U4_G64 && (c->hidden > 3008 || c->inter > 3008))
     return DG_ERR_UNSUPPORTED;
   return DG_OK;
 }
@@ -275,6 +275,7 @@ dg_status_t dg_sc_mlp_create(const dg_sc_mlp_config_t* cfg, const dg_sc_mlp_weig
     g->act = nullptr;
     g->act_d = reinterpret_cast<uint16_t*>(ws + L.act);
     g->y_moe = nullptr;
+    g->y_perm = nullptr;
     g->y_dense = reinterpret_cast<float*>(ws + L.y);
     g->tok_perm = nullptr;
     g->w_perm = nullptr;
@@ -294,7 +295,8 @@ dg_status_t dg_sc_mlp_create(const dg_sc_mlp_config_t* cfg, const dg_sc_mlp_weig
   m->dn.bi_d0 = m->dn.bi_d1 = m->dn.bi_exp = u16(weights->down.biases);
   m->gu.sc_slot_bytes = (int)round_up(128 * (H / 64) * 2, 128);
   m->dn.sc_slot_bytes = (int)round_up(128 * (D / 64) * 2, 128);
-  if (q4 && gemm_q4_smem_bytes(32, m->gu.sc_slot_bytes) > m->smem_optin) {
+  if (q4 && (gemm_q4_smem_bytes(32, m->gu.sc_slot_bytes) > m->smem_optin ||
+             gemm_q4_smem_bytes(32, m->dn.sc_slot_bytes) > m->smem_optin)) {
     delete m;
     return DG_ERR_UNSUPPORTED;
   }

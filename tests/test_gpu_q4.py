@@ -37,7 +37,7 @@ def test_tiny_q4(randvec):
     run_and_check(wl, p, mi.make_tokens(wl), ref_bf16_weights=True)
 
 
-@pytest.mark.parametrize("T", [1, 17, 300, 4100])
+@pytest.mark.parametrize("T", [1, 17, 300, 1100, 4100])
 def test_tiny_q4_ragged_token_counts(T):
     wl = mi.get_workload("tiny")
     p = mi.make_layer_inputs(wl, randvec=True, quantise=True)
