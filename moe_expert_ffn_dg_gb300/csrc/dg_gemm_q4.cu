@@ -10,25 +10,28 @@
 //
 // Dataflow of one tile (128 weight rows x up to BN token rows), in stages of
 // one group (64 along K):
-//   warp 0   TMA: code slabs (128 rows x 128 codes = 8 KB, 64B swizzle,
-//            two stages each) into a ring, and per tile the rows' scales and
-//            biases (bulk copies);
+//   warp 0   TMA: code slabs (128 rows x 256 codes = 16 KB, 128B swizzle,
+//            four stages each) into a ring, and per tile the rows' scales and
+//            biases (bulk copies; the rows are 2K/64 bytes, not TMA-able);
 //   warp 1   TMA: the tokens of each stage (BN rows x 64 bf16) into a ring;
 //   warp 2   TMEM owner and MMA issuer: four tcgen05.mma (K = 16) per stage,
 //            both operands in shared memory;
 //   warp 3   waits, for the issuer, until a stage's operands are ready and
 //            hands it over through a named barrier (see below);
-//   warps 4-19  dequantise, in four teams of four warps (one warp per 32
-//            weight rows): stage s of the sequence belongs to team s mod 4,
+//   warps 4..  dequantise, in NT teams of four warps (one warp per 32 weight
+//            rows): stage s of the CTA's sequence belongs to team s mod NT,
 //            whose threads expand one row's 64 codes each to bf16 (exact
 //            s * q + b, one rounding) into one of the team's own A stages, in
 //            the 128B-swizzled K-major layout the MMA reads;
-//   warps 20-23 epilogue, as for bf16 weights (GEGLU or weighted combine).
+//   last 4   epilogue, as for bf16 weights (GEGLU or the weighted rows).
 // Dequantised weights go to shared memory rather than TMEM: concurrent
 // tcgen05.st traffic slows A-from-TMEM MMAs about threefold on this part,
-// while shared-memory stores at the full store rate leave shared-memory MMAs
-// at their unloaded cost (55 cycles for N <= 128, 128 for N = 256).  TMEM
-// then holds only the two fp32 accumulators, so token tiles go up to 256.
+// while shared-memory stores (and proxy fences) at the full store rate leave
+// shared-memory MMAs at their unloaded cost (55 cycles for N <= 128, 128 for
+// N = 256).  TMEM then holds only the two fp32 accumulators, so token tiles
+// go up to 256.  Every ring slot has one consumer group that takes its uses
+// in order (the A stages belong to one team each), so an mbarrier parity
+// wait can never be two phases ahead of its slot.
 //
 // Why the issuer does not wait on mbarriers itself: on sm_103a, a shared-
 // memory access (an mbarrier poll or a plain load) by a thread that has
@@ -50,47 +53,54 @@ namespace {
 
 using namespace gemm;
 
-constexpr int kSlabK = 128;                    // codes per row of a slab (two stages)
-constexpr int kQSlabBytes = 128 * kSlabK / 2;  // 8 KB
-constexpr int kQBoxBytes = 16 * kSlabK / 2;    // one 16-row box of a slab
-constexpr int kAStageBytes = 128 * 128;        // 128 rows x 64 bf16
+constexpr int kSlabK = 256;                    // codes per row of a slab (four stages)
+constexpr int kQSlabBytes = 128 * kSlabK / 2;  // 16 KB
+constexpr int kAGroupBytes = 128 * 128;        // 128 rows x 64 bf16
 constexpr int kDequantWarp0 = 4;
-constexpr int kNumDequantWarps = 16;           // 4 teams x 4 lane quarters
-constexpr int kEpilogueWarp0 = kDequantWarp0 + kNumDequantWarps;
-constexpr int kThreadsQ = 32 * (kEpilogueWarp0 + 4);  // 768
+// Completion of stage s (its four MMAs) is signalled on sdone[s mod
+// kStageRing], one commit per stage: a tcgen05.commit costs about as much as
+// a quarter of a stage's MMAs, so the token and A slots freed by one stage
+// share it.  A slot's next writer waits for the stage that last used it,
+// NB (tokens) or M * NT (A) stages back; with the ring longer than both, no
+// parity wait can alias.
+constexpr int kStageRing = 32;
 
-// Per token-tile width: code slabs in flight (SQ, even: slots of even slabs
-// feed teams 0 and 1, odd ones teams 2 and 3), token stages in flight (NB,
-// BN x 128 bytes each) and A stages per team (M; 16 KB each).  Every ring
-// slot has one consumer group that takes its uses in order, so an mbarrier
-// parity wait can never be two phases ahead of the slot.  The token ring
-// covers the L2 latency plus the MMA time of a stage (4 MMAs: ~220 cycles
-// for BN <= 128, 512 for BN = 256); a team refills its A stage while the
-// other three teams' stages are multiplied (two stages each for the
-// narrowest tiles, whose stages are shortest).  All fit beside
-// double-buffered per-tile scales of up to 47 groups (K = 3008).
+// Per token-tile width: groups of 64 along K per stage (GPS: one stage is
+// 4 * GPS MMAs, one hand-off and one commit; narrow tiles take two groups, as
+// each stage's fixed cost is then shared by twice the MMAs of ~55 cycles),
+// dequantising teams (NT), A stages per team (M; GPS x 16 KB each), code
+// slabs in flight (SQ) and token stages in flight (NB, GPS x BN x 128 bytes
+// each), beside double-buffered per-tile scales and biases.  The token ring
+// covers the L2 latency plus the MMA time of a stage; a team refills its A
+// stage while the other teams' stages are multiplied.  With K up to 2944
+// (46 groups) every width fits.
 template <int BN>
 struct CfgQ {
-  static constexpr int kSQ = BN == 64 ? 4 : 2;
-  static constexpr int kNB = BN == 256 ? 3 : BN == 128 ? 6 : BN == 64 ? 10 : 8;
-  static constexpr int kM = BN == 32 ? 2 : 1;
-  static constexpr int kNA = 4 * kM;
-  static constexpr int kBStageBytes = BN * 128;
-  static constexpr int kBarBytes = 512;
+  static constexpr int kGPS = BN <= 64 ? 2 : 1;
+  static constexpr int kNT = BN == 128 ? 4 : 3;
+  static constexpr int kM = 1;
+  static constexpr int kNA = kNT * kM;
+  static constexpr int kSQ = 2;
+  static constexpr int kNB = BN == 256 ? 3 : BN == 128 ? 5 : BN == 64 ? 3 : 6;
+  static constexpr int kAStageBytes = kGPS * kAGroupBytes;
+  static constexpr int kBGroupBytes = BN * 128;
+  static constexpr int kBStageBytes = kGPS * kBGroupBytes;
+  static constexpr int kNumDequantWarps = 4 * kNT;
+  static constexpr int kEpilogueWarp0 = kDequantWarp0 + kNumDequantWarps;
+  static constexpr int kThreads = 32 * (kEpilogueWarp0 + 4);
+  static constexpr int kBarBytes = 1024;
+  static_assert(kNB < kStageRing && kM * kNT < kStageRing, "stage ring too short");
+  // mbarriers (qfull, qempty, bfull, afull, sdone, sfull, sempty, acc_full,
+  // acc_empty, drain), then the TMEM address and the abort flag
+  static_assert(8 * (2 * kSQ + kNB + kNA + kStageRing + 9) + 8 <= kBarBytes, "barrier area");
   static constexpr size_t kFixed = 1024 + (size_t)kSQ * kQSlabBytes +
                                    (size_t)kNB * kBStageBytes + (size_t)kNA * kAStageBytes +
                                    kBarBytes + kTileTableBytes;
 };
 
-// Team that owns stage g of a tile whose first code slab has the global
-// index slab0: slabs alternate between teams {0, 1} and {2, 3}.
-__device__ __forceinline__ int stage_team(uint32_t slab0, int g) {
-  return 2 * (int)((slab0 + (uint32_t)(g >> 1)) & 1u) + (g & 1);
-}
-
-// Four per-team stage counters in one register (16 bits each; only their
-// low bits matter, for the slot and the parity): the issuer must not touch
-// local memory while its MMAs are in flight.
+// Per-team stage counters in one register (16 bits each; only their low
+// bits matter, for the slot and the parity): the issuer must not touch local
+// memory while its MMAs are in flight.
 __device__ __forceinline__ uint32_t team_count(uint64_t packed, int team) {
   return (uint32_t)(packed >> (16 * team)) & 0xFFFFu;
 }
@@ -168,23 +178,22 @@ __device__ __forceinline__ void dequant32(const uint32_t (&w)[4], uint32_t s2, u
 }
 
 template <int MODE, int BN>
-__global__ void __launch_bounds__(kThreadsQ, 1)
+__global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
     k_grouped_gemm_q4(const __grid_constant__ GemmParams p) {
   using C = CfgQ<BN>;
-  constexpr int SQ = C::kSQ, NB = C::kNB, NA = C::kNA;
+  constexpr int SQ = C::kSQ, NB = C::kNB, NA = C::kNA, NT = C::kNT, GPS = C::kGPS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sQ = smem;
   uint8_t* sB = sQ + (size_t)SQ * kQSlabBytes;
   uint8_t* sA = sB + (size_t)NB * C::kBStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sA + (size_t)NA * kAStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sA + (size_t)NA * C::kAStageBytes);
   uint64_t* qfull = bars;
   uint64_t* qempty = qfull + SQ;
   uint64_t* bfull = qempty + SQ;
-  uint64_t* bempty = bfull + NB;
-  uint64_t* afull = bempty + NB;
-  uint64_t* aempty = afull + NA;
-  uint64_t* sfull = aempty + NA;
+  uint64_t* afull = bfull + NB;
+  uint64_t* sdone = afull + NA;
+  uint64_t* sfull = sdone + kStageRing;
   uint64_t* sempty = sfull + 2;
   uint64_t* acc_full = sempty + 2;
   uint64_t* acc_empty = acc_full + 2;
@@ -202,19 +211,14 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < SQ; ++s) {
       mbar_init(&qfull[s], 1);
-      mbar_init(&qempty[s], 8);  // the two teams of the slot
+      mbar_init(&qempty[s], C::kNumDequantWarps);
     }
-    for (int s = 0; s < NB; ++s) {
-      mbar_init(&bfull[s], 1);
-      mbar_init(&bempty[s], 1);
-    }
-    for (int a = 0; a < NA; ++a) {
-      mbar_init(&afull[a], 4);  // the four warps of one team
-      mbar_init(&aempty[a], 1);
-    }
+    for (int s = 0; s < NB; ++s) mbar_init(&bfull[s], 1);
+    for (int a = 0; a < NA; ++a) mbar_init(&afull[a], 4);  // the four warps of one team
+    for (int r = 0; r < kStageRing; ++r) mbar_init(&sdone[r], 1);
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sfull[a], 1);
-      mbar_init(&sempty[a], kNumDequantWarps);
+      mbar_init(&sempty[a], C::kNumDequantWarps);
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], 4);
     }
@@ -243,7 +247,8 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   // everything above touches only this CTA's resources; from here on the
   // kernel reads what earlier kernels wrote
   pdl_wait();
-  if (warp >= kEpilogueWarp0) build_tile_table(p, threadIdx.x - 32 * kEpilogueWarp0, s_start, s_off);
+  if (warp >= C::kEpilogueWarp0)
+    build_tile_table(p, threadIdx.x - 32 * C::kEpilogueWarp0, s_start, s_off);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -303,8 +308,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         }
         sarmed |= 1u << ss;
         sarmed_par = (sarmed_par & ~(1u << ss)) | (sph << ss);
-
-        const int nsl = (ng + 1) / 2;
+        const int nsl = (ng + 3) / 4;
         for (int sl = 0; sl < nsl; ++sl) {
           if (!mbar_wait(&qempty[qs], qph ^ 1u, abort_flag)) {
             report(p.status, kDevTimeout, kSiteGemmProducer, (unsigned)tile, (unsigned)sl);
@@ -324,8 +328,8 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
                 const int yg = td.y * 64 + 16 * c;
-                tma_load_2d_hint(&p.wa_d0, &qfull[qs], dst + (2 * c) * kQBoxBytes, x, yg, pol_w);
-                tma_load_2d_hint(&p.wa_d1, &qfull[qs], dst + (2 * c + 1) * kQBoxBytes, x, yg, pol_w);
+                tma_load_2d_hint(&p.wa_d0, &qfull[qs], dst + (2 * c) * kBoxBytes, x, yg, pol_w);
+                tma_load_2d_hint(&p.wa_d1, &qfull[qs], dst + (2 * c + 1) * kBoxBytes, x, yg, pol_w);
               }
             }
           } else {
@@ -354,7 +358,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     if (lane == 0) {
       const uint64_t pol_x = l2_policy_evict_last();
       int bs = 0;
-      uint32_t bph = 0, armed = 0, armed_par = 0;
+      uint32_t bph = 0, armed = 0, armed_par = 0, st = 0;  // st: global stage index
       bool ok = true;
       for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
         const int4 td = decode_tile(p, tile, nd, s_start, s_off);
@@ -362,24 +366,31 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         const int ng = dense ? p.kb_dense : p.kb_exp;
         const int nb64 = td.w / 64;
         const int nb16 = (td.w - 64 * nb64 + kBoxRows - 1) / kBoxRows;
-        const uint32_t stage_bytes = nb64 * 64 * 128 + nb16 * kBoxBytes;
+        const uint32_t group_bytes = nb64 * 64 * 128 + nb16 * kBoxBytes;
         const CUtensorMap* mb64 = dense ? &p.xb_d64 : &p.xb_exp64;
         const CUtensorMap* mb16 = dense ? &p.xb_d16 : &p.xb_exp16;
-        for (int g = 0; g < ng; ++g) {
-          if (!mbar_wait(&bempty[bs], bph ^ 1u, abort_flag)) {
-            report(p.status, kDevTimeout, kSiteGemmTokens, (unsigned)tile, (unsigned)g);
+        const int nst = (ng + GPS - 1) / GPS;
+        for (int k = 0; k < nst; ++k, ++st) {
+          // the slot's previous stage, NB back, must have been multiplied
+          const uint32_t w = st - (uint32_t)NB;
+          if (st >= (uint32_t)NB &&
+              !mbar_wait(&sdone[w % kStageRing], (w / kStageRing) & 1u, abort_flag)) {
+            report(p.status, kDevTimeout, kSiteGemmTokens, (unsigned)tile, (unsigned)k);
             *abort_flag = 1;
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&bfull[bs], stage_bytes);
-          uint8_t* b_dst = sB + (size_t)bs * C::kBStageBytes;
-          const int x = 64 * g;
-          for (int r = 0; r < nb64; ++r)
-            tma_load_2d_hint(mb64, &bfull[bs], b_dst + r * 64 * 128, x, td.z + 64 * r, pol_x);
-          for (int r = 0; r < nb16; ++r)
-            tma_load_2d_hint(mb16, &bfull[bs], b_dst + (64 * nb64 + kBoxRows * r) * 128, x,
-                             td.z + 64 * nb64 + kBoxRows * r, pol_x);
+          const int ngk = min(GPS, ng - GPS * k);
+          mbar_arrive_expect_tx(&bfull[bs], group_bytes * (uint32_t)ngk);
+          for (int gi = 0; gi < ngk; ++gi) {
+            uint8_t* b_dst = sB + (size_t)bs * C::kBStageBytes + (size_t)gi * C::kBGroupBytes;
+            const int x = 64 * (GPS * k + gi);
+            for (int r = 0; r < nb64; ++r)
+              tma_load_2d_hint(mb64, &bfull[bs], b_dst + r * 64 * 128, x, td.z + 64 * r, pol_x);
+            for (int r = 0; r < nb16; ++r)
+              tma_load_2d_hint(mb16, &bfull[bs], b_dst + (64 * nb64 + kBoxRows * r) * 128, x,
+                               td.z + 64 * nb64 + kBoxRows * r, pol_x);
+          }
           armed |= 1u << bs;
           armed_par = (armed_par & ~(1u << bs)) | (bph << bs);
           if (++bs == NB) {
@@ -398,7 +409,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     // Learns that a stage's operands are ready only through handoff(): it
     // touches no mbarrier while its MMAs are in flight.
     int bs = 0, local = 0;
-    uint32_t slab0 = 0;
+    uint32_t st = 0;  // global stage index
     uint64_t cnt = 0;
     bool stop = false, issued = false;
     for (int tile = blockIdx.x; tile < ntiles && !stop; tile += gridDim.x, ++local) {
@@ -409,31 +420,38 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       const int acc = local & 1;
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
       const uint32_t idesc = idesc_bf16_f32(128, nb * kBoxRows);
-      for (int g = 0; g < ng; ++g) {
+      const int nst = (ng + GPS - 1) / GPS;
+      for (int k = 0; k < nst; ++k, ++st) {
         if (handoff(false)) {
           stop = true;
           break;
         }
         tc_fence_after();
-        const int team = stage_team(slab0, g);
-        const uint32_t as = (uint32_t)team + 4u * (team_count(cnt, team) % C::kM);
+        const int team = (int)(st % NT);
+        const uint32_t as = (uint32_t)team + NT * (team_count(cnt, team) % C::kM);
         cnt += 1ull << (16 * team);
         if (lane == 0) {
-          const uint32_t a0 = smem_u32(sA + (size_t)as * kAStageBytes);
-          const uint32_t b0 = smem_u32(sB + (size_t)bs * C::kBStageBytes);
+          // descriptors of the stage's first K step; each further step of 16
+          // (32 bytes) adds 2 to the address field
+          // (a group further: 16 KB of A, BN x 128 bytes of B)
+          const uint64_t da = sw128_kmajor_desc(smem_u32(sA + (size_t)as * C::kAStageBytes));
+          const uint64_t db = sw128_kmajor_desc(smem_u32(sB + (size_t)bs * C::kBStageBytes));
+          const int ngk = min(GPS, ng - GPS * k);
+          umma_bf16(d_tmem, da, db, idesc, k != 0 ? 1u : 0u);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            umma_bf16(d_tmem, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k),
-                      idesc, (g | k) != 0 ? 1u : 0u);
-          umma_commit(&bempty[bs]);
-          umma_commit(&aempty[as]);
-          if (g == ng - 1) umma_commit(&acc_full[acc]);
+          for (int kk = 1; kk < 4; ++kk) umma_bf16(d_tmem, da + 2 * kk, db + 2 * kk, idesc, 1u);
+          if (GPS == 2 && ngk == 2) {
+            const uint64_t da1 = da + (kAGroupBytes >> 4), db1 = db + (C::kBGroupBytes >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) umma_bf16(d_tmem, da1 + 2 * kk, db1 + 2 * kk, idesc, 1u);
+          }
+          umma_commit(&sdone[st % kStageRing]);
+          if (k == nst - 1) umma_commit(&acc_full[acc]);
         }
         issued = true;
         if (++bs == NB) bs = 0;
         __syncwarp();
       }
-      slab0 += (uint32_t)(ng + 1) / 2;
     }
     // every MMA issued here must have completed before TMEM is released
     if (lane == 0 && issued) {
@@ -443,7 +461,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
   } else if (warp == 3) {
     // ------------------------------------------------- waiter for the issuer
     int bs = 0, local = 0;
-    uint32_t bph = 0, slab0 = 0;
+    uint32_t bph = 0, st = 0;
     uint64_t cnt = 0;
     bool stop = false;
     for (int tile = blockIdx.x; tile < ntiles && !stop; tile += gridDim.x, ++local) {
@@ -452,25 +470,26 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       const int ng = dense ? p.kb_dense : p.kb_exp;
       const int acc = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
-      for (int g = 0; g < ng; ++g) {
+      const int nst = (ng + GPS - 1) / GPS;
+      for (int k = 0; k < nst; ++k, ++st) {
         bool ok = true;
         unsigned what = 0;
-        const int team = stage_team(slab0, g);
+        const int team = (int)(st % NT);
         const uint32_t n = team_count(cnt, team);
-        const uint32_t as = (uint32_t)team + 4u * (n % C::kM);
+        const uint32_t as = (uint32_t)team + NT * (n % C::kM);
         const uint32_t aph = (n / C::kM) & 1u;
         cnt += 1ull << (16 * team);
-        if (g == 0 && !mbar_wait(&acc_empty[acc], (use & 1u) ^ 1u, abort_flag)) {
+        if (k == 0 && !mbar_wait(&acc_empty[acc], (use & 1u) ^ 1u, abort_flag)) {
           ok = false;
           what = 0xffffffffu;
         }
         if (ok && !mbar_wait(&afull[as], aph, abort_flag)) {
           ok = false;
-          what = 0x10000u + g;
+          what = 0x10000u + k;
         }
         if (ok && !mbar_wait(&bfull[bs], bph, abort_flag)) {
           ok = false;
-          what = 0x20000u + g;
+          what = 0x20000u + k;
         }
         if (++bs == NB) {
           bs = 0;
@@ -485,28 +504,25 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
           break;
         }
       }
-      slab0 += (uint32_t)(ng + 1) / 2;
     }
-  } else if (warp >= kDequantWarp0 && warp < kEpilogueWarp0) {
+  } else if (warp < C::kEpilogueWarp0) {
     // ------------------------------------------------- dequantise into A stages
-    const int q = warp & 3;                          // 32-row quarter of the tile
+    const int q = warp & 3;                        // 32-row quarter of the tile
     const int team = (warp - kDequantWarp0) >> 2;
-    const int row = 32 * q + lane;                   // weight row of the tile
+    const int row = 32 * q + lane;                 // weight row of the tile
     // this thread's row in an A stage (128B-swizzled K-major: 8-row atoms of
-    // 1024 bytes, 16-byte chunk c of row r at chunk c ^ (r & 7))
+    // 1024 bytes, 16-byte chunk c of row r at chunk c ^ (r & 7)); the code
+    // slabs use the same swizzle on 128-byte rows
     const uint32_t a_row = smem_u32(sA) + (uint32_t)((row >> 3) * 1024 + (row & 7) * 128);
     const int rsw = row & 7;
-    // its row in a code slab (64B swizzle: 16-byte chunk c of row r at chunk
-    // c ^ ((r >> 1) & 3))
-    const int qsw = (row >> 1) & 3;
-    const int half = team & 1;  // which group of a slab this team expands
-    int local = 0;
-    uint32_t slab0 = 0, j = 0;  // global index of the tile's first slab; own stages
+    int qs = 0, local = 0;
+    uint32_t qph = 0, s0 = 0, j = 0;  // stage base of the tile; own stages so far
     bool ok = true;
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++local) {
       const int4 td = decode_tile(p, tile, nd, s_start, s_off);
       const bool dense = td.x == p.E;
       const int ng = dense ? p.kb_dense : p.kb_exp;
+      const int nsl = (ng + 3) / 4;
       const int ss = local & 1;
       const uint32_t sph = (uint32_t)(local >> 1) & 1u;
       if (!mbar_wait(&sfull[ss], sph, abort_flag)) {
@@ -517,54 +533,62 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
       const uint16_t* sc_row =
           reinterpret_cast<const uint16_t*>(sScale + (size_t)ss * 2 * slot_bytes) + row * ng;
       const uint16_t* bi_row = sc_row + slot_bytes / 2;
-      const int nsl = (ng + 1) / 2;
-      for (int sl = 0; sl < nsl; ++sl) {
-        const uint32_t X = slab0 + (uint32_t)sl;  // global slab index
-        if ((int)(X & 1u) != (team >> 1)) continue;  // the other pair of teams' slab
-        const uint32_t qs = X % SQ, qph = (X / SQ) & 1u;
+      for (int sl = 0; sl < nsl && ok; ++sl) {
         if (!mbar_wait(&qfull[qs], qph, abort_flag)) {
           if (lane == 0) report(p.status, kDevTimeout, kSiteGemmDequant, (unsigned)tile, (unsigned)sl);
           *abort_flag = 1;
           ok = false;
           break;
         }
-        const int g = 2 * sl + half;  // this team's group of 64 codes
-        if (g < ng) {
-          const uint32_t as = (uint32_t)team + 4u * (j % C::kM), use = j / C::kM;
+        const uint8_t* qrow = sQ + (size_t)qs * kQSlabBytes + row * 128;
+        // the slab's stages (4 / GPS of them, fewer at the tile's end)
+#pragma unroll 1
+        for (int k = (4 * sl) / GPS; k < (4 * sl + 4) / GPS && GPS * k < ng; ++k) {
+          const uint32_t stg = s0 + (uint32_t)k;  // global stage index
+          if ((int)(stg % NT) != team) continue;
+          const uint32_t as = (uint32_t)team + NT * (j % C::kM);
+          // the slot's previous stage (this team's, M own stages back)
+          const uint32_t w = stg - (uint32_t)(C::kM * NT);
+          const bool first_use = j < (uint32_t)C::kM;
           ++j;
-          if (!mbar_wait(&aempty[as], (use & 1u) ^ 1u, abort_flag)) {
+          if (!first_use && !mbar_wait(&sdone[w % kStageRing], (w / kStageRing) & 1u, abort_flag)) {
             if (lane == 0)
-              report(p.status, kDevTimeout, kSiteGemmDequant, (unsigned)tile, 0x10000u + sl);
+              report(p.status, kDevTimeout, kSiteGemmDequant, (unsigned)tile, 0x10000u + k);
             *abort_flag = 1;
             ok = false;
-            // the code slab is still released below so the producer drains
-          } else {
-            const uint8_t* qrow = sQ + (size_t)qs * kQSlabBytes + row * (kSlabK / 2);
-            const int c = 2 * half;  // the group's two 32-code chunks: c and c + 1
+            break;  // the code slab is still released below so the producer drains
+          }
+          const int ngk = min(GPS, ng - GPS * k);
+#pragma unroll 1
+          for (int gi = 0; gi < ngk; ++gi) {
+            const int g = GPS * k + gi, gs = g & 3;  // group in the tile, in the slab
             uint32_t w0[4], w1[4];
-            lds_u32x4(qrow + ((c ^ qsw) << 4), w0);
-            lds_u32x4(qrow + (((c + 1) ^ qsw) << 4), w1);
+            lds_u32x4(qrow + (((2 * gs) ^ rsw) << 4), w0);
+            lds_u32x4(qrow + (((2 * gs + 1) ^ rsw) << 4), w1);
             const uint32_t s = sc_row[g], b = bi_row[g];
             const uint32_t s2 = s | (s << 16), b2 = b | (b << 16);
             uint32_t o[32];
             dequant32(w0, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
             dequant32(w1, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[16]));
-            const uint32_t dst = a_row + as * (uint32_t)kAStageBytes;
+            const uint32_t dst = a_row + as * (uint32_t)C::kAStageBytes + gi * (uint32_t)kAGroupBytes;
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch)
               sts_u32x4(dst + (uint32_t)((ch ^ rsw) << 4), o[4 * ch], o[4 * ch + 1],
                         o[4 * ch + 2], o[4 * ch + 3]);
-            // make the generic-proxy stores visible to the tensor core
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&afull[as]);
           }
+          // make the generic-proxy stores visible to the tensor core
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&afull[as]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&qempty[qs]);
-        if (!ok) break;
+        if (++qs == SQ) {
+          qs = 0;
+          qph ^= 1u;
+        }
       }
-      slab0 += (uint32_t)nsl;
+      s0 += (uint32_t)((ng + GPS - 1) / GPS);
       __syncwarp();
       if (ok && lane == 0) mbar_arrive(&sempty[ss]);
     }
@@ -606,7 +630,7 @@ cudaError_t launch_q4(const GemmParams& p, int grid, cudaStream_t s) {
   cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm_q4<MODE, BN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  return launch_pdl(k_grouped_gemm_q4<MODE, BN>, dim3(grid), dim3(kThreadsQ), smem, s, p);
+  return launch_pdl(k_grouped_gemm_q4<MODE, BN>, dim3(grid), dim3(CfgQ<BN>::kThreads), smem, s, p);
 }
 
 }  // namespace

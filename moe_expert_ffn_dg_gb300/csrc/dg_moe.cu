@@ -88,8 +88,8 @@ dg_status_t check_config(const dg_moe_config_t* c) {
   const bool q4w = c->expert_fmt == DG_FMT_AFFINE_U4_G64 && c->dense_fmt == DG_FMT_AFFINE_U4_G64;
   if (!bf16w && !q4w) return DG_ERR_UNSUPPORTED;
   // 4-bit: one tile's scale and bias rows (128 x K/64 each, twice) must fit
-  // in shared memory beside the pipelines
-  if (q4w && (c->hidden > 3008 || c->expert_inter > 3008 || c->dense_inter > 3008))
+  // in shared memory beside the narrowest tiles' pipelines
+  if (q4w && (c->hidden > 2944 || c->expert_inter > 2944 || c->dense_inter > 2944))
     return DG_ERR_UNSUPPORTED;
   if (c->router_fmt != DG_FMT_BF16 && c->router_fmt != DG_FMT_AFFINE_U8_G64)
     return DG_ERR_UNSUPPORTED;

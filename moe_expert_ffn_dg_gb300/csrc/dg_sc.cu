@@ -159,7 +159,7 @@ dg_status_t sc_check_config(const dg_sc_mlp_config_t* c) {
     return DG_ERR_UNSUPPORTED;
   if (c->max_tokens > (1 << 20)) return DG_ERR_UNSUPPORTED;
   if (c->fmt != DG_FMT_BF16 && c->fmt != DG_FMT_AFFINE_U4_G64) return DG_ERR_UNSUPPORTED;
-  if (c->fmt == DG_FMT_AFFINE_U4_G64 && (c->hidden > 3008 || c->inter > 3008))
+  if (c->fmt == DG_FMT_AFFINE_U4_G64 && (c->hidden > 2944 || c->inter > 2944))
     return DG_ERR_UNSUPPORTED;
   return DG_OK;
 }
