@@ -169,6 +169,35 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
 dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tokens,
                            float layer_scalar, dg_stream_t stream, const dg_moe_debug_t* dbg);
 
+/* The block fused with its neighbours in the decoder layer ("DiffusionGemma
+ * port — plan & parity strategy", Reference dossier §2 DecoderLayer): the
+ * attention half's last step and the next layer's first one.
+ *
+ *   h       = x + post_attention_layernorm(attn_out)   (bf16 planes:
+ *             n = bf16(rms(attn_out) * w_post_attn), h = bf16(x + n))
+ *   out     = the block on h                           (as dg_moe_forward)
+ *   next_in = bf16(rms(out) * w_next_in)              (the next layer's
+ *             input_layernorm, optional)
+ *
+ * The router kernels build h from x and attn_out where they read the block
+ * input (no separate pass); the combine writes next_in beside out.  x is the
+ * decoder layer's input (the attention residual). */
+typedef struct {
+  const void* attn_out;     /* bf16 [n_tokens, H]: self-attention output (o_proj), before its norm */
+  const void* w_post_attn;  /* bf16 [H]: post_attention_layernorm weight of this layer */
+  const void* w_next_in;    /* bf16 [H]: the next layer's input_layernorm weight, or NULL */
+  void* next_in;            /* bf16 [n_tokens, H]: receives next_in; required with w_next_in */
+  void* h_mid;              /* bf16 [n_tokens, H]: receives h, or NULL (kept in the workspace) */
+} dg_moe_neighbours_t;
+
+/* x: bf16 [n_tokens, H]; out: bf16 [n_tokens, H] and may alias x (x is read
+ * only by the first kernel) or attn_out; next_in may alias x or attn_out but
+ * not out; h_mid aliases nothing.  All 16-byte aligned.  Otherwise as
+ * dg_moe_forward (dbg sees h as the block input). */
+dg_status_t dg_moe_forward_neighbours(dg_moe_t* m, const void* x, const dg_moe_neighbours_t* nb,
+                                      void* out, int n_tokens, float layer_scalar,
+                                      dg_stream_t stream, const dg_moe_debug_t* dbg);
+
 /* End-to-end forward with HOST buffers: copies h_in (host, bf16
  * [n_tokens, H]) into the workspace, runs dg_moe_forward, copies the result
  * to h_out (host) and synchronises the stream before returning.  Page-locked

@@ -31,7 +31,7 @@ EXPORTED = (
     "dg_moe_workspace_size", "dg_moe_create", "dg_moe_forward", "dg_moe_forward_host",
     "dg_moe_destroy", "dg_moe_last_device_status", "dg_moe_kernel_names",
     "dg_moe_set_profile_events", "dg_moe_status_string", "dg_moe_last_error",
-    "dg_moe_route_noalloc",
+    "dg_moe_route_noalloc", "dg_moe_forward_neighbours",
     "dg_sc_mlp_workspace_size", "dg_sc_mlp_create", "dg_sc_mlp_forward",
     "dg_sc_mlp_last_device_status", "dg_sc_mlp_destroy", "dg_sc_mlp_kernel_names",
     "dg_sc_mlp_set_profile_events",
@@ -56,6 +56,11 @@ class dg_moe_weights_t(ctypes.Structure):
                 ("router_scale", c_void_p), ("per_expert_scale", c_void_p),
                 ("w_pre_ff", c_void_p), ("w_pre_ff2", c_void_p), ("w_post_ff1", c_void_p),
                 ("w_post_ff2", c_void_p), ("w_post_ff", c_void_p), ("router_bias", c_void_p)]
+
+
+class dg_moe_neighbours_t(ctypes.Structure):
+    _fields_ = [("attn_out", c_void_p), ("w_post_attn", c_void_p), ("w_next_in", c_void_p),
+                ("next_in", c_void_p), ("h_mid", c_void_p)]
 
 
 class dg_moe_debug_t(ctypes.Structure):
@@ -100,6 +105,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dg_moe_forward.argtypes = [c_void_p, c_void_p, c_void_p, c_int, c_float, c_void_p,
                                    POINTER(dg_moe_debug_t)]
     lib.dg_moe_forward_host.argtypes = [c_void_p, c_void_p, c_void_p, c_int, c_float, c_void_p]
+    lib.dg_moe_forward_neighbours.argtypes = [c_void_p, c_void_p, POINTER(dg_moe_neighbours_t),
+                                              c_void_p, c_int, c_float, c_void_p,
+                                              POINTER(dg_moe_debug_t)]
     lib.dg_moe_destroy.argtypes = [c_void_p]
     lib.dg_moe_last_device_status.argtypes = [c_void_p, c_void_p, POINTER(c_uint), POINTER(c_uint)]
     lib.dg_moe_kernel_names.argtypes = [c_void_p, POINTER(c_char_p), POINTER(c_int)]
@@ -163,6 +171,15 @@ def dg_moe_forward(handle: int, h_in: int, h_out: int, n_tokens: int, layer_scal
                                          n_tokens, layer_scalar, c_void_p(stream),
                                          ctypes.byref(dbg) if dbg is not None else None),
            "dg_moe_forward", handle)
+
+
+def dg_moe_forward_neighbours(handle: int, x: int, nb: dg_moe_neighbours_t, out: int,
+                              n_tokens: int, layer_scalar: float, stream: int,
+                              dbg: dg_moe_debug_t | None = None) -> None:
+    _check(load_library().dg_moe_forward_neighbours(
+        c_void_p(handle), c_void_p(x), ctypes.byref(nb) if nb is not None else None,
+        c_void_p(out), n_tokens, layer_scalar, c_void_p(stream),
+        ctypes.byref(dbg) if dbg is not None else None), "dg_moe_forward_neighbours", handle)
 
 
 def dg_moe_forward_host(handle: int, h_in_host: int, h_out_host: int, n_tokens: int,

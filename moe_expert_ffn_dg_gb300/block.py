@@ -151,6 +151,31 @@ class MoEBlock:
                          self._stream(stream), dbg)
         return (out, tensors) if debug else out
 
+    def forward_neighbours(self, x: torch.Tensor, attn_out: torch.Tensor, w_post_attn: torch.Tensor,
+                           w_next_in: torch.Tensor = None, layer_scalar: float = 1.0,
+                           out: torch.Tensor = None, next_in: torch.Tensor = None,
+                           h_mid: torch.Tensor = None, stream=None):
+        """The block fused with the decoder layer's neighbours: x is the layer
+        input (attention residual), attn_out the attention output before its
+        post-norm; returns (out, next_in) where next_in is the next layer's
+        input norm of out (None without w_next_in).  h_mid, if given,
+        receives the block input x + post_attention_layernorm(attn_out)."""
+        for t in (x, attn_out):
+            assert t.dtype == torch.bfloat16 and t.is_contiguous() and t.shape[1] == self.hidden
+        assert x.shape == attn_out.shape
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty_like(x)
+        if w_next_in is not None and next_in is None:
+            next_in = torch.empty_like(x)
+        nb = B.dg_moe_neighbours_t(attn_out.data_ptr(), w_post_attn.data_ptr(),
+                                   w_next_in.data_ptr() if w_next_in is not None else None,
+                                   next_in.data_ptr() if w_next_in is not None else None,
+                                   h_mid.data_ptr() if h_mid is not None else None)
+        B.dg_moe_forward_neighbours(self.handle, x.data_ptr(), nb, out.data_ptr(), T,
+                                    float(layer_scalar), self._stream(stream))
+        return out, (next_in if w_next_in is not None else None)
+
     def forward_host(self, h_host: torch.Tensor, out_host: torch.Tensor, layer_scalar: float = 1.0,
                      stream=None) -> torch.Tensor:
         """End to end from host memory: copy in, forward, copy out, synchronise."""

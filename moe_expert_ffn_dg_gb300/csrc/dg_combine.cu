@@ -9,7 +9,8 @@
 // then two block reductions.  h and out may alias: each element of h is read
 // by the thread that writes the same element of out, before it writes.
 // y_moe is either read as the accumulated [T, H] rows or summed here from
-// the token's K weighted expert rows (large batches).
+// the token's K weighted expert rows (large batches).  Optionally the next
+// layer's input norm of the output plane is written beside it.
 #include "dg_kernels.h"
 
 namespace dg {
@@ -152,9 +153,12 @@ __global__ void __launch_bounds__(kThreads) k_combine(const CombineParams p) {
   block_sum2<NV>(ss, dummy, red);
   const float rs = 1.0f / sqrtf(ss / (float)H + p.eps);
   uint16_t* orow = p.out + (size_t)t * H;
+  uint2 ov[NV];
+  float sn = 0.f;
 #pragma unroll
   for (int j = 0; j < NV; ++j) {
     const int v = threadIdx.x + j * kThreads;
+    ov[j] = make_uint2(0u, 0u);
     if (v < nq) {
       float w3[4];
       bf16x4(p.w_post + 4 * v, w3);
@@ -163,7 +167,46 @@ __global__ void __launch_bounds__(kThreads) k_combine(const CombineParams p) {
             ((uint32_t)f32_to_bf16_rne((hv[j][1] + a[j][1] * rs * w3[1]) * p.layer_scalar) << 16);
       o.y = (uint32_t)f32_to_bf16_rne((hv[j][2] + a[j][2] * rs * w3[2]) * p.layer_scalar) |
             ((uint32_t)f32_to_bf16_rne((hv[j][3] + a[j][3] * rs * w3[3]) * p.layer_scalar) << 16);
-      *reinterpret_cast<uint2*>(orow + 4 * v) = o;
+      ov[j] = o;
+    }
+  }
+  if (p.w_next) {
+    // the next layer's input_layernorm on the bf16 output plane ("DiffusionGemma
+    // port — plan & parity strategy", Reference dossier §2 DecoderLayer:
+    // input_layernorm opens the next layer), fused here
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const float o4[4] = {__uint_as_float(ov[j].x << 16), __uint_as_float(ov[j].x & 0xffff0000u),
+                           __uint_as_float(ov[j].y << 16), __uint_as_float(ov[j].y & 0xffff0000u)};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sn = fmaf(o4[e], o4[e], sn);
+    }
+    block_sum2<NV>(sn, dummy, red);
+  }
+  // every input of the token is read by now: out may alias h
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const int v = threadIdx.x + j * kThreads;
+    if (v < nq) *reinterpret_cast<uint2*>(orow + 4 * v) = ov[j];
+  }
+  if (p.w_next) {
+    const float rn = 1.0f / sqrtf(sn / (float)H + p.eps);
+    uint16_t* nrow = p.next_out + (size_t)t * H;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int v = threadIdx.x + j * kThreads;
+      if (v < nq) {
+        float w4[4];
+        bf16x4(p.w_next + 4 * v, w4);
+        const float o4[4] = {__uint_as_float(ov[j].x << 16), __uint_as_float(ov[j].x & 0xffff0000u),
+                             __uint_as_float(ov[j].y << 16), __uint_as_float(ov[j].y & 0xffff0000u)};
+        uint2 q;
+        q.x = (uint32_t)f32_to_bf16_rne(o4[0] * rn * w4[0]) |
+              ((uint32_t)f32_to_bf16_rne(o4[1] * rn * w4[1]) << 16);
+        q.y = (uint32_t)f32_to_bf16_rne(o4[2] * rn * w4[2]) |
+              ((uint32_t)f32_to_bf16_rne(o4[3] * rn * w4[3]) << 16);
+        *reinterpret_cast<uint2*>(nrow + 4 * v) = q;
+      }
     }
   }
 }

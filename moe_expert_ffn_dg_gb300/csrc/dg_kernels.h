@@ -33,6 +33,13 @@ struct RouterParams {
   float* logits;     // [T, E] fp32 logits
   int32_t* chunk_counts;  // [nchunks, E] expert histogram per 256 tokens (zeroed)
   uint16_t* xd;      // bf16 [T, H]
+  // Fused attention half of the decoder layer: with attn non-null, h is the
+  // layer input (the attention residual) and the block input is built as
+  // bf16(h + bf16(rms(attn) * w_post_attn)), written to h_out by the first
+  // expert column (the later kernels then read h_out).
+  const uint16_t* attn;         // bf16 [T, H] or null
+  const uint16_t* w_post_attn;  // bf16 [H]
+  uint16_t* h_out;              // bf16 [T, H]
   float* y_moe;      // [T, H], zeroed here (null: not zeroed)
   int* n_refined;    // counter of tokens whose top-k was re-checked exactly
 };
@@ -112,6 +119,8 @@ struct CombineParams {
   const int32_t* inv;   // [T*K] grouped row of each assignment (with y_perm)
   int K;
   float* y_moe_out;     // with y_perm: the summed [T, H] rows written here, or null
+  const uint16_t* w_next;  // bf16 [H]: the next layer's input norm weight, or null
+  uint16_t* next_out;      // bf16 [T, H]: rms(out) * w_next, with w_next
   const uint16_t* h;
   const uint16_t* w_post1;
   const uint16_t* w_post2;

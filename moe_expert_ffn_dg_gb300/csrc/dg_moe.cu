@@ -26,7 +26,7 @@ const char* const kKernelNames[kNumKernels] = {
 struct Layout {
   size_t status, counters, r, xnorm, wnorm, logits, idx, w, chunk_counts, offsets, perm,
       tok_perm, w_perm, inv;
-  size_t xd, xe_perm, act, act_d, y_moe, y_dense, y_perm, stage_in, stage_out;
+  size_t xd, xe_perm, act, act_d, y_moe, y_dense, y_perm, hmid, stage_in, stage_out;
   size_t zero_begin, zero_end;  // counters and chunk counts, cleared per forward
   size_t total;
 };
@@ -60,6 +60,7 @@ Layout make_layout(const dg_moe_config_t& c) {
   L.w_perm = take(TK * 4);
   L.inv = take(TK * 4);
   L.xd = take(T * H * 2);
+  L.hmid = take(T * H * 2);  // the block input built by the fused attention half
   L.xe_perm = take(TK * H * 2);
   L.act = take(TK * I * 2);
   L.act_d = take(T * D * 2);
@@ -325,13 +326,11 @@ dg_status_t dg_moe_set_profile_events(dg_moe_t* m, dg_event_t* events, int n_eve
   return DG_OK;
 }
 
-dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tokens,
-                           float layer_scalar, dg_stream_t stream, const dg_moe_debug_t* dbg) {
-  if (!m) return DG_ERR_INVALID_ARG;
-  if (n_tokens < 0 || n_tokens > m->cfg.max_tokens) return DG_ERR_INVALID_ARG;
-  if (n_tokens == 0) return DG_OK;
-  if (!h_in || !h_out) return DG_ERR_INVALID_ARG;
-  if (!aligned(h_in, 16) || !aligned(h_out, 16)) return DG_ERR_ALIGNMENT;
+namespace {
+// One forward; nb (may be null) fuses the decoder layer's neighbours.
+dg_status_t forward_impl(dg_moe_t* m, const void* h_in, void* h_out, int n_tokens,
+                         float layer_scalar, dg_stream_t stream, const dg_moe_debug_t* dbg,
+                         const dg_moe_neighbours_t* nb) {
   const dg_moe_config_t& c = m->cfg;
   const Layout& L = m->L;
   uint8_t* ws = m->ws;
@@ -354,7 +353,7 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
   if ((err = cudaMemsetAsync(ws + L.zero_begin, 0, L.zero_end - L.zero_begin, s)) != cudaSuccess)
     return cuda_fail(m, "memset counters", err);
 
-  RouterParams rp;
+  RouterParams rp{};
   rp.h = static_cast<const uint16_t*>(h_in);
   rp.wr = m->w.router.q;
   rp.wr_scales = static_cast<const uint16_t*>(m->w.router.scales);
@@ -382,11 +381,22 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
   const bool partials = T >= kPartialRowsMinTokens;
   rp.y_moe = partials ? nullptr : reinterpret_cast<float*>(ws + L.y_moe);
   rp.n_refined = counters;
+  // the block input: h_in itself, or built by the router from the residual
+  // h_in and the attention output
+  const uint16_t* hb = rp.h;
+  if (nb) {
+    rp.attn = static_cast<const uint16_t*>(nb->attn_out);
+    rp.w_post_attn = static_cast<const uint16_t*>(nb->w_post_attn);
+    rp.h_out = static_cast<uint16_t*>(nb->h_mid ? nb->h_mid : ws + L.hmid);
+    hb = rp.h_out;
+  }
   mark(0);
   if (err == cudaSuccess) err = launch_router(rp, s);
+  rp.h = hb;
+  rp.attn = nullptr;
   mark(1);
   if (err == cudaSuccess) err = launch_router_select(rp, s);
-  ScatterParams sp;
+  ScatterParams sp{};
   sp.idx = rp.idx;
   sp.w = rp.w;
   sp.chunk_counts = reinterpret_cast<const int32_t*>(ws + L.chunk_counts);
@@ -402,8 +412,8 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
   mark(2);
   if (err == cudaSuccess) err = launch_route_scatter(sp, s);
 
-  GatherParams gp;
-  gp.h = rp.h;
+  GatherParams gp{};
+  gp.h = hb;
   gp.r = rp.r_out;
   gp.tok_perm = sp.tok_perm;
   gp.w_pre_ff2 = static_cast<const uint16_t*>(m->w.w_pre_ff2);
@@ -423,14 +433,18 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
   if (err == cudaSuccess)
     err = m->q4 ? launch_gemm_q4(1, bn, dn, m->num_sms, s) : launch_gemm(1, bn, dn, m->num_sms, s);
 
-  CombineParams cp;
+  CombineParams cp{};
   cp.y_dense = reinterpret_cast<const float*>(ws + L.y_dense);
   cp.y_moe = reinterpret_cast<const float*>(ws + L.y_moe);
   cp.y_perm = dn.y_perm;
   cp.inv = sp.inv;
   cp.K = K;
   cp.y_moe_out = partials && dbg && dbg->y_moe ? reinterpret_cast<float*>(ws + L.y_moe) : nullptr;
-  cp.h = rp.h;
+  cp.h = hb;
+  if (nb && nb->w_next_in) {
+    cp.w_next = static_cast<const uint16_t*>(nb->w_next_in);
+    cp.next_out = static_cast<uint16_t*>(nb->next_in);
+  }
   cp.w_post1 = static_cast<const uint16_t*>(m->w.w_post_ff1);
   cp.w_post2 = static_cast<const uint16_t*>(m->w.w_post_ff2);
   cp.w_post = static_cast<const uint16_t*>(m->w.w_post_ff);
@@ -464,6 +478,33 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
         return cuda_fail(m, "debug copy", err);
   }
   return DG_OK;
+}
+
+}  // namespace
+
+dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tokens,
+                           float layer_scalar, dg_stream_t stream, const dg_moe_debug_t* dbg) {
+  if (!m) return DG_ERR_INVALID_ARG;
+  if (n_tokens < 0 || n_tokens > m->cfg.max_tokens) return DG_ERR_INVALID_ARG;
+  if (n_tokens == 0) return DG_OK;
+  if (!h_in || !h_out) return DG_ERR_INVALID_ARG;
+  if (!aligned(h_in, 16) || !aligned(h_out, 16)) return DG_ERR_ALIGNMENT;
+  return forward_impl(m, h_in, h_out, n_tokens, layer_scalar, stream, dbg, nullptr);
+}
+
+dg_status_t dg_moe_forward_neighbours(dg_moe_t* m, const void* x, const dg_moe_neighbours_t* nb,
+                                      void* out, int n_tokens, float layer_scalar,
+                                      dg_stream_t stream, const dg_moe_debug_t* dbg) {
+  if (!m || !nb) return DG_ERR_INVALID_ARG;
+  if (n_tokens < 0 || n_tokens > m->cfg.max_tokens) return DG_ERR_INVALID_ARG;
+  if (n_tokens == 0) return DG_OK;
+  if (!x || !out || !nb->attn_out || !nb->w_post_attn) return DG_ERR_INVALID_ARG;
+  if (nb->w_next_in && !nb->next_in) return DG_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, out, nb->attn_out, nb->w_post_attn, nb->w_next_in, nb->next_in,
+                        nb->h_mid};
+  for (const void* q : ptrs)
+    if (q && !aligned(q, 16)) return DG_ERR_ALIGNMENT;
+  return forward_impl(m, x, out, n_tokens, layer_scalar, stream, dbg, nb);
 }
 
 dg_status_t dg_moe_forward_host(dg_moe_t* m, const void* h_in_host, void* h_out_host, int n_tokens,

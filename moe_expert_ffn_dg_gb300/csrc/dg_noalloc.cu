@@ -102,7 +102,7 @@ extern "C" dg_status_t dg_moe_route_noalloc(const dg_moe_config_t* cfg,
   // the histogram and the re-check counter must start at zero on every call
   if (cudaMemsetAsync(sc + L.counts, 0, L.r - L.counts, s) != cudaSuccess) return DG_ERR_CUDA;
 
-  RouterParams rp;
+  RouterParams rp{};
   rp.h = static_cast<const uint16_t*>(h_in);
   rp.wr = weights->router.q;
   rp.wr_scales = static_cast<const uint16_t*>(weights->router.scales);

@@ -65,6 +65,44 @@ __device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
   return (uint32_t)f32_to_bf16_rne(a) | ((uint32_t)f32_to_bf16_rne(b) << 16);
 }
 
+// The attention half of the decoder layer ends with h = residual +
+// post_attention_layernorm(attn) ("DiffusionGemma port — plan & parity
+// strategy", Reference dossier §2 DecoderLayer), both bf16 planes: the normed
+// attention n = bf16(attn * ra * w) and h = bf16(x + n), each rounded once
+// (x + n is exact in fp32 whenever it can change the bf16 result).  Eight
+// elements; ra = 1/rms of the token's attention row.
+__device__ __forceinline__ uint4 attn_residual8(const uint4& xv, const uint4& av, const uint4& wv,
+                                                float ra) {
+  float x[8], a[8], w[8];
+  unpack8(xv, x);
+  unpack8(av, a);
+  unpack8(wv, w);
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float n0 = __uint_as_float((uint32_t)f32_to_bf16_rne(a[2 * i] * ra * w[2 * i]) << 16);
+    const float n1 =
+        __uint_as_float((uint32_t)f32_to_bf16_rne(a[2 * i + 1] * ra * w[2 * i + 1]) << 16);
+    o[i] = pack2_bf16(x[2 * i] + n0, x[2 * i + 1] + n1);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// 1/rms of a bf16 row (fp32 rsqrt and one Newton step), summed by one warp.
+__device__ __forceinline__ float row_rinv(const uint4* row, int nvec, int H, float eps, int lane) {
+  float ss = 0.f;
+  for (int v = lane; v < nvec; v += 32) {
+    float f[8];
+    unpack8(__ldg(row + v), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+  }
+  ss = warp_sum_f(ss);
+  const float msq = ss / (float)H + eps;
+  float r = rsqrtf(msq);
+  return r * (1.5f - 0.5f * msq * r * r);
+}
+
 // Error-free transformations in fp32 (Knuth's TwoSum; Dekker's product via
 // FMA).  A pair (hi, lo) carries a sum whose rounding error is second order
 // (~n u^2 of the magnitudes), which keeps fp64 (slow on this part) out of
@@ -125,6 +163,7 @@ __global__ void __launch_bounds__(256) k_router_logits(const RouterParams p) {
   uint4* hs = reinterpret_cast<uint4*>(xs + (size_t)TB * kLogitSlices * LS);  // [TB][H/8]
   uint4* rss = hs + (size_t)TB * (H >> 3);                                    // router_scale
   uint4* wps = rss + (H >> 3);                                                // w_pre_ff
+  uint4* was = wps + (H >> 3);                   // w_post_attn (fused neighbour only)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * TB;
   const bool first_col = blockIdx.y == 0;
@@ -179,8 +218,27 @@ __global__ void __launch_bounds__(256) k_router_logits(const RouterParams p) {
   for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
     rss[v] = __ldg(reinterpret_cast<const uint4*>(p.router_scale) + v);
     if (first_col) wps[v] = __ldg(reinterpret_cast<const uint4*>(p.w_pre_ff) + v);
+    if (p.attn) was[v] = __ldg(reinterpret_cast<const uint4*>(p.w_post_attn) + v);
   }
   __syncthreads();
+  if (p.attn) {
+    // the block input from the attention half, in place of the residual
+    // rows; the first expert column publishes it
+    for (int tl = warp; tl < TB; tl += 8) {
+      const int t = t0 + tl;
+      if (t >= p.T) continue;
+      const uint4* arow = reinterpret_cast<const uint4*>(p.attn + (size_t)t * H);
+      const float ra = row_rinv(arow, nvec, H, p.eps, lane);
+      uint4* hrow = hs + (size_t)tl * nvec;
+      uint4* hout = reinterpret_cast<uint4*>(p.h_out + (size_t)t * H);
+      for (int v = lane; v < nvec; v += 32) {
+        const uint4 hv = attn_residual8(hrow[v], __ldg(arow + v), was[v], ra);
+        hrow[v] = hv;
+        if (first_col) hout[v] = hv;
+      }
+    }
+    __syncthreads();
+  }
 
   for (int tl = warp; tl < TB; tl += 8) {
     const int t = t0 + tl;
@@ -351,13 +409,15 @@ constexpr int kRK = 32;   // K per staged chunk
 constexpr int kXS = kRT + 4;
 constexpr int kWS = kRE + 4;
 
-template <bool U8>
+template <bool U8, bool FUSED>
 __global__ void __launch_bounds__(256, 3) k_router_logits_tile(const RouterParams p) {
   extern __shared__ __align__(16) uint8_t sm[];
   float* xT = reinterpret_cast<float*>(sm);           // [2][kRK][kXS]
   float* wT = xT + 2 * kRK * kXS;                     // [2][kRK][kWS]
   float* rs = wT + 2 * kRK * kWS;                     // [kRT] 1/rms
-  uint16_t* sc_s = reinterpret_cast<uint16_t*>(rs + kRT);  // [H] router_scale
+  float* ras = rs + kRT;                              // [kRT] 1/rms of attn (fused)
+  uint16_t* sc_s = reinterpret_cast<uint16_t*>(ras + kRT);  // [H] router_scale
+  uint16_t* wa_s = sc_s + p.H;                        // [H] w_post_attn (fused)
   const int H = p.H, E = p.E;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int t0 = blockIdx.x * kRT, e0 = blockIdx.y * kRE;
@@ -367,22 +427,37 @@ __global__ void __launch_bounds__(256, 3) k_router_logits_tile(const RouterParam
   pdl_trigger();
   pdl_wait();
 
-  for (int v = tid; v < nvec; v += 256)
+  constexpr bool fused = FUSED;
+  for (int v = tid; v < nvec; v += 256) {
     reinterpret_cast<uint4*>(sc_s)[v] = __ldg(reinterpret_cast<const uint4*>(p.router_scale) + v);
+    if (fused)
+      reinterpret_cast<uint4*>(wa_s)[v] = __ldg(reinterpret_cast<const uint4*>(p.w_post_attn) + v);
+  }
   __syncthreads();
 
-  // ---- per token: 1/rms (and, in the first expert column, |x|, xd, y_moe = 0)
+  // ---- per token: 1/rms (and, in the first expert column, |x|, xd, y_moe = 0;
+  // with the fused attention half, the block input is rebuilt from the
+  // residual and attention rows wherever it is read, and published here)
   for (int tl = warp; tl < kRT; tl += 8) {
     const int t = t0 + tl;
     if (t >= p.T) {
       if (lane == 0) rs[tl] = 0.f;
+      if (lane == 0) ras[tl] = 0.f;
       continue;
     }
     const uint4* hrow = reinterpret_cast<const uint4*>(p.h + (size_t)t * H);
+    const uint4* arow = reinterpret_cast<const uint4*>(fused ? p.attn + (size_t)t * H : p.h);
+    const float ra = fused ? row_rinv(arow, nvec, H, p.eps, lane) : 0.f;
+    if (lane == 0) ras[tl] = ra;
+    auto hvec = [&](int v) {
+      return fused ? attn_residual8(__ldg(hrow + v), __ldg(arow + v),
+                                    reinterpret_cast<const uint4*>(wa_s)[v], ra)
+                   : __ldg(hrow + v);
+    };
     float ss = 0.f;
     for (int v = lane; v < nvec; v += 32) {
       float f[8];
-      unpack8(__ldg(hrow + v), f);
+      unpack8(hvec(v), f);
 #pragma unroll
       for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
     }
@@ -394,9 +469,12 @@ __global__ void __launch_bounds__(256, 3) k_router_logits_tile(const RouterParam
     if (first_col) {
       float xnl = 0.f;
       uint4* xdrow = reinterpret_cast<uint4*>(p.xd + (size_t)t * H);
+      uint4* hout = reinterpret_cast<uint4*>(fused ? p.h_out + (size_t)t * H : p.xd);
       for (int v = lane; v < nvec; v += 32) {
         float f[8], sc[8], wp[8];
-        unpack8(__ldg(hrow + v), f);
+        const uint4 hv = hvec(v);
+        if (fused) hout[v] = hv;
+        unpack8(hv, f);
         unpack8(reinterpret_cast<const uint4*>(sc_s)[v], sc);
         unpack8(__ldg(reinterpret_cast<const uint4*>(p.w_pre_ff) + v), wp);
 #pragma unroll
@@ -432,13 +510,18 @@ __global__ void __launch_bounds__(256, 3) k_router_logits_tile(const RouterParam
   const bool need_norm = blockIdx.x == 0;
   const bool tok_ok = t0 + xt < p.T;
   const float rx = rs[xt];
+  const float rax = ras[xt];
   float wsq = 0.f;
-  uint4 hv;   // next chunk: 8 h values of token xt
+  uint4 hv;   // next chunk: 8 h values of token xt (the residual, when fused)
+  uint4 av;   // next chunk: 8 attention values of token xt (fused only)
   uint4 wv;   // next chunk: 8 router weights of expert we (bf16, or 8 codes in .x/.y)
   auto fetch = [&](int k0) {
     const int k = k0 + 8 * oc;
     hv = tok_ok ? __ldg(reinterpret_cast<const uint4*>(p.h + (size_t)(t0 + xt) * H + k))
                 : make_uint4(0u, 0u, 0u, 0u);
+    if (fused)
+      av = tok_ok ? __ldg(reinterpret_cast<const uint4*>(p.attn + (size_t)(t0 + xt) * H + k))
+                  : make_uint4(0u, 0u, 0u, 0u);
     if constexpr (!U8) {
       wv = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.wr) +
                                                 (size_t)e_load * H + k));
@@ -453,7 +536,8 @@ __global__ void __launch_bounds__(256, 3) k_router_logits_tile(const RouterParam
     float* xb = xT + buf * kRK * kXS + (8 * oc) * kXS + xt;
     float* wb = wT + buf * kRK * kWS + (8 * oc) * kWS + we;
     float f[8], sc[8];
-    unpack8(hv, f);
+    unpack8(fused ? attn_residual8(hv, av, reinterpret_cast<const uint4*>(wa_s)[k >> 3], rax) : hv,
+            f);
     unpack8(reinterpret_cast<const uint4*>(sc_s)[k >> 3], sc);
 #pragma unroll
     for (int i = 0; i < 8; ++i) xb[i * kXS] = f[i] * rx * sc[i] * cH;
@@ -546,17 +630,21 @@ __global__ void __launch_bounds__(256, 3) k_router_logits_tile(const RouterParam
 }
 
 size_t router_tile_smem(int H) {
-  return sizeof(float) * (2 * kRK * kXS + 2 * kRK * kWS + kRT) + (size_t)H * 2;
+  return sizeof(float) * (2 * kRK * kXS + 2 * kRK * kWS + 2 * kRT) + (size_t)H * 4;
 }
 
-template <bool U8>
-cudaError_t launch_router_tile(const RouterParams& p, cudaStream_t s) {
+template <bool U8, bool FUSED>
+cudaError_t launch_router_tile_f(const RouterParams& p, cudaStream_t s) {
   const size_t smem = router_tile_smem(p.H);
-  cudaError_t err = cudaFuncSetAttribute(k_router_logits_tile<U8>,
+  cudaError_t err = cudaFuncSetAttribute(k_router_logits_tile<U8, FUSED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const dim3 grid((p.T + kRT - 1) / kRT, (p.E + kRE - 1) / kRE);
-  return launch_pdl(k_router_logits_tile<U8>, grid, dim3(256), smem, s, p);
+  return launch_pdl(k_router_logits_tile<U8, FUSED>, grid, dim3(256), smem, s, p);
+}
+template <bool U8>
+cudaError_t launch_router_tile(const RouterParams& p, cudaStream_t s) {
+  return p.attn ? launch_router_tile_f<U8, true>(p, s) : launch_router_tile_f<U8, false>(p, s);
 }
 
 // Exact logits: sum_i W_ei (router_scale_i h_i) with every term exact in
@@ -1000,7 +1088,7 @@ __global__ void __launch_bounds__(256) k_gather_xe(const GatherParams p) {
 template <int TB>
 size_t router_smem(int H) {
   return sizeof(float) * (size_t)TB * kLogitSlices * (H / kLogitSlices + 4) +
-         (size_t)(TB + 2) * H * 2;
+         (size_t)(TB + 3) * H * 2;
 }
 
 template <int TB, bool U8>

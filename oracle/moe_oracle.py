@@ -57,7 +57,7 @@ __all__ = [
     "gelu_tanh",
     "router_logits", "select_topk", "routing_weights", "route",
     "geglu_mlp", "experts_forward", "dense_forward", "combine",
-    "permutation", "moe_block_forward", "sc_mlp_forward",
+    "permutation", "moe_block_forward", "sc_mlp_forward", "attn_residual", "next_input_norm",
 ]
 
 
@@ -69,8 +69,10 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
 
 def round_bf16(x: np.ndarray) -> np.ndarray:
     """Round float64 values to the nearest bf16 value (8 significant bits,
-    ties to even), returned as float64.  Used only by the bf16-activation
-    variant below; finite normal-range inputs."""
+    ties to even), returned as float64.  Used by the bf16-activation and
+    bf16-weight variants and for the bf16 planes around the block
+    (:func:`attn_residual`, :func:`next_input_norm`); finite normal-range
+    inputs."""
     x = np.asarray(x, dtype=np.float64)
     m, e = np.frexp(x)                       # x = m 2^e, 0.5 <= |m| < 1
     return np.ldexp(np.rint(m * 256.0) / 256.0, e)
@@ -304,3 +306,22 @@ def sc_mlp_forward(embeds_bits, signal_bits, p: dict, bf16_weights: bool = False
     sc = geglu_mlp(normed, decoded(p["gate"], bf16_weights), decoded(p["up"], bf16_weights),
                    decoded(p["down"], bf16_weights))
     return rms_norm(x + sc)
+
+
+def attn_residual(x_bits, attn_bits, w_post_attn) -> np.ndarray:
+    """The block's input from the attention half of the decoder layer:
+    ``h = residual + post_attention_layernorm(attn)`` ("DiffusionGemma port —
+    plan & parity strategy", Reference dossier §2 DecoderLayer), with the
+    normed attention output and the sum each a bf16 activation plane
+    ("diffgemma — architecture & implemented contract", Part III precision
+    policy), so each is rounded once.  Inputs bf16 bits [T, H] and the norm
+    weight; returns float64 values that are bf16 numbers."""
+    n = round_bf16(rms_norm(bf16_to_f64(attn_bits), to_f64(w_post_attn)))
+    return round_bf16(bf16_to_f64(x_bits) + n)
+
+
+def next_input_norm(out_bits, w_in_next) -> np.ndarray:
+    """The next decoder layer's input_layernorm of this layer's bf16 output
+    plane ("DiffusionGemma port ...", Reference dossier §2 DecoderLayer: the
+    layer opens with ``h = input_layernorm(x)``), rounded to bf16."""
+    return round_bf16(rms_norm(bf16_to_f64(out_bits), to_f64(w_in_next)))

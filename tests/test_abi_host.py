@@ -93,6 +93,9 @@ def test_create_rejects_bad_arguments_before_touching_the_gpu(lib):
 def test_null_handle_is_rejected_and_destroy_accepts_null(lib):
     assert lib.dg_moe_forward(None, 16, 16, 4, 1.0, None, None) == B.DG_ERR_INVALID_ARG
     assert lib.dg_moe_forward_host(None, 16, 16, 4, 1.0, None) == B.DG_ERR_INVALID_ARG
+    nb = B.dg_moe_neighbours_t(16, 16, None, None, None)
+    assert lib.dg_moe_forward_neighbours(None, 16, ctypes.byref(nb), 16, 4, 1.0, None,
+                                         None) == B.DG_ERR_INVALID_ARG
     assert lib.dg_moe_destroy(None) == B.DG_OK
     n = ctypes.c_int(0)
     assert lib.dg_moe_kernel_names(None, None, ctypes.byref(n)) == B.DG_ERR_INVALID_ARG

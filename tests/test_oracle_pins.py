@@ -540,3 +540,64 @@ def test_sc_permuting_tokens_permutes_outputs():
     a = o.sc_mlp_forward(p["embeds"], p["signal"], p)
     b = o.sc_mlp_forward(p["embeds"][pi], p["signal"][pi], p)
     np.testing.assert_array_equal(a[pi], b)
+
+
+# ---------------------------------------------------------------- decoder-layer neighbours
+
+def _planes(T=16, H=256, seed=3):
+    r = np.random.default_rng(seed)
+    bits = lambda a: mi.f32_to_bf16_bits(a.astype(np.float32))
+    return (bits(r.standard_normal((T, H))), bits(r.standard_normal((T, H)) * 3.0),
+            bits(r.uniform(0.5, 1.5, H)))
+
+
+def test_attn_residual_with_zero_attention_is_the_residual():
+    x, a, w = _planes()
+    got = o.attn_residual(x, np.zeros_like(a), w)
+    np.testing.assert_array_equal(got, o.bf16_to_f64(x))
+
+
+def test_attn_residual_constant_attention_rows_add_plus_minus_one():
+    # rows of a constant c normalise to sign(c) (1 - O(eps / c^2), which
+    # rounds to 1 in bf16), so with a unit weight h = bf16(x + sign(c))
+    x, _, _ = _planes()
+    T, H = x.shape
+    c = np.where(np.arange(T) % 2 == 0, 0.75, -2.5)
+    a = mi.f32_to_bf16_bits(np.repeat(c[:, None], H, 1).astype(np.float32))
+    ones = np.full(H, mi.BF16_ONE, dtype=np.uint16)
+    got = o.attn_residual(x, a, ones)
+    want = o.round_bf16(o.bf16_to_f64(x) + np.sign(c)[:, None])
+    np.testing.assert_array_equal(got, want)
+
+
+def test_attn_residual_against_torch_rms_norm():
+    import torch
+    x, a, w = _planes()
+    t = lambda b: torch.from_numpy(o.bf16_to_f64(b))
+    n = torch.nn.functional.rms_norm(t(a), (a.shape[1],), weight=t(w), eps=1e-6)
+    n = n.to(torch.bfloat16).to(torch.float64)          # torch's own rounding
+    want = (t(x) + n).to(torch.bfloat16).to(torch.float64).numpy()
+    got = o.attn_residual(x, a, w)
+    # torch rounds through fp32: identical except on the rare double-rounding case
+    diff = np.abs(got - want) / np.maximum(np.abs(want), 1e-30)
+    assert (got == want).mean() > 0.999 and diff.max() <= 2.0 ** -7
+
+
+def test_next_input_norm_constant_rows_give_the_weight():
+    _, _, w = _planes()
+    H = w.shape[0]
+    out = mi.f32_to_bf16_bits(np.array([[1.5] * H, [-0.25] * H], np.float32))
+    got = o.next_input_norm(out, w)
+    np.testing.assert_array_equal(got[0], o.bf16_to_f64(w))
+    np.testing.assert_array_equal(got[1], -o.bf16_to_f64(w))
+
+
+def test_next_input_norm_against_torch_rms_norm():
+    import torch
+    x, _, w = _planes()
+    t = lambda b: torch.from_numpy(o.bf16_to_f64(b))
+    want = torch.nn.functional.rms_norm(t(x), (x.shape[1],), weight=t(w), eps=1e-6)
+    want = want.to(torch.bfloat16).to(torch.float64).numpy()
+    got = o.next_input_norm(x, w)
+    diff = np.abs(got - want) / np.maximum(np.abs(want), 1e-30)
+    assert (got == want).mean() > 0.999 and diff.max() <= 2.0 ** -7
