@@ -8,7 +8,7 @@ that canvas with inputs resident in HBM.  The 1.56 GB of weights read per
 step are 12x the L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload canvas256|canvas256_q4|batch2048_zipf|stack30_q4|
+                  [--workload canvas256|canvas256_q4|canvas256_q4d8|batch2048_zipf|stack30_q4|
                               sc_canvas256|sc_canvas256_q4]
 
 Prints one JSON line.  ``--impl reference`` times the CPU oracle (the only
@@ -643,7 +643,7 @@ def run_ours(args):
                        "norm in, next layer's input norm out)" if args.neighbours else ""),
                    "tokens_per_step": wl.tokens,
                    "us_per_layer": ms * 1000.0, "parallelism": f"replicas x{world}",
-                   "weights": "bf16" if not wl.quant else f"u{wl.quant[0]} g64 affine experts and dense, u{wl.quant[2]} router, dequantised to bf16 on chip",
+                   "weights": "bf16" if not wl.quant else f"u{wl.quant[0]} g64 affine experts, u{wl.quant[1]} dense, u{wl.quant[2]} router, dequantised to bf16 on chip",
                    "l2": f"no flush: {alg['layer_bytes'] / 1e9:.3f} GB of weights per step, "
                          f"{alg['layer_bytes'] / 129e6:.1f}x the 129 MB L2",
                    "touched_experts": alg["touched_experts"]},
@@ -662,7 +662,9 @@ def run_ours(args):
                 **({"note": "the plain block through the host-buffer entry point"}
                    if args.neighbours else {})},
         "clocks": clk,
-        "gpu_launches": nk * args.steps,
+        # an 8-bit dense branch beside 4-bit experts adds a dense-only launch
+        # to each of the two GEMM slots
+        "gpu_launches": (nk + (2 if wl.quant and wl.quant[1] != wl.quant[0] else 0)) * args.steps,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, p, h_np)
@@ -686,8 +688,8 @@ def main():
     ap.add_argument("--neighbours", action="store_true",
                     help="time the block fused with the decoder layer's neighbouring norms")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=["canvas256", "canvas256_q4", "batch2048_zipf", "stack30_q4",
-                             "sc_canvas256", "sc_canvas256_q4"])
+                    choices=["canvas256", "canvas256_q4", "canvas256_q4d8", "batch2048_zipf",
+                             "stack30_q4", "sc_canvas256", "sc_canvas256_q4"])
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -1,17 +1,19 @@
-// Grouped tcgen05 GEMMs over 4-bit group-64 affine weights (sm_103a).
+// Grouped tcgen05 GEMMs over 4- or 8-bit group-64 affine weights (sm_103a).
 //
 // The weight format is the one of "DiffusionGemma port — plan & parity
 // strategy", Reference dossier §1 (OptiQ affine quantisation, group size 64,
-// 4-bit experts): per row, code words of 8 four-bit codes (code k of a word at
-// bits 4k), and per group of 64 codes a bf16 scale s and bias b; the weight is
-// s * q + b.  "diffgemma — architecture & implemented contract" (Part IV,
+// 4-bit experts, 8-bit where its predicate keeps 8 bits, as for the dense
+// MLP): per row, code words of 8 four-bit codes (code k of a word at bits 4k)
+// or bytes of 8-bit codes, and per group of 64 codes a bf16 scale s and bias
+// b; the weight is s * q + b.  "diffgemma — architecture & implemented contract" (Part IV,
 // measurements) names the dequantisation as the cost that dominates 4-bit
 // expert layers; here it runs beside the tensor core instead of in front of it.
 //
 // Dataflow of one tile (128 weight rows x up to BN token rows), in stages of
 // one group (64 along K):
-//   warp 0   TMA: code slabs (128 rows x 256 codes = 16 KB, 128B swizzle,
-//            four stages each) into a ring, and per tile the rows' scales and
+//   warp 0   TMA: code slabs (128 rows x 128 bytes = 16 KB, 128B swizzle:
+//            256 four-bit or 128 eight-bit codes a row) into a ring, and per
+//            tile the rows' scales and
 //            biases (bulk copies; the rows are 2K/64 bytes, not TMA-able);
 //   warp 1   TMA: the tokens of each stage (BN rows x 64 bf16) into a ring;
 //   warp 2   TMEM owner and MMA issuer: four tcgen05.mma (K = 16) per stage,
@@ -53,8 +55,8 @@ namespace {
 
 using namespace gemm;
 
-constexpr int kSlabK = 256;                    // codes per row of a slab (four stages)
-constexpr int kQSlabBytes = 128 * kSlabK / 2;  // 16 KB
+constexpr int kSlabWords = 32;                 // 32-bit code words per row of a slab
+constexpr int kQSlabBytes = 128 * kSlabWords * 4;  // 16 KB
 constexpr int kAGroupBytes = 128 * 128;        // 128 rows x 64 bf16
 constexpr int kDequantWarp0 = 4;
 // Completion of stage s (its four MMAs) is signalled on sdone[s mod
@@ -156,6 +158,30 @@ __device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 v) {
   return r;
 }
 
+// 16 eight-bit codes (four words, code k at byte k) -> 8 bf16 pairs in K
+// order, w = s * q + b rounded once to bf16.  q = 16 hi + lo with the two
+// nibbles exact as in dequant32 below, q itself exact in bf16 (8 bits), then
+// the group's fused multiply-add.
+__device__ __forceinline__ void dequant16_u8(const uint32_t (&w)[4], uint32_t s2, uint32_t b2,
+                                             uint32_t (&o)[8]) {
+  const __nv_bfloat162 s = as_bf162(s2), b = as_bf162(b2), m = as_bf162(0x43004300u),
+                       sixteen = as_bf162(0x41804180u);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t u = w[j] >> 4;
+#pragma unroll
+    for (int pp = 0; pp < 2; ++pp) {
+      // bytes 2pp and 2pp+1 of the word -> codes (low, high) of the pair
+      // result bytes [w byte 2pp, 0, w byte 2pp+1, 0] (selector 4 = a zero byte)
+      const uint32_t sel = 0x4140u + 0x0202u * pp;
+      const uint32_t lo = (__byte_perm(w[j], 0u, sel) & 0x000F000Fu) | 0x43004300u;
+      const uint32_t hi = (__byte_perm(u, 0u, sel) & 0x000F000Fu) | 0x43004300u;
+      const __nv_bfloat162 q = __hfma2(__hsub2(as_bf162(hi), m), sixteen, __hsub2(as_bf162(lo), m));
+      o[2 * j + pp] = as_u32(__hfma2(q, s, b));
+    }
+  }
+}
+
 // 32 codes (four words) -> 16 bf16 pairs in K order, w = s * q + b rounded
 // once to bf16.  A code q sits in the low mantissa bits of the bf16 128 + q
 // (0x4300 | q, exact); subtracting 128 leaves q exactly, then one fused
@@ -177,11 +203,12 @@ __device__ __forceinline__ void dequant32(const uint32_t (&w)[4], uint32_t s2, u
   }
 }
 
-template <int MODE, int BN>
+template <int MODE, int BN, int BITS>
 __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
     k_grouped_gemm_q4(const __grid_constant__ GemmParams p) {
   using C = CfgQ<BN>;
   constexpr int SQ = C::kSQ, NB = C::kNB, NA = C::kNA, NT = C::kNT, GPS = C::kGPS;
+  constexpr int GPSL = BITS == 4 ? 4 : 2;  // groups of 64 per code slab
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sQ = smem;
@@ -308,7 +335,7 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
         }
         sarmed |= 1u << ss;
         sarmed_par = (sarmed_par & ~(1u << ss)) | (sph << ss);
-        const int nsl = (ng + 3) / 4;
+        const int nsl = (ng + GPSL - 1) / GPSL;
         for (int sl = 0; sl < nsl; ++sl) {
           if (!mbar_wait(&qempty[qs], qph ^ 1u, abort_flag)) {
             report(p.status, kDevTimeout, kSiteGemmProducer, (unsigned)tile, (unsigned)sl);
@@ -318,7 +345,7 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
           }
           mbar_arrive_expect_tx(&qfull[qs], kQSlabBytes);
           uint8_t* dst = sQ + (size_t)qs * kQSlabBytes;
-          const int x = sl * (kSlabK / 8);  // u32 words
+          const int x = sl * kSlabWords;
           if (MODE == 0) {
             if (!dense) {
               tma_load_5d(&p.wa_exp, &qfull[qs], dst, x, 0, 0, 4 * td.y, td.x, pol_w);
@@ -522,7 +549,7 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
       const int4 td = decode_tile(p, tile, nd, s_start, s_off);
       const bool dense = td.x == p.E;
       const int ng = dense ? p.kb_dense : p.kb_exp;
-      const int nsl = (ng + 3) / 4;
+      const int nsl = (ng + GPSL - 1) / GPSL;
       const int ss = local & 1;
       const uint32_t sph = (uint32_t)(local >> 1) & 1u;
       if (!mbar_wait(&sfull[ss], sph, abort_flag)) {
@@ -541,9 +568,9 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
           break;
         }
         const uint8_t* qrow = sQ + (size_t)qs * kQSlabBytes + row * 128;
-        // the slab's stages (4 / GPS of them, fewer at the tile's end)
+        // the slab's stages (GPSL / GPS of them, fewer at the tile's end)
 #pragma unroll 1
-        for (int k = (4 * sl) / GPS; k < (4 * sl + 4) / GPS && GPS * k < ng; ++k) {
+        for (int k = (GPSL * sl) / GPS; k < (GPSL * sl + GPSL) / GPS && GPS * k < ng; ++k) {
           const uint32_t stg = s0 + (uint32_t)k;  // global stage index
           if ((int)(stg % NT) != team) continue;
           const uint32_t as = (uint32_t)team + NT * (j % C::kM);
@@ -561,15 +588,24 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
           const int ngk = min(GPS, ng - GPS * k);
 #pragma unroll 1
           for (int gi = 0; gi < ngk; ++gi) {
-            const int g = GPS * k + gi, gs = g & 3;  // group in the tile, in the slab
-            uint32_t w0[4], w1[4];
-            lds_u32x4(qrow + (((2 * gs) ^ rsw) << 4), w0);
-            lds_u32x4(qrow + (((2 * gs + 1) ^ rsw) << 4), w1);
+            const int g = GPS * k + gi, gs = g % GPSL;  // group in the tile, in the slab
             const uint32_t s = sc_row[g], b = bi_row[g];
             const uint32_t s2 = s | (s << 16), b2 = b | (b << 16);
             uint32_t o[32];
-            dequant32(w0, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
-            dequant32(w1, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[16]));
+            if (BITS == 4) {  // the group's 32 bytes: chunks 2gs, 2gs + 1
+              uint32_t w0[4], w1[4];
+              lds_u32x4(qrow + (((2 * gs) ^ rsw) << 4), w0);
+              lds_u32x4(qrow + (((2 * gs + 1) ^ rsw) << 4), w1);
+              dequant32(w0, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
+              dequant32(w1, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[16]));
+            } else {  // 64 bytes: chunks 4gs .. 4gs + 3
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                uint32_t wv[4];
+                lds_u32x4(qrow + (((4 * gs + c) ^ rsw) << 4), wv);
+                dequant16_u8(wv, s2, b2, *reinterpret_cast<uint32_t(*)[8]>(&o[8 * c]));
+              }
+            }
             const uint32_t dst = a_row + as * (uint32_t)C::kAStageBytes + gi * (uint32_t)kAGroupBytes;
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch)
@@ -624,13 +660,28 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
   }
 }
 
-template <int MODE, int BN>
+template <int MODE, int BN, int BITS>
 cudaError_t launch_q4(const GemmParams& p, int grid, cudaStream_t s) {
   const size_t smem = CfgQ<BN>::kFixed + 4 * (size_t)p.sc_slot_bytes;
-  cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm_q4<MODE, BN>,
+  cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm_q4<MODE, BN, BITS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  return launch_pdl(k_grouped_gemm_q4<MODE, BN>, dim3(grid), dim3(CfgQ<BN>::kThreads), smem, s, p);
+  return launch_pdl(k_grouped_gemm_q4<MODE, BN, BITS>, dim3(grid), dim3(CfgQ<BN>::kThreads), smem,
+                    s, p);
+}
+
+template <int BITS>
+cudaError_t launch_bits(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s) {
+  if (mode == 0) {
+    if (bn == 256) return launch_q4<0, 256, BITS>(p, grid, s);
+    if (bn == 128) return launch_q4<0, 128, BITS>(p, grid, s);
+    if (bn == 64) return launch_q4<0, 64, BITS>(p, grid, s);
+    return launch_q4<0, 32, BITS>(p, grid, s);
+  }
+  if (bn == 256) return launch_q4<1, 256, BITS>(p, grid, s);
+  if (bn == 128) return launch_q4<1, 128, BITS>(p, grid, s);
+  if (bn == 64) return launch_q4<1, 64, BITS>(p, grid, s);
+  return launch_q4<1, 32, BITS>(p, grid, s);
 }
 
 }  // namespace
@@ -643,17 +694,9 @@ size_t gemm_q4_smem_bytes(int bn, int sc_slot_bytes) {
   return fixed + 4 * (size_t)sc_slot_bytes;
 }
 
-cudaError_t launch_gemm_q4(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s) {
-  if (mode == 0) {
-    if (bn == 256) return launch_q4<0, 256>(p, grid, s);
-    if (bn == 128) return launch_q4<0, 128>(p, grid, s);
-    if (bn == 64) return launch_q4<0, 64>(p, grid, s);
-    return launch_q4<0, 32>(p, grid, s);
-  }
-  if (bn == 256) return launch_q4<1, 256>(p, grid, s);
-  if (bn == 128) return launch_q4<1, 128>(p, grid, s);
-  if (bn == 64) return launch_q4<1, 64>(p, grid, s);
-  return launch_q4<1, 32>(p, grid, s);
+cudaError_t launch_gemm_affine(int mode, int bn, int bits, const GemmParams& p, int grid,
+                               cudaStream_t s) {
+  return bits == 8 ? launch_bits<8>(mode, bn, p, grid, s) : launch_bits<4>(mode, bn, p, grid, s);
 }
 
 }  // namespace dg

@@ -87,14 +87,19 @@ inline bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t rows, 
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box);
 }
 
-// Row-major 4-bit code matrix [rows, K] (u32 words of 8 codes) read in boxes
-// of box_rows x 32 words (256 codes, 128 bytes).
-inline bool encode_q4_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K,
-                    uint32_t box_rows) {
-  const uint64_t dims[2] = {K / 8, rows};
-  const uint64_t strides[1] = {K / 2};
+// Row-major affine code matrix [rows, K] (4-bit: u32 words of 8 codes;
+// 8-bit: one byte a code) read as u32 words in boxes of box_rows x 32 words
+// (128 bytes: 256 or 128 codes).
+inline bool encode_q_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K,
+                          uint32_t box_rows, int bits) {
+  const uint64_t dims[2] = {K * bits / 32, rows};
+  const uint64_t strides[1] = {K * bits / 8};
   const uint32_t box[2] = {32, box_rows};
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, base, dims, strides, box);
+}
+inline bool encode_q4_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K,
+                           uint32_t box_rows) {
+  return encode_q_rows(map, base, rows, K, box_rows, 4);
 }
 
 // gate_up weights as [groups][2 halves][n/16 chunks][16 rows][K]: one box of
@@ -102,15 +107,16 @@ inline bool encode_q4_rows(CUtensorMap* map, const void* base, uint64_t rows, ui
 // the 16 matching up rows, four times.  half_stride is the byte distance from
 // a gate row to its up row; group_stride the distance between groups.
 // rank 5 (with a group dimension) for the expert stack, rank 4 for the
-// dense pair.  q4: 4-bit code words instead of bf16.
+// dense pair.  qbits 4 or 8: affine code words (128 bytes of a row per box)
+// instead of bf16 (qbits 0).
 inline bool encode_gate_up(CUtensorMap* map, const void* gate, uint64_t K, uint64_t n,
                     uint64_t half_stride, int rank, uint64_t groups, uint64_t group_stride,
-                    bool q4 = false) {
-  const uint64_t row_bytes = q4 ? K / 2 : K * 2;
-  const uint64_t dims[5] = {q4 ? K / 8 : K, 16, 2, n / 16, groups};
+                    int qbits = 0) {
+  const uint64_t row_bytes = qbits ? K * qbits / 8 : K * 2;
+  const uint64_t dims[5] = {qbits ? K * qbits / 32 : K, 16, 2, n / 16, groups};
   const uint64_t strides[4] = {row_bytes, half_stride, 16 * row_bytes, group_stride};
-  const uint32_t box[5] = {q4 ? 32u : 64u, 16, 2, 4, 1};
-  return encode_tiled(map, q4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+  const uint32_t box[5] = {qbits ? 32u : 64u, 16, 2, 4, 1};
+  return encode_tiled(map, qbits ? CU_TENSOR_MAP_DATA_TYPE_UINT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                       rank, gate, dims, strides, box);
 }
 

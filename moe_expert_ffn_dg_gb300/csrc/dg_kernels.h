@@ -169,7 +169,9 @@ cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s);
 size_t gemm_smem_bytes(int bn);
 // 4-bit weights, dequantised into TMEM; same modes.  bn is 64 or 128.
-cudaError_t launch_gemm_q4(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s);
+// Grouped GEMM over group-64 affine weights of `bits` (4 or 8) bits.
+cudaError_t launch_gemm_affine(int mode, int bn, int bits, const GemmParams& p, int grid,
+                               cudaStream_t s);
 size_t gemm_q4_smem_bytes(int bn, int sc_slot_bytes);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 

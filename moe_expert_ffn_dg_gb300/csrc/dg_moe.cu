@@ -25,7 +25,7 @@ const char* const kKernelNames[kNumKernels] = {
 
 struct Layout {
   size_t status, counters, r, xnorm, wnorm, logits, idx, w, chunk_counts, offsets, perm,
-      tok_perm, w_perm, inv;
+      tok_perm, w_perm, inv, zero16;
   size_t xd, xe_perm, act, act_d, y_moe, y_dense, y_perm, hmid, stage_in, stage_out;
   size_t zero_begin, zero_end;  // counters and chunk counts, cleared per forward
   size_t total;
@@ -59,6 +59,7 @@ Layout make_layout(const dg_moe_config_t& c) {
   L.tok_perm = take(TK * 4);
   L.w_perm = take(TK * 4);
   L.inv = take(TK * 4);
+  L.zero16 = take(16);  // expert offsets {0} of a launch with no experts
   L.xd = take(T * H * 2);
   L.hmid = take(T * H * 2);  // the block input built by the fused attention half
   L.xe_perm = take(TK * H * 2);
@@ -84,9 +85,11 @@ dg_status_t check_config(const dg_moe_config_t* c) {
   if (c->hidden % 128 || c->expert_inter % 64 || c->dense_inter % 64) return DG_ERR_UNSUPPORTED;
   if (c->hidden > 8192 || c->n_experts > 256 || c->top_k > 16) return DG_ERR_UNSUPPORTED;
   if (c->max_tokens > (1 << 20)) return DG_ERR_UNSUPPORTED;
-  // expert and dense weights: both bf16, or both 4-bit group-64 affine
+  // expert and dense weights: both bf16, or 4-bit group-64 affine experts
+  // with a 4- or 8-bit dense branch
   const bool bf16w = c->expert_fmt == DG_FMT_BF16 && c->dense_fmt == DG_FMT_BF16;
-  const bool q4w = c->expert_fmt == DG_FMT_AFFINE_U4_G64 && c->dense_fmt == DG_FMT_AFFINE_U4_G64;
+  const bool q4w = c->expert_fmt == DG_FMT_AFFINE_U4_G64 &&
+                   (c->dense_fmt == DG_FMT_AFFINE_U4_G64 || c->dense_fmt == DG_FMT_AFFINE_U8_G64);
   if (!bf16w && !q4w) return DG_ERR_UNSUPPORTED;
   // 4-bit: one tile's scale and bias rows (128 x K/64 each, twice) must fit
   // in shared memory beside the narrowest tiles' pipelines
@@ -131,7 +134,10 @@ struct dg_moe {
   int num_sms;
   GemmParams gu;
   GemmParams dn;
-  bool q4;  // 4-bit expert and dense weights
+  bool q4;  // 4-bit expert weights (and 4- or 8-bit dense)
+  int dense_bits;     // 4 or 8 with q4
+  GemmParams gu_d;    // dense-only launches when the dense bits differ (8-bit)
+  GemmParams dn_d;
   size_t smem_optin;  // largest dynamic shared memory a block may opt into
   dg_event_t* prof;
   int n_prof;
@@ -210,12 +216,14 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
   // same way when dense_up lies above dense_gate, else 16-row boxes of each
   const bool q4 = c.expert_fmt == DG_FMT_AFFINE_U4_G64;
   m->q4 = q4;
+  const int db = c.dense_fmt == DG_FMT_AFFINE_U8_G64 ? 8 : 4;  // dense code bits (q4)
+  m->dense_bits = q4 ? db : 0;
   const uint64_t wb2 = q4 ? 1 : 4;  // bytes of two weights
   ok = ok && encode_gate_up(&m->gu.wa_exp, weights->gate_up.q, H, I, I * H * wb2 / 2, 5, E,
-                            2 * I * H * wb2 / 2, q4);
+                            2 * I * H * wb2 / 2, q4 ? 4 : 0);
   if (q4) {
-    ok = ok && encode_q4_rows(&m->gu.wa_d0, weights->dense_gate.q, D, H, 16);
-    ok = ok && encode_q4_rows(&m->gu.wa_d1, weights->dense_up.q, D, H, 16);
+    ok = ok && encode_q_rows(&m->gu.wa_d0, weights->dense_gate.q, D, H, 16, db);
+    ok = ok && encode_q_rows(&m->gu.wa_d1, weights->dense_up.q, D, H, 16, db);
   } else {
     ok = ok && encode_bf16_rows(&m->gu.wa_d0, weights->dense_gate.q, D, H, 16);
     ok = ok && encode_bf16_rows(&m->gu.wa_d1, weights->dense_up.q, D, H, 16);
@@ -223,7 +231,8 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
   {
     const uintptr_t g = (uintptr_t)weights->dense_gate.q, u = (uintptr_t)weights->dense_up.q;
     m->gu.dense_5d = u > g && ((u - g) % 16) == 0 && (u - g) < (1ull << 40) &&
-                     encode_gate_up(&m->gu.wa_d5, weights->dense_gate.q, H, D, u - g, 4, 1, 0, q4);
+                     encode_gate_up(&m->gu.wa_d5, weights->dense_gate.q, H, D, u - g, 4, 1, 0,
+                                    q4 ? db : 0);
     if (!m->gu.dense_5d) m->gu.wa_d5 = m->gu.wa_d0;
   }
   // gate_up B: xe_perm / xd rows
@@ -234,7 +243,7 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
   // down A: [E*H, I] and [H, D] in 128-row boxes; B: act / act_d rows
   if (q4) {
     ok = ok && encode_q4_rows(&m->dn.wa_exp, weights->down.q, E * H, I, 128);
-    ok = ok && encode_q4_rows(&m->dn.wa_d0, weights->dense_down.q, H, D, 128);
+    ok = ok && encode_q_rows(&m->dn.wa_d0, weights->dense_down.q, H, D, 128, db);
   } else {
     ok = ok && encode_bf16_rows(&m->dn.wa_exp, weights->down.q, E * H, I, 128);
     ok = ok && encode_bf16_rows(&m->dn.wa_d0, weights->dense_down.q, H, D, 128);
@@ -251,7 +260,8 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
     return DG_ERR_CUDA;
   }
   // the device status word starts clear
-  if (cudaMemset(ws + L.status, 0, sizeof(DevStatus)) != cudaSuccess) {
+  if (cudaMemset(ws + L.status, 0, sizeof(DevStatus)) != cudaSuccess ||
+      cudaMemset(ws + L.zero16, 0, 16) != cudaSuccess) {
     delete m;
     return DG_ERR_CUDA;
   }
@@ -295,6 +305,20 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
              gemm_q4_smem_bytes(32, m->dn.sc_slot_bytes) > m->smem_optin)) {
     delete m;
     return DG_ERR_UNSUPPORTED;
+  }
+  if (q4 && db != 4) {
+    // the dense branch in launches of its own (no expert tiles), the expert
+    // launches without dense tiles
+    m->gu_d = m->gu;
+    m->dn_d = m->dn;
+    for (GemmParams* g : {&m->gu_d, &m->dn_d}) {
+      g->E = 0;
+      g->mt_exp = 0;
+      g->offsets = reinterpret_cast<const int32_t*>(ws + L.zero16);
+      g->wa_exp = g->wa_d0;  // valid maps, never read
+    }
+    m->gu.mt_dense = 0;
+    m->dn.mt_dense = 0;
   }
   *out = m;
   return DG_OK;
@@ -426,12 +450,23 @@ dg_status_t forward_impl(dg_moe_t* m, const void* h_in, void* h_out, int n_token
   gu.T = dn.T = T;
   gu.bn = dn.bn = bn;
   dn.y_perm = partials ? reinterpret_cast<float*>(ws + L.y_perm) : nullptr;
+  // 8-bit dense weights beside 4-bit experts: a dense-only launch after each
+  // expert launch (the same profiling slot)
+  const bool split = m->q4 && m->dense_bits != 4;
+  GemmParams gu_d = m->gu_d, dn_d = m->dn_d;
+  gu_d.T = dn_d.T = T;
+  gu_d.bn = dn_d.bn = bn;
+  dn_d.y_perm = dn.y_perm;
   mark(4);
   if (err == cudaSuccess)
-    err = m->q4 ? launch_gemm_q4(0, bn, gu, m->num_sms, s) : launch_gemm(0, bn, gu, m->num_sms, s);
+    err = m->q4 ? launch_gemm_affine(0, bn, 4, gu, m->num_sms, s)
+                : launch_gemm(0, bn, gu, m->num_sms, s);
+  if (err == cudaSuccess && split) err = launch_gemm_affine(0, bn, m->dense_bits, gu_d, m->num_sms, s);
   mark(5);
   if (err == cudaSuccess)
-    err = m->q4 ? launch_gemm_q4(1, bn, dn, m->num_sms, s) : launch_gemm(1, bn, dn, m->num_sms, s);
+    err = m->q4 ? launch_gemm_affine(1, bn, 4, dn, m->num_sms, s)
+                : launch_gemm(1, bn, dn, m->num_sms, s);
+  if (err == cudaSuccess && split) err = launch_gemm_affine(1, bn, m->dense_bits, dn_d, m->num_sms, s);
 
   CombineParams cp{};
   cp.y_dense = reinterpret_cast<const float*>(ws + L.y_dense);

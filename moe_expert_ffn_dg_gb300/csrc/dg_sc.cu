@@ -234,7 +234,7 @@ dg_status_t dg_sc_mlp_create(const dg_sc_mlp_config_t* cfg, const dg_sc_mlp_weig
   {
     const uintptr_t g = (uintptr_t)weights->gate.q, u = (uintptr_t)weights->up.q;
     m->gu.dense_5d = u > g && ((u - g) % 16) == 0 && (u - g) < (1ull << 40) &&
-                     encode_gate_up(&m->gu.wa_d5, weights->gate.q, H, D, u - g, 4, 1, 0, q4);
+                     encode_gate_up(&m->gu.wa_d5, weights->gate.q, H, D, u - g, 4, 1, 0, q4 ? 4 : 0);
     if (!m->gu.dense_5d) m->gu.wa_d5 = m->gu.wa_d0;
   }
   ok = ok && encode_bf16_rows(&m->gu.xb_d64, ws + L.x, T, H, 64);
@@ -334,10 +334,12 @@ dg_status_t dg_sc_mlp_forward(dg_sc_mlp_t* m, const void* embeds, const void* si
                        : pick_bn(T);
   gu.bn = dn.bn = bn;
   if (err == cudaSuccess)
-    err = m->q4 ? launch_gemm_q4(0, bn, gu, m->num_sms, s) : launch_gemm(0, bn, gu, m->num_sms, s);
+    err = m->q4 ? launch_gemm_affine(0, bn, 4, gu, m->num_sms, s)
+                : launch_gemm(0, bn, gu, m->num_sms, s);
   mark(2);
   if (err == cudaSuccess)
-    err = m->q4 ? launch_gemm_q4(1, bn, dn, m->num_sms, s) : launch_gemm(1, bn, dn, m->num_sms, s);
+    err = m->q4 ? launch_gemm_affine(1, bn, 4, dn, m->num_sms, s)
+                : launch_gemm(1, bn, dn, m->num_sms, s);
   mark(3);
   if (err == cudaSuccess)
     err = launch_pdl(k_sc_post, dim3(T), dim3(kScThreads), 0, s,

@@ -88,6 +88,11 @@ WORKLOADS = {
     "canvas256_q4": Workload("canvas256_q4", 256, 2816, 128, 8, 704, 2112,
                              seed=1, weight_std=0.02, router_std=0.02,
                              quant=(4, 4, 8), draw_seed=1),
+    # the dense branch at 8 bits (the pages' quantisation predicate for the
+    # dense MLP), experts at 4, router at 8
+    "canvas256_q4d8": Workload("canvas256_q4d8", 256, 2816, 128, 8, 704, 2112,
+                               seed=1, weight_std=0.02, router_std=0.02,
+                               quant=(4, 8, 8), draw_seed=1),
     "batch2048_zipf": Workload("batch2048_zipf", 2048, 2816, 128, 8, 704,
                                2112, seed=2, weight_std=0.02, router_std=0.02,
                                zipf_beta=0.02),

@@ -130,3 +130,21 @@ def test_stack30_q4_first_layers_teacher_forced():
               f"min {counts.min()}")
         blk.close()
         x = out
+
+
+# ---------------------------------------------------------------- 8-bit dense branch
+
+@pytest.mark.parametrize("T", [32, 1, 17, 300, 1100, 4100])
+def test_tiny_q4_dense_u8(T):
+    # experts 4-bit, dense 8-bit: the dense tiles run in launches of their own
+    wl = mi.get_workload("tiny", quant=(4, 8, 8))
+    p = mi.make_layer_inputs(wl, randvec=True, quantise=True)
+    assert p["dense_gate"]["bits"] == 8 and p["gate_up"]["bits"] == 4
+    run_and_check(wl, p, mi.make_tokens(wl, tokens=T), ref_bf16_weights=True)
+
+
+def test_canvas256_q4_dense_u8():
+    wl = mi.get_workload("canvas256_q4d8")
+    p = mi.make_layer_inputs(wl)
+    res, *_ = run_and_check(wl, p, mi.make_tokens(wl))
+    print("canvas256_q4d8", res)
