@@ -41,8 +41,9 @@ FALLBACK_BF16_TFLOPS = 1900.0
 
 def workload_desc(wl):
     if wl.quant:
-        wdesc = (f"N(0,{wl.weight_std}) draws in group-64 affine {wl.quant[0]}-bit (experts), "
-                 f"{wl.quant[1]}-bit (dense), {wl.quant[2]}-bit (router)")
+        fm = lambda b: "NVFP4 (e2m1, e4m3 per 16, fp32 per matrix)" if b == 16 else f"group-64 affine {b}-bit"
+        wdesc = (f"N(0,{wl.weight_std}) draws in {fm(wl.quant[0])} (experts), "
+                 f"{fm(wl.quant[1])} (dense), {fm(wl.quant[2])} (router)")
     else:
         wdesc = f"bf16 weights N(0,{wl.weight_std})"
     extra = f", Zipf router bias beta {wl.zipf_beta}" if wl.zipf_beta else ""
@@ -53,8 +54,11 @@ def workload_desc(wl):
 
 
 def weight_bytes(n, bits):
-    """Bytes of n weights: bf16, or group-64 affine codes plus a bf16 scale
-    and bias per 64 weights."""
+    """Bytes of n weights: bf16, group-64 affine codes plus a bf16 scale and
+    bias per 64 weights, or NVFP4 (bits code 16) codes plus an e4m3 scale per
+    16 weights."""
+    if bits == 16:
+        return n // 2 + n // 16
     return 2 * n if bits is None else n * bits // 8 + n // 64 * 4
 
 
@@ -643,7 +647,7 @@ def run_ours(args):
                        "norm in, next layer's input norm out)" if args.neighbours else ""),
                    "tokens_per_step": wl.tokens,
                    "us_per_layer": ms * 1000.0, "parallelism": f"replicas x{world}",
-                   "weights": "bf16" if not wl.quant else f"u{wl.quant[0]} g64 affine experts, u{wl.quant[1]} dense, u{wl.quant[2]} router, dequantised to bf16 on chip",
+                   "weights": "bf16" if not wl.quant else ("NVFP4 experts and dense" if wl.quant[0] == 16 else f"u{wl.quant[0]} g64 affine experts, u{wl.quant[1]} dense") + f", u{wl.quant[2]} router, decoded to bf16 on chip",
                    "l2": f"no flush: {alg['layer_bytes'] / 1e9:.3f} GB of weights per step, "
                          f"{alg['layer_bytes'] / 129e6:.1f}x the 129 MB L2",
                    "touched_experts": alg["touched_experts"]},
@@ -688,7 +692,8 @@ def main():
     ap.add_argument("--neighbours", action="store_true",
                     help="time the block fused with the decoder layer's neighbouring norms")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=["canvas256", "canvas256_q4", "canvas256_q4d8", "batch2048_zipf",
+                    choices=["canvas256", "canvas256_q4", "canvas256_q4d8", "canvas256_fp4",
+                             "batch2048_zipf",
                              "stack30_q4", "sc_canvas256", "sc_canvas256_q4"])
     args = ap.parse_args()
     if args.warmup < 3:

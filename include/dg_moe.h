@@ -47,6 +47,13 @@
  *    per group of 64 along the input dimension K.  q: 4-bit codes packed 8
  *    per uint32 word, element k at bits 4 (k % 8) of word k / 8, [.., K/8];
  *    or uint8 [.., K]; scales and biases bf16 [.., K/64].
+ *  - NVFP4 tensors (DG_FMT_NVFP4_G16; "diffgemma — architecture & implemented
+ *    contract", §8: the nvfp4 expert profile, K a multiple of 16):
+ *    W = e2m1(q) * e4m3(scale) * global.  q: two e2m1 codes a byte, element
+ *    k in the low nibble of byte k / 2 for even k, [.., K/2] (the same nibble
+ *    order as the 4-bit affine words); scales: one fp8 e4m3 byte per 16
+ *    consecutive elements along K, [.., K/16]; biases: the fp32 matrix
+ *    scales, one per expert of a stack [E], or one [1] for a 2-D tensor.
  *  - Every call is asynchronous on the given stream (a cudaStream_t) unless
  *    it says otherwise; nothing synchronises the host, and routing counts
  *    stay on the device.
@@ -82,7 +89,8 @@ typedef enum {
 typedef enum {
   DG_FMT_BF16 = 0,
   DG_FMT_AFFINE_U4_G64 = 1,
-  DG_FMT_AFFINE_U8_G64 = 2
+  DG_FMT_AFFINE_U8_G64 = 2,
+  DG_FMT_NVFP4_G16 = 3
 } dg_format_t;
 
 /* Shape and format of one layer.  Supported: hidden % 128 == 0,
@@ -106,7 +114,10 @@ typedef struct {
 } dg_moe_config_t;
 
 /* A weight tensor: bf16 uses q only (the bf16 array); affine formats use all
- * three.  All pointers 16-byte aligned. */
+ * three (NVFP4: codes, block scales, fp32 matrix scales).  All pointers
+ * 16-byte aligned (NVFP4 matrix scales: 4-byte aligned).  Supported format
+ * pairs (expert, dense): bf16 + bf16, 4-bit affine + 4- or 8-bit affine,
+ * NVFP4 + NVFP4. */
 typedef struct {
   const void* q;
   const void* scales;

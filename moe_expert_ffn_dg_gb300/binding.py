@@ -26,6 +26,7 @@ DG_ERR_WORKSPACE = 7
 DG_FMT_BF16 = 0
 DG_FMT_AFFINE_U4_G64 = 1
 DG_FMT_AFFINE_U8_G64 = 2
+DG_FMT_NVFP4_G16 = 3
 
 EXPORTED = (
     "dg_moe_workspace_size", "dg_moe_create", "dg_moe_forward", "dg_moe_forward_host",

@@ -29,13 +29,25 @@ def _to_device(a: np.ndarray, device) -> torch.Tensor:
     raise TypeError(f"unsupported dtype {a.dtype}")
 
 
+def _quant_to_device(v: dict, device) -> dict:
+    if v.get("fmt") == "nvfp4":
+        return {"fmt": "nvfp4", "q": _to_device(v["q"], device),
+                "scales": _to_device(v["scales"], device),
+                "globals": _to_device(np.asarray(v["globals"], np.float32), device)}
+    return {"bits": v["bits"], "group": v["group"], "q": _to_device(v["q"], device),
+            "scales": _to_device(v["scales"], device), "biases": _to_device(v["biases"], device)}
+
+
 def params_to_device(p: dict, device) -> dict:
-    """Copy a layer's parameters (bf16 bit patterns as uint16 arrays, or
-    group-wise affine dicts {bits, group, q, scales, biases}) to the device."""
+    """Copy a layer's parameters (bf16 bit patterns as uint16 arrays,
+    group-wise affine dicts {bits, group, q, scales, biases} or NVFP4 dicts
+    {fmt, q, scales, globals}) to the device."""
     out = {}
     for k in WEIGHTS:
         v = p[k]
-        if isinstance(v, dict):
+        if isinstance(v, dict) and v.get("fmt") == "nvfp4":
+            out[k] = _quant_to_device(v, device)
+        elif isinstance(v, dict):
             out[k] = {"bits": v["bits"], "group": v["group"],
                       "q": _to_device(v["q"], device),
                       "scales": _to_device(v["scales"], device),
@@ -52,10 +64,14 @@ def params_to_device(p: dict, device) -> dict:
 def _fmt(w) -> int:
     if not isinstance(w, dict):
         return B.DG_FMT_BF16
+    if w.get("fmt") == "nvfp4":
+        return B.DG_FMT_NVFP4_G16
     return {4: B.DG_FMT_AFFINE_U4_G64, 8: B.DG_FMT_AFFINE_U8_G64}[w["bits"]]
 
 
 def _qt(w) -> B.dg_qtensor_t:
+    if isinstance(w, dict) and w.get("fmt") == "nvfp4":
+        return B.dg_qtensor_t(w["q"].data_ptr(), w["scales"].data_ptr(), w["globals"].data_ptr())
     if isinstance(w, dict):
         return B.dg_qtensor_t(w["q"].data_ptr(), w["scales"].data_ptr(), w["biases"].data_ptr())
     return B.dg_qtensor_t(w.data_ptr(), None, None)

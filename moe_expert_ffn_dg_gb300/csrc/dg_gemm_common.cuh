@@ -108,18 +108,27 @@ __device__ __forceinline__ bool wait_no_abort(uint64_t* bar, uint32_t parity) {
 // MODE 0 (gate_up): lanes 32q..32q+15 hold gate and 32q+16..32q+31 up of the
 // same 16 features; pair them with one shuffle and write
 // act = bf16(gelu_tanh(gate) * up).
+// g_lo / g_hi scale the accumulator first (NVFP4 matrix scales).
 // MODE 1 (down): 128 output channels; the dense branch stores its f32
 // output; experts either store w * y as the f32 row of the assignment
 // (y_perm, summed per token later) or add it into the f32 per-token
 // accumulator (y_moe).
 template <int MODE>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int4 td, uint32_t tbase,
-                                              int ncols, int q, int lane) {
+                                              int ncols, int q, int lane, float g_lo = 1.f,
+                                              float g_hi = 1.f) {
   const bool dense = td.x == p.E;
+  // scale of the accumulator (NVFP4 matrix scales; 1 otherwise): in gate_up
+  // tiles lanes 0..15 of a quarter hold gate rows, 16..31 up rows
+  const float gsc = (MODE == 0 && lane >= 16) ? g_hi : g_lo;
   for (int c0 = 0; c0 < ncols; c0 += 16) {
     __syncwarp();
     float v[16];
     tmem_ld16(tbase + (uint32_t)c0, v);
+    if (gsc != 1.f) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] *= gsc;
+    }
     if (MODE == 0) {
       const int ld = dense ? p.D : p.I;
       uint16_t* out = dense ? p.act_d : p.act;

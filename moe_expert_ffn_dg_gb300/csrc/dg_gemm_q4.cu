@@ -5,7 +5,11 @@
 // 4-bit experts, 8-bit where its predicate keeps 8 bits, as for the dense
 // MLP): per row, code words of 8 four-bit codes (code k of a word at bits 4k)
 // or bytes of 8-bit codes, and per group of 64 codes a bf16 scale s and bias
-// b; the weight is s * q + b.  "diffgemma — architecture & implemented contract" (Part IV,
+// b; the weight is s * q + b.  The same kernel takes NVFP4 weights ("diffgemma
+// — architecture & implemented contract", §8 nvfp4 expert profile): e2m1
+// codes in the 4-bit slab layout, an e4m3 scale per 16 codes and an fp32
+// scale per matrix; a code times its block scale is exact in bf16, and the
+// matrix scale multiplies the fp32 accumulator in the epilogue.  "diffgemma — architecture & implemented contract" (Part IV,
 // measurements) names the dequantisation as the cost that dominates 4-bit
 // expert layers; here it runs beside the tensor core instead of in front of it.
 //
@@ -182,6 +186,40 @@ __device__ __forceinline__ void dequant16_u8(const uint32_t (&w)[4], uint32_t s2
   }
 }
 
+// NVFP4: 32 e2m1 codes (four words, two a byte, low nibble first) of two
+// blocks of 16 -> 16 bf16 pairs in K order, each code times its block's
+// e4m3 scale (exact: at most 6 significant bits).  The hardware converts a
+// byte's two codes to f16 exactly; the products are formed in fp32 and packed.
+__device__ __forceinline__ void dequant32_nvfp4(const uint32_t (&w)[4], float s_a, float s_b,
+                                                uint32_t (&o)[16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float sc = j < 2 ? s_a : s_b;  // words 0-1: block a, 2-3: block b
+    uint32_t h[4];
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w[j]));
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) {
+      __half2 hv;
+      memcpy(&hv, &h[pp], 4);
+      const float2 f = __half22float2(hv);
+      o[4 * j + pp] = as_u32(__floats2bfloat162_rn(f.x * sc, f.y * sc));
+    }
+  }
+}
+
+// e4m3 byte (non-negative) -> float: the 7 magnitude bits placed at float
+// bits 20..26 read as 2^(e-127) (1 + m/8) (or m 2^-129 for e = 0), times 2^120.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
+  return __uint_as_float((c & 0x7Fu) << 20) * 0x1p120f;
+}
+
 // 32 codes (four words) -> 16 bf16 pairs in K order, w = s * q + b rounded
 // once to bf16.  A code q sits in the low mantissa bits of the bf16 128 + q
 // (0x4300 | q, exact); subtracting 128 leaves q exactly, then one fused
@@ -203,12 +241,13 @@ __device__ __forceinline__ void dequant32(const uint32_t (&w)[4], uint32_t s2, u
   }
 }
 
-template <int MODE, int BN, int BITS>
+template <int MODE, int BN, int QF>
 __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
     k_grouped_gemm_q4(const __grid_constant__ GemmParams p) {
   using C = CfgQ<BN>;
   constexpr int SQ = C::kSQ, NB = C::kNB, NA = C::kNA, NT = C::kNT, GPS = C::kGPS;
-  constexpr int GPSL = BITS == 4 ? 4 : 2;  // groups of 64 per code slab
+  constexpr bool NVFP4 = QF == kQfNvfp4;
+  constexpr int GPSL = QF == 8 ? 2 : 4;  // groups of 64 per code slab
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sQ = smem;
@@ -295,7 +334,9 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
         const int4 td = decode_tile(p, tile, nd, s_start, s_off);
         const bool dense = td.x == p.E;
         const int ng = dense ? p.kb_dense : p.kb_exp;  // groups of 64 per row
-        const uint32_t rowb = 2u * (uint32_t)ng;        // scale bytes per row
+        // scale bytes per row: affine bf16 s (and b, in the second half of
+        // the slot); NVFP4 one e4m3 per 16 codes, across the whole slot
+        const uint32_t rowb = NVFP4 ? 4u * (uint32_t)ng : 2u * (uint32_t)ng;
         const int ss = local & 1;
         const uint32_t sph = (uint32_t)(local >> 1) & 1u;
         if (!mbar_wait(&sempty[ss], sph ^ 1u, abort_flag)) {
@@ -305,7 +346,7 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
         }
         uint8_t* dsc = sScale + (size_t)ss * 2 * slot_bytes;
         uint8_t* dbi = dsc + slot_bytes;
-        mbar_arrive_expect_tx(&sfull[ss], 2u * 128u * rowb);
+        mbar_arrive_expect_tx(&sfull[ss], (NVFP4 ? 1u : 2u) * 128u * rowb);
         if (MODE == 0) {
           // 16-row blocks in the order of the interleaved slab: block 2c+h
           // holds gate (h = 0) or up (h = 1) rows 16c..16c+15 of the tile
@@ -323,15 +364,28 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
               sc = p.sc_exp;
               bi = p.bi_exp;
             }
-            bulk_g2s(dsc + (size_t)16 * blk * rowb, sc + src_row * ng, 16 * rowb, &sfull[ss], pol_w);
-            bulk_g2s(dbi + (size_t)16 * blk * rowb, bi + src_row * ng, 16 * rowb, &sfull[ss], pol_w);
+            if (NVFP4) {
+              bulk_g2s(dsc + (size_t)16 * blk * rowb,
+                       reinterpret_cast<const uint8_t*>(sc) + src_row * rowb, 16 * rowb,
+                       &sfull[ss], pol_w);
+            } else {
+              bulk_g2s(dsc + (size_t)16 * blk * rowb, sc + src_row * ng, 16 * rowb, &sfull[ss],
+                       pol_w);
+              bulk_g2s(dbi + (size_t)16 * blk * rowb, bi + src_row * ng, 16 * rowb, &sfull[ss],
+                       pol_w);
+            }
           }
         } else {
           const size_t src_row = (dense ? (size_t)0 : (size_t)td.x * p.H) + 128 * (size_t)td.y;
           const uint16_t* sc = dense ? p.sc_d0 : p.sc_exp;
           const uint16_t* bi = dense ? p.bi_d0 : p.bi_exp;
-          bulk_g2s(dsc, sc + src_row * ng, 128 * rowb, &sfull[ss], pol_w);
-          bulk_g2s(dbi, bi + src_row * ng, 128 * rowb, &sfull[ss], pol_w);
+          if (NVFP4) {
+            bulk_g2s(dsc, reinterpret_cast<const uint8_t*>(sc) + src_row * rowb, 128 * rowb,
+                     &sfull[ss], pol_w);
+          } else {
+            bulk_g2s(dsc, sc + src_row * ng, 128 * rowb, &sfull[ss], pol_w);
+            bulk_g2s(dbi, bi + src_row * ng, 128 * rowb, &sfull[ss], pol_w);
+          }
         }
         sarmed |= 1u << ss;
         sarmed_par = (sarmed_par & ~(1u << ss)) | (sph << ss);
@@ -560,6 +614,8 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
       const uint16_t* sc_row =
           reinterpret_cast<const uint16_t*>(sScale + (size_t)ss * 2 * slot_bytes) + row * ng;
       const uint16_t* bi_row = sc_row + slot_bytes / 2;
+      // NVFP4: this row's e4m3 block scales, 4 per group
+      const uint8_t* e4_row = sScale + (size_t)ss * 2 * slot_bytes + (size_t)row * 4 * ng;
       for (int sl = 0; sl < nsl && ok; ++sl) {
         if (!mbar_wait(&qfull[qs], qph, abort_flag)) {
           if (lane == 0) report(p.status, kDevTimeout, kSiteGemmDequant, (unsigned)tile, (unsigned)sl);
@@ -589,16 +645,27 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
 #pragma unroll 1
           for (int gi = 0; gi < ngk; ++gi) {
             const int g = GPS * k + gi, gs = g % GPSL;  // group in the tile, in the slab
-            const uint32_t s = sc_row[g], b = bi_row[g];
-            const uint32_t s2 = s | (s << 16), b2 = b | (b << 16);
             uint32_t o[32];
-            if (BITS == 4) {  // the group's 32 bytes: chunks 2gs, 2gs + 1
+            if (NVFP4) {  // the group's 32 bytes: chunks 2gs, 2gs + 1; 4 blocks of 16
+              uint32_t w0[4], w1[4];
+              lds_u32x4(qrow + (((2 * gs) ^ rsw) << 4), w0);
+              lds_u32x4(qrow + (((2 * gs + 1) ^ rsw) << 4), w1);
+              const uint32_t e4 = *reinterpret_cast<const uint32_t*>(e4_row + 4 * g);
+              dequant32_nvfp4(w0, e4m3_to_f32(e4 & 0xFFu), e4m3_to_f32((e4 >> 8) & 0xFFu),
+                              *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
+              dequant32_nvfp4(w1, e4m3_to_f32((e4 >> 16) & 0xFFu), e4m3_to_f32(e4 >> 24),
+                              *reinterpret_cast<uint32_t(*)[16]>(&o[16]));
+            } else if (QF == 4) {  // the group's 32 bytes: chunks 2gs, 2gs + 1
+              const uint32_t s = sc_row[g], b = bi_row[g];
+              const uint32_t s2 = s | (s << 16), b2 = b | (b << 16);
               uint32_t w0[4], w1[4];
               lds_u32x4(qrow + (((2 * gs) ^ rsw) << 4), w0);
               lds_u32x4(qrow + (((2 * gs + 1) ^ rsw) << 4), w1);
               dequant32(w0, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
               dequant32(w1, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[16]));
             } else {  // 64 bytes: chunks 4gs .. 4gs + 3
+              const uint32_t s = sc_row[g], b = bi_row[g];
+              const uint32_t s2 = s | (s << 16), b2 = b | (b << 16);
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
                 uint32_t wv[4];
@@ -644,7 +711,16 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
-      epilogue_tile<MODE>(p, td, tbase, nb * kBoxRows, q, lane);
+      float g_lo = 1.f, g_hi = 1.f;  // NVFP4 matrix scales (gate / up lanes)
+      if (NVFP4) {
+        if (td.x != p.E) {
+          g_lo = g_hi = __ldg(p.g_exp + td.x);
+        } else {
+          g_lo = __ldg(p.g_d0);
+          g_hi = MODE == 0 ? __ldg(p.g_d1) : g_lo;
+        }
+      }
+      epilogue_tile<MODE>(p, td, tbase, nb * kBoxRows, q, lane, g_lo, g_hi);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
@@ -660,13 +736,13 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
   }
 }
 
-template <int MODE, int BN, int BITS>
+template <int MODE, int BN, int QF>
 cudaError_t launch_q4(const GemmParams& p, int grid, cudaStream_t s) {
   const size_t smem = CfgQ<BN>::kFixed + 4 * (size_t)p.sc_slot_bytes;
-  cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm_q4<MODE, BN, BITS>,
+  cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm_q4<MODE, BN, QF>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  return launch_pdl(k_grouped_gemm_q4<MODE, BN, BITS>, dim3(grid), dim3(CfgQ<BN>::kThreads), smem,
+  return launch_pdl(k_grouped_gemm_q4<MODE, BN, QF>, dim3(grid), dim3(CfgQ<BN>::kThreads), smem,
                     s, p);
 }
 
@@ -694,9 +770,10 @@ size_t gemm_q4_smem_bytes(int bn, int sc_slot_bytes) {
   return fixed + 4 * (size_t)sc_slot_bytes;
 }
 
-cudaError_t launch_gemm_affine(int mode, int bn, int bits, const GemmParams& p, int grid,
+cudaError_t launch_gemm_affine(int mode, int bn, int qf, const GemmParams& p, int grid,
                                cudaStream_t s) {
-  return bits == 8 ? launch_bits<8>(mode, bn, p, grid, s) : launch_bits<4>(mode, bn, p, grid, s);
+  if (qf == kQfNvfp4) return launch_bits<kQfNvfp4>(mode, bn, p, grid, s);
+  return qf == 8 ? launch_bits<8>(mode, bn, p, grid, s) : launch_bits<4>(mode, bn, p, grid, s);
 }
 
 }  // namespace dg

@@ -34,6 +34,12 @@ inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 inline dg_status_t check_qtensor(const dg_qtensor_t& t, dg_format_t fmt) {
   if (!t.q) return DG_ERR_INVALID_ARG;
   if (!aligned(t.q, 16)) return DG_ERR_ALIGNMENT;
+  if (fmt == DG_FMT_NVFP4_G16) {
+    // block scale rows are fetched with bulk copies; matrix scales are floats
+    if (!t.scales || !t.biases) return DG_ERR_INVALID_ARG;
+    if (!aligned(t.scales, 16) || !aligned(t.biases, 4)) return DG_ERR_ALIGNMENT;
+    return DG_OK;
+  }
   if (fmt != DG_FMT_BF16) {
     if (!t.scales || !t.biases) return DG_ERR_INVALID_ARG;
     // 4-bit scale rows are fetched with bulk copies (16-byte granules)

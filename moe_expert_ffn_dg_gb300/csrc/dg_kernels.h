@@ -95,6 +95,11 @@ struct GemmParams {
   uint16_t* act_d;       // gate_up out: bf16 [T, D]
   float* y_moe;          // down out: f32 [T, H] (accumulated), when y_perm is null
   float* y_perm;         // down out: f32 [T*K, H], w * expert output per grouped row, or null
+  // NVFP4 matrix scales (fp32), applied to the accumulator: per expert, and
+  // for the dense tensors (gate_up: gate and up; down: d0)
+  const float* g_exp;
+  const float* g_d0;
+  const float* g_d1;
   float* y_dense;        // down out: f32 [T, H]
   const int32_t* tok_perm;
   const float* w_perm;
@@ -169,8 +174,11 @@ cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s);
 size_t gemm_smem_bytes(int bn);
 // 4-bit weights, dequantised into TMEM; same modes.  bn is 64 or 128.
-// Grouped GEMM over group-64 affine weights of `bits` (4 or 8) bits.
-cudaError_t launch_gemm_affine(int mode, int bn, int bits, const GemmParams& p, int grid,
+// Grouped GEMM over quantised weights: qf 4 or 8 (group-64 affine codes of
+// that many bits) or kQfNvfp4 (e2m1 codes, e4m3 scales per 16, fp32 matrix
+// scales).
+constexpr int kQfNvfp4 = 16;
+cudaError_t launch_gemm_affine(int mode, int bn, int qf, const GemmParams& p, int grid,
                                cudaStream_t s);
 size_t gemm_q4_smem_bytes(int bn, int sc_slot_bytes);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);

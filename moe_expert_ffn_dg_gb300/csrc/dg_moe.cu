@@ -88,8 +88,9 @@ dg_status_t check_config(const dg_moe_config_t* c) {
   // expert and dense weights: both bf16, or 4-bit group-64 affine experts
   // with a 4- or 8-bit dense branch
   const bool bf16w = c->expert_fmt == DG_FMT_BF16 && c->dense_fmt == DG_FMT_BF16;
-  const bool q4w = c->expert_fmt == DG_FMT_AFFINE_U4_G64 &&
-                   (c->dense_fmt == DG_FMT_AFFINE_U4_G64 || c->dense_fmt == DG_FMT_AFFINE_U8_G64);
+  const bool q4w = (c->expert_fmt == DG_FMT_AFFINE_U4_G64 &&
+                    (c->dense_fmt == DG_FMT_AFFINE_U4_G64 || c->dense_fmt == DG_FMT_AFFINE_U8_G64)) ||
+                   (c->expert_fmt == DG_FMT_NVFP4_G16 && c->dense_fmt == DG_FMT_NVFP4_G16);
   if (!bf16w && !q4w) return DG_ERR_UNSUPPORTED;
   // 4-bit: one tile's scale and bias rows (128 x K/64 each, twice) must fit
   // in shared memory beside the narrowest tiles' pipelines
@@ -134,8 +135,9 @@ struct dg_moe {
   int num_sms;
   GemmParams gu;
   GemmParams dn;
-  bool q4;  // 4-bit expert weights (and 4- or 8-bit dense)
-  int dense_bits;     // 4 or 8 with q4
+  bool q4;  // quantised expert weights (4-bit affine or NVFP4) and dense
+  int qf_exp;         // expert code format: 4 or kQfNvfp4 (with q4)
+  int dense_bits;     // dense code format: 4, 8 or kQfNvfp4 (with q4)
   GemmParams gu_d;    // dense-only launches when the dense bits differ (8-bit)
   GemmParams dn_d;
   size_t smem_optin;  // largest dynamic shared memory a block may opt into
@@ -214,10 +216,13 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
   bool ok = true;
   // gate_up A: experts through the interleaving 5-D view; the dense pair the
   // same way when dense_up lies above dense_gate, else 16-row boxes of each
-  const bool q4 = c.expert_fmt == DG_FMT_AFFINE_U4_G64;
+  const bool nvfp4 = c.expert_fmt == DG_FMT_NVFP4_G16;
+  const bool q4 = c.expert_fmt == DG_FMT_AFFINE_U4_G64 || nvfp4;
   m->q4 = q4;
-  const int db = c.dense_fmt == DG_FMT_AFFINE_U8_G64 ? 8 : 4;  // dense code bits (q4)
-  m->dense_bits = q4 ? db : 0;
+  m->qf_exp = nvfp4 ? kQfNvfp4 : 4;
+  // dense code bits in the slabs (NVFP4 codes are 4-bit, in the affine layout)
+  const int db = c.dense_fmt == DG_FMT_AFFINE_U8_G64 ? 8 : 4;
+  m->dense_bits = !q4 ? 0 : (c.dense_fmt == DG_FMT_NVFP4_G16 ? kQfNvfp4 : db);
   const uint64_t wb2 = q4 ? 1 : 4;  // bytes of two weights
   ok = ok && encode_gate_up(&m->gu.wa_exp, weights->gate_up.q, H, I, I * H * wb2 / 2, 5, E,
                             2 * I * H * wb2 / 2, q4 ? 4 : 0);
@@ -299,6 +304,15 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
   m->dn.bi_exp = u16(weights->down.biases);
   m->dn.sc_d0 = m->dn.sc_d1 = u16(weights->dense_down.scales);
   m->dn.bi_d0 = m->dn.bi_d1 = u16(weights->dense_down.biases);
+  // NVFP4 matrix scales (the biases slot of its tensors)
+  auto f32p = [](const void* v) { return static_cast<const float*>(v); };
+  m->gu.g_exp = f32p(weights->gate_up.biases);
+  m->gu.g_d0 = f32p(weights->dense_gate.biases);
+  m->gu.g_d1 = f32p(weights->dense_up.biases);
+  m->dn.g_exp = f32p(weights->down.biases);
+  m->dn.g_d0 = m->dn.g_d1 = f32p(weights->dense_down.biases);
+  // one tile's scales: affine s and b (bf16 per 64) or NVFP4 e4m3 per 16,
+  // both 128 x K/16 bytes over the slot pair
   m->gu.sc_slot_bytes = (int)round_up(128 * (H / 64) * 2, 128);
   m->dn.sc_slot_bytes = (int)round_up(128 * (I > D ? I : D) / 64 * 2, 128);
   if (q4 && (gemm_q4_smem_bytes(32, m->gu.sc_slot_bytes) > m->smem_optin ||
@@ -306,7 +320,7 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
     delete m;
     return DG_ERR_UNSUPPORTED;
   }
-  if (q4 && db != 4) {
+  if (q4 && m->dense_bits != m->qf_exp) {
     // the dense branch in launches of its own (no expert tiles), the expert
     // launches without dense tiles
     m->gu_d = m->gu;
@@ -452,19 +466,19 @@ dg_status_t forward_impl(dg_moe_t* m, const void* h_in, void* h_out, int n_token
   dn.y_perm = partials ? reinterpret_cast<float*>(ws + L.y_perm) : nullptr;
   // 8-bit dense weights beside 4-bit experts: a dense-only launch after each
   // expert launch (the same profiling slot)
-  const bool split = m->q4 && m->dense_bits != 4;
+  const bool split = m->q4 && m->dense_bits != m->qf_exp;
   GemmParams gu_d = m->gu_d, dn_d = m->dn_d;
   gu_d.T = dn_d.T = T;
   gu_d.bn = dn_d.bn = bn;
   dn_d.y_perm = dn.y_perm;
   mark(4);
   if (err == cudaSuccess)
-    err = m->q4 ? launch_gemm_affine(0, bn, 4, gu, m->num_sms, s)
+    err = m->q4 ? launch_gemm_affine(0, bn, m->qf_exp, gu, m->num_sms, s)
                 : launch_gemm(0, bn, gu, m->num_sms, s);
   if (err == cudaSuccess && split) err = launch_gemm_affine(0, bn, m->dense_bits, gu_d, m->num_sms, s);
   mark(5);
   if (err == cudaSuccess)
-    err = m->q4 ? launch_gemm_affine(1, bn, 4, dn, m->num_sms, s)
+    err = m->q4 ? launch_gemm_affine(1, bn, m->qf_exp, dn, m->num_sms, s)
                 : launch_gemm(1, bn, dn, m->num_sms, s);
   if (err == cudaSuccess && split) err = launch_gemm_affine(1, bn, m->dense_bits, dn_d, m->num_sms, s);
 

@@ -50,9 +50,11 @@ __all__ = [
     "zipf_router_bias",
     "SC_WORKLOADS",
     "make_sc_inputs",
+    "quantize_nvfp4",
 ]
 
 BF16_ONE = np.uint16(0x3F80)
+NVFP4 = 16   # weight "bits" code of the NVFP4 format in a workload's quant tuple
 
 
 @dataclasses.dataclass(frozen=True)
@@ -93,6 +95,10 @@ WORKLOADS = {
     "canvas256_q4d8": Workload("canvas256_q4d8", 256, 2816, 128, 8, 704, 2112,
                                seed=1, weight_std=0.02, router_std=0.02,
                                quant=(4, 8, 8), draw_seed=1),
+    # NVFP4 experts and dense (the pages' nvfp4 profile), 8-bit router
+    "canvas256_fp4": Workload("canvas256_fp4", 256, 2816, 128, 8, 704, 2112,
+                              seed=1, weight_std=0.02, router_std=0.02,
+                              quant=(16, 16, 8), draw_seed=1),
     "batch2048_zipf": Workload("batch2048_zipf", 2048, 2816, 128, 8, 704,
                                2112, seed=2, weight_std=0.02, router_std=0.02,
                                zipf_beta=0.02),
@@ -182,6 +188,76 @@ def quantize_affine(w_bits: np.ndarray, bits: int, group: int = 64) -> dict:
             "scales": s_bits, "biases": b_bits}
 
 
+# e2m1 magnitudes by code (bits e1 e0 m): 0, 0.5, 1, 1.5, 2, 3, 4, 6
+_E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _e4m3_encode(v: np.ndarray) -> np.ndarray:
+    """Non-negative float64 -> fp8 e4m3 (bias 7, no infinity, max 448) codes,
+    rounded to nearest, ties to even; values above 448 saturate."""
+    v = np.minimum(np.asarray(v, np.float64), 448.0)
+    code = np.zeros(v.shape, np.uint8)
+    pos = v > 0
+    e = np.floor(np.log2(np.where(pos, v, 1.0)))
+    sub = pos & (e < -6)
+    m_sub = np.rint(np.where(sub, v, 0.0) / 2.0 ** -9)          # ties to even
+    code = np.where(sub, m_sub.astype(np.uint8), code)            # 8 -> 2^-6, code 8
+    nrm = pos & ~sub
+    en = np.where(nrm, e, 0.0)
+    m = np.rint((np.where(nrm, v, 1.0) / 2.0 ** en - 1.0) * 8.0)
+    carry = m >= 8
+    en = np.where(carry, en + 1, en)
+    m = np.where(carry, 0, m)
+    c = ((en + 7).astype(np.int64) << 3) | m.astype(np.int64)
+    code = np.where(nrm, np.minimum(c, 0x7E).astype(np.uint8), code)
+    return code
+
+
+def _e4m3_value(code: np.ndarray) -> np.ndarray:
+    c = np.asarray(code, np.int64)
+    e, m = (c >> 3) & 15, c & 7
+    return np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * 2.0 ** (e - 7))
+
+
+def _e2m1_encode(x: np.ndarray) -> np.ndarray:
+    """float64 -> e2m1 codes (sign bit 3), nearest magnitude with ties to the
+    even code, saturating at 6."""
+    a = np.abs(x)
+    d = np.abs(a[..., None] - _E2M1_MAG)
+    best = np.argmin(d + 1e-9 * (np.arange(8) & 1), axis=-1)   # ties: even code
+    return (best | np.where(x < 0, 8, 0)).astype(np.uint8)
+
+
+def quantize_nvfp4(w_bits: np.ndarray) -> dict:
+    """Encode bf16 weights [..., K] in NVFP4 ("diffgemma — architecture &
+    implemented contract", §8 quantisation profiles: nvfp4 experts, K a
+    multiple of 16): e2m1 codes, two a byte (element k in the low nibble of
+    byte k // 2 when k is even), one fp8 e4m3 scale per 16 consecutive
+    elements along K, and one fp32 scale per matrix (per expert for a stack).
+    global = amax / (6 * 448); block scale = e4m3(block amax / 6 / global);
+    code = e2m1(w / (block scale * global)).  The decoded weight is
+    e2m1 * block scale * global."""
+    w = _bits_to_f32(w_bits).astype(np.float64)
+    K = w.shape[-1]
+    if K % 16:
+        raise ValueError("K must be a multiple of 16")
+    lead = w.shape[:-1]
+    mats = w.reshape(-1, *w.shape[-2:]) if w.ndim >= 2 else w.reshape(1, 1, K)
+    amax = np.abs(mats).reshape(mats.shape[0], -1).max(axis=1)
+    g = np.where(amax > 0, amax / (6.0 * 448.0), 1.0).astype(np.float32)
+    gf = g.astype(np.float64)[:, None, None]
+    blocks = mats.reshape(mats.shape[0], mats.shape[1], K // 16, 16)
+    bamax = np.abs(blocks).max(axis=-1)
+    sc = _e4m3_encode(bamax / 6.0 / gf)
+    sv = _e4m3_value(sc)[..., None] * gf[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        codes = _e2m1_encode(np.where(sv > 0, blocks / np.where(sv > 0, sv, 1.0), 0.0))
+    codes = codes.reshape(*lead, K)
+    packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+    return {"fmt": "nvfp4", "q": packed, "scales": sc.reshape(*lead, K // 16),
+            "globals": g if w.ndim == 3 else g[:1]}
+
+
 def _normal_bf16(rng: np.random.Generator, shape, std: float) -> np.ndarray:
     x = rng.standard_normal(shape, dtype=np.float32)
     x *= np.float32(std)
@@ -265,12 +341,14 @@ def make_layer_inputs(wl: Workload, layer: int = 0, randvec: bool = False,
         p["layer_scalar"] = float(_bits_to_f32(f32_to_bf16_bits(v))[0])
     do_q = wl.quantised if quantise is None else quantise
     if do_q:
+        # bits 4 / 8: group-64 affine; NVFP4 (code 16): e2m1 with e4m3 scales
         eb, db, rb = wl.quant if wl.quant is not None else (4, 4, 8)
+        quant = lambda w, b: quantize_nvfp4(w) if b == NVFP4 else quantize_affine(w, b)
         p["router"] = quantize_affine(p["router"], rb)
-        p["gate_up"] = quantize_affine(p["gate_up"], eb)
-        p["down"] = quantize_affine(p["down"], eb)
+        p["gate_up"] = quant(p["gate_up"], eb)
+        p["down"] = quant(p["down"], eb)
         for n in ("dense_gate", "dense_up", "dense_down"):
-            p[n] = quantize_affine(p[n], db)
+            p[n] = quant(p[n], db)
     return p
 
 

@@ -58,6 +58,7 @@ __all__ = [
     "router_logits", "select_topk", "routing_weights", "route",
     "geglu_mlp", "experts_forward", "dense_forward", "combine",
     "permutation", "moe_block_forward", "sc_mlp_forward", "attn_residual", "next_input_norm",
+    "e4m3_value", "e2m1_value", "dequant_nvfp4",
 ]
 
 
@@ -102,11 +103,50 @@ def dequant_affine(qt: dict) -> np.ndarray:
     return w.reshape(*codes.shape[:-1], K)
 
 
+def e2m1_value(codes) -> np.ndarray:
+    """fp4 e2m1 (sign, 2 exponent bits with bias 1, 1 mantissa bit): e = 0
+    gives m / 2, else 2^(e-1) (1 + m/2); the values 0, 0.5, 1, 1.5, 2, 3, 4, 6."""
+    c = np.asarray(codes, np.int64)
+    e, m = (c >> 1) & 3, c & 1
+    mag = np.where(e == 0, 0.5 * m, 2.0 ** (e - 1) * (1.0 + 0.5 * m))
+    return np.where(c & 8, -mag, mag)
+
+
+def e4m3_value(codes) -> np.ndarray:
+    """fp8 e4m3 (bias 7, no infinity): e = 0 gives m 2^-9, else
+    (1 + m/8) 2^(e-7); sign bit 7 (the block scales are non-negative)."""
+    c = np.asarray(codes, np.int64)
+    e, m = (c >> 3) & 15, c & 7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    return np.where(c & 0x80, -mag, mag)
+
+
+def dequant_nvfp4(qt: dict) -> np.ndarray:
+    """Decode an NVFP4 tensor to float64: e2m1 code * e4m3 scale of its block
+    of 16 along K * the matrix's fp32 scale ("diffgemma — architecture &
+    implemented contract", §8: nvfp4 expert profile, K a multiple of 16).
+    ``q``: two codes a byte, element k in the low nibble of byte k // 2 for
+    even k; ``scales``: e4m3 bytes [..., K/16]; ``globals``: one float32 per
+    matrix (per expert of a stack)."""
+    q = np.asarray(qt["q"])
+    codes = np.stack([q & 0xF, q >> 4], axis=-1).reshape(*q.shape[:-1], q.shape[-1] * 2)
+    K = codes.shape[-1]
+    v = e2m1_value(codes).reshape(*codes.shape[:-1], K // 16, 16)
+    v = v * e4m3_value(qt["scales"])[..., None]
+    g = np.asarray(qt["globals"], np.float64)
+    v = v.reshape(*codes.shape[:-1], K)
+    if v.ndim == 3:
+        v = v * g[:, None, None]
+    else:
+        v = v * g[0]
+    return v
+
+
 def to_f64(t) -> np.ndarray:
-    """A weight given as bf16 bits (uint16), as a group-wise affine dict, or
-    already as float64 -> float64."""
+    """A weight given as bf16 bits (uint16), as a group-wise affine or NVFP4
+    dict, or already as float64 -> float64."""
     if isinstance(t, dict):
-        return dequant_affine(t)
+        return dequant_nvfp4(t) if t.get("fmt") == "nvfp4" else dequant_affine(t)
     t = np.asarray(t)
     if t.dtype == np.float64:
         return t
@@ -114,7 +154,10 @@ def to_f64(t) -> np.ndarray:
 
 
 def _slice(t, e):
-    """Expert e of a stacked weight (bf16 bits or affine dict)."""
+    """Expert e of a stacked weight (bf16 bits, affine or NVFP4 dict)."""
+    if isinstance(t, dict) and t.get("fmt") == "nvfp4":
+        return {"fmt": "nvfp4", "q": t["q"][e], "scales": t["scales"][e],
+                "globals": t["globals"][e:e + 1]}
     if isinstance(t, dict):
         return {"bits": t["bits"], "group": t["group"], "q": t["q"][e],
                 "scales": t["scales"][e], "biases": t["biases"][e]}
@@ -180,9 +223,12 @@ def route(h, Wr, router_scale, pes, k, bias=None):
 
 def decoded(t, bf16_weights: bool = False) -> np.ndarray:
     """A weight as float64; with bf16_weights, a group-wise affine weight is
-    rounded to bf16 after its exact decode (bf16 weights are unchanged)."""
+    rounded to bf16 after its exact decode (bf16 weights are unchanged, and so
+    are NVFP4 weights: a code times its e4m3 block scale is a bf16 number,
+    the matrix scale is applied to the fp32 product)."""
     w = to_f64(t)
-    return round_bf16(w) if (bf16_weights and isinstance(t, dict)) else w
+    affine = isinstance(t, dict) and t.get("fmt") != "nvfp4"
+    return round_bf16(w) if (bf16_weights and affine) else w
 
 
 def geglu_mlp(x: np.ndarray, W_gate: np.ndarray, W_up: np.ndarray,

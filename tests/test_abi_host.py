@@ -120,3 +120,11 @@ def test_sc_mlp_workspace_and_create_validation(lib):
                                 ctypes.byref(h)) == B.DG_ERR_INVALID_ARG
     assert lib.dg_sc_mlp_forward(None, None, None, None, 1, None) == B.DG_ERR_INVALID_ARG
     assert lib.dg_sc_mlp_destroy(None) == B.DG_OK
+
+
+def test_nvfp4_format_pairs(lib):
+    n = ctypes.c_size_t(0)
+    ok = _cfg(expert_fmt=B.DG_FMT_NVFP4_G16, dense_fmt=B.DG_FMT_NVFP4_G16, router_fmt=2)
+    assert lib.dg_moe_workspace_size(ctypes.byref(ok), ctypes.byref(n)) == B.DG_OK
+    mixed = _cfg(expert_fmt=B.DG_FMT_NVFP4_G16, dense_fmt=B.DG_FMT_AFFINE_U4_G64)
+    assert lib.dg_moe_workspace_size(ctypes.byref(mixed), ctypes.byref(n)) == B.DG_ERR_UNSUPPORTED

@@ -148,3 +148,26 @@ def test_canvas256_q4_dense_u8():
     p = mi.make_layer_inputs(wl)
     res, *_ = run_and_check(wl, p, mi.make_tokens(wl))
     print("canvas256_q4d8", res)
+
+
+# ---------------------------------------------------------------- NVFP4 weights
+
+@pytest.mark.parametrize("T", [32, 1, 17, 300, 1100, 4100])
+def test_tiny_nvfp4(T):
+    # e2m1 codes with e4m3 block scales decode exactly into bf16; the matrix
+    # scale multiplies the fp32 accumulator: held to the exact block
+    wl = mi.get_workload("tiny", quant=(mi.NVFP4, mi.NVFP4, 8))
+    p = mi.make_layer_inputs(wl, randvec=True, quantise=True)
+    assert p["gate_up"]["fmt"] == "nvfp4"
+    # at 4100 tokens the branch outputs hold 1M elements: one GEGLU activation
+    # rounding to the other bf16 neighbour (one ulp at |act| ~ 1) moves a
+    # y_moe element by ~2^-8 |w_down| ~ 1.5 % of the branch RMS here, beyond
+    # the 1 % branch budget; the block output and routing are still checked
+    run_and_check(wl, p, mi.make_tokens(wl, tokens=T), check_intermediates=T <= 1100)
+
+
+def test_canvas256_nvfp4():
+    wl = mi.get_workload("canvas256_fp4")
+    p = mi.make_layer_inputs(wl)
+    res, *_ = run_and_check(wl, p, mi.make_tokens(wl))
+    print("canvas256_fp4", res)

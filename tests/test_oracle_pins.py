@@ -601,3 +601,62 @@ def test_next_input_norm_against_torch_rms_norm():
     got = o.next_input_norm(x, w)
     diff = np.abs(got - want) / np.maximum(np.abs(want), 1e-30)
     assert (got == want).mean() > 0.999 and diff.max() <= 2.0 ** -7
+
+
+# ---------------------------------------------------------------- NVFP4 weights
+
+def test_e4m3_decode_matches_torch_float8():
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)   # no NaN
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(o.e4m3_value(codes), want)
+
+
+def test_e2m1_decode_values():
+    # the sixteen fp4 e2m1 values (sign, exponent bias 1, one mantissa bit)
+    want = [0, 0.5, 1, 1.5, 2, 3, 4, 6, -0.0, -0.5, -1, -1.5, -2, -3, -4, -6]
+    np.testing.assert_array_equal(o.e2m1_value(np.arange(16)), want)
+
+
+def test_nvfp4_decode_bit_by_bit():
+    w = mi._normal_bf16(np.random.default_rng(5), (3, 8, 48), 0.02)
+    qt = mi.quantize_nvfp4(w)
+    got = o.dequant_nvfp4(qt)
+    ref = np.zeros((3, 8, 48))
+    e2m1 = {0: 0.0, 1: 0.5, 2: 1.0, 3: 1.5, 4: 2.0, 5: 3.0, 6: 4.0, 7: 6.0}
+    for e in range(3):
+        for r in range(8):
+            for k in range(48):
+                byte = int(qt["q"][e, r, k // 2])
+                c = (byte >> 4) if k % 2 else (byte & 15)
+                v = e2m1[c & 7] * (-1 if c & 8 else 1)
+                sc = int(qt["scales"][e, r, k // 16])
+                ex, m = sc >> 3, sc & 7
+                s = m * 2.0 ** -9 if ex == 0 else (1 + m / 8) * 2.0 ** (ex - 7)
+                ref[e, r, k] = v * s * float(qt["globals"][e])
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_nvfp4_round_trip_error_bound():
+    # within one e2m1 step of the block scale (the widest step, 4 -> 6, is 2),
+    # beyond saturation at 6 when the e4m3 scale rounded down
+    w = mi._normal_bf16(np.random.default_rng(6), (4, 32, 256), 0.02)
+    qt = mi.quantize_nvfp4(w)
+    wf = o.bf16_to_f64(w)
+    deq = o.dequant_nvfp4(qt)
+    sg = (o.e4m3_value(qt["scales"]) * qt["globals"].astype(np.float64)[:, None, None])
+    sg = np.repeat(sg, 16, axis=-1)
+    err = np.abs(wf - deq)
+    assert np.all(err <= 1.0 * sg + np.maximum(np.abs(wf) - 6 * sg, 0) + 1e-12)
+    # the decode of the block maximum is its nearest level: relative error small
+    assert np.abs(deq - wf).mean() < 0.1 * np.abs(wf).mean()
+
+
+def test_nvfp4_block_times_scale_is_bf16_exact():
+    # an e2m1 value times an e4m3 scale has at most 6 significant bits, so the
+    # GPU's bf16 decode of it is exact; the matrix scale comes after the sum
+    w = mi._normal_bf16(np.random.default_rng(7), (2, 16, 64), 0.02)
+    qt = mi.quantize_nvfp4(w)
+    q = qt["q"]
+    codes = np.stack([q & 0xF, q >> 4], -1).reshape(*q.shape[:-1], q.shape[-1] * 2)
+    v = o.e2m1_value(codes).reshape(2, 16, 4, 16) * o.e4m3_value(qt["scales"])[..., None]
+    np.testing.assert_array_equal(o.round_bf16(v), v)
