@@ -57,6 +57,19 @@ def test_tiny_smaller_batch_than_max_tokens():
     blk.close()
 
 
+def test_empty_batch_launches_nothing_and_leaves_the_handle_usable():
+    wl = mi.get_workload("tiny")
+    p = mi.make_layer_inputs(wl, randvec=True)
+    blk = make_block(wl, p)
+    h = torch.empty(0, wl.hidden, dtype=torch.bfloat16, device="cuda")
+    out = blk.forward(h, 1.0)
+    torch.cuda.synchronize()
+    assert out.shape == (0, wl.hidden)
+    assert blk.device_status()[0] == 0
+    run_and_check(wl, p, mi.make_tokens(wl, tokens=5), blk=blk)
+    blk.close()
+
+
 def test_zero_tokens_route_to_first_experts_and_give_zero():
     wl = mi.get_workload("tiny")
     p = mi.make_layer_inputs(wl, randvec=True)
