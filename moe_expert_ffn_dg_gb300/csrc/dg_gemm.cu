@@ -235,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
       const int nb = (td.w + kBoxRows - 1) / kBoxRows;
       const int acc = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
+      const EpiRows pre = epilogue_rows<MODE>(p, td, lane);  // requested before the wait
       if (!mbar_wait(&acc_full[acc], use & 1u, abort_flag)) {
         if (lane == 0) report(p.status, kDevTimeout, kSiteGemmEpilogue, (unsigned)tile, 0u);
         *abort_flag = 1;
@@ -242,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
-      epilogue_tile<MODE>(p, td, tbase, nb * kBoxRows, q, lane);
+      epilogue_tile<MODE>(p, td, tbase, nb * kBoxRows, q, lane, pre);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);

@@ -113,15 +113,54 @@ __device__ __forceinline__ bool wait_no_abort(uint64_t* bar, uint32_t parity) {
 // output; experts either store w * y as the f32 row of the assignment
 // (y_perm, summed per token later) or add it into the f32 per-token
 // accumulator (y_moe).
+// Expert tiles of the down GEMM: lane l holds the routing weight (and, for
+// the reduction into y_moe, the token) of grouped row r0 + l of the tile.
+__device__ __forceinline__ void fetch_tile_rows(const GemmParams& p, int4 td, int lane, int r0,
+                                                float& w, int& t) {
+  const int r = r0 + lane;
+  w = 0.f;
+  t = 0;
+  if (r < td.w) {
+    w = __ldg(p.w_perm + td.z + r);
+    if (!p.y_perm) t = __ldg(p.tok_perm + td.z + r);
+  }
+}
+// The first two blocks of 32 rows, fetched before the epilogue waits for the
+// tile's accumulator so that their latency is hidden behind the wait.
+struct EpiRows {
+  float w[2];
+  int t[2];
+};
+template <int MODE>
+__device__ __forceinline__ EpiRows epilogue_rows(const GemmParams& p, int4 td, int lane) {
+  EpiRows e{{0.f, 0.f}, {0, 0}};
+  if (MODE == 1 && td.x != p.E) {
+    fetch_tile_rows(p, td, lane, 0, e.w[0], e.t[0]);
+    fetch_tile_rows(p, td, lane, 32, e.w[1], e.t[1]);
+  }
+  return e;
+}
+
 template <int MODE>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int4 td, uint32_t tbase,
-                                              int ncols, int q, int lane, float g_lo = 1.f,
-                                              float g_hi = 1.f) {
+                                              int ncols, int q, int lane, const EpiRows& pre,
+                                              float g_lo = 1.f, float g_hi = 1.f) {
   const bool dense = td.x == p.E;
   // scale of the accumulator (NVFP4 matrix scales; 1 otherwise): in gate_up
   // tiles lanes 0..15 of a quarter hold gate rows, 16..31 up rows
   const float gsc = (MODE == 0 && lane >= 16) ? g_hi : g_lo;
+  // routing rows of the current and the next block of 32 grouped rows; the
+  // block after next is fetched as a block is entered, so the loads overlap
+  // the stores
+  const bool rows = MODE == 1 && !dense;
+  float w_cur = pre.w[0], w_nxt = pre.w[1];
+  int t_cur = pre.t[0], t_nxt = pre.t[1];
   for (int c0 = 0; c0 < ncols; c0 += 16) {
+    if (rows && c0 > 0 && (c0 & 31) == 0) {
+      w_cur = w_nxt;
+      t_cur = t_nxt;
+      fetch_tile_rows(p, td, lane, c0 + 32, w_nxt, t_nxt);
+    }
     __syncwarp();
     float v[16];
     tmem_ld16(tbase + (uint32_t)c0, v);
@@ -153,25 +192,19 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int4 td, uint
         if (c0 + j < td.w) p.y_dense[(size_t)(td.z + c0 + j) * p.H + feat] = v[j];
     } else if (p.y_perm) {
       // lane l holds channel 32q + l of 16 grouped rows: each store writes
-      // 128 contiguous bytes of one row
+      // 128 contiguous bytes of one row; streaming stores (the rows are read
+      // once, by the combine) keep L2 for the token rows and weights
       const int feat = td.y * 128 + 32 * q + lane;
-      const float wl = (lane < 16 && c0 + lane < td.w) ? p.w_perm[td.z + c0 + lane] : 0.f;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const float wj = __shfl_sync(0xffffffffu, wl, j);
-        if (c0 + j < td.w) p.y_perm[(size_t)(td.z + c0 + j) * p.H + feat] = wj * v[j];
+        const float wj = __shfl_sync(0xffffffffu, w_cur, (c0 & 16) + j);
+        if (c0 + j < td.w) __stcs(p.y_perm + (size_t)(td.z + c0 + j) * p.H + feat, wj * v[j]);
       }
     } else {
       // Routing-weighted add into the f32 per-token accumulator, four
       // features per vector reduction: transpose each 4 x 4 block of
       // (lane in quad) x (token) values across the quad, so lane 4i + r ends
       // up with features 4i..4i+3 of token 4m + r.
-      int tok = 0;
-      float wt = 0.f;
-      if (lane < 16 && c0 + lane < td.w) {
-        tok = p.tok_perm[td.z + c0 + lane];
-        wt = p.w_perm[td.z + c0 + lane];
-      }
       const int r = lane & 3;
       float* ybase = p.y_moe + td.y * 128 + 32 * q + (lane & ~3);
 #pragma unroll
@@ -191,8 +224,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int4 td, uint
           if (r & 1) a[j] = recv;
           else a[j + 1] = recv;
         }
-        const int tj = __shfl_sync(0xffffffffu, tok, 4 * m + r);
-        const float wj = __shfl_sync(0xffffffffu, wt, 4 * m + r);
+        const int tj = __shfl_sync(0xffffffffu, t_cur, (c0 & 16) + 4 * m + r);
+        const float wj = __shfl_sync(0xffffffffu, w_cur, (c0 & 16) + 4 * m + r);
         if (c0 + 4 * m + r < td.w) {
           float* dst = ybase + (size_t)tj * p.H;
           asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(wj * a[0]),

@@ -704,13 +704,7 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
       const int nb = (td.w + kBoxRows - 1) / kBoxRows;
       const int acc = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
-      if (!mbar_wait(&acc_full[acc], use & 1u, abort_flag)) {
-        if (lane == 0) report(p.status, kDevTimeout, kSiteGemmEpilogue, (unsigned)tile, 0u);
-        *abort_flag = 1;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
+      // per-tile values the epilogue needs, requested before the wait
       float g_lo = 1.f, g_hi = 1.f;  // NVFP4 matrix scales (gate / up lanes)
       if (NVFP4) {
         if (td.x != p.E) {
@@ -720,7 +714,15 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
           g_hi = MODE == 0 ? __ldg(p.g_d1) : g_lo;
         }
       }
-      epilogue_tile<MODE>(p, td, tbase, nb * kBoxRows, q, lane, g_lo, g_hi);
+      const EpiRows pre = epilogue_rows<MODE>(p, td, lane);
+      if (!mbar_wait(&acc_full[acc], use & 1u, abort_flag)) {
+        if (lane == 0) report(p.status, kDevTimeout, kSiteGemmEpilogue, (unsigned)tile, 0u);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
+      epilogue_tile<MODE>(p, td, tbase, nb * kBoxRows, q, lane, pre, g_lo, g_hi);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
