@@ -70,19 +70,30 @@ def peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
+def code_digest(paths):
+    """sha256 (16 hex digits) of the sources with comments and whitespace
+    removed: it changes when the compiled code can, not when a comment does."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for path in paths:
+        src = open(path).read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(re.sub(r"\s+", "", src).encode())
+    return h.hexdigest()[:16]
+
+
 def gate_up_traffic():
     """DRAM bytes per gate_up launch from the committed ncu capture, while the
     GEMM sources are the ones it was taken on (None otherwise)."""
-    import hashlib
     path = os.path.join(ROOT, "profiles", "gemm_gate_up_canvas256.json")
     if not os.path.exists(path):
         return None
     rec = json.load(open(path))
     csrc = os.path.join(ROOT, "moe_expert_ffn_dg_gb300", "csrc")
-    h = hashlib.sha256()
-    for f in rec.get("hashed_sources", ["dg_gemm.cu", "dg_common.cuh", "dg_kernels.h"]):
-        h.update(open(os.path.join(csrc, f), "rb").read())
-    return rec["dram_bytes_per_launch"] if h.hexdigest()[:16] == rec["gemm_source_sha256_16"] else None
+    digest = code_digest([os.path.join(csrc, f) for f in rec["hashed_sources"]])
+    return rec["dram_bytes_per_launch"] if digest == rec["gemm_code_digest"] else None
 
 
 def traffic_for(wl):
