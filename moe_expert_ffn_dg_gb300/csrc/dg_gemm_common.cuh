@@ -1,6 +1,7 @@
-// Pieces shared by the grouped GEMM kernels (bf16 weights through shared
-// memory, 4-bit weights dequantised into TMEM): the persistent tile schedule,
-// TMA loads of rank 4 and 5, the drain wait and the per-mode epilogue.
+// Pieces shared by the grouped GEMM kernels (bf16 weights loaded into shared
+// memory by TMA; quantised weights dequantised into shared memory): the
+// persistent tile schedule, TMA loads of rank 4 and 5, the drain wait and the
+// per-mode epilogue.
 #pragma once
 
 #include "dg_kernels.h"

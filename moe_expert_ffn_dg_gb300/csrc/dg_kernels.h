@@ -10,7 +10,7 @@
 
 namespace dg {
 
-// Token rows per tile of the grouped GEMMs is bounded by BN (128 or 256);
+// Token rows per tile of the grouped GEMMs are bounded by BN (32 to 256);
 // tiles are {group, feature tile, first row, rows}; group == E is the dense
 // branch.
 struct RouterParams {
@@ -173,8 +173,8 @@ cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s);
 // mode 0: gate_up + GEGLU, mode 1: down + weighted scatter
 cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s);
 size_t gemm_smem_bytes(int bn);
-// 4-bit weights, dequantised into TMEM; same modes.  bn is 64 or 128.
-// Grouped GEMM over quantised weights: qf 4 or 8 (group-64 affine codes of
+// Grouped GEMM over quantised weights, dequantised to bf16 in shared memory;
+// same modes, bn 32, 64, 128 or 256.  qf 4 or 8 (group-64 affine codes of
 // that many bits) or kQfNvfp4 (e2m1 codes, e4m3 scales per 16, fp32 matrix
 // scales).
 constexpr int kQfNvfp4 = 16;
