@@ -19,7 +19,9 @@
 // "DiffusionGemma Explained", MLP).
 // mode 1 (down): 128 output channels per tile; experts add w * y into the f32
 // per-token accumulator (the routing-weighted combine, "DiffusionGemma
-// Explained", MOEBlock.forward), the dense branch stores its f32 output.
+// Explained", MOEBlock.forward), or, from 1024 tokens, store it as the
+// assignment's f32 row for the combine to sum; the dense branch stores its f32
+// output.
 //
 // Tiles {group, feature tile, first row, rows} (group == E is the dense
 // branch) are decoded from the expert offsets in each CTA and dealt

@@ -1,5 +1,6 @@
-"""Host-side model of the barrier protocol of the quantised grouped GEMM
-(moe_expert_ffn_dg_gb300/csrc/dg_gemm_q4.cu), run on random tile sequences.
+"""Host-side models of the barrier protocols of the grouped GEMMs
+(moe_expert_ffn_dg_gb300/csrc/dg_gemm_q4.cu for quantised weights,
+dg_gemm.cu for bf16 weights), run on random tile sequences.
 
 The kernel's roles hand shared-memory slots and TMEM accumulators to one
 another through mbarriers, and an mbarrier wait compares only the parity of
@@ -27,15 +28,17 @@ import re
 
 import pytest
 
-SRC = os.path.join(os.path.dirname(os.path.dirname(__file__)), "moe_expert_ffn_dg_gb300",
-                   "csrc", "dg_gemm_q4.cu")
+CSRC = os.path.join(os.path.dirname(os.path.dirname(__file__)), "moe_expert_ffn_dg_gb300",
+                    "csrc")
+SRC = os.path.join(CSRC, "dg_gemm_q4.cu")
+SRC_BF16 = os.path.join(CSRC, "dg_gemm.cu")
 
 
 # ----------------------------------------------------------------- constants
 
 def _c_eval(expr: str, env: dict) -> int:
     """Evaluate a constant expression of the kernel source: integers, names
-    already evaluated, comparisons, * + - and right-nested ?: chains."""
+    already evaluated, comparisons, * / + - and right-nested ?: chains."""
     expr = expr.strip()
     if "?" in expr:
         cond, rest = expr.split("?", 1)
@@ -51,9 +54,9 @@ def _c_eval(expr: str, env: dict) -> int:
         a, b = rest[:cut], rest[cut + 1:]
         return _c_eval(a, env) if _c_eval(cond, env) else _c_eval(b, env)
     py = re.sub(r"\b[A-Za-z_]\w*\b", lambda m: str(env[m.group(0)]), expr)
-    if not re.fullmatch(r"[\d\s<>=!*+\-()]+", py):
+    if not re.fullmatch(r"[\d\s<>=!*/+\-()]+", py):
         raise ValueError(f"unexpected constant expression: {expr!r}")
-    return int(eval(py))  # digits and operators only
+    return int(eval(py.replace("/", "//")))  # digits and operators only; C division
 
 
 def kernel_config(bn: int) -> dict:
@@ -375,3 +378,130 @@ def test_model_catches_planted_mistakes(plant):
         except ProtocolError:
             caught += 1
     assert caught > 0, plant
+
+
+# ------------------------------------------------------- bf16-weight kernel
+
+def bf16_stages(bn: int) -> int:
+    src = open(SRC_BF16).read()
+    env = {"BN": bn}
+    env["kATileBytes"] = _c_eval(re.search(r"constexpr int kATileBytes = ([^;]+);", src).group(1),
+                                 env)
+    body = re.search(r"struct Cfg \{(.*?)\n\};", src, re.S).group(1)
+    for name, expr in re.findall(r"static constexpr int (k\w+) = ([^;]+);", body):
+        env[name] = _c_eval(expr, env)
+    return env["kStages"]
+
+
+def run_bf16_cta(S, tiles, seed, plant=None):
+    """The bf16 kernel: one producer fills a ring of S (weight, token) stages,
+    one thread issues the MMAs and frees each stage with a commit, four
+    epilogue warps drain the two accumulators."""
+    rnd = random.Random(seed)
+    world = {"version": 0}
+    full = [Bar(f"full{i}", 1) for i in range(S)]
+    empty = [Bar(f"empty{i}", 1) for i in range(S)]
+    acc_full = [Bar(f"acc_full{i}", 1) for i in range(2)]
+    acc_empty = [Bar(f"acc_empty{i}", 4) for i in range(2)]
+    n_stages = sum(tiles)
+    stage_tile = [t for t, n in enumerate(tiles) for _ in range(n)]
+    stage_last = [k == n - 1 for n in tiles for k in range(n)]
+    held = [None] * S          # stage whose operands sit in the slot (landed)
+    free = [True] * S
+    acc_busy = [None] * 2
+    pending, mma_queue, epi_done = [], [], [0, 0]
+
+    def producer():
+        for st in range(n_stages):
+            s = st % S
+            if plant != "skip_empty_wait":
+                yield from wait(empty[s], st // S)
+            if not free[s]:
+                raise ProtocolError(f"stage {st} overwrites slot {s} before its MMAs ended")
+            free[s] = False
+
+            def put(s=s, st=st):
+                held[s] = st
+            pending.append((full[s], put))
+            yield
+
+    def issuer():
+        st = 0
+        for local, n in enumerate(tiles):
+            acc = local & 1
+            yield from wait(acc_empty[acc], local >> 1)
+            if acc_busy[acc] is not None:
+                raise ProtocolError(f"tile {local} overwrites accumulator {acc}")
+            acc_busy[acc] = local
+            for _ in range(n):
+                yield from wait(full[st % S], st // S + 1)
+                if held[st % S] != st:
+                    raise ProtocolError(f"MMA of stage {st} reads slot holding {held[st % S]}")
+                mma_queue.append(st)
+                world["version"] += 1
+                st += 1
+                yield
+
+    def epilogue():
+        for local in range(len(tiles)):
+            acc = local & 1
+            yield from wait(acc_full[acc], (local >> 1) + 1)
+            if acc_busy[acc] != local:
+                raise ProtocolError(f"epilogue of tile {local} finds tile {acc_busy[acc]}")
+            yield
+            epi_done[acc] += 1
+            if epi_done[acc] == 4:
+                epi_done[acc] = 0
+                acc_busy[acc] = None
+            acc_empty[acc].arrive(world)
+
+    live = [producer(), issuer()] + [epilogue() for _ in range(4)]
+    idle = 0
+    while live or pending or mma_queue:
+        choices = len(live) + (1 if pending else 0) + (1 if mma_queue else 0)
+        pick = rnd.randrange(choices)
+        before = world["version"] + len(pending) + len(mma_queue)
+        if pick < len(live):
+            co = live[pick]
+            try:
+                next(co)
+            except StopIteration:
+                live.remove(co)
+                world["version"] += 1
+        elif pending and pick == len(live):
+            bar, action = pending.pop(rnd.randrange(len(pending)))
+            action()
+            bar.arrive(world)
+        else:
+            st = mma_queue.pop(0)
+            held[st % S] = None
+            free[st % S] = True
+            empty[st % S].arrive(world)
+            if stage_last[st]:
+                acc_full[stage_tile[st] & 1].arrive(world)
+        after = world["version"] + len(pending) + len(mma_queue)
+        idle = 0 if after != before else idle + 1
+        if idle > 5000 * (len(live) + 1):
+            raise ProtocolError("no role can make progress (deadlock)")
+    return True
+
+
+@pytest.mark.parametrize("bn", [64, 128, 256])
+def test_bf16_protocol_has_no_alias_overwrite_or_deadlock(bn):
+    S = bf16_stages(bn)
+    assert 3 <= S <= 8
+    rnd = random.Random(bn)
+    for seed in range(6):
+        tiles = random_tiles(rnd, 8) + [44, 11, 33, 1, 1]
+        rnd.shuffle(tiles)
+        assert run_bf16_cta(S, tiles, seed)
+
+
+def test_bf16_model_catches_a_skipped_slot_wait():
+    caught = 0
+    for seed in range(20):
+        try:
+            run_bf16_cta(bf16_stages(128), [11] * 8, seed, plant="skip_empty_wait")
+        except ProtocolError:
+            caught += 1
+    assert caught > 0
