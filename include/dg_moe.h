@@ -252,12 +252,22 @@ const char* dg_moe_last_error(const dg_moe_t* m);
  * Scratch: a fixed 8 MiB array in the library's device memory, held on
  * every GPU that loads the library until the process exits.  It needs
  * about n_tokens * (2 H + 4 E + 8) bytes; larger calls return
- * DG_ERR_UNSUPPORTED (a 256-token canvas at H 2816 needs 1.6 MB).  The first
- * call on a device looks up the array's device address (a CUDA runtime
- * query, no allocation), so make that first call before any stream
- * capture.  Every call on a device shares the one array: calls that can
- * overlap on the GPU (different streams without ordering) race.  Allocates
- * nothing. */
+ * DG_ERR_UNSUPPORTED (a 256-token canvas at H 2816 needs 1.6 MB).  The
+ * array's device address belongs to the CUDA context current at the call
+ * (normally the device's primary context): the first call in each context
+ * looks it up and raises the routing kernels' shared-memory limits (CUDA
+ * runtime queries and attributes, no allocation) and caches it under the
+ * context's unique id, so a context created later (after cudaDeviceReset,
+ * say) gets its own lookup.  Make that first call before any stream
+ * capture.  Every call in a context shares the one array and finds the
+ * previous call's contents in it (the parts that must start at zero are
+ * cleared on the stream): calls that can overlap on the GPU (different
+ * streams without ordering) race.  The same argument checks as
+ * dg_moe_create applies to the routing fields (cfg: hidden, n_experts,
+ * top_k, router_fmt, rms_eps >= 0, flags == 0; weights: router tensor and
+ * its 8-bit scales and biases, router_scale, w_pre_ff, per_expert_scale,
+ * router_bias alignment), then h_in 16-byte and the outputs 4-byte aligned.
+ * Allocates nothing. */
 dg_status_t dg_moe_route_noalloc(const dg_moe_config_t* cfg, const dg_moe_weights_t* weights,
                                  const void* h_in, int n_tokens, int32_t* idx_out, float* w_out,
                                  dg_stream_t stream);

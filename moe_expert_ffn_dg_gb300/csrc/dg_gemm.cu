@@ -263,14 +263,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
 
 template <int MODE, int BN>
 cudaError_t launch_mode_bn(const GemmParams& p, int grid, cudaStream_t s) {
-  using C = Cfg<BN>;
-  cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm<MODE, BN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
-  if (err != cudaSuccess) return err;
-  return launch_pdl(k_grouped_gemm<MODE, BN>, dim3(grid), dim3(kThreads), C::kSmem, s, p);
+  return launch_pdl(k_grouped_gemm<MODE, BN>, dim3(grid), dim3(kThreads), Cfg<BN>::kSmem, s, p);
+}
+
+template <int MODE, int BN>
+cudaError_t allow_smem() {
+  return cudaFuncSetAttribute(k_grouped_gemm<MODE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)Cfg<BN>::kSmem);
 }
 
 }  // namespace
+
+cudaError_t prepare_gemm_bf16() {
+  cudaError_t e;
+  if ((e = allow_smem<0, 64>()) != cudaSuccess || (e = allow_smem<0, 128>()) != cudaSuccess ||
+      (e = allow_smem<0, 256>()) != cudaSuccess || (e = allow_smem<1, 64>()) != cudaSuccess ||
+      (e = allow_smem<1, 128>()) != cudaSuccess || (e = allow_smem<1, 256>()) != cudaSuccess)
+    return e;
+  return cudaSuccess;
+}
 
 size_t gemm_smem_bytes(int bn) {
   return bn == 256 ? Cfg<256>::kSmem : bn == 128 ? Cfg<128>::kSmem : Cfg<64>::kSmem;

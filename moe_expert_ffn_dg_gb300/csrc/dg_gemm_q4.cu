@@ -9,9 +9,11 @@
 // — architecture & implemented contract", §8 nvfp4 expert profile): e2m1
 // codes in the 4-bit slab layout, an e4m3 scale per 16 codes and an fp32
 // scale per matrix; a code times its block scale is exact in bf16, and the
-// matrix scale multiplies the fp32 accumulator in the epilogue.  "diffgemma — architecture & implemented contract" (Part IV,
-// measurements) names the dequantisation as the cost that dominates 4-bit
-// expert layers; here it runs beside the tensor core instead of in front of it.
+// matrix scale multiplies the fp32 accumulator in the epilogue.  "Independent
+// GGUF Forward Pass and Bit-Identical Cross-Backend Consistency for a 26B
+// Text-Diffusion Model" (§1 contribution 6, §4 bottleneck ablation) names the
+// per-expert 4-bit dequantisation as the cost that dominates; here it runs
+// beside the tensor core instead of in front of it.
 //
 // Dataflow of one tile (128 weight rows x up to BN token rows), in stages of
 // one group (64 along K):
@@ -741,11 +743,29 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
 template <int MODE, int BN, int QF>
 cudaError_t launch_q4(const GemmParams& p, int grid, cudaStream_t s) {
   const size_t smem = CfgQ<BN>::kFixed + 4 * (size_t)p.sc_slot_bytes;
-  cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm_q4<MODE, BN, QF>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
   return launch_pdl(k_grouped_gemm_q4<MODE, BN, QF>, dim3(grid), dim3(CfgQ<BN>::kThreads), smem,
                     s, p);
+}
+
+// The scale slots depend on the shapes, so every instance may use up to the
+// device's opt-in maximum; launches that would exceed it are refused at
+// handle creation.
+template <int QF>
+cudaError_t allow_smem_q4(int smem_max) {
+  cudaError_t e = cudaSuccess;
+  auto one = [&](auto kernel) {
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+  };
+  one(k_grouped_gemm_q4<0, 32, QF>);
+  one(k_grouped_gemm_q4<0, 64, QF>);
+  one(k_grouped_gemm_q4<0, 128, QF>);
+  one(k_grouped_gemm_q4<0, 256, QF>);
+  one(k_grouped_gemm_q4<1, 32, QF>);
+  one(k_grouped_gemm_q4<1, 64, QF>);
+  one(k_grouped_gemm_q4<1, 128, QF>);
+  one(k_grouped_gemm_q4<1, 256, QF>);
+  return e;
 }
 
 template <int BITS>
@@ -770,6 +790,13 @@ size_t gemm_q4_smem_bytes(int bn, int sc_slot_bytes) {
                        : bn == 64  ? CfgQ<64>::kFixed
                                    : CfgQ<32>::kFixed;
   return fixed + 4 * (size_t)sc_slot_bytes;
+}
+
+cudaError_t prepare_gemm_affine(int smem_max) {
+  cudaError_t e;
+  if ((e = allow_smem_q4<4>(smem_max)) != cudaSuccess) return e;
+  if ((e = allow_smem_q4<8>(smem_max)) != cudaSuccess) return e;
+  return allow_smem_q4<kQfNvfp4>(smem_max);
 }
 
 cudaError_t launch_gemm_affine(int mode, int bn, int qf, const GemmParams& p, int grid,

@@ -49,6 +49,37 @@ inline dg_status_t check_qtensor(const dg_qtensor_t& t, dg_format_t fmt) {
   return DG_OK;
 }
 
+// Configuration fields the routing kernels use (shared by the block's
+// handle creation and the allocation-free routing entry point).
+inline dg_status_t check_router_config(const dg_moe_config_t* c) {
+  if (!c) return DG_ERR_INVALID_ARG;
+  if (c->hidden <= 0 || c->n_experts <= 0 || c->top_k <= 0 || c->rms_eps < 0.f || c->flags != 0)
+    return DG_ERR_INVALID_ARG;
+  if (c->top_k > c->n_experts) return DG_ERR_INVALID_ARG;
+  if (c->hidden % 128) return DG_ERR_UNSUPPORTED;
+  if (c->hidden > 8192 || c->n_experts > 256 || c->top_k > 16) return DG_ERR_UNSUPPORTED;
+  if (c->router_fmt != DG_FMT_BF16 && c->router_fmt != DG_FMT_AFFINE_U8_G64)
+    return DG_ERR_UNSUPPORTED;
+  return DG_OK;
+}
+
+// Weights the routing kernels read: the router matrix (and its 8-bit scales
+// and biases), router_scale and w_pre_ff (16-byte vector loads),
+// per_expert_scale (bf16 loads) and the optional f32 router_bias.
+inline dg_status_t check_router_weights(const dg_moe_config_t& c, const dg_moe_weights_t* w) {
+  if (!w) return DG_ERR_INVALID_ARG;
+  dg_status_t s;
+  if ((s = check_qtensor(w->router, c.router_fmt)) != DG_OK) return s;
+  for (const void* v : {w->router_scale, w->w_pre_ff}) {
+    if (!v) return DG_ERR_INVALID_ARG;
+    if (!aligned(v, 16)) return DG_ERR_ALIGNMENT;
+  }
+  if (!w->per_expert_scale) return DG_ERR_INVALID_ARG;
+  if (!aligned(w->per_expert_scale, 2)) return DG_ERR_ALIGNMENT;
+  if (w->router_bias && !aligned(w->router_bias, 4)) return DG_ERR_ALIGNMENT;
+  return DG_OK;
+}
+
 inline PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {

@@ -166,6 +166,15 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// Raise the dynamic shared-memory limits of the kernels to what their
+// launches may use (router and quantised GEMMs: the device's opt-in maximum
+// smem_max, as their sizes depend on the shapes; bf16 GEMMs: their fixed
+// tile sizes).  The limits belong to the current device; they are set once
+// per handle at creation instead of before every launch.
+cudaError_t prepare_router(int smem_max);
+cudaError_t prepare_gemm_bf16();
+cudaError_t prepare_gemm_affine(int smem_max);
+
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s);
 cudaError_t launch_router_select(const RouterParams& p, cudaStream_t s);
 cudaError_t launch_route_scatter(const ScatterParams& p, cudaStream_t s);

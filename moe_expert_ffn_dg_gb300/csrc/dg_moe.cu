@@ -77,13 +77,10 @@ Layout make_layout(const dg_moe_config_t& c) {
 
 
 dg_status_t check_config(const dg_moe_config_t* c) {
-  if (!c) return DG_ERR_INVALID_ARG;
-  if (c->hidden <= 0 || c->n_experts <= 0 || c->top_k <= 0 || c->expert_inter <= 0 ||
-      c->dense_inter <= 0 || c->max_tokens <= 0 || c->rms_eps < 0.f || c->flags != 0)
-    return DG_ERR_INVALID_ARG;
-  if (c->top_k > c->n_experts) return DG_ERR_INVALID_ARG;
-  if (c->hidden % 128 || c->expert_inter % 64 || c->dense_inter % 64) return DG_ERR_UNSUPPORTED;
-  if (c->hidden > 8192 || c->n_experts > 256 || c->top_k > 16) return DG_ERR_UNSUPPORTED;
+  dg_status_t s = check_router_config(c);
+  if (s != DG_OK) return s;
+  if (c->expert_inter <= 0 || c->dense_inter <= 0 || c->max_tokens <= 0) return DG_ERR_INVALID_ARG;
+  if (c->expert_inter % 64 || c->dense_inter % 64) return DG_ERR_UNSUPPORTED;
   if (c->max_tokens > (1 << 20)) return DG_ERR_UNSUPPORTED;
   // expert and dense weights: both bf16, or 4-bit group-64 affine experts
   // with a 4- or 8-bit dense branch
@@ -96,30 +93,23 @@ dg_status_t check_config(const dg_moe_config_t* c) {
   // in shared memory beside the narrowest tiles' pipelines
   if (q4w && (c->hidden > 2944 || c->expert_inter > 2944 || c->dense_inter > 2944))
     return DG_ERR_UNSUPPORTED;
-  if (c->router_fmt != DG_FMT_BF16 && c->router_fmt != DG_FMT_AFFINE_U8_G64)
-    return DG_ERR_UNSUPPORTED;
   return DG_OK;
 }
 
 
 dg_status_t check_weights(const dg_moe_config_t& c, const dg_moe_weights_t* w) {
-  if (!w) return DG_ERR_INVALID_ARG;
   dg_status_t s;
-  if ((s = check_qtensor(w->router, c.router_fmt)) != DG_OK) return s;
+  if ((s = check_router_weights(c, w)) != DG_OK) return s;
   if ((s = check_qtensor(w->gate_up, c.expert_fmt)) != DG_OK) return s;
   if ((s = check_qtensor(w->down, c.expert_fmt)) != DG_OK) return s;
   if ((s = check_qtensor(w->dense_gate, c.dense_fmt)) != DG_OK) return s;
   if ((s = check_qtensor(w->dense_up, c.dense_fmt)) != DG_OK) return s;
   if ((s = check_qtensor(w->dense_down, c.dense_fmt)) != DG_OK) return s;
-  const void* vecs[] = {w->router_scale, w->w_pre_ff, w->w_pre_ff2, w->w_post_ff1,
-                        w->w_post_ff2, w->w_post_ff};
+  const void* vecs[] = {w->w_pre_ff2, w->w_post_ff1, w->w_post_ff2, w->w_post_ff};
   for (const void* v : vecs) {
     if (!v) return DG_ERR_INVALID_ARG;
     if (!aligned(v, 16)) return DG_ERR_ALIGNMENT;
   }
-  if (!w->per_expert_scale) return DG_ERR_INVALID_ARG;
-  if (!aligned(w->per_expert_scale, 2)) return DG_ERR_ALIGNMENT;
-  if (w->router_bias && !aligned(w->router_bias, 4)) return DG_ERR_ALIGNMENT;
   return DG_OK;
 }
 
@@ -210,6 +200,12 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
   }
   m->smem_optin = (size_t)optin;
   const dg_moe_config_t& c = m->cfg;
+  const bool quantised = c.expert_fmt != DG_FMT_BF16;
+  if (prepare_router(optin) != cudaSuccess ||
+      (quantised ? prepare_gemm_affine(optin) : prepare_gemm_bf16()) != cudaSuccess) {
+    delete m;
+    return DG_ERR_CUDA;
+  }
   const uint64_t H = c.hidden, E = c.n_experts, I = c.expert_inter, D = c.dense_inter;
   const uint64_t T = c.max_tokens, TK = T * c.top_k;
   uint8_t* ws = m->ws;

@@ -9,22 +9,22 @@
 // kernels' scratch in a fixed array that lives in this library's device
 // memory for as long as the library is loaded, on every GPU that loads it.
 // The caller passes only the inputs and the two outputs.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "../../include/dg_moe.h"
+#include "dg_host.h"
 #include "dg_kernels.h"
 
 using namespace dg;
+using namespace dg::host;
 
 namespace {
 
 // Fixed device scratch for the allocation-free routing entry point.
 constexpr size_t kRouteScratchBytes = size_t(8) << 20;
 static __device__ __align__(256) unsigned char g_route_scratch[kRouteScratchBytes];
-
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices];
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -51,21 +51,69 @@ RouteScratch route_scratch_layout(size_t T, size_t H, size_t E) {
   return s;
 }
 
-bool aligned_to(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+// The scratch array's device address belongs to a CUDA context: a device's
+// primary context, or a context the caller created, and a new context
+// (after cudaDeviceReset, say) loads the library's device code again at
+// another address.  So the address is looked up once per context and cached
+// under the context's unique id, which the driver never reuses; the kernels'
+// shared-memory limits are raised in the same set-up.
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+constexpr int kMaxContexts = 64;
+std::mutex g_scratch_mu;
+ScratchEntry g_scratch[kMaxContexts];
+int g_n_scratch = 0;
 
-// Device address of the scratch array on the current device, looked up once
-// per device (the array's name is only a host-side stand-in).
+PFN_cuCtxGetCurrent_v4000 g_get_ctx = nullptr;
+PFN_cuCtxGetId_v12000 g_get_ctx_id = nullptr;
+
+bool driver_fns() {
+  if (g_get_ctx && g_get_ctx_id) return true;
+  void* a = nullptr;
+  void* b = nullptr;
+  cudaDriverEntryPointQueryResult qa, qb;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 4000, cudaEnableDefault, &qa) !=
+          cudaSuccess ||
+      qa != cudaDriverEntryPointSuccess ||
+      cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) !=
+          cudaSuccess ||
+      qb != cudaDriverEntryPointSuccess)
+    return false;
+  g_get_ctx = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(a);
+  g_get_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(b);
+  return true;
+}
+
+// Device address of the scratch array in the current context (the array's
+// name is only a host-side stand-in for it).
 dg_status_t scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return DG_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return DG_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
+  if (!driver_fns()) return DG_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  void* p = nullptr;
+  if (g_get_ctx(&ctx) != CUDA_SUCCESS) return DG_ERR_CUDA;
+  if (!ctx) {
+    // no context yet: the runtime query sets up the device's primary one
     if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) return DG_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+    if (g_get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return DG_ERR_CUDA;
   }
-  *out = g_scratch_ptr[dev];
+  unsigned long long id = 0;
+  if (g_get_ctx_id(ctx, &id) != CUDA_SUCCESS) return DG_ERR_CUDA;
+  for (int i = 0; i < g_n_scratch; ++i)
+    if (g_scratch[i].ctx_id == id) {
+      *out = g_scratch[i].ptr;
+      return DG_OK;
+    }
+  int dev = 0, optin = 0;
+  if (!p && (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p)) return DG_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+      prepare_router(optin) != cudaSuccess)
+    return DG_ERR_CUDA;
+  if (g_n_scratch < kMaxContexts) g_scratch[g_n_scratch++] = {id, p};
+  *out = p;
   return DG_OK;
 }
 
@@ -75,27 +123,21 @@ extern "C" dg_status_t dg_moe_route_noalloc(const dg_moe_config_t* cfg,
                                             const dg_moe_weights_t* weights, const void* h_in,
                                             int n_tokens, int32_t* idx_out, float* w_out,
                                             dg_stream_t stream) {
-  if (!cfg || !weights) return DG_ERR_INVALID_ARG;
+  // the same checks as handle creation applies to the fields routing uses
+  dg_status_t st = check_router_config(cfg);
+  if (st != DG_OK) return st;
+  if ((st = check_router_weights(*cfg, weights)) != DG_OK) return st;
+  if (n_tokens < 0) return DG_ERR_INVALID_ARG;
   const int H = cfg->hidden, E = cfg->n_experts, K = cfg->top_k;
-  if (H <= 0 || E <= 0 || K <= 0 || K > E || n_tokens < 0) return DG_ERR_INVALID_ARG;
-  if (H % 128 || H > 8192 || E > 256 || K > 16) return DG_ERR_UNSUPPORTED;
-  if (cfg->router_fmt != DG_FMT_BF16 && cfg->router_fmt != DG_FMT_AFFINE_U8_G64)
-    return DG_ERR_UNSUPPORTED;
   const bool u8 = cfg->router_fmt == DG_FMT_AFFINE_U8_G64;
-  if (!weights->router.q || !weights->router_scale || !weights->per_expert_scale ||
-      !weights->w_pre_ff || (u8 && (!weights->router.scales || !weights->router.biases)))
-    return DG_ERR_INVALID_ARG;
   if (n_tokens == 0) return DG_OK;
   if (!h_in || !idx_out || !w_out) return DG_ERR_INVALID_ARG;
-  if (!aligned_to(weights->router.q, 16) || !aligned_to(weights->router_scale, 16) ||
-      !aligned_to(weights->w_pre_ff, 16) || !aligned_to(h_in, 16) || !aligned_to(idx_out, 4) ||
-      !aligned_to(w_out, 4))
-    return DG_ERR_ALIGNMENT;
+  if (!aligned(h_in, 16) || !aligned(idx_out, 4) || !aligned(w_out, 4)) return DG_ERR_ALIGNMENT;
   const RouteScratch L = route_scratch_layout((size_t)n_tokens, (size_t)H, (size_t)E);
   if (L.total > kRouteScratchBytes) return DG_ERR_UNSUPPORTED;  // beyond the fixed scratch
 
   void* base = nullptr;
-  dg_status_t st = scratch_address(&base);
+  st = scratch_address(&base);
   if (st != DG_OK) return st;
   uint8_t* sc = static_cast<uint8_t*>(base);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -636,9 +636,6 @@ size_t router_tile_smem(int H) {
 template <bool U8, bool FUSED>
 cudaError_t launch_router_tile_f(const RouterParams& p, cudaStream_t s) {
   const size_t smem = router_tile_smem(p.H);
-  cudaError_t err = cudaFuncSetAttribute(k_router_logits_tile<U8, FUSED>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
   const dim3 grid((p.T + kRT - 1) / kRT, (p.E + kRE - 1) / kRE);
   return launch_pdl(k_router_logits_tile<U8, FUSED>, grid, dim3(256), smem, s, p);
 }
@@ -1094,14 +1091,26 @@ size_t router_smem(int H) {
 template <int TB, bool U8>
 cudaError_t launch_router_tb(const RouterParams& p, cudaStream_t s) {
   const size_t smem = router_smem<TB>(p.H);
-  cudaError_t err = cudaFuncSetAttribute(k_router_logits<TB, U8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
   const dim3 grid((p.T + TB - 1) / TB, (p.E + kLogitExperts - 1) / kLogitExperts);
   return launch_pdl(k_router_logits<TB, U8>, grid, dim3(256), smem, s, p);
 }
 
 }  // namespace
+
+cudaError_t prepare_router(int smem_max) {
+  cudaError_t e = cudaSuccess;
+  auto one = [&](auto kernel) {
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+  };
+  one(k_router_logits<4, false>);
+  one(k_router_logits<4, true>);
+  one(k_router_logits_tile<false, false>);
+  one(k_router_logits_tile<false, true>);
+  one(k_router_logits_tile<true, false>);
+  one(k_router_logits_tile<true, true>);
+  return e;
+}
 
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s) {
   // four tokens per block give a single canvas enough blocks; from a few

@@ -219,6 +219,10 @@ dg_status_t dg_sc_mlp_create(const dg_sc_mlp_config_t* cfg, const dg_sc_mlp_weig
     return DG_ERR_CUDA;
   }
   m->smem_optin = (size_t)optin;
+  if ((m->q4 ? prepare_gemm_affine(optin) : prepare_gemm_bf16()) != cudaSuccess) {
+    delete m;
+    return DG_ERR_CUDA;
+  }
   const uint64_t H = cfg->hidden, D = cfg->inter, T = cfg->max_tokens;
   uint8_t* ws = m->ws;
   const bool q4 = m->q4;

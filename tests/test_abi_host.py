@@ -128,3 +128,60 @@ def test_nvfp4_format_pairs(lib):
     assert lib.dg_moe_workspace_size(ctypes.byref(ok), ctypes.byref(n)) == B.DG_OK
     mixed = _cfg(expert_fmt=B.DG_FMT_NVFP4_G16, dense_fmt=B.DG_FMT_AFFINE_U4_G64)
     assert lib.dg_moe_workspace_size(ctypes.byref(mixed), ctypes.byref(n)) == B.DG_ERR_UNSUPPORTED
+
+
+def _route_noalloc(lib, cfg, w, h=0x10000, T=4, idx=0x20000, wo=0x30000):
+    return lib.dg_moe_route_noalloc(None if cfg is None else ctypes.byref(cfg),
+                                    None if w is None else ctypes.byref(w), h, T, idx, wo, None)
+
+
+def test_route_noalloc_rejects_bad_arguments_before_any_cuda_call(lib):
+    """Every rejection below returns before the scratch array is looked up or
+    any kernel launched, so it runs without a GPU."""
+    ok_cfg, ok_w = _cfg(), _weights()
+    assert _route_noalloc(lib, None, ok_w) == B.DG_ERR_INVALID_ARG
+    assert _route_noalloc(lib, ok_cfg, None) == B.DG_ERR_INVALID_ARG
+    for bad, code in [(dict(top_k=129), B.DG_ERR_INVALID_ARG),        # K > E
+                      (dict(top_k=0), B.DG_ERR_INVALID_ARG),
+                      (dict(hidden=0), B.DG_ERR_INVALID_ARG),
+                      (dict(rms_eps=-1.0), B.DG_ERR_INVALID_ARG),
+                      (dict(flags=2), B.DG_ERR_INVALID_ARG),
+                      (dict(hidden=2880), B.DG_ERR_UNSUPPORTED),      # H % 128
+                      (dict(n_experts=512), B.DG_ERR_UNSUPPORTED),
+                      (dict(router_fmt=B.DG_FMT_AFFINE_U4_G64), B.DG_ERR_UNSUPPORTED)]:
+        assert _route_noalloc(lib, _cfg(**bad), ok_w) == code, bad
+    # weights the routing kernels read
+    w = _weights()
+    w.router.q = None
+    assert _route_noalloc(lib, ok_cfg, w) == B.DG_ERR_INVALID_ARG
+    w = _weights()
+    w.router.q = 0x10008
+    assert _route_noalloc(lib, ok_cfg, w) == B.DG_ERR_ALIGNMENT
+    w = _weights()
+    w.router_scale = 0x10004
+    assert _route_noalloc(lib, ok_cfg, w) == B.DG_ERR_ALIGNMENT
+    w = _weights()
+    w.w_pre_ff = None
+    assert _route_noalloc(lib, ok_cfg, w) == B.DG_ERR_INVALID_ARG
+    w = _weights()
+    w.per_expert_scale = 0x10001
+    assert _route_noalloc(lib, ok_cfg, w) == B.DG_ERR_ALIGNMENT
+    w = _weights()
+    w.router_bias = 0x10002          # f32 loads need 4-byte alignment
+    assert _route_noalloc(lib, ok_cfg, w) == B.DG_ERR_ALIGNMENT
+    # the 8-bit router needs its scales and biases (2-byte aligned)
+    u8 = _cfg(router_fmt=B.DG_FMT_AFFINE_U8_G64)
+    assert _route_noalloc(lib, u8, _weights()) == B.DG_ERR_INVALID_ARG
+    w = _weights()
+    w.router.scales, w.router.biases = 0x10001, 0x10000
+    assert _route_noalloc(lib, u8, w) == B.DG_ERR_ALIGNMENT
+    # token count and the per-call buffers
+    assert _route_noalloc(lib, ok_cfg, ok_w, T=-1) == B.DG_ERR_INVALID_ARG
+    assert _route_noalloc(lib, ok_cfg, ok_w, T=0) == B.DG_OK    # nothing to do
+    assert _route_noalloc(lib, ok_cfg, ok_w, h=None) == B.DG_ERR_INVALID_ARG
+    assert _route_noalloc(lib, ok_cfg, ok_w, idx=None) == B.DG_ERR_INVALID_ARG
+    assert _route_noalloc(lib, ok_cfg, ok_w, h=0x10008) == B.DG_ERR_ALIGNMENT
+    assert _route_noalloc(lib, ok_cfg, ok_w, idx=0x20002) == B.DG_ERR_ALIGNMENT
+    assert _route_noalloc(lib, ok_cfg, ok_w, wo=0x30001) == B.DG_ERR_ALIGNMENT
+    # beyond the fixed scratch: refused on the host
+    assert _route_noalloc(lib, ok_cfg, ok_w, T=4096) == B.DG_ERR_UNSUPPORTED

@@ -28,9 +28,15 @@ def _built():
     pkg.load_library()
 
 
-@pytest.mark.parametrize("name", ["tiny", "canvas256"])
-def test_noalloc_routing_equals_forward_routing_twice(name):
-    wl = mi.get_workload(name)
+@pytest.mark.parametrize("name,tokens", [
+    ("tiny", 0), ("canvas256", 0),
+    # 8-bit router (the 4-bit canvas workload quantises its router to 8 bits)
+    ("canvas256_q4", 0),
+    # from 4096 tokens the logits come from the register-tiled kernel; at
+    # hidden 256 that still fits the fixed scratch
+    ("tiny", 4100)])
+def test_noalloc_routing_equals_forward_routing_twice(name, tokens):
+    wl = mi.get_workload(name, **({"tokens": tokens} if tokens else {}))
     p = mi.make_layer_inputs(wl, randvec=True)
     h = to_dev_bf16(mi.make_tokens(wl))
     blk = make_block(wl, p)
