@@ -301,31 +301,13 @@ def run_stack(args):
     names = B.dg_moe_kernel_names(blocks[0].handle)
     nk = len(names)
     prof_layer = L // 2
-    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
-               for _ in range(args.steps)]
-    for evs in ev_sets:
-        for e in evs:
-            e.record(stream)
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(0)
-    time.sleep(0.3)
-    torch.cuda.synchronize(dev)
-    start.record(stream)
-    for i in range(args.steps):
-        B.dg_moe_set_profile_events(blocks[prof_layer].handle, [e.cuda_event for e in ev_sets[i]])
-        step(h)
-    stop.record(stream)
-    torch.cuda.synchronize(dev)
-    B.dg_moe_set_profile_events(blocks[prof_layer].handle, None)
-    clk = clocks.stop()
+    elapsed_ms, clk = time_steps(lambda: step(h), stream, dev, args.steps)
     st = blocks[0].device_status()
     if st[0] != 0:
         raise RuntimeError(f"device status after timing: {st}")
-    ms_step = start.elapsed_time(stop) / args.steps
-    per_kernel = np.zeros(nk)
-    for evs in ev_sets:
-        per_kernel += [evs[j].elapsed_time(evs[j + 1]) for j in range(nk)]
-    per_kernel_us = per_kernel / len(ev_sets) * 1000.0
+    ms_step = elapsed_ms / args.steps
+    per_kernel_us = kernel_split(blocks[prof_layer], lambda: step(h), stream, dev,
+                                 max(3, min(args.steps, 20)), B.dg_moe_set_profile_events, names)
 
     # end to end: pinned host input -> device, all layers, output -> host
     h_host = torch.from_numpy(h_np.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -372,7 +354,7 @@ def run_stack(args):
                 "d2h_bytes_per_step": int(o_host.numel() * 2), "steps": e2e_steps,
                 "note": "per layer: tokens / (end-to-end step time / layers)"},
         "clocks": clk,
-        "gpu_launches": nk * L * args.steps,
+        "gpu_launches": launches_per_forward(wl, nk) * L * args.steps,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, p0, h_np, max_seconds=20.0)
@@ -449,32 +431,13 @@ def run_sc(args):
     torch.cuda.synchronize(dev)
     if sc.device_status() != 0:
         raise RuntimeError("device status after warm-up")
-    stride = max(1, args.steps // 200)
-    ev_sets = {i: [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
-               for i in range(0, args.steps, stride)}
-    for evs in ev_sets.values():
-        for ev in evs:
-            ev.record(stream)
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(0)
-    time.sleep(0.3)
-    torch.cuda.synchronize(dev)
-    start.record(stream)
-    for i in range(args.steps):
-        evs = ev_sets.get(i)
-        B.dg_sc_mlp_set_profile_events(sc.handle, [x.cuda_event for x in evs] if evs else None)
-        sc.forward(e, sig, out=out)
-    stop.record(stream)
-    torch.cuda.synchronize(dev)
-    B.dg_sc_mlp_set_profile_events(sc.handle, None)
-    clk = clocks.stop()
+    elapsed_ms, clk = time_steps(lambda: sc.forward(e, sig, out=out), stream, dev, args.steps)
     if sc.device_status() != 0:
         raise RuntimeError("device status after timing")
-    ms = start.elapsed_time(stop) / args.steps
-    per_kernel = np.zeros(nk)
-    for evs in ev_sets.values():
-        per_kernel += [evs[j].elapsed_time(evs[j + 1]) for j in range(nk)]
-    per_kernel_us = per_kernel / len(ev_sets) * 1000.0
+    ms = elapsed_ms / args.steps
+    per_kernel_us = kernel_split(sc, lambda: sc.forward(e, sig, out=out), stream, dev,
+                                 max(3, min(args.steps, 200)), B.dg_sc_mlp_set_profile_events,
+                                 names)
 
     # end to end: pinned host embeddings and signal in, output back, synchronised
     e_host = torch.from_numpy(p["embeds"].view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -530,12 +493,189 @@ def run_sc(args):
     print(json.dumps(line))
 
 
-def run_ours(args):
+def time_steps(fwd, stream, dev, steps, local=0, dist=None):
+    """Wall time of `steps` back-to-back forwards on the device (CUDA events
+    on the launching stream, nothing recorded between the kernels), with
+    nvidia-smi clocks sampled meanwhile.  Returns (elapsed ms, clocks)."""
+    import torch
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for _ in range(steps):
+        fwd()
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    return start.elapsed_time(stop), clocks.stop()
+
+
+def kernel_split(blk, fwd, stream, dev, steps, set_events, names):
+    """Average device time of each kernel of a forward, from a separate pass
+    with an event recorded between consecutive kernels (the events stop the
+    kernels' programmatic overlap, so these times are a little longer than
+    the kernels take inside an event-free step)."""
+    import torch
+    nk = len(names)
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(steps)]
+    # torch creates the CUDA event at its first record(): record every event
+    # once so the handles given to the library are real
+    for evs in ev_sets:
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize(dev)
+    for evs in ev_sets:
+        set_events(blk.handle, [e.cuda_event for e in evs])
+        fwd()
+    torch.cuda.synchronize(dev)
+    set_events(blk.handle, None)
+    per_kernel = np.zeros(nk)
+    for evs in ev_sets:
+        per_kernel += [evs[j].elapsed_time(evs[j + 1]) for j in range(nk)]
+    return per_kernel / len(ev_sets) * 1000.0
+
+
+ROUTER_TC_MIN_TOKENS = 1024  # the library's tensor-core router threshold
+
+
+def launches_per_forward(wl, nk):
+    # an 8-bit dense branch beside 4-bit experts adds a dense-only launch to
+    # each of the two GEMM slots; from 1024 tokens the router slot holds two
+    # launches (prep and the router GEMM)
+    return (nk + (2 if wl.quant and wl.quant[1] != wl.quant[0] else 0)
+            + (1 if wl.tokens >= ROUTER_TC_MIN_TOKENS else 0))
+
+
+def measure_layer(wl, p, h_np, dev, steps, warmup, local=0, neighbours=False, dist=None,
+                  budget_s=None):
+    """Time one MoE layer on its workload: an event-free pass for the step
+    time, a separate pass for the per-kernel split, the routing of the timed
+    tokens for the touched-expert count, and the roofline fractions.
+    Returns (result dict, block, forward closure)."""
     import torch
 
     import moe_expert_ffn_dg_gb300 as pkg
     import moe_inputs as mi
     from moe_expert_ffn_dg_gb300 import binding as B
+    from moe_expert_ffn_dg_gb300 import replicas
+
+    blk = pkg.MoEBlock.from_params(p, hidden=wl.hidden, n_experts=wl.n_experts, top_k=wl.top_k,
+                                   expert_inter=wl.expert_inter, dense_inter=wl.dense_inter,
+                                   max_tokens=wl.tokens, device=dev)
+    h = torch.from_numpy(h_np.view(np.int16)).to(dev).view(torch.bfloat16)
+    out = torch.empty_like(h)
+    stream = torch.cuda.current_stream(dev)
+    names = B.dg_moe_kernel_names(blk.handle)
+    ls = float(p.get("layer_scalar", 1.0))
+    if neighbours:
+        # the decoder layer's neighbours fused in: h is the layer input, attn
+        # the attention output (N(0, 4)), norm weights U(0.5, 1.5)
+        g = np.random.default_rng(wl.seed + 200)
+        dbf = lambda a: torch.from_numpy(mi.f32_to_bf16_bits(a.astype(np.float32)).view(np.int16)).to(dev).view(torch.bfloat16)
+        attn = dbf(g.standard_normal((wl.tokens, wl.hidden)) * 4.0)
+        w_pa, w_next = dbf(g.uniform(0.5, 1.5, wl.hidden)), dbf(g.uniform(0.5, 1.5, wl.hidden))
+        nxt = torch.empty_like(h)
+
+    def fwd():
+        if neighbours:
+            blk.forward_neighbours(h, attn, w_pa, w_next, ls, out=out, next_in=nxt)
+        else:
+            blk.forward(h, ls, out=out)
+
+    t0 = time.perf_counter()
+    for _ in range(max(warmup, 3)):
+        fwd()
+    torch.cuda.synchronize(dev)
+    t_warm = (time.perf_counter() - t0) / max(warmup, 3)
+    st = blk.device_status()
+    if st[0] != 0:
+        raise RuntimeError(f"{wl.name}: device status after warm-up: {st}")
+    if budget_s:
+        steps = max(10, min(steps, int(budget_s / max(t_warm, 1e-6))))
+    elapsed_ms, clk = time_steps(fwd, stream, dev, steps, local, dist)
+    elapsed_ms = replicas.max_over_ranks(elapsed_ms, dist, dev)
+    st = blk.device_status()
+    if st[0] != 0:
+        raise RuntimeError(f"{wl.name}: device status after timing: {st}")
+    ms = elapsed_ms / steps
+    per_kernel_us = kernel_split(blk, fwd, stream, dev, max(3, min(steps, 200)),
+                                 B.dg_moe_set_profile_events, names)
+    # routing of the timed tokens (for the touched-expert count)
+    _, dbg = blk.forward(h, ls, debug=True)
+    counts = np.diff(dbg["offsets"].cpu().numpy())
+    alg = algorithmic(wl, counts)
+    if neighbours:
+        alg["layer_bytes"] += 2 * wl.tokens * wl.hidden * 2 + 2 * wl.hidden * 2  # attn in, next_in out
+    hbm, bf16_burst, bf16_sus, src = peaks()
+    T, H, K, I, D = wl.tokens, wl.hidden, wl.top_k, wl.expert_inter, wl.dense_inter
+    gu = names.index("gemm_gate_up")
+    gu_s = per_kernel_us[gu] * 1e-6
+    t_roof = max(alg["layer_bytes"] / (hbm * 1e9), alg["layer_flops"] / (bf16_sus * 1e12))
+    gu_flops = 2 * T * K * H * 2 * I + 2 * T * H * 2 * D
+    tensor_bound = alg["layer_flops"] / (bf16_sus * 1e12) > alg["layer_bytes"] / (hbm * 1e9)
+    if tensor_bound:
+        achieved = gu_flops / gu_s / 1e12
+        roof = {"bound": "tensor", "kernel": "gemm_gate_up", "achieved": achieved,
+                "peak": bf16_sus, "unit": "TFLOP/s", "frac": achieved / bf16_sus, "traffic": None,
+                "peak_source": f"{src} (MEASURED_PEAKS.json bf16_tflops_sustained)",
+                "algorithmic_flops_per_launch": gu_flops, "us_per_launch": per_kernel_us[gu]}
+    else:
+        achieved = alg["gate_up_bytes"] / gu_s / 1e9
+        roof = {"bound": "hbm", "kernel": "gemm_gate_up", "achieved": achieved, "peak": hbm,
+                "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic_for(wl),
+                "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else src,
+                "algorithmic_bytes_per_launch": alg["gate_up_bytes"],
+                "us_per_launch": per_kernel_us[gu]}
+    res = {
+        "workload": workload_desc(wl), "tokens_per_step": T, "steps": steps,
+        "us_per_layer": ms * 1000.0, "value": T / (ms / 1000.0), "unit": UNIT,
+        "touched_experts": alg["touched_experts"],
+        "expert_loads": {"max": int(counts.max()), "empty": int((counts == 0).sum())},
+        "roofline": roof,
+        "layer_roofline": {"bytes": alg["layer_bytes"], "flops": alg["layer_flops"],
+                           "t_roof_us": t_roof * 1e6, "frac": t_roof / (ms / 1000.0),
+                           "basis": f"max(bytes / {hbm} GB/s, flops / {bf16_sus} TF/s) ({src}); "
+                                    f"against the nominal 8 TB/s / 2.25 PF: "
+                                    f"{max(alg['layer_bytes'] / 8e12, alg['layer_flops'] / 2.25e15) / (ms / 1000.0):.3f}"},
+        "kernels_us": {n: round(float(v), 3) for n, v in zip(names, per_kernel_us)},
+        "kernels_note": "separate pass with an event between kernels (no overlap between them)",
+        "clocks": clk,
+        "gpu_launches": launches_per_forward(wl, len(names)) * steps,
+        "ms_per_step": ms,
+    }
+    return res, blk, fwd
+
+
+# The configurations of the specification measured beside the headline in
+# the default run: the 4-bit canvas, the Zipf-skewed batch of 8 canvases and
+# one layer of the 30-layer 4-bit stack at its 16 384 tokens.
+EXTRA_CONFIGS = ("canvas256_q4", "batch2048_zipf", "stack30_q4_layer")
+
+
+def extra_config(name, dev, steps, warmup):
+    import moe_inputs as mi
+    if name == "stack30_q4_layer":
+        wl = mi.get_workload("stack30_q4")
+        p = mi.make_layer_inputs(wl, layer=0)
+        h_np = mi.make_tokens(wl)
+        res, blk, _ = measure_layer(wl, p, h_np, dev, steps, warmup, budget_s=2.0)
+        res["workload"] = ("stack30_q4 layer 0 (one layer of the 30-layer stack, its own "
+                           "weights and layer scalar): " + workload_desc(wl))
+    else:
+        wl = mi.get_workload(name)
+        p = mi.make_layer_inputs(wl)
+        res, blk, _ = measure_layer(wl, p, mi.make_tokens(wl), dev, steps, warmup, budget_s=2.0)
+    blk.close()
+    return res
+
+
+def run_ours(args):
+    import torch
+
+    import moe_expert_ffn_dg_gb300 as pkg
+    import moe_inputs as mi
     from moe_expert_ffn_dg_gb300 import replicas
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -557,70 +697,8 @@ def run_ours(args):
     # each replica processes its own canvas (data parallel over canvases)
     h_np = mi.make_tokens(mi.get_workload(args.workload, seed=replicas.replica_seed(wl.seed, rank),
                                           tokens=wl.tokens))
-    blk = pkg.MoEBlock.from_params(p, hidden=wl.hidden, n_experts=wl.n_experts, top_k=wl.top_k,
-                                   expert_inter=wl.expert_inter, dense_inter=wl.dense_inter,
-                                   max_tokens=wl.tokens, device=dev)
-    h = torch.from_numpy(h_np.view(np.int16)).to(dev).view(torch.bfloat16)
-    out = torch.empty_like(h)
-    stream = torch.cuda.current_stream(dev)
-    names = B.dg_moe_kernel_names(blk.handle)
-    nk = len(names)
-    if args.neighbours:
-        # the decoder layer's neighbours fused in: h is the layer input, attn
-        # the attention output (N(0, 4)), norm weights U(0.5, 1.5)
-        g = np.random.default_rng(wl.seed + 200)
-        dbf = lambda a: torch.from_numpy(mi.f32_to_bf16_bits(a.astype(np.float32)).view(np.int16)).to(dev).view(torch.bfloat16)
-        attn = dbf(g.standard_normal((wl.tokens, wl.hidden)) * 4.0)
-        w_pa, w_next = dbf(g.uniform(0.5, 1.5, wl.hidden)), dbf(g.uniform(0.5, 1.5, wl.hidden))
-        nxt = torch.empty_like(h)
-
-    def fwd():
-        if args.neighbours:
-            blk.forward_neighbours(h, attn, w_pa, w_next, 1.0, out=out, next_in=nxt)
-        else:
-            blk.forward(h, 1.0, out=out)
-
-    for _ in range(max(args.warmup, 3)):
-        fwd()
-    torch.cuda.synchronize(dev)
-    st = blk.device_status()
-    if st[0] != 0:
-        raise RuntimeError(f"device status after warm-up: {st}")
-
-    # per-kernel events on every `stride`-th step of the timed region
-    stride = max(1, args.steps // 200)
-    ev_sets = {}
-    for i in range(0, args.steps, stride):
-        ev_sets[i] = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    # torch creates the CUDA event at its first record(): record every event
-    # once so the handles given to the library are real
-    for evs in ev_sets.values():
-        for e in evs:
-            e.record(stream)
-
-    clocks = ClockSampler(local)
-    time.sleep(0.3)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    start.record(stream)
-    for i in range(args.steps):
-        evs = ev_sets.get(i)
-        B.dg_moe_set_profile_events(blk.handle, [e.cuda_event for e in evs] if evs else None)
-        fwd()
-    stop.record(stream)
-    torch.cuda.synchronize(dev)
-    B.dg_moe_set_profile_events(blk.handle, None)
-    clk = clocks.stop()
-    elapsed_ms = replicas.max_over_ranks(start.elapsed_time(stop), dist, dev)
-    st = blk.device_status()
-    if st[0] != 0:
-        raise RuntimeError(f"device status after timing: {st}")
-    per_kernel = np.zeros(nk)
-    for evs in ev_sets.values():
-        per_kernel += [evs[j].elapsed_time(evs[j + 1]) for j in range(nk)]
-    per_kernel_us = per_kernel / len(ev_sets) * 1000.0
+    res, blk, fwd = measure_layer(wl, p, h_np, dev, args.steps, args.warmup, local,
+                                  neighbours=args.neighbours, dist=dist)
 
     # end to end through the host-buffer entry point: H2D of h, forward,
     # D2H of the output, stream synchronised every step
@@ -634,56 +712,44 @@ def run_ours(args):
     for _ in range(e2e_steps):
         blk.forward_host(h_host, o_host, 1.0)
     e2e_s = time.perf_counter() - t0
+    blk.close()
 
-    # routing of the timed canvas (for the touched-expert count)
-    _, dbg = blk.forward(h, 1.0, debug=True)
-    counts = np.diff(dbg["offsets"].cpu().numpy())
-    alg = algorithmic(wl, counts)
-    if args.neighbours:
-        alg["layer_bytes"] += 2 * wl.tokens * wl.hidden * 2 + 2 * wl.hidden * 2  # attn in, next_in out
-    hbm, bf16_burst, bf16_sus, src = peaks()
-
-    ms = elapsed_ms / args.steps
+    ms = res["ms_per_step"]
     value = replicas.aggregate_throughput(world, wl.tokens, ms / 1000.0)
-    gu = names.index("gemm_gate_up")
-    gu_s = per_kernel_us[gu] * 1e-6
-    achieved = alg["gate_up_bytes"] / gu_s / 1e9
-    t_roof = max(alg["layer_bytes"] / (hbm * 1e9), alg["layer_flops"] / (bf16_sus * 1e12))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_desc(wl) + (
+        "config": {"workload": res["workload"] + (
                        "; fused with the decoder layer's neighbours (post-attention residual "
                        "norm in, next layer's input norm out)" if args.neighbours else ""),
                    "tokens_per_step": wl.tokens,
                    "us_per_layer": ms * 1000.0, "parallelism": f"replicas x{world}",
                    "weights": "bf16" if not wl.quant else ("NVFP4 experts and dense" if wl.quant[0] == 16 else f"u{wl.quant[0]} g64 affine experts, u{wl.quant[1]} dense") + f", u{wl.quant[2]} router, decoded to bf16 on chip",
-                   "l2": f"no flush: {alg['layer_bytes'] / 1e9:.3f} GB of weights per step, "
-                         f"{alg['layer_bytes'] / 129e6:.1f}x the 129 MB L2",
-                   "touched_experts": alg["touched_experts"]},
-        "roofline": {"bound": "hbm", "kernel": "gemm_gate_up", "achieved": achieved, "peak": hbm,
-                     "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic_for(wl),
-                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else src,
-                     "algorithmic_bytes_per_launch": alg["gate_up_bytes"],
-                     "us_per_launch": per_kernel_us[gu]},
-        "layer_roofline": {"bytes": alg["layer_bytes"], "flops": alg["layer_flops"],
-                           "t_roof_us": t_roof * 1e6, "frac": t_roof / (ms / 1000.0),
-                           "basis": f"max(bytes / {hbm} GB/s, flops / {bf16_sus} TF/s) ({src})"},
-        "kernels_us": {n: round(float(v), 3) for n, v in zip(names, per_kernel_us)},
+                   "l2": f"no flush: {res['layer_roofline']['bytes'] / 1e9:.3f} GB of weights per "
+                         f"step, {res['layer_roofline']['bytes'] / 129e6:.1f}x the 129 MB L2",
+                   "touched_experts": res["touched_experts"],
+                   "timing": "value and ms_per_step from an event-free pass; kernels_us from a "
+                             "separate pass"},
+        "roofline": res["roofline"],
+        "layer_roofline": res["layer_roofline"],
+        "kernels_us": res["kernels_us"],
         "e2e": {"value": world * wl.tokens * e2e_steps / e2e_s, "unit": UNIT,
                 "h2d_bytes_per_step": int(h_host.numel() * 2),
                 "d2h_bytes_per_step": int(o_host.numel() * 2), "steps": e2e_steps,
                 **({"note": "the plain block through the host-buffer entry point"}
                    if args.neighbours else {})},
-        "clocks": clk,
-        # an 8-bit dense branch beside 4-bit experts adds a dense-only launch
-        # to each of the two GEMM slots
-        "gpu_launches": (nk + (2 if wl.quant and wl.quant[1] != wl.quant[0] else 0)) * args.steps,
+        "clocks": res["clocks"],
+        "gpu_launches": res["gpu_launches"],
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, p, h_np)
-    blk.close()
+    # the other configurations, one GPU, in the same process (rank 0 of a
+    # single-GPU run only)
+    if world == 1 and not args.no_extra and args.workload == WORKLOAD and not args.tokens \
+            and not args.neighbours:
+        line["extra_configs"] = {n: extra_config(n, dev, args.steps, args.warmup)
+                                 for n in EXTRA_CONFIGS}
     if dist:
         dist.barrier()
         dist.destroy_process_group()
@@ -698,6 +764,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time the headline configuration only")
     ap.add_argument("--tokens", type=int, default=0,
                     help="token count of a one-layer workload (default: the workload's own)")
     ap.add_argument("--neighbours", action="store_true",

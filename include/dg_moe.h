@@ -235,6 +235,19 @@ dg_status_t dg_moe_kernel_names(const dg_moe_t* m, const char** names, int* n);
  * borrowed (created and destroyed by the caller). */
 dg_status_t dg_moe_set_profile_events(dg_moe_t* m, dg_event_t* events, int n_events);
 
+/* Test of the bounded device waits.  Arms the next forward of this handle
+ * (one forward only): in its gate_up GEMM, block 0's epilogue waits on a
+ * shared-memory barrier that nothing ever arrives on.  After 10 ms the wait
+ * gives up as every wait of the kernels does when its limit runs out: it
+ * records a timeout in the workspace status word (site 3, the GEMM
+ * epilogue; info 0x57A11), the block stops its copy and MMA roles, waits for
+ * the copies and MMAs already in flight and releases its tensor memory; the
+ * other blocks finish normally.  That forward's output is not meaningful.
+ * dg_moe_last_device_status then returns DG_ERR_TIMEOUT (and clears the
+ * word); the handle and the CUDA context stay usable, and the next forward
+ * runs normally.  Nothing faults, traps or hangs. */
+dg_status_t dg_moe_arm_wait_timeout_test(dg_moe_t* m);
+
 /* Text of the last CUDA failure seen by this handle (the call and the CUDA
  * error), "" if none.  Owned by the handle; valid until the next call. */
 const char* dg_moe_last_error(const dg_moe_t* m);

@@ -32,7 +32,7 @@ EXPORTED = (
     "dg_moe_workspace_size", "dg_moe_create", "dg_moe_forward", "dg_moe_forward_host",
     "dg_moe_destroy", "dg_moe_last_device_status", "dg_moe_kernel_names",
     "dg_moe_set_profile_events", "dg_moe_status_string", "dg_moe_last_error",
-    "dg_moe_route_noalloc", "dg_moe_forward_neighbours",
+    "dg_moe_route_noalloc", "dg_moe_forward_neighbours", "dg_moe_arm_wait_timeout_test",
     "dg_sc_mlp_workspace_size", "dg_sc_mlp_create", "dg_sc_mlp_forward",
     "dg_sc_mlp_last_device_status", "dg_sc_mlp_destroy", "dg_sc_mlp_kernel_names",
     "dg_sc_mlp_set_profile_events",
@@ -113,6 +113,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dg_moe_last_device_status.argtypes = [c_void_p, c_void_p, POINTER(c_uint), POINTER(c_uint)]
     lib.dg_moe_kernel_names.argtypes = [c_void_p, POINTER(c_char_p), POINTER(c_int)]
     lib.dg_moe_set_profile_events.argtypes = [c_void_p, POINTER(c_void_p), c_int]
+    lib.dg_moe_arm_wait_timeout_test.argtypes = [c_void_p]
     lib.dg_moe_route_noalloc.argtypes = [POINTER(dg_moe_config_t), POINTER(dg_moe_weights_t),
                                          c_void_p, c_int, c_void_p, c_void_p, c_void_p]
     lib.dg_sc_mlp_workspace_size.argtypes = [POINTER(dg_sc_mlp_config_t), POINTER(c_size_t)]
@@ -229,6 +230,14 @@ def dg_moe_kernel_names(handle: int) -> list:
 def dg_moe_set_profile_events(handle: int, events) -> None:
     """events: list of cudaEvent_t handles (ints), or None to switch off."""
     _set_profile_events(load_library().dg_moe_set_profile_events, handle, events)
+
+
+def dg_moe_arm_wait_timeout_test(handle: int) -> None:
+    """Arm the bounded-wait test for the handle's next forward (see
+    include/dg_moe.h): one device wait runs out after 10 ms and reports
+    DG_ERR_TIMEOUT through dg_moe_last_device_status."""
+    _check(load_library().dg_moe_arm_wait_timeout_test(c_void_p(handle)),
+           "dg_moe_arm_wait_timeout_test")
 
 
 def dg_sc_mlp_kernel_names(handle: int) -> list:

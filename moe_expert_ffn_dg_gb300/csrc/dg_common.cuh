@@ -98,9 +98,9 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 }
 
 // Wait until the phase with the given parity has completed.  Gives up after
-// kWaitLimitNs, or as soon as *abort becomes non-zero; returns false then.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort) {
+// limit_ns, or as soon as *abort becomes non-zero; returns false then.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
@@ -108,9 +108,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          volatile int* abort) {
+  return mbar_wait_for(bar, parity, abort, kWaitLimitNs);
+}
+
+// Limit of the bounded-wait test (GemmParams::test_stall): CTA 0's epilogue
+// waits this long on a barrier nothing arrives on, then reports a timeout
+// and winds the CTA down as any wait that runs out does.
+constexpr unsigned long long kTestStallNs = 10000000ull;  // 10 ms
+constexpr unsigned int kTestStallInfo = 0x57A11u;
 
 // ------------------------------------------------------------------ PDL
 

@@ -52,6 +52,10 @@ template <int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_constant__ GemmParams p) {
   using C = Cfg<BN>;
   constexpr int S = C::kStages;
+  // router logits: one set of kRouterAcc accumulators (the whole TMEM);
+  // the projections: two accumulators, so an epilogue overlaps the next tile
+  constexpr uint32_t kTmemCols = MODE == 2 ? 512u : (uint32_t)C::kTmemCols;
+  static_assert(MODE != 2 || BN * kRouterAcc == 512, "router accumulators fill TMEM");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sA = smem;
@@ -61,7 +65,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
   uint64_t* acc_full = empty + S;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* stall = drain + 1;  // bounded-wait test: never arrived on
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(stall + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* s_start = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full) + 256);  // [E + 1]
   int* s_off = s_start + kMaxGroups + 2;                                            // [E + 1]
@@ -79,6 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
       mbar_init(&acc_empty[a], 4);
     }
     mbar_init(drain, 1);
+    mbar_init(stall, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -95,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
     tma_prefetch_map(&p.xb_d16);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, C::kTmemCols);
+    tmem_alloc(tmem_holder, kTmemCols);
     tmem_relinquish();
   }
   // everything above touches only this CTA's resources; from here on the
@@ -108,17 +114,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
   const uint32_t tmem_base = *tmem_holder;
   const int nd = (p.T + p.bn - 1) / p.bn * p.mt_dense;
   const int ntiles = nd + s_start[p.E];
+  // deal the tiles to only as many CTAs as keep the number of rounds, so that
+  // the last round is full (no lone CTAs streaming one more tile at the end)
+  const int rounds = (ntiles + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int nct = rounds > 0 ? (ntiles + rounds - 1) / rounds : 1;
+  const int first = (int)blockIdx.x < nct ? (int)blockIdx.x : ntiles;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol_w = l2_policy_evict_first();  // weights: read once per forward
-      const uint64_t pol_x = l2_policy_evict_last();   // token rows: reused by feature tiles
+      // weights are read once per forward (evict first) and token rows reused
+      // by the feature tiles (evict last); the router's two weight planes are
+      // read by every token tile and its token rows once: the other way round
+      const uint64_t pol_w = MODE == 2 ? l2_policy_evict_last() : l2_policy_evict_first();
+      const uint64_t pol_x = MODE == 2 ? l2_policy_evict_first() : l2_policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_par = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      for (int tile = first; tile < ntiles && ok; tile += nct) {
         const int4 td = decode_tile(p, tile, nd, s_start, s_off);
         const bool dense = td.x == p.E;
         const int kbn = dense ? p.kb_dense : p.kb_exp;
@@ -153,15 +167,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                                  pol_w);
               }
             }
-          } else {
+          } else if (MODE == 1) {
             const CUtensorMap* ma = dense ? &p.wa_d0 : &p.wa_exp;
             tma_load_2d_hint(ma, &full[stage], a_dst, x, (dense ? 0 : td.x * p.H) + td.y * 128,
                              pol_w);
+          } else {
+            // router: 128 rows of the [E, 2H] planes (hi | lo)
+            tma_load_2d_hint(&p.wa_d0, &full[stage], a_dst, x, td.y * 128, pol_w);
           }
+          // router: the token rows [h | h] along K against the planes (hi | lo)
+          const int xb = MODE == 2 ? x % p.H : x;
           for (int j = 0; j < nb64; ++j)
-            tma_load_2d_hint(mb64, &full[stage], b_dst + j * 64 * 128, x, td.z + 64 * j, pol_x);
+            tma_load_2d_hint(mb64, &full[stage], b_dst + j * 64 * 128, xb, td.z + 64 * j, pol_x);
           for (int j = 0; j < nb16; ++j)
-            tma_load_2d_hint(mb16, &full[stage], b_dst + (64 * nb64 + kBoxRows * j) * 128, x,
+            tma_load_2d_hint(mb16, &full[stage], b_dst + (64 * nb64 + kBoxRows * j) * 128, xb,
                              td.z + 64 * nb64 + kBoxRows * j, pol_x);
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
@@ -184,13 +203,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
       uint32_t phase = 0;
       int local = 0;
       bool ok = true, issued = false;
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++local) {
+      for (int tile = first; tile < ntiles && ok; tile += nct, ++local) {
         const int4 td = decode_tile(p, tile, nd, s_start, s_off);
         const bool dense = td.x == p.E;
         const int nb = (td.w + kBoxRows - 1) / kBoxRows;
         const int kbn = dense ? p.kb_dense : p.kb_exp;
-        const int acc = local & 1;
-        const uint32_t use = (uint32_t)(local >> 1);
+        const int acc = MODE == 2 ? 0 : (local & 1);
+        const uint32_t use = MODE == 2 ? (uint32_t)local : (uint32_t)(local >> 1);
         if (!mbar_wait(&acc_empty[acc], (use & 1u) ^ 1u, abort_flag)) {
           report(p.status, kDevTimeout, kSiteGemmMma, (unsigned)tile, 0xffffffffu);
           *abort_flag = 1;
@@ -209,10 +228,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
           tc_fence_after();
           const uint32_t a0 = smem_u32(sA + (size_t)stage * kATileBytes);
           const uint32_t b0 = smem_u32(sB + (size_t)stage * C::kBTileBytes);
+          // router: K block kb goes to accumulator kb mod kRouterAcc
+          const uint32_t dk = MODE == 2 ? d_tmem + (uint32_t)((kb % kRouterAcc) * BN) : d_tmem;
+          const bool fresh = MODE == 2 ? kb < kRouterAcc : kb == 0;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            umma_bf16(d_tmem, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k),
-                      idesc, (kb | k) != 0 ? 1u : 0u);
+            umma_bf16(dk, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k), idesc,
+                      (!fresh || k != 0) ? 1u : 0u);
           umma_commit(&empty[stage]);
           issued = true;
           if (++stage == S) {
@@ -232,11 +254,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int local = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
+    bool stalled = false;
+    if (p.test_stall && blockIdx.x == 0 && !mbar_wait_for(stall, 0u, abort_flag, kTestStallNs)) {
+      if (lane == 0) report(p.status, kDevTimeout, kSiteGemmEpilogue, kTestStallInfo, 0u);
+      *abort_flag = 1;
+      stalled = true;
+    }
+    for (int tile = first; tile < ntiles && !stalled; tile += nct, ++local) {
       const int4 td = decode_tile(p, tile, nd, s_start, s_off);
       const int nb = (td.w + kBoxRows - 1) / kBoxRows;
-      const int acc = local & 1;
-      const uint32_t use = (uint32_t)(local >> 1);
+      const int acc = MODE == 2 ? 0 : (local & 1);
+      const uint32_t use = MODE == 2 ? (uint32_t)local : (uint32_t)(local >> 1);
       const EpiRows pre = epilogue_rows<MODE>(p, td, lane);  // requested before the wait
       if (!mbar_wait(&acc_full[acc], use & 1u, abort_flag)) {
         if (lane == 0) report(p.status, kDevTimeout, kSiteGemmEpilogue, (unsigned)tile, 0u);
@@ -245,7 +273,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
-      epilogue_tile<MODE>(p, td, tbase, nb * kBoxRows, q, lane, pre);
+      if constexpr (MODE == 2)
+        epilogue_router<BN>(p, td, tbase, nb * kBoxRows, q, lane);
+      else
+        epilogue_tile<MODE>(p, td, tbase, nb * kBoxRows, q, lane, pre);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
@@ -257,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -268,6 +299,7 @@ cudaError_t launch_mode_bn(const GemmParams& p, int grid, cudaStream_t s) {
 
 template <int MODE, int BN>
 cudaError_t allow_smem() {
+  static_assert(MODE != 2 || BN == kRouterBn, "router tiles");
   return cudaFuncSetAttribute(k_grouped_gemm<MODE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)Cfg<BN>::kSmem);
 }
@@ -276,6 +308,7 @@ cudaError_t allow_smem() {
 
 cudaError_t prepare_gemm_bf16() {
   cudaError_t e;
+  if ((e = allow_smem<2, kRouterBn>()) != cudaSuccess) return e;
   if ((e = allow_smem<0, 64>()) != cudaSuccess || (e = allow_smem<0, 128>()) != cudaSuccess ||
       (e = allow_smem<0, 256>()) != cudaSuccess || (e = allow_smem<1, 64>()) != cudaSuccess ||
       (e = allow_smem<1, 128>()) != cudaSuccess || (e = allow_smem<1, 256>()) != cudaSuccess)
@@ -288,6 +321,7 @@ size_t gemm_smem_bytes(int bn) {
 }
 
 cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s) {
+  if (mode == 2) return launch_mode_bn<2, kRouterBn>(p, grid, s);
   if (mode == 0) {
     if (bn == 256) return launch_mode_bn<0, 256>(p, grid, s);
     if (bn == 128) return launch_mode_bn<0, 128>(p, grid, s);

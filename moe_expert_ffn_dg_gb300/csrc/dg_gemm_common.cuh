@@ -238,5 +238,44 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int4 td, uint
   }
 }
 
+// Router logits (mode 2) from the kRouterAcc accumulators of one tile:
+// lane = expert row of the tile (32q + lane), column = token.  The
+// accumulators are summed as an error-free fp32 pair (TwoSum), scaled by
+// r[t] H^-1/2 in double and rounded once, then the bias is added.
+template <int BN>
+__device__ __forceinline__ void epilogue_router(const GemmParams& p, int4 td, uint32_t tbase,
+                                                int ncols, int q, int lane) {
+  const int e = td.y * 128 + 32 * q + lane;
+  const int nacc = p.kb_dense < kRouterAcc ? p.kb_dense : kRouterAcc;
+  const double bias = (p.z_bias && e < p.z_E) ? (double)__ldg(p.z_bias + e) : 0.0;
+  for (int c0 = 0; c0 < ncols; c0 += 16) {
+    float hi[16], lo[16];
+    __syncwarp();
+    tmem_ld16(tbase + (uint32_t)c0, hi);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) lo[j] = 0.f;
+    for (int a = 1; a < nacc; ++a) {
+      float v[16];
+      tmem_ld16(tbase + (uint32_t)(a * BN + c0), v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float s = __fadd_rn(hi[j], v[j]);
+        const float bb = __fsub_rn(s, hi[j]);
+        const float err = __fadd_rn(__fsub_rn(hi[j], __fsub_rn(s, bb)), __fsub_rn(v[j], bb));
+        hi[j] = s;
+        lo[j] = __fadd_rn(lo[j], err);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int t = td.z + c0 + j;
+      if (c0 + j < td.w && e < p.z_E) {
+        const double rc = (double)__ldg(p.z_r + t) * (double)p.z_cH;
+        p.z_out[(size_t)t * p.z_E + e] = (float)(((double)hi[j] + (double)lo[j]) * rc + bias);
+      }
+    }
+  }
+}
+
 }  // namespace gemm
 }  // namespace dg

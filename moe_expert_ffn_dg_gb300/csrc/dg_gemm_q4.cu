@@ -99,8 +99,8 @@ struct CfgQ {
   static constexpr int kBarBytes = 1024;
   static_assert(kNB < kStageRing && kM * kNT < kStageRing, "stage ring too short");
   // mbarriers (qfull, qempty, bfull, afull, sdone, sfull, sempty, acc_full,
-  // acc_empty, drain), then the TMEM address and the abort flag
-  static_assert(8 * (2 * kSQ + kNB + kNA + kStageRing + 9) + 8 <= kBarBytes, "barrier area");
+  // acc_empty, drain, stall), then the TMEM address and the abort flag
+  static_assert(8 * (2 * kSQ + kNB + kNA + kStageRing + 10) + 8 <= kBarBytes, "barrier area");
   static constexpr size_t kFixed = 1024 + (size_t)kSQ * kQSlabBytes +
                                    (size_t)kNB * kBStageBytes + (size_t)kNA * kAStageBytes +
                                    kBarBytes + kTileTableBytes;
@@ -266,7 +266,8 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
   uint64_t* acc_full = sempty + 2;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* stall = drain + 1;  // bounded-wait test: never arrived on
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(stall + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* s_start = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + C::kBarBytes);
   int* s_off = s_start + kMaxGroups + 2;
@@ -291,6 +292,7 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
       mbar_init(&acc_empty[a], 4);
     }
     mbar_init(drain, 1);
+    mbar_init(stall, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -323,6 +325,11 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
   const uint32_t tmem_base = *tmem_holder;
   const int nd = (p.T + p.bn - 1) / p.bn * p.mt_dense;
   const int ntiles = nd + s_start[p.E];
+  // deal the tiles to only as many CTAs as keep the number of rounds, so that
+  // the last round is full (no lone CTAs streaming one more tile at the end)
+  const int rounds = (ntiles + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int nct = rounds > 0 ? (ntiles + rounds - 1) / rounds : 1;
+  const int first = (int)blockIdx.x < nct ? (int)blockIdx.x : ntiles;
 
   if (warp == 0) {
     // ------------------------------------------------- weight codes + scales
@@ -332,7 +339,7 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
       uint32_t qph = 0, qarmed = 0, qarmed_par = 0, sarmed = 0, sarmed_par = 0;
       bool ok = true;
       int local = 0;
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++local) {
+      for (int tile = first; tile < ntiles && ok; tile += nct, ++local) {
         const int4 td = decode_tile(p, tile, nd, s_start, s_off);
         const bool dense = td.x == p.E;
         const int ng = dense ? p.kb_dense : p.kb_exp;  // groups of 64 per row
@@ -443,7 +450,7 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
       int bs = 0;
       uint32_t bph = 0, armed = 0, armed_par = 0, st = 0;  // st: global stage index
       bool ok = true;
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      for (int tile = first; tile < ntiles && ok; tile += nct) {
         const int4 td = decode_tile(p, tile, nd, s_start, s_off);
         const bool dense = td.x == p.E;
         const int ng = dense ? p.kb_dense : p.kb_exp;
@@ -495,7 +502,7 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
     uint32_t st = 0;  // global stage index
     uint64_t cnt = 0;
     bool stop = false, issued = false;
-    for (int tile = blockIdx.x; tile < ntiles && !stop; tile += gridDim.x, ++local) {
+    for (int tile = first; tile < ntiles && !stop; tile += nct, ++local) {
       const int4 td = decode_tile(p, tile, nd, s_start, s_off);
       const bool dense = td.x == p.E;
       const int ng = dense ? p.kb_dense : p.kb_exp;
@@ -547,7 +554,7 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
     uint32_t bph = 0, st = 0;
     uint64_t cnt = 0;
     bool stop = false;
-    for (int tile = blockIdx.x; tile < ntiles && !stop; tile += gridDim.x, ++local) {
+    for (int tile = first; tile < ntiles && !stop; tile += nct, ++local) {
       const int4 td = decode_tile(p, tile, nd, s_start, s_off);
       const bool dense = td.x == p.E;
       const int ng = dense ? p.kb_dense : p.kb_exp;
@@ -601,7 +608,7 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
     int qs = 0, local = 0;
     uint32_t qph = 0, s0 = 0, j = 0;  // stage base of the tile; own stages so far
     bool ok = true;
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++local) {
+    for (int tile = first; tile < ntiles && ok; tile += nct, ++local) {
       const int4 td = decode_tile(p, tile, nd, s_start, s_off);
       const bool dense = td.x == p.E;
       const int ng = dense ? p.kb_dense : p.kb_exp;
@@ -701,7 +708,13 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
     // ------------------------------------------------- epilogue
     const int q = warp & 3;
     int local = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
+    bool stalled = false;
+    if (p.test_stall && blockIdx.x == 0 && !mbar_wait_for(stall, 0u, abort_flag, kTestStallNs)) {
+      if (lane == 0) report(p.status, kDevTimeout, kSiteGemmEpilogue, kTestStallInfo, 0u);
+      *abort_flag = 1;
+      stalled = true;
+    }
+    for (int tile = first; tile < ntiles && !stalled; tile += nct, ++local) {
       const int4 td = decode_tile(p, tile, nd, s_start, s_off);
       const int nb = (td.w + kBoxRows - 1) / kBoxRows;
       const int acc = local & 1;

@@ -42,6 +42,13 @@ struct RouterParams {
   uint16_t* h_out;              // bf16 [T, H]
   float* y_moe;      // [T, H], zeroed here (null: not zeroed)
   int* n_refined;    // counter of tokens whose top-k was re-checked exactly
+  // Tensor-core logits (large batches): the prep kernel writes the router
+  // rows times router_scale as two bf16 planes [E, 2H] (hi | lo, an exact
+  // split for a bf16 router), r, xd, |W'_e| (wnorm) and r H^-1/2 |h_t|
+  // (xnorm); the router GEMM then writes the logits, and the selection
+  // bounds their error with the tensor-core bound.
+  int logits_tc;
+  uint16_t* planes;
 };
 
 struct ScatterParams {
@@ -115,6 +122,17 @@ struct GemmParams {
   const uint16_t* sc_d1;
   const uint16_t* bi_d1;
   int sc_slot_bytes;  // shared-memory bytes of one tile's scale (or bias) rows
+  // Router GEMM (mode 2): logits [T, z_E] f32 = r[t] H^-1/2 (sum over the
+  // eight accumulators) + bias[e]
+  float* z_out;
+  const float* z_r;
+  const float* z_bias;
+  int z_E;
+  float z_cH;
+  // Bounded-wait test: non-zero makes CTA 0's epilogue wait on a barrier
+  // nothing arrives on until kTestStallNs runs out (status kDevTimeout at
+  // kSiteGemmEpilogue, info kTestStallInfo); 0 in every ordinary launch.
+  int test_stall;
 };
 
 struct CombineParams {
@@ -179,7 +197,19 @@ cudaError_t launch_router(const RouterParams& p, cudaStream_t s);
 cudaError_t launch_router_select(const RouterParams& p, cudaStream_t s);
 cudaError_t launch_route_scatter(const ScatterParams& p, cudaStream_t s);
 cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s);
-// mode 0: gate_up + GEGLU, mode 1: down + weighted scatter
+// From this many tokens on, the router logits come from the tensor cores
+// (prep kernel + router GEMM); below, from the CUDA-core kernel.
+constexpr int kRouterTcMinTokens = 1024;
+// Token rows per tile of the router GEMM and its accumulators: K (2H) is
+// dealt to kRouterAcc TMEM accumulators in turn (kRouterAcc x 64 columns),
+// summed error-free in the epilogue, so each accumulator adds only 1/8 of the
+// products.
+constexpr int kRouterBn = 64;
+constexpr int kRouterAcc = 8;
+cudaError_t launch_router_prep_tc(const RouterParams& p, cudaStream_t s);
+
+// mode 0: gate_up + GEGLU, mode 1: down + weighted scatter, mode 2: router
+// logits (bn = kRouterBn)
 cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s);
 size_t gemm_smem_bytes(int bn);
 // Grouped GEMM over quantised weights, dequantised to bf16 in shared memory;

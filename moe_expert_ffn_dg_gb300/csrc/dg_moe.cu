@@ -1,6 +1,7 @@
 // C-ABI implementation of the MoE FFN block: argument validation, workspace
 // layout, TMA descriptors and the launch sequence of one forward.
 #include <cudaTypedefs.h>
+#include <math.h>
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
@@ -25,7 +26,7 @@ const char* const kKernelNames[kNumKernels] = {
 
 struct Layout {
   size_t status, counters, r, xnorm, wnorm, logits, idx, w, chunk_counts, offsets, perm,
-      tok_perm, w_perm, inv, zero16;
+      tok_perm, w_perm, inv, zero16, planes;
   size_t xd, xe_perm, act, act_d, y_moe, y_dense, y_perm, hmid, stage_in, stage_out;
   size_t zero_begin, zero_end;  // counters and chunk counts, cleared per forward
   size_t total;
@@ -60,6 +61,9 @@ Layout make_layout(const dg_moe_config_t& c) {
   L.w_perm = take(TK * 4);
   L.inv = take(TK * 4);
   L.zero16 = take(16);  // expert offsets {0} of a launch with no experts
+  // router rows times router_scale as bf16 planes (hi | lo), for the
+  // tensor-core logits of large batches
+  L.planes = T >= (size_t)kRouterTcMinTokens ? take(E * 2 * H * 2) : 0;
   L.xd = take(T * H * 2);
   L.hmid = take(T * H * 2);  // the block input built by the fused attention half
   L.xe_perm = take(TK * H * 2);
@@ -130,9 +134,11 @@ struct dg_moe {
   int dense_bits;     // dense code format: 4, 8 or kQfNvfp4 (with q4)
   GemmParams gu_d;    // dense-only launches when the dense bits differ (8-bit)
   GemmParams dn_d;
+  GemmParams gr;      // router logits on the tensor cores (large batches)
   size_t smem_optin;  // largest dynamic shared memory a block may opt into
   dg_event_t* prof;
   int n_prof;
+  int stall_armed;  // the next forward runs the bounded-wait test
   char last_error[256];
 };
 
@@ -201,8 +207,10 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
   m->smem_optin = (size_t)optin;
   const dg_moe_config_t& c = m->cfg;
   const bool quantised = c.expert_fmt != DG_FMT_BF16;
-  if (prepare_router(optin) != cudaSuccess ||
-      (quantised ? prepare_gemm_affine(optin) : prepare_gemm_bf16()) != cudaSuccess) {
+  // the bf16 GEMM kernels serve the router logits of large batches in every
+  // weight format
+  if (prepare_router(optin) != cudaSuccess || prepare_gemm_bf16() != cudaSuccess ||
+      (quantised && prepare_gemm_affine(optin) != cudaSuccess)) {
     delete m;
     return DG_ERR_CUDA;
   }
@@ -316,6 +324,29 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
     delete m;
     return DG_ERR_UNSUPPORTED;
   }
+  if (T >= (uint64_t)kRouterTcMinTokens) {
+    // router GEMM: the planes [E, 2H] are the weight side (M = 128 experts a
+    // tile), the token rows of the block input the other; no expert groups
+    GemmParams& g = m->gr;
+    if (!encode_bf16_rows(&g.wa_d0, ws + L.planes, E, 2 * H, 128)) {
+      delete m;
+      return DG_ERR_CUDA;
+    }
+    g.wa_exp = g.wa_d1 = g.wa_d5 = g.wa_d0;
+    g.offsets = reinterpret_cast<const int32_t*>(ws + L.zero16);
+    g.E = 0;
+    g.H = (int)H;
+    g.mt_exp = 0;
+    g.kb_exp = 0;
+    g.mt_dense = (int)((E + 127) / 128);
+    g.kb_dense = (int)(2 * H / 64);
+    g.z_out = reinterpret_cast<float*>(ws + L.logits);
+    g.z_r = reinterpret_cast<const float*>(ws + L.r);
+    g.z_bias = weights->router_bias;
+    g.z_E = (int)E;
+    g.z_cH = (float)(1.0 / sqrt((double)H));
+    g.status = reinterpret_cast<DevStatus*>(ws + L.status);
+  }
   if (q4 && m->dense_bits != m->qf_exp) {
     // the dense branch in launches of its own (no expert tiles), the expert
     // launches without dense tiles
@@ -349,6 +380,12 @@ dg_status_t dg_moe_kernel_names(const dg_moe_t* m, const char** names, int* n) {
   *n = kNumKernels;
   if (names)
     for (int i = 0; i < kNumKernels; ++i) names[i] = kKernelNames[i];
+  return DG_OK;
+}
+
+dg_status_t dg_moe_arm_wait_timeout_test(dg_moe_t* m) {
+  if (!m) return DG_ERR_INVALID_ARG;
+  m->stall_armed = 1;
   return DG_OK;
 }
 
@@ -425,7 +462,25 @@ dg_status_t forward_impl(dg_moe_t* m, const void* h_in, void* h_out, int n_token
     hb = rp.h_out;
   }
   mark(0);
-  if (err == cudaSuccess) err = launch_router(rp, s);
+  if (T >= kRouterTcMinTokens) {
+    // tensor-core logits: prep (r, xd, planes, norms), then the router GEMM
+    // over the block input
+    rp.logits_tc = 1;
+    rp.planes = reinterpret_cast<uint16_t*>(ws + L.planes);
+    if (err == cudaSuccess) err = launch_router_prep_tc(rp, s);
+    GemmParams gr = m->gr;
+    gr.T = T;
+    gr.bn = kRouterBn;
+    if (err == cudaSuccess &&
+        !(encode_bf16_rows(&gr.xb_d64, hb, (uint64_t)T, (uint64_t)H, 64) &&
+          encode_bf16_rows(&gr.xb_d16, hb, (uint64_t)T, (uint64_t)H, 16)))
+      return cuda_fail(m, "router token map", cudaErrorInvalidValue);
+    gr.xb_exp64 = gr.xb_d64;
+    gr.xb_exp16 = gr.xb_d16;
+    if (err == cudaSuccess) err = launch_gemm(2, kRouterBn, gr, m->num_sms, s);
+  } else if (err == cudaSuccess) {
+    err = launch_router(rp, s);
+  }
   rp.h = hb;
   rp.attn = nullptr;
   mark(1);
@@ -457,6 +512,8 @@ dg_status_t forward_impl(dg_moe_t* m, const void* h_in, void* h_out, int n_token
   mark(3);
   if (err == cudaSuccess) err = launch_gather(gp, m->num_sms, s);
   GemmParams gu = m->gu, dn = m->dn;
+  gu.test_stall = m->stall_armed;
+  m->stall_armed = 0;
   gu.T = dn.T = T;
   gu.bn = dn.bn = bn;
   dn.y_perm = partials ? reinterpret_cast<float*>(ws + L.y_perm) : nullptr;

@@ -140,6 +140,128 @@ __device__ __forceinline__ double df_value(float hi, float lo) { return (double)
 constexpr float kLogitBoundNoBias = 3.814697265625e-06f;  // 2^-18
 constexpr float kLogitBoundBias = 1.52587890625e-05f;     // 2^-16
 
+// Error bound of the tensor-core logits (router GEMM), relative to
+// r H^-1/2 |h_t| |W'_e| + |bias_e| with W'_e = W_e * router_scale.  A
+// tensor-core MMA adds 16 exact products of bf16 operands to its fp32
+// accumulator; its rounding is not specified, so each MMA is allowed an
+// error of up to 17 units in the last place of the largest magnitude among
+// its addends and the accumulator (every addend truncated after alignment),
+// which the accumulator's running sum of |terms| bounds.  Each of the
+// kRouterAcc accumulators adds 2H / (16 kRouterAcc) MMAs, so the products
+// carry at most 17 (2H / 128) 2^-23 sum_i |W'_ei h_i| (x 1.3 margin); the
+// two-plane split of W' (exact for a bf16 router, 2^-18 for the decoded
+// 8-bit one) and the final rounding add 2^-17.  The factor r H^-1/2 is
+// common to the token's logits (it cannot change their order); with a bias
+// its error acts per expert and 2^-16 is added, as for the CUDA-core logits.
+__host__ __device__ inline float tc_logit_bound(int H, bool bias) {
+  const int mmas = (2 * H + 16 * kRouterAcc - 1) / (16 * kRouterAcc);
+  return 17.0f * (float)mmas * 1.1920928955078125e-07f * 1.3f + 7.62939453125e-06f +
+         (bias ? kLogitBoundBias : 0.0f);
+}
+
+// Prep of the tensor-core logits.  Warp per token (blocks [0, nbt)): 1/rms
+// (fp32 rsqrt and one Newton step), r H^-1/2 |h_t| (rounded up: a bound),
+// xd = bf16(h / rms(h) * w_pre_ff), the zeroed y_moe row when the down GEMM
+// reduces with atomics, and with the fused attention half the block input
+// built and published.  Warp per expert (the blocks after): W' = W * router_scale
+// in fp32 (exact for bf16 weights: 8 + 8 significant bits; one rounding
+// after the exact 8-bit decode s q + b otherwise), split into the bf16
+// planes hi = bf16(W') and lo = bf16(W' - hi) of row e of [E, 2H], and
+// |W'_e| rounded up.
+template <bool U8, bool FUSED>
+__global__ void __launch_bounds__(256) k_router_prep_tc(const RouterParams p, int nbt) {
+  pdl_trigger();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = p.H, nvec = H >> 3;
+  const float cH = (float)(1.0 / sqrt((double)H));
+  if ((int)blockIdx.x < nbt) {
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= p.T) return;
+    const uint4* hrow = reinterpret_cast<const uint4*>(p.h + (size_t)t * H);
+    const uint4* arow = reinterpret_cast<const uint4*>(FUSED ? p.attn + (size_t)t * H : p.h);
+    const uint4* wav = reinterpret_cast<const uint4*>(p.w_post_attn);
+    const float ra = FUSED ? row_rinv(arow, nvec, H, p.eps, lane) : 0.f;
+    auto hvec = [&](int v) {
+      return FUSED ? attn_residual8(__ldg(hrow + v), __ldg(arow + v), __ldg(wav + v), ra)
+                   : __ldg(hrow + v);
+    };
+    float ss = 0.f;
+    for (int v = lane; v < nvec; v += 32) {
+      float f[8];
+      unpack8(hvec(v), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+    }
+    ss = warp_sum_f(ss);
+    const float msq = ss / (float)H + p.eps;
+    float rf = rsqrtf(msq);
+    rf = rf * (1.5f - 0.5f * msq * rf * rf);
+    uint4* xdrow = reinterpret_cast<uint4*>(p.xd + (size_t)t * H);
+    uint4* hout = reinterpret_cast<uint4*>(FUSED ? p.h_out + (size_t)t * H : p.xd);
+    const uint4* wpv = reinterpret_cast<const uint4*>(p.w_pre_ff);
+    for (int v = lane; v < nvec; v += 32) {
+      float f[8], wp[8];
+      const uint4 hv = hvec(v);
+      if (FUSED) hout[v] = hv;
+      unpack8(hv, f);
+      unpack8(__ldg(wpv + v), wp);
+      uint4 o;
+      o.x = pack2_bf16(f[0] * rf * wp[0], f[1] * rf * wp[1]);
+      o.y = pack2_bf16(f[2] * rf * wp[2], f[3] * rf * wp[3]);
+      o.z = pack2_bf16(f[4] * rf * wp[4], f[5] * rf * wp[5]);
+      o.w = pack2_bf16(f[6] * rf * wp[6], f[7] * rf * wp[7]);
+      xdrow[v] = o;
+    }
+    if (lane == 0) {
+      p.r_out[t] = rf;
+      p.xnorm_out[t] = rf * cH * sqrtf(ss) * 1.001f;  // rounded up: used in a bound
+    }
+    if (p.y_moe) {
+      float4* yr = reinterpret_cast<float4*>(p.y_moe + (size_t)t * H);
+      for (int v = lane; v < (H >> 2); v += 32) yr[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
+  const int e = ((int)blockIdx.x - nbt) * 8 + warp;
+  if (e >= p.E) return;
+  const int ngroups = H >> 6;
+  const uint4* sv = reinterpret_cast<const uint4*>(p.router_scale);
+  uint4* phi = reinterpret_cast<uint4*>(p.planes + (size_t)e * 2 * H);
+  uint4* plo = reinterpret_cast<uint4*>(p.planes + (size_t)e * 2 * H + H);
+  float wsq = 0.f;
+  for (int v = lane; v < nvec; v += 32) {
+    float w[8], sc[8];
+    unpack8(__ldg(sv + v), sc);
+    if constexpr (!U8) {
+      unpack8(__ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.wr) +
+                                                   (size_t)e * H) + v), w);
+    } else {
+      const uint2 q2 = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(p.wr) +
+                                                            (size_t)e * H) + v);
+      const int g = (8 * v) >> 6;
+      const float gs = bf16_to_f32(p.wr_scales[(size_t)e * ngroups + g]);
+      const float gb = bf16_to_f32(p.wr_biases[(size_t)e * ngroups + g]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        w[i] = fmaf(gs, (float)((((i < 4) ? q2.x : q2.y) >> (8 * (i & 3))) & 0xffu), gb);
+    }
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float a = w[2 * i] * sc[2 * i], b = w[2 * i + 1] * sc[2 * i + 1];
+      wsq = fmaf(a, a, fmaf(b, b, wsq));
+      const uint16_t ah = f32_to_bf16_rne(a), bh = f32_to_bf16_rne(b);
+      hw[i] = (uint32_t)ah | ((uint32_t)bh << 16);
+      lw[i] = pack2_bf16(a - bf16_to_f32(ah), b - bf16_to_f32(bh));
+    }
+    phi[v] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    plo[v] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
+  wsq = warp_sum_f(wsq);
+  if (lane == 0) p.wnorm_out[e] = sqrtf(wsq) * 1.001f;  // rounded up: a bound
+}
+
 constexpr int kLogitEPT = 2;                    // experts per thread of k_router_logits
 constexpr int kLogitExperts = 32 * kLogitEPT;  // experts per block of k_router_logits
 constexpr int kLogitSlices = 8;    // K slices per expert (lanes of one warp)
@@ -724,7 +846,8 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
   if (valid) {
     const float* z = p.logits + (size_t)t * E;
     const float xnt = p.xnorm_out[t];
-    const float bound = p.router_bias ? kLogitBoundBias : kLogitBoundNoBias;
+    const float bound = p.logits_tc ? tc_logit_bound(H, p.router_bias != nullptr)
+                                    : (p.router_bias ? kLogitBoundBias : kLogitBoundNoBias);
     float el[kMaxSlots];
 #pragma unroll
     for (int s = 0; s < kMaxSlots; ++s) {
@@ -1120,6 +1243,16 @@ cudaError_t launch_router(const RouterParams& p, cudaStream_t s) {
     return p.router_u8 ? launch_router_tile<true>(p, s) : launch_router_tile<false>(p, s);
   }
   return p.router_u8 ? launch_router_tb<4, true>(p, s) : launch_router_tb<4, false>(p, s);
+}
+
+cudaError_t launch_router_prep_tc(const RouterParams& p, cudaStream_t s) {
+  const int nbt = (p.T + 7) / 8, nbe = (p.E + 7) / 8;
+  const dim3 grid(nbt + nbe);
+  if (p.attn)
+    return p.router_u8 ? launch_pdl(k_router_prep_tc<true, true>, grid, dim3(256), 0, s, p, nbt)
+                       : launch_pdl(k_router_prep_tc<false, true>, grid, dim3(256), 0, s, p, nbt);
+  return p.router_u8 ? launch_pdl(k_router_prep_tc<true, false>, grid, dim3(256), 0, s, p, nbt)
+                     : launch_pdl(k_router_prep_tc<false, false>, grid, dim3(256), 0, s, p, nbt);
 }
 
 cudaError_t launch_router_select(const RouterParams& p, cudaStream_t s) {

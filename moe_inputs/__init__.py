@@ -21,6 +21,8 @@ plan & parity strategy", Reference dossier §1 top-level config):
 * ``batch2048_zipf`` 8 canvases (2048 tokens), bf16, and a per-expert router
                 logit bias beta*ln(p) with p Zipf(1.2) over a seeded expert
                 permutation, so that expert loads are skewed.
+* ``batch2048_zipf_b1`` the same with beta 1 (the literal bias): routing
+                collapses onto about eight experts (stress case).
 * ``stack30_q4``  30 stacked layers, 64 canvases (16384 tokens), 4-bit
                 weights, 8-bit router, layer scalars U(0.5, 1.5).
 
@@ -102,6 +104,11 @@ WORKLOADS = {
     "batch2048_zipf": Workload("batch2048_zipf", 2048, 2816, 128, 8, 704,
                                2112, seed=2, weight_std=0.02, router_std=0.02,
                                zipf_beta=0.02),
+    # the literal reading of the Zipf bias (beta 1): routing collapses onto
+    # a handful of experts; a stress case of the same draws
+    "batch2048_zipf_b1": Workload("batch2048_zipf_b1", 2048, 2816, 128, 8, 704,
+                                  2112, seed=2, weight_std=0.02, router_std=0.02,
+                                  zipf_beta=1.0),
     "stack30_q4": Workload("stack30_q4", 16384, 2816, 128, 8, 704, 2112,
                            seed=4, weight_std=0.02, router_std=0.02,
                            n_layers=30, quant=(4, 4, 8),
@@ -249,9 +256,11 @@ def quantize_nvfp4(w_bits: np.ndarray) -> dict:
     blocks = mats.reshape(mats.shape[0], mats.shape[1], K // 16, 16)
     bamax = np.abs(blocks).max(axis=-1)
     sc = _e4m3_encode(bamax / 6.0 / gf)
-    sv = _e4m3_value(sc)[..., None] * gf[..., None]
-    with np.errstate(divide="ignore", invalid="ignore"):
-        codes = _e2m1_encode(np.where(sv > 0, blocks / np.where(sv > 0, sv, 1.0), 0.0))
+    codes = np.empty(blocks.shape, np.uint8)
+    for m in range(blocks.shape[0]):   # one matrix at a time bounds the memory
+        sv = _e4m3_value(sc[m])[..., None] * gf[m, ..., None]
+        with np.errstate(divide="ignore", invalid="ignore"):
+            codes[m] = _e2m1_encode(np.where(sv > 0, blocks[m] / np.where(sv > 0, sv, 1.0), 0.0))
     codes = codes.reshape(*lead, K)
     packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
     return {"fmt": "nvfp4", "q": packed, "scales": sc.reshape(*lead, K // 16),
