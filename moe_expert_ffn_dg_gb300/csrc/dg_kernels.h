@@ -197,6 +197,10 @@ cudaError_t launch_router(const RouterParams& p, cudaStream_t s);
 cudaError_t launch_router_select(const RouterParams& p, cudaStream_t s);
 cudaError_t launch_route_scatter(const ScatterParams& p, cudaStream_t s);
 cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s);
+// The grouping (offsets, perm, tok_perm, w_perm, inv) and the grouped expert
+// rows in one token-major kernel.
+cudaError_t launch_scatter_gather(const ScatterParams& sp, const GatherParams& gp,
+                                  cudaStream_t s);
 // From this many tokens on, the router logits come from the tensor cores
 // (prep kernel + router GEMM); below, from the CUDA-core kernel.
 constexpr int kRouterTcMinTokens = 1024;

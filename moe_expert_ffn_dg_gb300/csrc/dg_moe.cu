@@ -17,10 +17,9 @@ using namespace dg::host;
 
 namespace {
 
-constexpr int kNumKernels = 7;
+constexpr int kNumKernels = 6;
 const char* const kKernelNames[kNumKernels] = {
-    "router_logits", "router_select", "route_scatter", "gather_xe",
-    "gemm_gate_up", "gemm_down", "combine"};
+    "router_logits", "router_select", "scatter_gather", "gemm_gate_up", "gemm_down", "combine"};
 
 
 
@@ -498,8 +497,6 @@ dg_status_t forward_impl(dg_moe_t* m, const void* h_in, void* h_out, int n_token
   sp.w_perm = reinterpret_cast<float*>(ws + L.w_perm);
   sp.inv = partials ? reinterpret_cast<int32_t*>(ws + L.inv) : nullptr;
   sp.status = status;
-  mark(2);
-  if (err == cudaSuccess) err = launch_route_scatter(sp, s);
 
   GatherParams gp{};
   gp.h = hb;
@@ -509,8 +506,8 @@ dg_status_t forward_impl(dg_moe_t* m, const void* h_in, void* h_out, int n_token
   gp.TK = TK;
   gp.H = H;
   gp.xe_perm = reinterpret_cast<uint16_t*>(ws + L.xe_perm);
-  mark(3);
-  if (err == cudaSuccess) err = launch_gather(gp, m->num_sms, s);
+  mark(2);
+  if (err == cudaSuccess) err = launch_scatter_gather(sp, gp, s);
   GemmParams gu = m->gu, dn = m->dn;
   gu.test_stall = m->stall_armed;
   m->stall_armed = 0;
@@ -524,12 +521,12 @@ dg_status_t forward_impl(dg_moe_t* m, const void* h_in, void* h_out, int n_token
   gu_d.T = dn_d.T = T;
   gu_d.bn = dn_d.bn = bn;
   dn_d.y_perm = dn.y_perm;
-  mark(4);
+  mark(3);
   if (err == cudaSuccess)
     err = m->q4 ? launch_gemm_affine(0, bn, m->qf_exp, gu, m->num_sms, s)
                 : launch_gemm(0, bn, gu, m->num_sms, s);
   if (err == cudaSuccess && split) err = launch_gemm_affine(0, bn, m->dense_bits, gu_d, m->num_sms, s);
-  mark(5);
+  mark(4);
   if (err == cudaSuccess)
     err = m->q4 ? launch_gemm_affine(1, bn, m->qf_exp, dn, m->num_sms, s)
                 : launch_gemm(1, bn, dn, m->num_sms, s);
@@ -555,9 +552,9 @@ dg_status_t forward_impl(dg_moe_t* m, const void* h_in, void* h_out, int n_token
   cp.eps = c.rms_eps;
   cp.layer_scalar = layer_scalar;
   cp.out = static_cast<uint16_t*>(h_out);
-  mark(6);
+  mark(5);
   if (err == cudaSuccess) err = launch_combine(cp, s);
-  mark(7);
+  mark(6);
   if (err != cudaSuccess) return cuda_fail(m, failed[0] ? failed : "launch", err);
 
   if (dbg) {

@@ -293,10 +293,10 @@ __global__ void __launch_bounds__(256) k_router_logits(const RouterParams p) {
   const float cH = (float)(1.0 / sqrt((double)H));
   const int ngroups = H >> 6;
 
-  // thread (expert el, slice j); its first weight step is requested before
-  // the router input is built, so the latency overlaps phase 1
+  // thread (expert el, slice j); its first weight runs are requested before
+  // the dependency wait and the router input is built (the router weights
+  // are constant), so their latency overlaps both
   pdl_trigger();
-  pdl_wait();
   constexpr int EPT = kLogitEPT;
   const int el = threadIdx.x >> 3, j = threadIdx.x & 7;
   int ee[EPT];
@@ -325,10 +325,13 @@ __global__ void __launch_bounds__(256) k_router_logits(const RouterParams p) {
       }
     }
   };
-  // two runs in flight, requested before the router input is built
-  uint4 raw_a[EPT][2], raw_b[EPT][2];
-  load_run(0, raw_a);
-  load_run(16, raw_b);
+  // kRuns runs in flight (a register ring; run c + 16 kRuns is requested as
+  // run c is consumed)
+  constexpr int kRuns = 4;
+  uint4 ring[kRuns][EPT][2];
+#pragma unroll
+  for (int r = 0; r < kRuns; ++r) load_run(16 * r, ring[r]);
+  pdl_wait();
 
   // ---- phase 1: h rows and vectors in one round of loads, router input, xd
   for (int i = threadIdx.x; i < TB * nvec; i += blockDim.x) {
@@ -444,8 +447,9 @@ __global__ void __launch_bounds__(256) k_router_logits(const RouterParams p) {
 #pragma unroll
     for (int q = 0; q < EPT; ++q) {
       if constexpr (!U8) {
-        const uint32_t wd[8] = {raw_a[q][0].x, raw_a[q][0].y, raw_a[q][0].z, raw_a[q][0].w,
-                                raw_a[q][1].x, raw_a[q][1].y, raw_a[q][1].z, raw_a[q][1].w};
+        const uint32_t wd[8] = {ring[0][q][0].x, ring[0][q][0].y, ring[0][q][0].z,
+                                ring[0][q][0].w, ring[0][q][1].x, ring[0][q][1].y,
+                                ring[0][q][1].z, ring[0][q][1].w};
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           w2[q][i] = make_float2(__uint_as_float(wd[i] << 16), __uint_as_float(wd[i] & 0xffff0000u));
@@ -453,7 +457,8 @@ __global__ void __launch_bounds__(256) k_router_logits(const RouterParams p) {
         // a 16-run never straddles a 64-group (16 | k0)
         const float gs = bf16_to_f32(p.wr_scales[(size_t)ee[q] * ngroups + (k0 >> 6)]);
         const float gb = bf16_to_f32(p.wr_biases[(size_t)ee[q] * ngroups + (k0 >> 6)]);
-        const uint32_t wd[4] = {raw_a[q][0].x, raw_a[q][0].y, raw_a[q][0].z, raw_a[q][0].w};
+        const uint32_t wd[4] = {ring[0][q][0].x, ring[0][q][0].y, ring[0][q][0].z,
+                                ring[0][q][0].w};
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           w2[q][i] = make_float2(fmaf(gs, (float)((wd[i >> 1] >> (16 * (i & 1))) & 0xffu), gb),
@@ -465,11 +470,13 @@ __global__ void __launch_bounds__(256) k_router_logits(const RouterParams p) {
       }
     }
 #pragma unroll
-    for (int q = 0; q < EPT; ++q) {
-      raw_a[q][0] = raw_b[q][0];
-      raw_a[q][1] = raw_b[q][1];
-    }
-    load_run(c + 32, raw_b);
+    for (int r = 0; r + 1 < kRuns; ++r)
+#pragma unroll
+      for (int q = 0; q < EPT; ++q) {
+        ring[r][q][0] = ring[r + 1][q][0];
+        ring[r][q][1] = ring[r + 1][q][1];
+      }
+    load_run(c + 16 * kRuns, ring[kRuns - 1]);
 #pragma unroll
     for (int t = 0; t < TB; ++t) {
       const float4* xv =
@@ -1164,6 +1171,98 @@ __global__ void __launch_bounds__(256, 1) k_route_scatter(const ScatterParams p)
   }
 }
 
+// Grouping and expert rows in one pass, token-major.  A block of 256 threads
+// takes TPB consecutive tokens (one 256-token chunk holds them all) with
+// 8 / TPB warps per token.  It rebuilds from the per-chunk histograms what
+// it needs: the expert offsets (exclusive scan of the totals; block 0
+// publishes them), per expert the assignments in earlier chunks, and the
+// chunk's per-expert token bit masks.  The stable position of assignment
+// (t, j) with expert e is then offset[e] + earlier chunks' count + the
+// chunk's tokens before t that chose e (assignments sorted by expert, then
+// token).  Each token's row of h is read once; xe = bf16(h / rms(h) *
+// w_pre_ff2) is formed once and stored at its K grouped rows.
+template <int TPB>
+__global__ void __launch_bounds__(256) k_scatter_gather(const ScatterParams sp,
+                                                        const GatherParams gp) {
+  __shared__ unsigned s_mask[256][kChunkTokens / 32];  // [expert][token word]
+  __shared__ int s_tmp[256];
+  __shared__ int s_base[256];
+  __shared__ int s_pos[TPB][16];
+  pdl_trigger();
+  pdl_wait();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = sp.E, K = sp.K, T = sp.T;
+  const int t0 = blockIdx.x * TPB;
+  const int chunk = t0 / kChunkTokens, c0 = chunk * kChunkTokens;
+  const int nchunks = (T + kChunkTokens - 1) / kChunkTokens;
+  for (int i = tid; i < 256 * (kChunkTokens / 32); i += 256) (&s_mask[0][0])[i] = 0u;
+  int tot = 0, bef = 0;
+  if (tid < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      const int v = sp.chunk_counts[(size_t)c * E + tid];
+      tot += v;
+      if (c < chunk) bef += v;
+    }
+  }
+  int total;
+  const int base = block_excl_scan256(tot, s_tmp, &total);  // synchronises: masks are clear
+  s_base[tid] = base + bef;
+  if (blockIdx.x == 0) {
+    if (tid < E) sp.offsets[tid] = base;
+    if (tid == 0) sp.offsets[E] = total;
+  }
+  const int nc = min(kChunkTokens, T - c0);
+  for (int i = tid; i < nc * K; i += 256) {
+    const int tl = i / K;
+    const int e = sp.idx[(size_t)(c0 + tl) * K + (i - tl * K)];
+    if ((unsigned)e < (unsigned)E) atomicOr(&s_mask[e][tl >> 5], 1u << (tl & 31));
+    else report(sp.status, kDevBounds, kSiteScatter, (unsigned)(c0 + tl), (unsigned)e);
+  }
+  __syncthreads();
+  if (tid < TPB * K) {
+    const int tt = tid / K, j = tid - tt * K, t = t0 + tt;
+    if (t < T) {
+      const int e = sp.idx[(size_t)t * K + j];
+      int pos = 0;
+      if ((unsigned)e < (unsigned)E) {
+        const int tl = t - c0;
+        int rank = __popc(s_mask[e][tl >> 5] & ((1u << (tl & 31)) - 1u));
+        for (int w = 0; w < (tl >> 5); ++w) rank += __popc(s_mask[e][w]);
+        pos = s_base[e] + rank;
+        sp.perm[pos] = t * K + j;
+        sp.tok_perm[pos] = t;
+        sp.w_perm[pos] = sp.w[(size_t)t * K + j];
+        if (sp.inv) sp.inv[t * K + j] = pos;
+      }
+      s_pos[tt][j] = pos;  // an out-of-range expert was reported; its row is not read
+    }
+  }
+  __syncthreads();
+  constexpr int WPT = 8 / TPB;  // warps per token
+  const int tt = warp / WPT, part = warp - tt * WPT, t = t0 + tt;
+  if (t >= T) return;
+  const int nvec = gp.H >> 3;
+  const float r = gp.r[t];
+  const uint4* hrow = reinterpret_cast<const uint4*>(gp.h + (size_t)t * gp.H);
+  const uint4* wv = reinterpret_cast<const uint4*>(gp.w_pre_ff2);
+  int pos[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) pos[j] = j < K ? s_pos[tt][j] : 0;
+  for (int v = part * 32 + lane; v < nvec; v += 32 * WPT) {
+    float f[8], w[8];
+    unpack8(__ldg(hrow + v), f);
+    unpack8(__ldg(wv + v), w);
+    uint4 o;
+    o.x = pack2_bf16(f[0] * r * w[0], f[1] * r * w[1]);
+    o.y = pack2_bf16(f[2] * r * w[2], f[3] * r * w[3]);
+    o.z = pack2_bf16(f[4] * r * w[4], f[5] * r * w[5]);
+    o.w = pack2_bf16(f[6] * r * w[6], f[7] * r * w[7]);
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < K) reinterpret_cast<uint4*>(gp.xe_perm + (size_t)pos[j] * gp.H)[v] = o;
+  }
+}
+
 // Warp per grouped row; loads of four vectors per round.
 __global__ void __launch_bounds__(256) k_gather_xe(const GatherParams p) {
   pdl_trigger();
@@ -1264,6 +1363,15 @@ cudaError_t launch_router_select(const RouterParams& p, cudaStream_t s) {
 cudaError_t launch_route_scatter(const ScatterParams& p, cudaStream_t s) {
   const int grid = (p.T + kChunkTokens - 1) / kChunkTokens;
   return launch_pdl(k_route_scatter, dim3(grid), dim3(256), 0, s, p);
+}
+
+cudaError_t launch_scatter_gather(const ScatterParams& sp, const GatherParams& gp,
+                                  cudaStream_t s) {
+  // small batches: two tokens a block (four warps each) for enough blocks;
+  // large ones: eight (a warp each), so the per-block rebuild is shared
+  if (sp.T < kRouterTcMinTokens)
+    return launch_pdl(k_scatter_gather<2>, dim3((sp.T + 1) / 2), dim3(256), 0, s, sp, gp);
+  return launch_pdl(k_scatter_gather<8>, dim3((sp.T + 7) / 8), dim3(256), 0, s, sp, gp);
 }
 
 cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s) {
