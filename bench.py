@@ -537,14 +537,15 @@ def kernel_split(blk, fwd, stream, dev, steps, set_events, names):
     return per_kernel / len(ev_sets) * 1000.0
 
 
-ROUTER_TC_MIN_TOKENS = 1024  # the library's tensor-core router threshold
+ROUTER_TC_MIN_TOKENS = 1024  # the library's two-pass selection threshold
 
 
 def launches_per_forward(wl, nk):
     # an 8-bit dense branch beside 4-bit experts adds a dense-only launch to
-    # each of the two GEMM slots; from 1024 tokens the router slot holds two
-    # launches (prep and the router GEMM)
-    return (nk + (2 if wl.quant and wl.quant[1] != wl.quant[0] else 0)
+    # each of the two GEMM slots; the router slot holds two launches (prep and
+    # the router GEMM), and from 1024 tokens so does the selection slot (fast
+    # pass and re-check pass)
+    return (nk + (2 if wl.quant and wl.quant[1] != wl.quant[0] else 0) + 1
             + (1 if wl.tokens >= ROUTER_TC_MIN_TOKENS else 0))
 
 

@@ -36,7 +36,11 @@ namespace {
 
 using namespace gemm;
 
+// Warps 0 producer, 1 MMA issuer, 2-5 epilogue; the router mode adds warp 6,
+// which waits on the stage barriers for the issuer (see the waiter below).
 constexpr int kThreads = 192;
+template <int MODE>
+constexpr int threads_of() { return MODE == 2 ? kThreads + 32 : kThreads; }
 constexpr int kATileBytes = 128 * 128;  // 128 rows x 64 bf16
 
 template <int BN>
@@ -49,7 +53,8 @@ struct Cfg {
 };
 
 template <int MODE, int BN>
-__global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(threads_of<MODE>(), 1)
+    k_grouped_gemm(const __grid_constant__ GemmParams p) {
   using C = Cfg<BN>;
   constexpr int S = C::kStages;
   // router logits: one set of kRouterAcc accumulators (the whole TMEM);
@@ -107,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
   // everything above touches only this CTA's resources; from here on the
   // kernel reads what earlier kernels wrote
   pdl_wait();
-  if (warp >= 2) build_tile_table(p, threadIdx.x - 64, s_start, s_off);
+  if (warp >= 2 && warp < 6) build_tile_table(p, threadIdx.x - 64, s_start, s_off);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -136,12 +141,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
         const int4 td = decode_tile(p, tile, nd, s_start, s_off);
         const bool dense = td.x == p.E;
         const int kbn = dense ? p.kb_dense : p.kb_exp;
+        // router: this tile's K range (split-K) and expert tile
+        const int2 kr = MODE == 2 ? router_krange(p, td.y, kbn) : make_int2(0, kbn);
         const int nb64 = td.w / 64;
         const int nb16 = (td.w - 64 * nb64 + kBoxRows - 1) / kBoxRows;
         const uint32_t bytes = kATileBytes + nb64 * 64 * 128 + nb16 * kBoxBytes;
         const CUtensorMap* mb64 = dense ? &p.xb_d64 : &p.xb_exp64;
         const CUtensorMap* mb16 = dense ? &p.xb_d16 : &p.xb_exp16;
-        for (int kb = 0; kb < kbn; ++kb) {
+        for (int kb = kr.x; kb < kr.y; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             report(p.status, kDevTimeout, kSiteGemmProducer, (unsigned)tile, (unsigned)kb);
             *abort_flag = 1;
@@ -173,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
                              pol_w);
           } else {
             // router: 128 rows of the [E, 2H] planes (hi | lo)
-            tma_load_2d_hint(&p.wa_d0, &full[stage], a_dst, x, td.y * 128, pol_w);
+            tma_load_2d_hint(&p.wa_d0, &full[stage], a_dst, x, router_etile(p, td.y) * 128, pol_w);
           }
           // router: the token rows [h | h] along K against the planes (hi | lo)
           const int xb = MODE == 2 ? x % p.H : x;
@@ -196,6 +203,83 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
           if (!wait_no_abort(&full[s], (armed_par >> s) & 1u))
             report(p.status, kDevTimeout, kSiteGemmDrain, (unsigned)s, 0u);
     }
+  } else if (MODE == 2 && warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    // (router) The router GEMM is bound by MMA issue, not by memory: its
+    // issuer learns that a stage is ready only through handoff() with the
+    // waiter warp, as a shared-memory poll by a thread with MMAs in flight
+    // waits for them to complete.
+    int stage = 0;
+    bool stop = false, issued = false;
+    for (int tile = first; tile < ntiles && !stop; tile += nct) {
+      const int4 td = decode_tile(p, tile, nd, s_start, s_off);
+      const int nb = (td.w + kBoxRows - 1) / kBoxRows;
+      const int2 kr = router_krange(p, td.y, p.kb_dense);
+      const uint32_t idesc = idesc_bf16_f32(128, nb * kBoxRows);
+      for (int kb = kr.x; kb < kr.y; ++kb) {
+        if (handoff(false)) {
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a0 = smem_u32(sA + (size_t)stage * kATileBytes);
+          const uint32_t b0 = smem_u32(sB + (size_t)stage * C::kBTileBytes);
+          const uint32_t dk = tmem_base + (uint32_t)(((kb - kr.x) % kRouterAcc) * BN);
+          const bool fresh = kb - kr.x < kRouterAcc;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_bf16(dk, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k), idesc,
+                      (!fresh || k != 0) ? 1u : 0u);
+          umma_commit(&empty[stage]);
+          if (kb == kr.y - 1) umma_commit(&acc_full[0]);
+        }
+        issued = true;
+        if (++stage == S) stage = 0;
+        __syncwarp();
+      }
+    }
+    if (lane == 0 && issued) {
+      umma_commit(drain);
+      if (!wait_no_abort(drain, 0u)) report(p.status, kDevTimeout, kSiteGemmDrain, 99u, 0u);
+    }
+  } else if (MODE == 2 && warp == 6) {
+    // ------------------------------------------------------------ waiter
+    // (router) the bounded waits of the issuer: the accumulators free before
+    // a tile's first stage, each stage's operands landed; "stop" (a wait
+    // that ran out) travels in the reduced predicate, so both warps leave
+    // on the same round
+    int stage = 0, local = 0;
+    uint32_t phase = 0;
+    bool stop = false;
+    for (int tile = first; tile < ntiles && !stop; tile += nct, ++local) {
+      const int4 td = decode_tile(p, tile, nd, s_start, s_off);
+      const int2 kr = router_krange(p, td.y, p.kb_dense);
+      for (int kb = kr.x; kb < kr.y; ++kb) {
+        bool ok = true;
+        unsigned what = 0;
+        if (kb == kr.x && !mbar_wait(&acc_empty[0], ((uint32_t)local & 1u) ^ 1u, abort_flag)) {
+          ok = false;
+          what = 0xffffffffu;
+        }
+        if (ok && !mbar_wait(&full[stage], phase, abort_flag)) {
+          ok = false;
+          what = (unsigned)kb;
+        }
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (!ok) {
+          if (lane == 0) report(p.status, kDevTimeout, kSiteGemmMma, (unsigned)tile, what);
+          *abort_flag = 1;
+        }
+        if (handoff(!ok)) {
+          stop = true;
+          break;
+        }
+      }
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -208,6 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
         const bool dense = td.x == p.E;
         const int nb = (td.w + kBoxRows - 1) / kBoxRows;
         const int kbn = dense ? p.kb_dense : p.kb_exp;
+        // router: this tile's K range (split-K) and expert tile
+        const int2 kr = MODE == 2 ? router_krange(p, td.y, kbn) : make_int2(0, kbn);
         const int acc = MODE == 2 ? 0 : (local & 1);
         const uint32_t use = MODE == 2 ? (uint32_t)local : (uint32_t)(local >> 1);
         if (!mbar_wait(&acc_empty[acc], (use & 1u) ^ 1u, abort_flag)) {
@@ -218,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         const uint32_t idesc = idesc_bf16_f32(128, nb * kBoxRows);
-        for (int kb = 0; kb < kbn; ++kb) {
+        for (int kb = kr.x; kb < kr.y; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag)) {
             report(p.status, kDevTimeout, kSiteGemmMma, (unsigned)tile, (unsigned)kb);
             *abort_flag = 1;
@@ -229,8 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
           const uint32_t a0 = smem_u32(sA + (size_t)stage * kATileBytes);
           const uint32_t b0 = smem_u32(sB + (size_t)stage * C::kBTileBytes);
           // router: K block kb goes to accumulator kb mod kRouterAcc
-          const uint32_t dk = MODE == 2 ? d_tmem + (uint32_t)((kb % kRouterAcc) * BN) : d_tmem;
-          const bool fresh = MODE == 2 ? kb < kRouterAcc : kb == 0;
+          const uint32_t dk =
+              MODE == 2 ? d_tmem + (uint32_t)(((kb - kr.x) % kRouterAcc) * BN) : d_tmem;
+          const bool fresh = MODE == 2 ? kb - kr.x < kRouterAcc : kb == 0;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             umma_bf16(dk, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k), idesc,
@@ -250,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
         if (!wait_no_abort(drain, 0u)) report(p.status, kDevTimeout, kSiteGemmDrain, 99u, 0u);
       }
     }
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int local = 0;
@@ -294,7 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_grouped_gemm(const __grid_const
 
 template <int MODE, int BN>
 cudaError_t launch_mode_bn(const GemmParams& p, int grid, cudaStream_t s) {
-  return launch_pdl(k_grouped_gemm<MODE, BN>, dim3(grid), dim3(kThreads), Cfg<BN>::kSmem, s, p);
+  return launch_pdl(k_grouped_gemm<MODE, BN>, dim3(grid), dim3(threads_of<MODE>()), Cfg<BN>::kSmem,
+                    s, p);
 }
 
 template <int MODE, int BN>

@@ -92,6 +92,22 @@ __device__ __forceinline__ void tma_load_5d(const CUtensorMap* map, uint64_t* ba
       : "memory");
 }
 
+// Named barrier 1 between an MMA issuer warp and its waiter warp (64
+// threads, both block), OR-reducing one predicate: returns true if either
+// side passed true.
+constexpr int kHandoffBarrier = 1;
+__device__ __forceinline__ bool handoff(bool stop) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "barrier.cta.red.or.pred p, %2, 64, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)stop), "n"(kHandoffBarrier)
+      : "memory");
+  return r != 0;
+}
 // Wait that ignores the abort flag (used to drain in-flight copies and MMAs
 // before the CTA exits); bounded by kWaitLimitNs.
 __device__ __forceinline__ bool wait_no_abort(uint64_t* bar, uint32_t parity) {
@@ -238,15 +254,32 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, int4 td, uint
   }
 }
 
+// Router GEMM tiles: feature tile y = expert tile * z_split + K range.
+__device__ __forceinline__ int router_etile(const GemmParams& p, int y) {
+  return p.z_split > 1 ? y / p.z_split : y;
+}
+// K blocks [x, y) of the range of feature tile y (ranges of equal length,
+// the last one shorter).
+__device__ __forceinline__ int2 router_krange(const GemmParams& p, int y, int kbn) {
+  if (p.z_split <= 1) return make_int2(0, kbn);
+  const int r = y % p.z_split, len = (kbn + p.z_split - 1) / p.z_split;
+  const int lo = r * len < kbn ? r * len : kbn;
+  return make_int2(lo, lo + len < kbn ? lo + len : kbn);
+}
+
 // Router logits (mode 2) from the kRouterAcc accumulators of one tile:
 // lane = expert row of the tile (32q + lane), column = token.  The
 // accumulators are summed as an error-free fp32 pair (TwoSum), scaled by
 // r[t] H^-1/2 in double and rounded once, then the bias is added.
+// With a K split the pair's sum is rounded once to fp32 and stored unscaled
+// as the range's partial.
 template <int BN>
 __device__ __forceinline__ void epilogue_router(const GemmParams& p, int4 td, uint32_t tbase,
                                                 int ncols, int q, int lane) {
-  const int e = td.y * 128 + 32 * q + lane;
-  const int nacc = p.kb_dense < kRouterAcc ? p.kb_dense : kRouterAcc;
+  const int e = router_etile(p, td.y) * 128 + 32 * q + lane;
+  const int2 kr = router_krange(p, td.y, p.kb_dense);
+  const int nacc = kr.y - kr.x < kRouterAcc ? kr.y - kr.x : kRouterAcc;
+  float* part = p.z_split > 1 ? p.z_part + (size_t)(td.y % p.z_split) * p.T * p.z_E : nullptr;
   const double bias = (p.z_bias && e < p.z_E) ? (double)__ldg(p.z_bias + e) : 0.0;
   for (int c0 = 0; c0 < ncols; c0 += 16) {
     float hi[16], lo[16];
@@ -270,8 +303,12 @@ __device__ __forceinline__ void epilogue_router(const GemmParams& p, int4 td, ui
     for (int j = 0; j < 16; ++j) {
       const int t = td.z + c0 + j;
       if (c0 + j < td.w && e < p.z_E) {
-        const double rc = (double)__ldg(p.z_r + t) * (double)p.z_cH;
-        p.z_out[(size_t)t * p.z_E + e] = (float)(((double)hi[j] + (double)lo[j]) * rc + bias);
+        if (part) {
+          part[(size_t)t * p.z_E + e] = (float)((double)hi[j] + (double)lo[j]);
+        } else {
+          const double rc = (double)__ldg(p.z_r + t) * (double)p.z_cH;
+          p.z_out[(size_t)t * p.z_E + e] = (float)(((double)hi[j] + (double)lo[j]) * rc + bias);
+        }
       }
     }
   }

@@ -122,22 +122,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
-// Named barrier 1 between the MMA issuer warp and its waiter warp (64
-// threads, both block), OR-reducing one predicate: returns true if either
-// side passed true.
-constexpr int kHandoffBarrier = 1;
-__device__ __forceinline__ bool handoff(bool stop) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 q, %1, 0;\n\t"
-      "barrier.cta.red.or.pred p, %2, 64, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(r)
-      : "r"((uint32_t)stop), "n"(kHandoffBarrier)
-      : "memory");
-  return r != 0;
-}
 // Store 16 bytes at a shared-memory address.
 __device__ __forceinline__ void sts_u32x4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                           uint32_t d) {

@@ -49,6 +49,17 @@ struct RouterParams {
   // bounds their error with the tensor-core bound.
   int logits_tc;
   uint16_t* planes;
+  // Two-pass selection (large batches): the fast pass writes the outputs of
+  // the tokens whose top-k is certain and lists the others (flagged [T],
+  // count *n_flagged, zeroed); the re-check pass finishes those.  Null: one
+  // pass does both.
+  int32_t* flagged;
+  int* n_flagged;
+  // Split-K router GEMM (z_split > 1): the logits come as z_split fp32
+  // partial sums [z_split, T, E] of sum_i W'_ei h_i, which the selection adds
+  // (error-free) and scales by r H^-1/2 itself, writing the logits.
+  const float* z_part;
+  int z_split;
 };
 
 struct ScatterParams {
@@ -123,8 +134,12 @@ struct GemmParams {
   const uint16_t* bi_d1;
   int sc_slot_bytes;  // shared-memory bytes of one tile's scale (or bias) rows
   // Router GEMM (mode 2): logits [T, z_E] f32 = r[t] H^-1/2 (sum over the
-  // eight accumulators) + bias[e]
+  // eight accumulators) + bias[e]; with z_split > 1 the K blocks are split in
+  // z_split ranges over as many CTAs (feature tile = expert tile * z_split +
+  // range) and each writes its unscaled fp32 partial to z_part[range, T, E].
   float* z_out;
+  float* z_part;
+  int z_split;
   const float* z_r;
   const float* z_bias;
   int z_E;
@@ -194,15 +209,17 @@ cudaError_t prepare_gemm_bf16();
 cudaError_t prepare_gemm_affine(int smem_max);
 
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s);
-cudaError_t launch_router_select(const RouterParams& p, cudaStream_t s);
+cudaError_t launch_router_select(const RouterParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_route_scatter(const ScatterParams& p, cudaStream_t s);
 cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s);
 // The grouping (offsets, perm, tok_perm, w_perm, inv) and the grouped expert
 // rows in one token-major kernel.
 cudaError_t launch_scatter_gather(const ScatterParams& sp, const GatherParams& gp,
                                   cudaStream_t s);
-// From this many tokens on, the router logits come from the tensor cores
-// (prep kernel + router GEMM); below, from the CUDA-core kernel.
+// The block's router logits come from the tensor cores (prep kernel + router
+// GEMM); the CUDA-core logit kernels serve the allocation-free routing entry
+// point.  From this many tokens on, the selection runs in two passes (a fast
+// one, then the re-check of the tokens near a tie).
 constexpr int kRouterTcMinTokens = 1024;
 // Token rows per tile of the router GEMM and its accumulators: K (2H) is
 // dealt to kRouterAcc TMEM accumulators in turn (kRouterAcc x 64 columns),
@@ -211,6 +228,20 @@ constexpr int kRouterTcMinTokens = 1024;
 constexpr int kRouterBn = 64;
 constexpr int kRouterAcc = 8;
 cudaError_t launch_router_prep_tc(const RouterParams& p, cudaStream_t s);
+
+// K ranges of the router GEMM for T tokens: enough CTAs for about one wave
+// (kRouterCtaTarget) while each range keeps at least one K block per
+// accumulator; kb = 2H / 64 K blocks, E experts.
+constexpr int kRouterCtaTarget = 160;
+inline int router_split(int T, int E, int kb) {
+  const int tiles = ((T + kRouterBn - 1) / kRouterBn) * ((E + 127) / 128);
+  int s = (kRouterCtaTarget + tiles - 1) / tiles;
+  const int smax = kb / kRouterAcc > 1 ? kb / kRouterAcc : 1;
+  s = s < 1 ? 1 : (s > smax ? smax : s);
+  // ranges of ceil(kb / s) blocks: none may be left empty
+  while (s > 1 && (s - 1) * ((kb + s - 1) / s) >= kb) --s;
+  return s;
+}
 
 // mode 0: gate_up + GEGLU, mode 1: down + weighted scatter, mode 2: router
 // logits (bn = kRouterBn)

@@ -25,7 +25,7 @@ const char* const kKernelNames[kNumKernels] = {
 
 struct Layout {
   size_t status, counters, r, xnorm, wnorm, logits, idx, w, chunk_counts, offsets, perm,
-      tok_perm, w_perm, inv, zero16, planes;
+      tok_perm, w_perm, inv, zero16, planes, flagged, zpart;
   size_t xd, xe_perm, act, act_d, y_moe, y_dense, y_perm, hmid, stage_in, stage_out;
   size_t zero_begin, zero_end;  // counters and chunk counts, cleared per forward
   size_t total;
@@ -44,7 +44,7 @@ Layout make_layout(const dg_moe_config_t& c) {
     return o;
   };
   L.status = take(sizeof(DevStatus));
-  L.counters = take(16 * sizeof(int));  // [0] n_refined
+  L.counters = take(16 * sizeof(int));  // [0] n_refined, [1] flagged tokens
   L.chunk_counts = take(nchunks * E * 4);
   L.zero_begin = L.counters;
   L.zero_end = L.chunk_counts + nchunks * E * 4;
@@ -61,8 +61,22 @@ Layout make_layout(const dg_moe_config_t& c) {
   L.inv = take(TK * 4);
   L.zero16 = take(16);  // expert offsets {0} of a launch with no experts
   // router rows times router_scale as bf16 planes (hi | lo), for the
-  // tensor-core logits of large batches
-  L.planes = T >= (size_t)kRouterTcMinTokens ? take(E * 2 * H * 2) : 0;
+  // tensor-core logits
+  L.planes = take(E * 2 * H * 2);
+  // split-K partial logits: the largest split times tokens over the batch
+  // sizes the handle accepts (beyond one wave of token tiles there is no split)
+  {
+    const int kb = (int)(2 * H / 64);
+    size_t most = 0;
+    for (size_t n = 1; n <= (T + kRouterBn - 1) / kRouterBn && n <= (size_t)kRouterCtaTarget; ++n) {
+      const size_t t = n * kRouterBn < T ? n * kRouterBn : T;
+      const size_t sp = (size_t)router_split((int)t, (int)E, kb);
+      if (sp > 1 && sp * t > most) most = sp * t;
+    }
+    L.zpart = take(most * E * 4);
+  }
+  // tokens left to the re-check pass of the two-pass selection
+  L.flagged = T >= (size_t)kRouterTcMinTokens ? take(T * 4) : 0;
   L.xd = take(T * H * 2);
   L.hmid = take(T * H * 2);  // the block input built by the fused attention half
   L.xe_perm = take(TK * H * 2);
@@ -323,7 +337,7 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
     delete m;
     return DG_ERR_UNSUPPORTED;
   }
-  if (T >= (uint64_t)kRouterTcMinTokens) {
+  {
     // router GEMM: the planes [E, 2H] are the weight side (M = 128 experts a
     // tile), the token rows of the block input the other; no expert groups
     GemmParams& g = m->gr;
@@ -340,6 +354,7 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
     g.mt_dense = (int)((E + 127) / 128);
     g.kb_dense = (int)(2 * H / 64);
     g.z_out = reinterpret_cast<float*>(ws + L.logits);
+    g.z_part = reinterpret_cast<float*>(ws + L.zpart);
     g.z_r = reinterpret_cast<const float*>(ws + L.r);
     g.z_bias = weights->router_bias;
     g.z_E = (int)E;
@@ -461,15 +476,26 @@ dg_status_t forward_impl(dg_moe_t* m, const void* h_in, void* h_out, int n_token
     hb = rp.h_out;
   }
   mark(0);
-  if (T >= kRouterTcMinTokens) {
+  {
     // tensor-core logits: prep (r, xd, planes, norms), then the router GEMM
-    // over the block input
+    // over the block input (split over K ranges while the token tiles alone
+    // would leave most SMs idle)
+    const int split = router_split(T, E, 2 * H / 64);
     rp.logits_tc = 1;
     rp.planes = reinterpret_cast<uint16_t*>(ws + L.planes);
+    rp.z_split = split;
+    rp.z_part = reinterpret_cast<const float*>(ws + L.zpart);
+    if (T >= kRouterTcMinTokens) {
+      // two-pass selection
+      rp.flagged = reinterpret_cast<int32_t*>(ws + L.flagged);
+      rp.n_flagged = counters + 1;
+    }
     if (err == cudaSuccess) err = launch_router_prep_tc(rp, s);
     GemmParams gr = m->gr;
     gr.T = T;
     gr.bn = kRouterBn;
+    gr.z_split = split;
+    gr.mt_dense *= split;
     if (err == cudaSuccess &&
         !(encode_bf16_rows(&gr.xb_d64, hb, (uint64_t)T, (uint64_t)H, 64) &&
           encode_bf16_rows(&gr.xb_d16, hb, (uint64_t)T, (uint64_t)H, 16)))
@@ -477,13 +503,11 @@ dg_status_t forward_impl(dg_moe_t* m, const void* h_in, void* h_out, int n_token
     gr.xb_exp64 = gr.xb_d64;
     gr.xb_exp16 = gr.xb_d16;
     if (err == cudaSuccess) err = launch_gemm(2, kRouterBn, gr, m->num_sms, s);
-  } else if (err == cudaSuccess) {
-    err = launch_router(rp, s);
   }
   rp.h = hb;
   rp.attn = nullptr;
   mark(1);
-  if (err == cudaSuccess) err = launch_router_select(rp, s);
+  if (err == cudaSuccess) err = launch_router_select(rp, m->num_sms, s);
   ScatterParams sp{};
   sp.idx = rp.idx;
   sp.w = rp.w;

@@ -170,6 +170,6 @@ extern "C" dg_status_t dg_moe_route_noalloc(const dg_moe_config_t* cfg,
   rp.y_moe = nullptr;  // no accumulator to clear: routing only
   rp.n_refined = reinterpret_cast<int*>(sc + L.nref);
   if (launch_router(rp, s) != cudaSuccess) return DG_ERR_CUDA;
-  if (launch_router_select(rp, s) != cudaSuccess) return DG_ERR_CUDA;
+  if (launch_router_select(rp, 0, s) != cudaSuccess) return DG_ERR_CUDA;
   return DG_OK;
 }

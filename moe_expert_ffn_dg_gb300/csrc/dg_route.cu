@@ -153,10 +153,15 @@ constexpr float kLogitBoundBias = 1.52587890625e-05f;     // 2^-16
 // 8-bit one) and the final rounding add 2^-17.  The factor r H^-1/2 is
 // common to the token's logits (it cannot change their order); with a bias
 // its error acts per expert and 2^-16 is added, as for the CUDA-core logits.
-__host__ __device__ inline float tc_logit_bound(int H, bool bias) {
-  const int mmas = (2 * H + 16 * kRouterAcc - 1) / (16 * kRouterAcc);
+// With the K blocks split in S ranges (split-K over CTAs) an accumulator
+// adds the MMAs of ceil(range / kRouterAcc) K blocks; each range's sum is
+// rounded once to fp32 (2^-24 of the sum of |terms|) and the ranges are
+// added error-free.
+__host__ __device__ inline float tc_logit_bound(int H, int S, bool bias) {
+  const int kb = 2 * H / 64, len = (kb + S - 1) / S;
+  const int mmas = 4 * ((len + kRouterAcc - 1) / kRouterAcc);
   return 17.0f * (float)mmas * 1.1920928955078125e-07f * 1.3f + 7.62939453125e-06f +
-         (bias ? kLogitBoundBias : 0.0f);
+         (S > 1 ? 5.9604644775390625e-08f : 0.0f) + (bias ? kLogitBoundBias : 0.0f);
 }
 
 // Prep of the tensor-core logits.  Warp per token (blocks [0, nbt)): 1/rms
@@ -833,34 +838,64 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 // [w H/8, (w+1) H/8) of the hidden dimension and walks every (token,
 // candidate) job of the block four at a time; the eight partial sums of a
 // job are combined in a fixed order.
-template <bool U8>
+template <bool U8, int SLOTS, int MODE>
 __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
   __shared__ int s_cand[kSelTokens][256];
   __shared__ int s_ncand[kSelTokens];
   __shared__ double s_zx[kSelTokens][256];
   __shared__ double s_ss[kSelTokens];
+  __shared__ int s_tok[kSelTokens];
   const int H = p.H, E = p.E, K = p.K;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kSelTokens + warp;
-  const bool valid = t < p.T;
   pdl_trigger();
   pdl_wait();
+  // groups of eight tokens: consecutive ones (modes 0, 1), or the tokens the
+  // fast pass flagged (mode 2, a persistent loop over the list)
+  const int nflag = MODE == 2 ? *p.n_flagged : 0;
+  const int ngrp = MODE == 2 ? (nflag + kSelTokens - 1) / kSelTokens : (int)gridDim.x;
+  for (int grp = blockIdx.x; grp < ngrp; grp += (MODE == 2 ? (int)gridDim.x : ngrp)) {
+  int t;
+  bool valid;
+  if (MODE == 2) {
+    const int i = grp * kSelTokens + warp;
+    valid = i < nflag;
+    t = valid ? p.flagged[i] : 0;
+  } else {
+    t = grp * kSelTokens + warp;
+    valid = t < p.T;
+  }
+  if (lane == 0) s_tok[warp] = t;
 
   // ---- A: selection on the fp32 logits, candidate list if near a tie
-  float zl[kMaxSlots];
+  float zl[SLOTS];
   uint32_t taken = 0, certain = 0;  // slot masks of this lane
   int ncand = 0;
   if (valid) {
     const float* z = p.logits + (size_t)t * E;
     const float xnt = p.xnorm_out[t];
-    const float bound = p.logits_tc ? tc_logit_bound(H, p.router_bias != nullptr)
+    const float bound = p.logits_tc ? tc_logit_bound(H, p.z_split > 1 ? p.z_split : 1,
+                                                     p.router_bias != nullptr)
                                     : (p.router_bias ? kLogitBoundBias : kLogitBoundNoBias);
-    float el[kMaxSlots];
+    // split-K logits: the partial sums added error-free, then scaled by
+    // r H^-1/2 in double and rounded once (as the unsplit epilogue does);
+    // the logits are written for the record
+    const double rc = p.z_split > 1 ? (double)p.r_out[t] / sqrt((double)H) : 0.0;
+    float el[SLOTS];
 #pragma unroll
-    for (int s = 0; s < kMaxSlots; ++s) {
+    for (int s = 0; s < SLOTS; ++s) {
       const int e = 32 * s + lane;
       if (e < E) {
-        const float v = z[e];
+        float v;
+        if (p.z_split > 1) {
+          float hi = 0.f, lo = 0.f;
+          for (int r = 0; r < p.z_split; ++r)
+            df_add(hi, lo, p.z_part[((size_t)r * p.T + t) * E + e]);
+          v = (float)(((double)hi + (double)lo) * rc +
+                      (p.router_bias ? (double)p.router_bias[e] : 0.0));
+          if (MODE != 2) p.logits[(size_t)t * E + e] = v;
+        } else {
+          v = z[e];
+        }
         zl[s] = isnan(v) ? -INFINITY : v;
         const float b = p.router_bias ? fabsf(p.router_bias[e]) : 0.f;
         el[s] = bound * (p.wnorm_out[e] * xnt + b) + 1e-30f;
@@ -872,14 +907,14 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
     // k rounds: each lane's best untaken slot (ties to the lower expert),
     // then the warp's largest key and, among lanes holding it, the lowest
     // expert index (two integer reductions per round)
-    uint32_t zk[kMaxSlots];
+    uint32_t zk[SLOTS];
 #pragma unroll
-    for (int s = 0; s < kMaxSlots; ++s) zk[s] = order_key(zl[s]);
+    for (int s = 0; s < SLOTS; ++s) zk[s] = order_key(zl[s]);
     for (int k = 0; k < K; ++k) {
       uint32_t bk = 0;
       uint32_t be = 0xffffffffu;
 #pragma unroll
-      for (int s = 0; s < kMaxSlots; ++s) {
+      for (int s = 0; s < SLOTS; ++s) {
         const int e = 32 * s + lane;
         if (e < E && !((taken >> s) & 1u) && zk[s] > bk) {  // slots ascend in e
           bk = zk[s];
@@ -892,7 +927,7 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
     }
     uint32_t lk = 0xffffffffu, uk = 0u;
 #pragma unroll
-    for (int s = 0; s < kMaxSlots; ++s) {
+    for (int s = 0; s < SLOTS; ++s) {
       if (32 * s + lane >= E) continue;
       if ((taken >> s) & 1u) lk = min(lk, order_key(zl[s] - el[s]));
       else uk = max(uk, order_key(zl[s] + el[s]));
@@ -910,22 +945,28 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
       // bound >= L2.  Those are the candidates (ascending expert order); they
       // get exact logits.
 #pragma unroll
-      for (int s = 0; s < kMaxSlots; ++s)
+      for (int s = 0; s < SLOTS; ++s)
         if (((taken >> s) & 1u) && zl[s] - el[s] > U) certain |= 1u << s;
       uint32_t l2k = 0xffffffffu;
 #pragma unroll
-      for (int s = 0; s < kMaxSlots; ++s)
+      for (int s = 0; s < SLOTS; ++s)
         if (((taken & ~certain) >> s) & 1u) l2k = min(l2k, order_key(zl[s] - el[s]));
       const float L2 = key_value(__reduce_min_sync(kFull, l2k));
       const unsigned lt = (1u << lane) - 1u;
 #pragma unroll
-      for (int s = 0; s < kMaxSlots; ++s) {
+      for (int s = 0; s < SLOTS; ++s) {
         const bool c = 32 * s + lane < E && !((certain >> s) & 1u) && zl[s] + el[s] >= L2;
         const unsigned ms = __ballot_sync(kFull, c);
         if (c) s_cand[warp][ncand + __popc(ms & lt)] = 32 * s + lane;
         ncand += __popc(ms);
       }
     }
+  }
+  if (MODE == 1 && ncand > 0) {
+    // near a tie: left to the re-check pass, which writes this token's outputs
+    if (lane == 0) p.flagged[atomicAdd(p.n_flagged, 1)] = t;
+    valid = false;
+    ncand = 0;
   }
   if (lane == 0) s_ncand[warp] = ncand;
   __syncthreads();
@@ -941,7 +982,7 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
     njobs += s_ncand[w] > 0 ? s_ncand[w] + 1 : 0;
   }
   first[kSelTokens] = njobs;
-  if (njobs > 0) {
+  if (MODE != 1 && njobs > 0) {
     const int nvec = H >> 3;
     const int ngroups = H >> 6;
     const uint4* sv = reinterpret_cast<const uint4*>(p.router_scale);
@@ -952,7 +993,7 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
         if (job >= first[q]) w = q;
       const int c = job - first[w] - 1;
       const int e = c >= 0 ? s_cand[w][c] : -1;
-      const int tt = blockIdx.x * kSelTokens + w;
+      const int tt = s_tok[w];
       const uint4* hrow = reinterpret_cast<const uint4*>(p.h + (size_t)tt * H);
       // kB independent (hi, lo) chains, one per vector of a batch
       constexpr int kB = 4;  // vectors per lane in flight
@@ -1022,8 +1063,7 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
     }
   }
   __syncthreads();
-  if (!valid) return;
-
+  if (valid) {
   // ---- C: reselection among the candidates, weights, outputs
   if (ncand > 0) {
     if (lane == 0) atomicAdd(p.n_refined, 1);
@@ -1032,14 +1072,14 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
     // candidates by exact logit (ties to the lower index).
     int ncert = 0;
 #pragma unroll
-    for (int s = 0; s < kMaxSlots; ++s) ncert += __popc(__ballot_sync(kFull, (certain >> s) & 1u));
+    for (int s = 0; s < SLOTS; ++s) ncert += __popc(__ballot_sync(kFull, (certain >> s) & 1u));
     taken = certain;
     uint32_t usedc = 0;
     for (int k = ncert; k < K; ++k) {
       double bv = -INFINITY;
       int be = 0x7fffffff;
 #pragma unroll
-      for (int q = 0; q < kMaxSlots; ++q) {
+      for (int q = 0; q < SLOTS; ++q) {
         const int c = lane + 32 * q;
         if (c < ncand && !((usedc >> q) & 1u)) {
           const int e = s_cand[warp][c];
@@ -1054,7 +1094,7 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
       if (be == 0x7fffffff) break;
       if ((be & 31) == lane) taken |= 1u << (be >> 5);
 #pragma unroll
-      for (int q = 0; q < kMaxSlots; ++q) {
+      for (int q = 0; q < SLOTS; ++q) {
         const int c = lane + 32 * q;
         if (c < ncand && s_cand[warp][c] == be) usedc |= 1u << q;
       }
@@ -1062,13 +1102,13 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
   }
   float zmax = -INFINITY;
 #pragma unroll
-  for (int s = 0; s < kMaxSlots; ++s)
+  for (int s = 0; s < SLOTS; ++s)
     if ((taken >> s) & 1u) zmax = fmaxf(zmax, zl[s]);
   zmax = warp_max_f(zmax);
-  float ex[kMaxSlots];
+  float ex[SLOTS];
   float se = 0.f;
 #pragma unroll
-  for (int s = 0; s < kMaxSlots; ++s) {
+  for (int s = 0; s < SLOTS; ++s) {
     ex[s] = ((taken >> s) & 1u) ? expf(zl[s] - zmax) : 0.f;
     se += ex[s];
   }
@@ -1076,7 +1116,7 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
   int running = 0;
   const unsigned lt = (1u << lane) - 1u;
 #pragma unroll
-  for (int s = 0; s < kMaxSlots; ++s) {
+  for (int s = 0; s < SLOTS; ++s) {
     const unsigned ms = __ballot_sync(kFull, (taken >> s) & 1u);
     if ((taken >> s) & 1u) {
       const int e = 32 * s + lane;
@@ -1087,6 +1127,9 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
     }
     running += __popc(ms);
   }
+  }  // valid
+  __syncthreads();  // the next group reuses the shared arrays
+  }  // groups
 }
 
 // Exclusive scan over the 256 threads of a block; returns the exclusive
@@ -1354,10 +1397,23 @@ cudaError_t launch_router_prep_tc(const RouterParams& p, cudaStream_t s) {
                      : launch_pdl(k_router_prep_tc<false, false>, grid, dim3(256), 0, s, p, nbt);
 }
 
-cudaError_t launch_router_select(const RouterParams& p, cudaStream_t s) {
+template <bool U8, int SLOTS>
+cudaError_t launch_select_slots(const RouterParams& p, int num_sms, cudaStream_t s) {
   const int grid = (p.T + kSelTokens - 1) / kSelTokens;
-  return p.router_u8 ? launch_pdl(k_router_select<true>, dim3(grid), dim3(256), 0, s, p)
-                     : launch_pdl(k_router_select<false>, dim3(grid), dim3(256), 0, s, p);
+  if (!p.flagged) return launch_pdl(k_router_select<U8, SLOTS, 0>, dim3(grid), dim3(256), 0, s, p);
+  // large batches: a fast pass over all tokens, then the near-tie tokens
+  cudaError_t err = launch_pdl(k_router_select<U8, SLOTS, 1>, dim3(grid), dim3(256), 0, s, p);
+  if (err != cudaSuccess) return err;
+  const int g2 = grid < 2 * num_sms ? grid : 2 * num_sms;
+  return launch_pdl(k_router_select<U8, SLOTS, 2>, dim3(g2), dim3(256), 0, s, p);
+}
+
+cudaError_t launch_router_select(const RouterParams& p, int num_sms, cudaStream_t s) {
+  if (p.E <= 128)
+    return p.router_u8 ? launch_select_slots<true, 4>(p, num_sms, s)
+                       : launch_select_slots<false, 4>(p, num_sms, s);
+  return p.router_u8 ? launch_select_slots<true, 8>(p, num_sms, s)
+                     : launch_select_slots<false, 8>(p, num_sms, s);
 }
 
 cudaError_t launch_route_scatter(const ScatterParams& p, cudaStream_t s) {
