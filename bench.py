@@ -537,16 +537,16 @@ def kernel_split(blk, fwd, stream, dev, steps, set_events, names):
     return per_kernel / len(ev_sets) * 1000.0
 
 
-ROUTER_TC_MIN_TOKENS = 1024  # the library's two-pass selection threshold
+ROUTER_TC_MIN_TOKENS = 1024  # the library's tensor-core router threshold
 
 
 def launches_per_forward(wl, nk):
     # an 8-bit dense branch beside 4-bit experts adds a dense-only launch to
-    # each of the two GEMM slots; the router slot holds two launches (prep and
-    # the router GEMM), and from 1024 tokens so does the selection slot (fast
+    # each of the two GEMM slots; from 1024 tokens the router slot holds two
+    # launches (prep and the router GEMM) and so does the selection slot (fast
     # pass and re-check pass)
-    return (nk + (2 if wl.quant and wl.quant[1] != wl.quant[0] else 0) + 1
-            + (1 if wl.tokens >= ROUTER_TC_MIN_TOKENS else 0))
+    return (nk + (2 if wl.quant and wl.quant[1] != wl.quant[0] else 0)
+            + (2 if wl.tokens >= ROUTER_TC_MIN_TOKENS else 0))
 
 
 def measure_layer(wl, p, h_np, dev, steps, warmup, local=0, neighbours=False, dist=None,

@@ -166,7 +166,8 @@ dg_status_t dg_moe_workspace_size(const dg_moe_config_t* cfg, size_t* bytes);
 /* Validate cfg and weights, and build the handle: TMA descriptors for the
  * weights and for workspace buffers, launch shapes.  workspace: device
  * memory of at least dg_moe_workspace_size() bytes, 1024-byte aligned,
- * used only by this handle.  Allocates no device memory and launches no
+ * used only by this handle, or shared by handles of one shape whose
+ * forwards run one after another on one stream (a layer stack).  Allocates no device memory and launches no
  * kernel; clears the workspace's status word with one blocking memset.
  * Validation errors are returned before any CUDA call.  On error *out is
  * set to NULL. */
@@ -190,8 +191,9 @@ dg_status_t dg_moe_forward(dg_moe_t* m, const void* h_in, void* h_out, int n_tok
  *   next_in = bf16(rms(out) * w_next_in)              (the next layer's
  *             input_layernorm, optional)
  *
- * The router kernels build h from x and attn_out where they read the block
- * input (no separate pass); the combine writes next_in beside out.  x is the
+ * The router's prep kernel builds h from x and attn_out and publishes it (in
+ * h_mid or the workspace) for the later kernels; the combine writes next_in
+ * beside out.  x is the
  * decoder layer's input (the attention residual). */
 typedef struct {
   const void* attn_out;     /* bf16 [n_tokens, H]: self-attention output (o_proj), before its norm */
@@ -225,13 +227,18 @@ dg_status_t dg_moe_destroy(dg_moe_t* m);
 dg_status_t dg_moe_last_device_status(dg_moe_t* m, dg_stream_t stream, unsigned int* where,
                                       unsigned int* info);
 
-/* Number of kernels one forward launches, and their names (static strings).
- * names may be NULL; *n receives the count. */
+/* Number of profiling slots of one forward, and their names (static
+ * strings): router_logits (prep + router GEMM), router_select (one pass, or
+ * the fast pass and the re-check pass from 1024 tokens), scatter_gather,
+ * gemm_gate_up, gemm_down (each with a dense-only launch after it when an
+ * 8-bit dense branch sits beside 4-bit experts), combine.  names may be
+ * NULL; *n receives the count. */
 dg_status_t dg_moe_kernel_names(const dg_moe_t* m, const char** names, int* n);
 
 /* Profiling: when events is non-NULL, every later forward records events[i]
- * on its stream just before kernel i and events[n_kernels] after the last
- * one; n_events must be n_kernels + 1.  NULL switches it off.  Events are
+ * on its stream just before the launches of slot i and events[n_slots] after
+ * the last one; n_events must be n_slots + 1.  The events separate the
+ * launches, which then no longer overlap their neighbours' start and end.  NULL switches it off.  Events are
  * borrowed (created and destroyed by the caller). */
 dg_status_t dg_moe_set_profile_events(dg_moe_t* m, dg_event_t* events, int n_events);
 
@@ -256,8 +263,10 @@ const char* dg_moe_last_error(const dg_moe_t* m);
  * pages have no counterpart: this is a library convenience.  Some callers
  * cannot call cudaMalloc (an allocator hook or arena that owns all device
  * memory, a host framework that forbids allocation on its hot path); this
- * entry point needs no handle and no workspace.  It runs the same routing
- * kernels as dg_moe_forward on h_in (bf16 [n_tokens, H]) with the router
+ * entry point needs no handle and no workspace.  It computes the same
+ * routing as dg_moe_forward (the same selection, exact re-check included;
+ * its logits come from the CUDA-core logit kernels, which need no weight
+ * planes) on h_in (bf16 [n_tokens, H]) with the router
  * weights of `weights` (router, router_scale, per_expert_scale, w_pre_ff,
  * router_bias; cfg gives H, E, K, router_fmt and rms_eps) and writes
  * idx_out (int32 [n_tokens, K], ascending experts per token) and w_out

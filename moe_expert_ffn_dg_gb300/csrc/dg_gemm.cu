@@ -43,19 +43,29 @@ template <int MODE>
 constexpr int threads_of() { return MODE == 2 ? kThreads + 32 : kThreads; }
 constexpr int kATileBytes = 128 * 128;  // 128 rows x 64 bf16
 
-template <int BN>
+// Stage ring of one CTA: the router GEMM keeps the whole 192 KB (one CTA an
+// SM, all TMEM); the projections take kProjRingBytes with kProjCtasPerSm
+// CTAs an SM.
+constexpr int kRouterRingBytes = 192 * 1024;
+constexpr int kProjRingBytes = 192 * 1024 / kProjCtasPerSm;
+template <int MODE>
+constexpr int ring_of() { return MODE == 2 ? kRouterRingBytes : kProjRingBytes; }
+template <int MODE>
+constexpr int ctas_of() { return MODE == 2 ? 1 : kProjCtasPerSm; }
+
+template <int BN, int RING = kProjRingBytes>
 struct Cfg {
   static constexpr int kBTileBytes = BN * 128;
-  static constexpr int kStages = (192 * 1024) / (kATileBytes + kBTileBytes);
+  static constexpr int kStages = RING / (kATileBytes + kBTileBytes);
   static constexpr int kTmemCols = 2 * BN;
   static constexpr size_t kSmem =
       1024 + (size_t)kStages * (kATileBytes + kBTileBytes) + 256 + kTileTableBytes;
 };
 
 template <int MODE, int BN>
-__global__ void __launch_bounds__(threads_of<MODE>(), 1)
+__global__ void __launch_bounds__(threads_of<MODE>(), ctas_of<MODE>())
     k_grouped_gemm(const __grid_constant__ GemmParams p) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, ring_of<MODE>()>;
   constexpr int S = C::kStages;
   // router logits: one set of kRouterAcc accumulators (the whole TMEM);
   // the projections: two accumulators, so an epilogue overlaps the next tile
@@ -381,7 +391,8 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1)
 
 template <int MODE, int BN>
 cudaError_t launch_mode_bn(const GemmParams& p, int grid, cudaStream_t s) {
-  return launch_pdl(k_grouped_gemm<MODE, BN>, dim3(grid), dim3(threads_of<MODE>()), Cfg<BN>::kSmem,
+  return launch_pdl(k_grouped_gemm<MODE, BN>, dim3(grid * ctas_of<MODE>()),
+                    dim3(threads_of<MODE>()), Cfg<BN, ring_of<MODE>()>::kSmem,
                     s, p);
 }
 
@@ -389,7 +400,7 @@ template <int MODE, int BN>
 cudaError_t allow_smem() {
   static_assert(MODE != 2 || BN == kRouterBn, "router tiles");
   return cudaFuncSetAttribute(k_grouped_gemm<MODE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)Cfg<BN>::kSmem);
+                              (int)Cfg<BN, ring_of<MODE>()>::kSmem);
 }
 
 }  // namespace

@@ -216,10 +216,11 @@ cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s);
 // rows in one token-major kernel.
 cudaError_t launch_scatter_gather(const ScatterParams& sp, const GatherParams& gp,
                                   cudaStream_t s);
-// The block's router logits come from the tensor cores (prep kernel + router
-// GEMM); the CUDA-core logit kernels serve the allocation-free routing entry
-// point.  From this many tokens on, the selection runs in two passes (a fast
-// one, then the re-check of the tokens near a tie).
+// From this many tokens on, the router logits come from the tensor cores
+// (prep kernel + router GEMM) and the selection runs in two passes (a fast
+// one, then the re-check of the tokens near a tie); below, from the
+// CUDA-core logit kernel (which also serves the allocation-free entry point)
+// and one selection pass.
 constexpr int kRouterTcMinTokens = 1024;
 // Token rows per tile of the router GEMM and its accumulators: K (2H) is
 // dealt to kRouterAcc TMEM accumulators in turn (kRouterAcc x 64 columns),
@@ -242,6 +243,10 @@ inline int router_split(int T, int E, int kb) {
   while (s > 1 && (s - 1) * ((kb + s - 1) / s) >= kb) --s;
   return s;
 }
+
+// CTAs of the bf16 projection GEMMs per SM (grid = SMs times this), each
+// with its share of the 192 KB stage ring.
+constexpr int kProjCtasPerSm = 1;
 
 // mode 0: gate_up + GEGLU, mode 1: down + weighted scatter, mode 2: router
 // logits (bn = kRouterBn)

@@ -61,14 +61,16 @@ Layout make_layout(const dg_moe_config_t& c) {
   L.inv = take(TK * 4);
   L.zero16 = take(16);  // expert offsets {0} of a launch with no experts
   // router rows times router_scale as bf16 planes (hi | lo), for the
-  // tensor-core logits
-  L.planes = take(E * 2 * H * 2);
+  // tensor-core logits of large batches
+  const bool tc = T >= (size_t)kRouterTcMinTokens;
+  L.planes = tc ? take(E * 2 * H * 2) : 0;
   // split-K partial logits: the largest split times tokens over the batch
   // sizes the handle accepts (beyond one wave of token tiles there is no split)
   {
     const int kb = (int)(2 * H / 64);
     size_t most = 0;
-    for (size_t n = 1; n <= (T + kRouterBn - 1) / kRouterBn && n <= (size_t)kRouterCtaTarget; ++n) {
+    for (size_t n = kRouterTcMinTokens / kRouterBn;
+         tc && n <= (T + kRouterBn - 1) / kRouterBn && n <= (size_t)kRouterCtaTarget; ++n) {
       const size_t t = n * kRouterBn < T ? n * kRouterBn : T;
       const size_t sp = (size_t)router_split((int)t, (int)E, kb);
       if (sp > 1 && sp * t > most) most = sp * t;
@@ -337,7 +339,7 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
     delete m;
     return DG_ERR_UNSUPPORTED;
   }
-  {
+  if (T >= (uint64_t)kRouterTcMinTokens) {
     // router GEMM: the planes [E, 2H] are the weight side (M = 128 experts a
     // tile), the token rows of the block input the other; no expert groups
     GemmParams& g = m->gr;
@@ -476,20 +478,17 @@ dg_status_t forward_impl(dg_moe_t* m, const void* h_in, void* h_out, int n_token
     hb = rp.h_out;
   }
   mark(0);
-  {
+  if (T >= kRouterTcMinTokens) {
     // tensor-core logits: prep (r, xd, planes, norms), then the router GEMM
     // over the block input (split over K ranges while the token tiles alone
-    // would leave most SMs idle)
+    // would leave most SMs idle), and the selection in two passes
     const int split = router_split(T, E, 2 * H / 64);
     rp.logits_tc = 1;
     rp.planes = reinterpret_cast<uint16_t*>(ws + L.planes);
     rp.z_split = split;
     rp.z_part = reinterpret_cast<const float*>(ws + L.zpart);
-    if (T >= kRouterTcMinTokens) {
-      // two-pass selection
-      rp.flagged = reinterpret_cast<int32_t*>(ws + L.flagged);
-      rp.n_flagged = counters + 1;
-    }
+    rp.flagged = reinterpret_cast<int32_t*>(ws + L.flagged);
+    rp.n_flagged = counters + 1;
     if (err == cudaSuccess) err = launch_router_prep_tc(rp, s);
     GemmParams gr = m->gr;
     gr.T = T;
@@ -503,6 +502,10 @@ dg_status_t forward_impl(dg_moe_t* m, const void* h_in, void* h_out, int n_token
     gr.xb_exp64 = gr.xb_d64;
     gr.xb_exp16 = gr.xb_d16;
     if (err == cudaSuccess) err = launch_gemm(2, kRouterBn, gr, m->num_sms, s);
+  } else if (err == cudaSuccess) {
+    // small batches: the CUDA-core logit kernel (latency-bound either way,
+    // and it keeps the tighter bound), one selection pass
+    err = launch_router(rp, s);
   }
   rp.h = hb;
   rp.attn = nullptr;

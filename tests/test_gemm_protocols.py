@@ -383,10 +383,15 @@ def test_model_catches_planted_mistakes(plant):
 # ------------------------------------------------------- bf16-weight kernel
 
 def bf16_stages(bn: int) -> int:
+    """Stages of the projection GEMMs' ring (the router GEMM keeps a ring of
+    its own size, one CTA an SM)."""
     src = open(SRC_BF16).read()
+    hdr = open(os.path.join(CSRC, "dg_kernels.h")).read()
     env = {"BN": bn}
-    env["kATileBytes"] = _c_eval(re.search(r"constexpr int kATileBytes = ([^;]+);", src).group(1),
-                                 env)
+    env["kProjCtasPerSm"] = int(re.search(r"constexpr int kProjCtasPerSm = (\d+);", hdr).group(1))
+    for name in ("kATileBytes", "kProjRingBytes"):
+        env[name] = _c_eval(re.search(rf"constexpr int {name} = ([^;]+);", src).group(1), env)
+    env["RING"] = env["kProjRingBytes"]
     body = re.search(r"struct Cfg \{(.*?)\n\};", src, re.S).group(1)
     for name, expr in re.findall(r"static constexpr int (k\w+) = ([^;]+);", body):
         env[name] = _c_eval(expr, env)

@@ -233,12 +233,11 @@ def tc_logit_bound(H, S):
     return 17 * mmas * 2.0 ** -23 * 1.3 + 2.0 ** -17 + (2.0 ** -24 if S > 1 else 0.0)
 
 
-@pytest.mark.parametrize("name,tokens,u8", [("tiny", 0, False), ("canvas256", 0, False),
-                                            ("canvas256", 0, True), ("batch2048_zipf", 0, False),
-                                            ("tiny", 4100, True)])
+@pytest.mark.parametrize("name,tokens,u8", [("tiny", 1100, False), ("canvas256", 1024, True),
+                                            ("batch2048_zipf", 0, False), ("tiny", 4100, True)])
 def test_tensor_core_logits_error_far_inside_their_bound(name, tokens, u8):
-    """The logits come from the router GEMM on the tensor cores, whose
-    accumulation order and rounding are not specified; routing stays exact
+    """From 1024 tokens the logits come from the router GEMM on the tensor
+    cores, whose accumulation order and rounding are not specified; routing stays exact
     because every token within the bound of a tie is re-checked in exact
     arithmetic.  Measured against the exact logits, the error must sit far
     inside that bound (here: below 1/16 of it), split over K or not."""
