@@ -43,17 +43,18 @@ template <int MODE>
 constexpr int threads_of() { return MODE == 2 ? kThreads + 32 : kThreads; }
 constexpr int kATileBytes = 128 * 128;  // 128 rows x 64 bf16
 
-// Stage ring of one CTA: the router GEMM keeps the whole 192 KB (one CTA an
-// SM, all TMEM); the projections take kProjRingBytes with kProjCtasPerSm
-// CTAs an SM.
-constexpr int kRouterRingBytes = 192 * 1024;
-constexpr int kProjRingBytes = 192 * 1024 / kProjCtasPerSm;
-template <int MODE>
-constexpr int ring_of() { return MODE == 2 ? kRouterRingBytes : kProjRingBytes; }
-template <int MODE>
-constexpr int ctas_of() { return MODE == 2 ? 1 : kProjCtasPerSm; }
+// CTAs an SM and the stage ring of each: the projections run kProjCtasPerSm
+// CTAs an SM, each with its share of the 192 KB ring (measured: one CTA
+// streams weights at only ~45 GB/s, and two an SM lift one canvas's gate_up
+// from 180 to 164 us); the router GEMM and 256-token tiles keep one CTA an SM
+// (their accumulators fill the TMEM) and the whole ring.
+constexpr int kRingBytes = 192 * 1024;
+template <int MODE, int BN>
+constexpr int ctas_of() { return (MODE == 2 || BN == 256) ? 1 : kProjCtasPerSm; }
+template <int MODE, int BN>
+constexpr int ring_of() { return kRingBytes / ctas_of<MODE, BN>(); }
 
-template <int BN, int RING = kProjRingBytes>
+template <int BN, int RING>
 struct Cfg {
   static constexpr int kBTileBytes = BN * 128;
   static constexpr int kStages = RING / (kATileBytes + kBTileBytes);
@@ -63,9 +64,9 @@ struct Cfg {
 };
 
 template <int MODE, int BN>
-__global__ void __launch_bounds__(threads_of<MODE>(), ctas_of<MODE>())
+__global__ void __launch_bounds__(threads_of<MODE>(), ctas_of<MODE, BN>())
     k_grouped_gemm(const __grid_constant__ GemmParams p) {
-  using C = Cfg<BN, ring_of<MODE>()>;
+  using C = Cfg<BN, ring_of<MODE, BN>()>;
   constexpr int S = C::kStages;
   // router logits: one set of kRouterAcc accumulators (the whole TMEM);
   // the projections: two accumulators, so an epilogue overlaps the next tile
@@ -391,8 +392,8 @@ __global__ void __launch_bounds__(threads_of<MODE>(), ctas_of<MODE>())
 
 template <int MODE, int BN>
 cudaError_t launch_mode_bn(const GemmParams& p, int grid, cudaStream_t s) {
-  return launch_pdl(k_grouped_gemm<MODE, BN>, dim3(grid * ctas_of<MODE>()),
-                    dim3(threads_of<MODE>()), Cfg<BN, ring_of<MODE>()>::kSmem,
+  return launch_pdl(k_grouped_gemm<MODE, BN>, dim3(grid * ctas_of<MODE, BN>()),
+                    dim3(threads_of<MODE>()), Cfg<BN, ring_of<MODE, BN>()>::kSmem,
                     s, p);
 }
 
@@ -400,7 +401,7 @@ template <int MODE, int BN>
 cudaError_t allow_smem() {
   static_assert(MODE != 2 || BN == kRouterBn, "router tiles");
   return cudaFuncSetAttribute(k_grouped_gemm<MODE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)Cfg<BN, ring_of<MODE>()>::kSmem);
+                              (int)Cfg<BN, ring_of<MODE, BN>()>::kSmem);
 }
 
 }  // namespace
@@ -416,7 +417,9 @@ cudaError_t prepare_gemm_bf16() {
 }
 
 size_t gemm_smem_bytes(int bn) {
-  return bn == 256 ? Cfg<256>::kSmem : bn == 128 ? Cfg<128>::kSmem : Cfg<64>::kSmem;
+  return bn == 256   ? Cfg<256, ring_of<0, 256>()>::kSmem
+         : bn == 128 ? Cfg<128, ring_of<0, 128>()>::kSmem
+                     : Cfg<64, ring_of<0, 64>()>::kSmem;
 }
 
 cudaError_t launch_gemm(int mode, int bn, const GemmParams& p, int grid, cudaStream_t s) {

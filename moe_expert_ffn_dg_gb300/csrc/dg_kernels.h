@@ -222,21 +222,28 @@ cudaError_t launch_scatter_gather(const ScatterParams& sp, const GatherParams& g
 // CUDA-core logit kernel (which also serves the allocation-free entry point)
 // and one selection pass.
 constexpr int kRouterTcMinTokens = 1024;
-// Token rows per tile of the router GEMM and its accumulators: K (2H) is
-// dealt to kRouterAcc TMEM accumulators in turn (kRouterAcc x 64 columns),
-// summed error-free in the epilogue, so each accumulator adds only 1/8 of the
-// products.
-constexpr int kRouterBn = 64;
-constexpr int kRouterAcc = 8;
+// Token rows per tile of the router GEMM and its accumulators: a tile's K
+// range is dealt to kRouterAcc TMEM accumulators in turn (kRouterAcc x 256
+// columns), summed error-free in the epilogue.  Wide tiles keep the weight
+// planes' re-reads low (each tile reads all of them); the K split over CTAs
+// (router_split) keeps each accumulator's MMA count, and with it the error
+// bound, small.
+constexpr int kRouterBn = 256;
+constexpr int kRouterAcc = 2;
 cudaError_t launch_router_prep_tc(const RouterParams& p, cudaStream_t s);
 
-// K ranges of the router GEMM for T tokens: enough CTAs for about one wave
-// (kRouterCtaTarget) while each range keeps at least one K block per
-// accumulator; kb = 2H / 64 K blocks, E experts.
+// K ranges of the router GEMM for T tokens (kb = 2H / 64 K blocks, E
+// experts): enough CTAs for about one wave (kRouterCtaTarget), and at least
+// enough ranges that an accumulator adds no more than kRouterMaxAccMmas MMAs;
+// at most one range per K block per accumulator, and no range empty.
 constexpr int kRouterCtaTarget = 160;
+constexpr int kRouterMaxAccMmas = 44;
 inline int router_split(int T, int E, int kb) {
   const int tiles = ((T + kRouterBn - 1) / kRouterBn) * ((E + 127) / 128);
   int s = (kRouterCtaTarget + tiles - 1) / tiles;
+  const int kbs_max = kRouterAcc * (kRouterMaxAccMmas / 4);  // K blocks a range may hold
+  const int s_bound = (kb + kbs_max - 1) / kbs_max;
+  if (s < s_bound) s = s_bound;
   const int smax = kb / kRouterAcc > 1 ? kb / kRouterAcc : 1;
   s = s < 1 ? 1 : (s > smax ? smax : s);
   // ranges of ceil(kb / s) blocks: none may be left empty
@@ -244,9 +251,9 @@ inline int router_split(int T, int E, int kb) {
   return s;
 }
 
-// CTAs of the bf16 projection GEMMs per SM (grid = SMs times this), each
-// with its share of the 192 KB stage ring.
-constexpr int kProjCtasPerSm = 1;
+// CTAs of the bf16 projection GEMMs per SM (grid = SMs times this, for
+// token tiles up to 128), each with its share of the 192 KB stage ring.
+constexpr int kProjCtasPerSm = 2;
 
 // mode 0: gate_up + GEGLU, mode 1: down + weighted scatter, mode 2: router
 // logits (bn = kRouterBn)

@@ -65,12 +65,12 @@ Layout make_layout(const dg_moe_config_t& c) {
   const bool tc = T >= (size_t)kRouterTcMinTokens;
   L.planes = tc ? take(E * 2 * H * 2) : 0;
   // split-K partial logits: the largest split times tokens over the batch
-  // sizes the handle accepts (beyond one wave of token tiles there is no split)
+  // sizes the handle accepts
   {
     const int kb = (int)(2 * H / 64);
     size_t most = 0;
-    for (size_t n = kRouterTcMinTokens / kRouterBn;
-         tc && n <= (T + kRouterBn - 1) / kRouterBn && n <= (size_t)kRouterCtaTarget; ++n) {
+    for (size_t n = kRouterTcMinTokens / kRouterBn; tc && n <= (T + kRouterBn - 1) / kRouterBn;
+         ++n) {
       const size_t t = n * kRouterBn < T ? n * kRouterBn : T;
       const size_t sp = (size_t)router_split((int)t, (int)E, kb);
       if (sp > 1 && sp * t > most) most = sp * t;

@@ -388,10 +388,10 @@ def bf16_stages(bn: int) -> int:
     src = open(SRC_BF16).read()
     hdr = open(os.path.join(CSRC, "dg_kernels.h")).read()
     env = {"BN": bn}
-    env["kProjCtasPerSm"] = int(re.search(r"constexpr int kProjCtasPerSm = (\d+);", hdr).group(1))
-    for name in ("kATileBytes", "kProjRingBytes"):
+    ctas = int(re.search(r"constexpr int kProjCtasPerSm = (\d+);", hdr).group(1))
+    for name in ("kATileBytes", "kRingBytes"):
         env[name] = _c_eval(re.search(rf"constexpr int {name} = ([^;]+);", src).group(1), env)
-    env["RING"] = env["kProjRingBytes"]
+    env["RING"] = env["kRingBytes"] // (1 if bn == 256 else ctas)
     body = re.search(r"struct Cfg \{(.*?)\n\};", src, re.S).group(1)
     for name, expr in re.findall(r"static constexpr int (k\w+) = ([^;]+);", body):
         env[name] = _c_eval(expr, env)

@@ -213,23 +213,28 @@ def test_batch2048_zipf_beta1_stress():
 
 
 def router_split(T, E, H):
-    """K ranges of the router GEMM: about 160 CTAs while every range keeps
-    one K block (64) per each of the eight accumulators."""
+    """K ranges of the router GEMM (256-token tiles, two accumulators): about
+    160 CTAs, at least enough ranges for 44 MMAs an accumulator, at most one
+    K block per accumulator a range, no range empty."""
     kb = 2 * H // 64
-    tiles = -(-T // 64) * -(-E // 128)
-    return max(1, min(-(-160 // tiles), max(1, kb // 8)))
+    tiles = -(-T // 256) * -(-E // 128)
+    s = max(-(-160 // tiles), -(-kb // 22))
+    s = max(1, min(s, max(1, kb // 2)))
+    while s > 1 and (s - 1) * -(-kb // s) >= kb:
+        s -= 1
+    return s
 
 
 def tc_logit_bound(H, S):
     """The error bound the selection applies to the tensor-core logits,
     relative to r H^-1/2 |h_t| |W_e * router_scale| (no bias): up to 17 units
     in the last place per MMA of 16 products, over the MMAs one accumulator
-    adds (four per K block; the K blocks of a range dealt to eight
-    accumulators), with a 1.3 margin, plus 2^-17 for the weight split and
-    2^-24 for the rounding of a range's partial sum."""
+    adds (four per K block; a range's K blocks dealt to two accumulators),
+    with a 1.3 margin, plus 2^-17 for the weight split and 2^-24 for the
+    rounding of a range's partial sum."""
     kb = 2 * H // 64
     ln = -(-kb // S)
-    mmas = 4 * -(-ln // 8)
+    mmas = 4 * -(-ln // 2)
     return 17 * mmas * 2.0 ** -23 * 1.3 + 2.0 ** -17 + (2.0 ** -24 if S > 1 else 0.0)
 
 
