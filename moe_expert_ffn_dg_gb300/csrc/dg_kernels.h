@@ -232,21 +232,17 @@ constexpr int kRouterBn = 256;
 constexpr int kRouterAcc = 2;
 cudaError_t launch_router_prep_tc(const RouterParams& p, cudaStream_t s);
 
-// K ranges of the router GEMM for T tokens (kb = 2H / 64 K blocks, E
-// experts): enough CTAs for about one wave (kRouterCtaTarget), and at least
-// enough ranges that an accumulator adds no more than kRouterMaxAccMmas MMAs;
-// at most one range per K block per accumulator, and no range empty.
-constexpr int kRouterCtaTarget = 160;
+// K ranges of the router GEMM (kb = 2H / 64 K blocks): the fewest that keep
+// an accumulator to kRouterMaxAccMmas MMAs (the bound of the logits), none
+// empty.  More ranges would give more CTAs but more partial sums for the
+// selection to add, which costs more than it saves.
 constexpr int kRouterMaxAccMmas = 44;
 inline int router_split(int T, int E, int kb) {
-  const int tiles = ((T + kRouterBn - 1) / kRouterBn) * ((E + 127) / 128);
-  int s = (kRouterCtaTarget + tiles - 1) / tiles;
+  (void)T;
+  (void)E;
   const int kbs_max = kRouterAcc * (kRouterMaxAccMmas / 4);  // K blocks a range may hold
-  const int s_bound = (kb + kbs_max - 1) / kbs_max;
-  if (s < s_bound) s = s_bound;
-  const int smax = kb / kRouterAcc > 1 ? kb / kRouterAcc : 1;
-  s = s < 1 ? 1 : (s > smax ? smax : s);
-  // ranges of ceil(kb / s) blocks: none may be left empty
+  int s = (kb + kbs_max - 1) / kbs_max;
+  if (s < 1) s = 1;
   while (s > 1 && (s - 1) * ((kb + s - 1) / s) >= kb) --s;
   return s;
 }

@@ -971,72 +971,96 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
   if (lane == 0) s_ncand[warp] = ncand;
   __syncthreads();
 
-  // ---- B: exact logits of this warp's token when it is near a tie: its sum
-  // of squares and its candidates' dot products, four at a time over one
-  // pass of the token's row (lanes strided over the 8-element vectors, loads
-  // of four vectors in flight), each summed as error-free fp32 pairs, then by
-  // a fixed shuffle tree.
-  if (MODE != 1 && ncand > 0) {
+  // ---- B: exact logits.  Jobs of a near-tie token: its sum of squares
+  // (c = -1), then its candidates (c = 0 .. ncand-1).  One warp per job: the
+  // whole dot product over H, its loads issued in batches, lanes strided over
+  // the 8-element vectors, then a fixed shuffle tree.
+  int njobs = 0, first[kSelTokens + 1];
+#pragma unroll
+  for (int w = 0; w < kSelTokens; ++w) {
+    first[w] = njobs;
+    njobs += s_ncand[w] > 0 ? s_ncand[w] + 1 : 0;
+  }
+  first[kSelTokens] = njobs;
+  if (MODE != 1 && njobs > 0) {
     const int nvec = H >> 3;
     const int ngroups = H >> 6;
     const uint4* sv = reinterpret_cast<const uint4*>(p.router_scale);
-    const uint4* hrow = reinterpret_cast<const uint4*>(p.h + (size_t)t * H);
-    constexpr int kJ = 4;  // jobs a pass (job -1: the sum of squares)
-    for (int j0 = -1; j0 < ncand; j0 += kJ) {
-      float hi[kJ], lo[kJ];
-      int ej[kJ];
+    for (int job = warp; job < njobs; job += kSelTokens) {
+      int w = 0;
 #pragma unroll
-      for (int u = 0; u < kJ; ++u) {
-        const int job = j0 + u;
-        ej[u] = job < 0 ? -1 : (job < ncand ? s_cand[warp][job] : -2);
-        hi[u] = 0.f;
-        lo[u] = 0.f;
+      for (int q = 1; q < kSelTokens; ++q)
+        if (job >= first[q]) w = q;
+      const int c = job - first[w] - 1;
+      const int e = c >= 0 ? s_cand[w][c] : -1;
+      const int tt = s_tok[w];
+      const uint4* hrow = reinterpret_cast<const uint4*>(p.h + (size_t)tt * H);
+      // kB independent (hi, lo) chains, one per vector of a batch
+      constexpr int kB = 4;  // vectors per lane in flight
+      float hi4[kB], lo4[kB];
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        hi4[u] = 0.f;
+        lo4[u] = 0.f;
       }
-#pragma unroll 4
-      for (int v = lane; v < nvec; v += 32) {
-        const uint4 rh = __ldg(hrow + v), rs = __ldg(sv + v);
-        const int gi = (8 * v) >> 6;
+      for (int v0 = lane; v0 < nvec; v0 += 32 * kB) {
+        uint4 rh[kB], rs[kB], rw[kB];
 #pragma unroll
-        for (int u = 0; u < kJ; ++u) {
-          const int e = ej[u];
-          if (e == -1) {
-            exact_squares(rh, hi[u], lo[u]);
-          } else if (e >= 0) {
-            if constexpr (!U8) {
-              const uint4 rw = __ldg(reinterpret_cast<const uint4*>(
-                                         static_cast<const uint16_t*>(p.wr) + (size_t)e * H) + v);
-              exact_terms_bf16(rh, rs, rw, hi[u], lo[u]);
-            } else {
-              const uint2 q2 = __ldg(reinterpret_cast<const uint2*>(
-                                         static_cast<const uint8_t*>(p.wr) + (size_t)e * H) + v);
-              exact_terms_u8(rh, rs, q2.x, q2.y,
-                             bf16_to_f32(p.wr_scales[(size_t)e * ngroups + gi]),
-                             bf16_to_f32(p.wr_biases[(size_t)e * ngroups + gi]), hi[u], lo[u]);
+        for (int u = 0; u < kB; ++u) {
+          const int v = v0 + 32 * u;
+          if (v < nvec) {
+            rh[u] = __ldg(hrow + v);
+            if (e >= 0) {
+              rs[u] = __ldg(sv + v);
+              if constexpr (!U8) {
+                rw[u] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.wr) +
+                                                             (size_t)e * H) + v);
+              } else {
+                const uint2 q2 = __ldg(reinterpret_cast<const uint2*>(
+                                           static_cast<const uint8_t*>(p.wr) + (size_t)e * H) + v);
+                rw[u] = make_uint4(q2.x, q2.y, 0u, 0u);
+              }
             }
           }
         }
-      }
 #pragma unroll
-      for (int u = 0; u < kJ; ++u) {
-        float h2 = hi[u], l2 = lo[u];
-#pragma unroll
-        for (int o = 16; o; o >>= 1)
-          df_add2(h2, l2, __shfl_xor_sync(kFull, h2, o), __shfl_xor_sync(kFull, l2, o));
-        if (lane == 0) {
-          if (ej[u] == -1) s_ss[warp] = df_value(h2, l2);
-          else if (ej[u] >= 0) s_zx[warp][j0 + u] = df_value(h2, l2);
+        for (int u = 0; u < kB; ++u) {
+          const int v = v0 + 32 * u;
+          if (v >= nvec) continue;
+          if (e < 0) {
+            exact_squares(rh[u], hi4[u], lo4[u]);
+          } else if constexpr (!U8) {
+            exact_terms_bf16(rh[u], rs[u], rw[u], hi4[u], lo4[u]);
+          } else {
+            const int gi = (8 * v) >> 6;
+            exact_terms_u8(rh[u], rs[u], rw[u].x, rw[u].y,
+                           bf16_to_f32(p.wr_scales[(size_t)e * ngroups + gi]),
+                           bf16_to_f32(p.wr_biases[(size_t)e * ngroups + gi]), hi4[u], lo4[u]);
+          }
         }
       }
+      float hi = hi4[0], lo = lo4[0];
+#pragma unroll
+      for (int u = 1; u < kB; ++u) df_add2(hi, lo, hi4[u], lo4[u]);
+#pragma unroll
+      for (int o = 16; o; o >>= 1)
+        df_add2(hi, lo, __shfl_xor_sync(kFull, hi, o), __shfl_xor_sync(kFull, lo, o));
+      if (lane == 0) {
+        if (c < 0) s_ss[w] = df_value(hi, lo);
+        else s_zx[w][c] = df_value(hi, lo);
+      }
     }
-    __syncwarp();
+    __syncthreads();
     // exact logit = dot * (1/rms) * H^-1/2 + bias
     const double cHd = 1.0 / sqrt((double)H);
-    const double r64 = 1.0 / sqrt(s_ss[warp] / (double)H + (double)p.eps);
-    for (int c = lane; c < ncand; c += 32) {
-      const int e = s_cand[warp][c];
-      s_zx[warp][c] = s_zx[warp][c] * r64 * cHd + (p.router_bias ? (double)p.router_bias[e] : 0.0);
+    for (int i = threadIdx.x; i < kSelTokens * 256; i += blockDim.x) {
+      const int w = i >> 8, c = i & 255;
+      if (c < s_ncand[w]) {
+        const double r64 = 1.0 / sqrt(s_ss[w] / (double)H + (double)p.eps);
+        const int e = s_cand[w][c];
+        s_zx[w][c] = s_zx[w][c] * r64 * cHd + (p.router_bias ? (double)p.router_bias[e] : 0.0);
+      }
     }
-    __syncwarp();
   }
   __syncthreads();
   if (valid) {

@@ -213,13 +213,10 @@ def test_batch2048_zipf_beta1_stress():
 
 
 def router_split(T, E, H):
-    """K ranges of the router GEMM (256-token tiles, two accumulators): about
-    160 CTAs, at least enough ranges for 44 MMAs an accumulator, at most one
-    K block per accumulator a range, no range empty."""
+    """K ranges of the router GEMM (two accumulators): the fewest that keep
+    44 MMAs an accumulator, none empty."""
     kb = 2 * H // 64
-    tiles = -(-T // 256) * -(-E // 128)
-    s = max(-(-160 // tiles), -(-kb // 22))
-    s = max(1, min(s, max(1, kb // 2)))
+    s = max(1, -(-kb // 22))
     while s > 1 and (s - 1) * -(-kb // s) >= kb:
         s -= 1
     return s
