@@ -879,14 +879,14 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
     // split-K logits: the partial sums added error-free, then scaled by
     // r H^-1/2 in double and rounded once (as the unsplit epilogue does);
     // the logits are written for the record
-    const double rc = p.z_split > 1 ? (double)p.r_out[t] / sqrt((double)H) : 0.0;
+    const double rc = p.z_part ? (double)p.r_out[t] / sqrt((double)H) : 0.0;
     float el[SLOTS];
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) {
       const int e = 32 * s + lane;
       if (e < E) {
         float v;
-        if (p.z_split > 1) {
+        if (p.z_part) {
           float hi = 0.f, lo = 0.f;
           for (int r = 0; r < p.z_split; ++r)
             df_add(hi, lo, p.z_part[((size_t)r * p.T + t) * E + e]);
