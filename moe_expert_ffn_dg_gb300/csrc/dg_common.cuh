@@ -116,6 +116,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   return mbar_wait_for(bar, parity, abort, kWaitLimitNs);
 }
 
+// The same bounded wait for warps that wait long and whose latency matters
+// less (dequantising teams between their stages, epilogues between tiles,
+// producers ahead of their consumers): between polls the warp sleeps for a
+// pause that grows from 32 to max_ns, leaving the issue slots to the warps
+// that work.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort, unsigned max_ns = 256u) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  unsigned ns = 32u;
+  while (true) {
+    __nanosleep(ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (ns < max_ns) ns <<= 1;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 // Limit of the bounded-wait test (GemmParams::test_stall): CTA 0's epilogue
 // waits this long on a barrier nothing arrives on, then reports a timeout
 // and winds the CTA down as any wait that runs out does.

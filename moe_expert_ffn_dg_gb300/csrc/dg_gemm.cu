@@ -378,9 +378,6 @@ __global__ void __launch_bounds__(threads_of<MODE>(), ctas_of<MODE, BN>())
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
-      // the accumulators are free; the split-K sum reads global memory only
-      if constexpr (MODE == 2)
-        if (p.z_split > 1) router_reduce_quarter(p, td, q, lane);
     }
   }
 

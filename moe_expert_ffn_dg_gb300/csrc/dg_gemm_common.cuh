@@ -269,10 +269,11 @@ __device__ __forceinline__ int2 router_krange(const GemmParams& p, int y, int kb
 
 // Router logits (mode 2) from the kRouterAcc accumulators of one tile:
 // lane = expert row of the tile (32q + lane), column = token.  The
-// accumulators are summed as an error-free fp32 pair (TwoSum), scaled by
-// r[t] H^-1/2 in double and rounded once, then the bias is added.
+// accumulators are summed as an error-free fp32 pair (hi, lo) (TwoSum), then
+// z = hi rc + (lo rc + bias) with rc = r[t] H^-1/2 in fp32 (two fused
+// multiply-adds: a few units of fp32 rounding, inside the bound's 2^-17).
 // With a K split the pair's sum is rounded once to fp32 and stored unscaled
-// as the range's partial.
+// as the range's partial; the selection adds the ranges.
 template <int BN>
 __device__ __forceinline__ void epilogue_router(const GemmParams& p, int4 td, uint32_t tbase,
                                                 int ncols, int q, int lane) {
@@ -280,7 +281,7 @@ __device__ __forceinline__ void epilogue_router(const GemmParams& p, int4 td, ui
   const int2 kr = router_krange(p, td.y, p.kb_dense);
   const int nacc = kr.y - kr.x < kRouterAcc ? kr.y - kr.x : kRouterAcc;
   float* part = p.z_split > 1 ? p.z_part + (size_t)(td.y % p.z_split) * p.T * p.z_E : nullptr;
-  const double bias = (p.z_bias && e < p.z_E) ? (double)__ldg(p.z_bias + e) : 0.0;
+  const float bias = (p.z_bias && e < p.z_E) ? __ldg(p.z_bias + e) : 0.f;
   for (int c0 = 0; c0 < ncols; c0 += 16) {
     float hi[16], lo[16];
     __syncwarp();
@@ -304,51 +305,13 @@ __device__ __forceinline__ void epilogue_router(const GemmParams& p, int4 td, ui
       const int t = td.z + c0 + j;
       if (c0 + j < td.w && e < p.z_E) {
         if (part) {
-          part[(size_t)t * p.z_E + e] = (float)((double)hi[j] + (double)lo[j]);
+          part[(size_t)t * p.z_E + e] = __fadd_rn(hi[j], lo[j]);
         } else {
-          const double rc = (double)__ldg(p.z_r + t) * (double)p.z_cH;
-          p.z_out[(size_t)t * p.z_E + e] = (float)(((double)hi[j] + (double)lo[j]) * rc + bias);
+          const float rc = __ldg(p.z_r + t) * p.z_cH;
+          p.z_out[(size_t)t * p.z_E + e] = fmaf(hi[j], rc, fmaf(lo[j], rc, bias));
         }
       }
     }
-  }
-}
-
-// Split-K router logits, after a warp has stored its quarter's partial of
-// the tile: the warp publishes it (fence, then a counter per quarter); the
-// warp whose range completes the quarter adds the ranges' partials in range
-// order (so the result does not depend on which range came last) as an
-// error-free pair, scales by r[t] H^-1/2 in double, rounds once, adds the
-// bias and writes the logits.  No barrier between warps: each warp decides
-// on its own quarter.
-__device__ __forceinline__ void router_reduce_quarter(const GemmParams& p, int4 td, int q,
-                                                      int lane) {
-  __threadfence();  // this lane's partial stores, before the count
-  __syncwarp();
-  const int etile = router_etile(p, td.y);
-  const int key = ((td.z / p.bn) * ((p.z_E + 127) / 128) + etile) * 4 + q;
-  int old = 0;
-  if (lane == 0) old = atomicAdd(p.z_count + key, 1);
-  old = __shfl_sync(0xffffffffu, old, 0);
-  if (old != p.z_split - 1) return;
-  __threadfence();  // the other ranges' partials, after their counts
-  const int e = etile * 128 + 32 * q + lane;
-  if (e >= p.z_E) return;
-  const double bias = p.z_bias ? (double)__ldg(p.z_bias + e) : 0.0;
-  const size_t plane = (size_t)p.T * p.z_E;
-#pragma unroll 2
-  for (int j = 0; j < td.w; ++j) {
-    const int t = td.z + j;
-    float hi = 0.f, lo = 0.f;
-    for (int r = 0; r < p.z_split; ++r) {
-      const float v = __ldcg(p.z_part + r * plane + (size_t)t * p.z_E + e);
-      const float s = __fadd_rn(hi, v);
-      const float bb = __fsub_rn(s, hi);
-      lo = __fadd_rn(lo, __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(v, bb)));
-      hi = s;
-    }
-    const double rc = (double)__ldg(p.z_r + t) * (double)p.z_cH;
-    p.z_out[(size_t)t * p.z_E + e] = (float)(((double)hi + (double)lo) * rc + bias);
   }
 }
 

@@ -56,10 +56,9 @@ struct RouterParams {
   int32_t* flagged;
   int* n_flagged;
   // Split-K router GEMM: z_split K ranges (the bound depends on it); with
-  // z_part non-null the logits come as z_split fp32 partial sums
-  // [z_split, T, E] of sum_i W'_ei h_i, which the selection adds (error-free)
-  // and scales by r H^-1/2 itself, writing the logits; null when the router
-  // GEMM has done that.
+  // z_part non-null (z_split > 1) the logits come as z_split fp32 partial
+  // sums [z_split, T, E] of sum_i W'_ei h_i, which the selection adds
+  // (error-free) and scales by r H^-1/2 itself, writing the logits.
   const float* z_part;
   int z_split;
 };
@@ -142,11 +141,6 @@ struct GemmParams {
   float* z_out;
   float* z_part;
   int z_split;
-  // With z_split > 1: one counter per (token tile, expert tile, 32-expert
-  // quarter), zeroed per forward; the epilogue warp that completes a
-  // quarter's last range adds the ranges' partials in range order and writes
-  // the logits.
-  int* z_count;
   const float* z_r;
   const float* z_bias;
   int z_E;

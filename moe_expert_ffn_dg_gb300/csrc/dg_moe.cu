@@ -25,7 +25,7 @@ const char* const kKernelNames[kNumKernels] = {
 
 struct Layout {
   size_t status, counters, r, xnorm, wnorm, logits, idx, w, chunk_counts, offsets, perm,
-      tok_perm, w_perm, inv, zero16, planes, flagged, zpart, zcount;
+      tok_perm, w_perm, inv, zero16, planes, flagged, zpart;
   size_t xd, xe_perm, act, act_d, y_moe, y_dense, y_perm, hmid, stage_in, stage_out;
   size_t zero_begin, zero_end;  // counters and chunk counts, cleared per forward
   size_t total;
@@ -46,11 +46,8 @@ Layout make_layout(const dg_moe_config_t& c) {
   L.status = take(sizeof(DevStatus));
   L.counters = take(16 * sizeof(int));  // [0] n_refined, [1] flagged tokens
   L.chunk_counts = take(nchunks * E * 4);
-  // router GEMM: completed K ranges per (token tile, expert tile, 32-expert
-  // quarter)
-  L.zcount = take(((T + kRouterBn - 1) / kRouterBn) * ((E + 127) / 128) * 4 * 4);
   L.zero_begin = L.counters;
-  L.zero_end = L.zcount + ((T + kRouterBn - 1) / kRouterBn) * ((E + 127) / 128) * 4 * 4;
+  L.zero_end = L.chunk_counts + nchunks * E * 4;
   L.r = take(T * 4);
   L.xnorm = take(T * 4);
   L.wnorm = take(E * 4);
@@ -360,7 +357,6 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
     g.kb_dense = (int)(2 * H / 64);
     g.z_out = reinterpret_cast<float*>(ws + L.logits);
     g.z_part = reinterpret_cast<float*>(ws + L.zpart);
-    g.z_count = reinterpret_cast<int*>(ws + L.zcount);
     g.z_r = reinterpret_cast<const float*>(ws + L.r);
     g.z_bias = weights->router_bias;
     g.z_E = (int)E;
@@ -489,7 +485,8 @@ dg_status_t forward_impl(dg_moe_t* m, const void* h_in, void* h_out, int n_token
     const int split = router_split(T, E, 2 * H / 64);
     rp.logits_tc = 1;
     rp.planes = reinterpret_cast<uint16_t*>(ws + L.planes);
-    rp.z_split = split;  // for the bound: the router GEMM itself adds the ranges
+    rp.z_split = split;
+    rp.z_part = split > 1 ? reinterpret_cast<const float*>(ws + L.zpart) : nullptr;
     rp.flagged = reinterpret_cast<int32_t*>(ws + L.flagged);
     rp.n_flagged = counters + 1;
     if (err == cudaSuccess) err = launch_router_prep_tc(rp, s);

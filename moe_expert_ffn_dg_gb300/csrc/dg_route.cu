@@ -876,10 +876,10 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
     const float bound = p.logits_tc ? tc_logit_bound(H, p.z_split > 1 ? p.z_split : 1,
                                                      p.router_bias != nullptr)
                                     : (p.router_bias ? kLogitBoundBias : kLogitBoundNoBias);
-    // split-K logits: the partial sums added error-free, then scaled by
-    // r H^-1/2 in double and rounded once (as the unsplit epilogue does);
-    // the logits are written for the record
-    const double rc = p.z_part ? (double)p.r_out[t] / sqrt((double)H) : 0.0;
+    // split-K logits: the partial sums added error-free (hi, lo), then
+    // z = hi rc + (lo rc + bias) in fp32, as the unsplit epilogue does; the
+    // logits are written for the record
+    const float rc = p.z_part ? p.r_out[t] * (float)(1.0 / sqrt((double)H)) : 0.f;
     float el[SLOTS];
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) {
@@ -890,8 +890,7 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
           float hi = 0.f, lo = 0.f;
           for (int r = 0; r < p.z_split; ++r)
             df_add(hi, lo, p.z_part[((size_t)r * p.T + t) * E + e]);
-          v = (float)(((double)hi + (double)lo) * rc +
-                      (p.router_bias ? (double)p.router_bias[e] : 0.0));
+          v = fmaf(hi, rc, fmaf(lo, rc, p.router_bias ? p.router_bias[e] : 0.f));
           if (MODE != 2) p.logits[(size_t)t * E + e] = v;
         } else {
           v = z[e];
