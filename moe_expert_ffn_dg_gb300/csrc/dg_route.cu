@@ -851,14 +851,19 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
   pdl_wait();
   // groups of eight tokens: consecutive ones (modes 0, 1), or the tokens the
   // fast pass flagged (mode 2, a persistent loop over the list)
+  // (mode 2: G flagged tokens a group, as many as spread the list over the
+  // grid, so a short list still uses every block and a token's exact jobs
+  // spread over all eight warps)
   const int nflag = MODE == 2 ? *p.n_flagged : 0;
-  const int ngrp = MODE == 2 ? (nflag + kSelTokens - 1) / kSelTokens : (int)gridDim.x;
+  const int G = MODE == 2 ? min(kSelTokens, max(1, (nflag + (int)gridDim.x - 1) / (int)gridDim.x))
+                          : kSelTokens;
+  const int ngrp = MODE == 2 ? (nflag + G - 1) / G : (int)gridDim.x;
   for (int grp = blockIdx.x; grp < ngrp; grp += (MODE == 2 ? (int)gridDim.x : ngrp)) {
   int t;
   bool valid;
   if (MODE == 2) {
-    const int i = grp * kSelTokens + warp;
-    valid = i < nflag;
+    const int i = grp * G + warp;
+    valid = warp < G && i < nflag;
     t = valid ? p.flagged[i] : 0;
   } else {
     t = grp * kSelTokens + warp;
