@@ -130,20 +130,6 @@ __device__ __forceinline__ void sts_u32x4(uint32_t addr, uint32_t a, uint32_t b,
                : "memory");
 }
 
-// Shared-memory loads named as such: the stage pointers derive from an
-// address aligned through an integer, so the compiler cannot tell they are
-// shared and would issue generic loads.
-__device__ __forceinline__ uint32_t lds_u16(const void* p) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(smem_u32(p)) : "memory");
-  return v;
-}
-__device__ __forceinline__ uint32_t lds_u32(const void* p) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
-  return v;
-}
-
 __device__ __forceinline__ void lds_u32x4(const uint8_t* p, uint32_t (&w)[4]) {
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
@@ -657,13 +643,13 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
               uint32_t w0[4], w1[4];
               lds_u32x4(qrow + (((2 * gs) ^ rsw) << 4), w0);
               lds_u32x4(qrow + (((2 * gs + 1) ^ rsw) << 4), w1);
-              const uint32_t e4 = lds_u32(e4_row + 4 * g);
+              const uint32_t e4 = *reinterpret_cast<const uint32_t*>(e4_row + 4 * g);
               dequant32_nvfp4(w0, e4m3_to_f32(e4 & 0xFFu), e4m3_to_f32((e4 >> 8) & 0xFFu),
                               *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
               dequant32_nvfp4(w1, e4m3_to_f32((e4 >> 16) & 0xFFu), e4m3_to_f32(e4 >> 24),
                               *reinterpret_cast<uint32_t(*)[16]>(&o[16]));
             } else if (QF == 4) {  // the group's 32 bytes: chunks 2gs, 2gs + 1
-              const uint32_t s = lds_u16(sc_row + g), b = lds_u16(bi_row + g);
+              const uint32_t s = sc_row[g], b = bi_row[g];
               const uint32_t s2 = s | (s << 16), b2 = b | (b << 16);
               uint32_t w0[4], w1[4];
               lds_u32x4(qrow + (((2 * gs) ^ rsw) << 4), w0);
@@ -671,7 +657,7 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
               dequant32(w0, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[0]));
               dequant32(w1, s2, b2, *reinterpret_cast<uint32_t(*)[16]>(&o[16]));
             } else {  // 64 bytes: chunks 4gs .. 4gs + 3
-              const uint32_t s = lds_u16(sc_row + g), b = lds_u16(bi_row + g);
+              const uint32_t s = sc_row[g], b = bi_row[g];
               const uint32_t s2 = s | (s << 16), b2 = b | (b << 16);
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
