@@ -102,6 +102,9 @@ struct GemmParams {
   CUtensorMap xb_exp16;
   CUtensorMap xb_d64;
   CUtensorMap xb_d16;
+  // 256-row boxes of the same tensors: a full 256-token stage in one copy
+  CUtensorMap xb_exp256;
+  CUtensorMap xb_d256;
   // Tiles, decoded in each CTA from the expert offsets: first the dense tiles
   // (ceil(T/bn) token tiles x mt_dense feature tiles), then per expert e
   // ceil(n_e/bn) token tiles x mt_exp feature tiles, feature tile fastest.

@@ -243,11 +243,13 @@ dg_status_t dg_sc_mlp_create(const dg_sc_mlp_config_t* cfg, const dg_sc_mlp_weig
   }
   ok = ok && encode_bf16_rows(&m->gu.xb_d64, ws + L.x, T, H, 64);
   ok = ok && encode_bf16_rows(&m->gu.xb_d16, ws + L.x, T, H, 16);
+  ok = ok && encode_bf16_rows(&m->gu.xb_d256, ws + L.x, T, H, 256);
   // down: [H, D] in 128-row boxes over act
   if (q4) ok = ok && encode_q4_rows(&m->dn.wa_d0, weights->down.q, H, D, 128);
   else ok = ok && encode_bf16_rows(&m->dn.wa_d0, weights->down.q, H, D, 128);
   ok = ok && encode_bf16_rows(&m->dn.xb_d64, ws + L.act, T, D, 64);
   ok = ok && encode_bf16_rows(&m->dn.xb_d16, ws + L.act, T, D, 16);
+  ok = ok && encode_bf16_rows(&m->dn.xb_d256, ws + L.act, T, D, 256);
   if (!ok) {
     delete m;
     return DG_ERR_CUDA;
@@ -256,12 +258,14 @@ dg_status_t dg_sc_mlp_create(const dg_sc_mlp_config_t* cfg, const dg_sc_mlp_weig
   m->gu.wa_exp = m->gu.wa_d0;
   m->gu.xb_exp64 = m->gu.xb_d64;
   m->gu.xb_exp16 = m->gu.xb_d16;
+  m->gu.xb_exp256 = m->gu.xb_d256;
   m->dn.wa_exp = m->dn.wa_d0;
   m->dn.wa_d1 = m->dn.wa_d0;
   m->dn.wa_d5 = m->dn.wa_d0;
   m->dn.dense_5d = 0;
   m->dn.xb_exp64 = m->dn.xb_d64;
   m->dn.xb_exp16 = m->dn.xb_d16;
+  m->dn.xb_exp256 = m->dn.xb_d256;
   if (cudaMemset(ws + L.status, 0, sizeof(DevStatus)) != cudaSuccess ||
       cudaMemset(ws + L.zero, 0, 16) != cudaSuccess) {
     delete m;
