@@ -154,14 +154,14 @@ __global__ void __launch_bounds__(threads_of<MODE>(), ctas_of<MODE, BN>())
         const int kbn = dense ? p.kb_dense : p.kb_exp;
         // router: this tile's K range (split-K) and expert tile
         const int2 kr = MODE == 2 ? router_krange(p, td.y, kbn) : make_int2(0, kbn);
-        // a full 256-row token tile in one box (projections), else 64-row
-        // then 16-row boxes
-        const bool full256 = MODE != 2 && BN == 256 && td.w == 256;
-        const int nb64 = full256 ? 0 : td.w / 64;
-        const int nb16 = full256 ? 0 : (td.w - 64 * nb64 + kBoxRows - 1) / kBoxRows;
+        // a full BN-row token tile in one box (projections), else 64-row then
+        // 16-row boxes
+        const bool whole = MODE != 2 && td.w == BN;
+        const int nb64 = whole ? 0 : td.w / 64;
+        const int nb16 = whole ? 0 : (td.w - 64 * nb64 + kBoxRows - 1) / kBoxRows;
         const uint32_t bytes =
-            kATileBytes + (full256 ? 256u * 128u : nb64 * 64 * 128 + nb16 * kBoxBytes);
-        const CUtensorMap* mb256 = dense ? &p.xb_d256 : &p.xb_exp256;
+            kATileBytes + (whole ? BN * 128u : nb64 * 64 * 128 + nb16 * kBoxBytes);
+        const CUtensorMap* mbf = full_stage_map<BN>(p, dense);
         const CUtensorMap* mb64 = dense ? &p.xb_d64 : &p.xb_exp64;
         const CUtensorMap* mb16 = dense ? &p.xb_d16 : &p.xb_exp16;
         for (int kb = kr.x; kb < kr.y; ++kb) {
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), ctas_of<MODE, BN>())
           }
           // router: the token rows [h | h] along K against the planes (hi | lo)
           const int xb = MODE == 2 ? x % p.H : x;
-          if (full256) tma_load_2d_hint(mb256, &full[stage], b_dst, xb, td.z, pol_x);
+          if (whole) tma_load_2d_hint(mbf, &full[stage], b_dst, xb, td.z, pol_x);
           for (int j = 0; j < nb64; ++j)
             tma_load_2d_hint(mb64, &full[stage], b_dst + j * 64 * 128, xb, td.z + 64 * j, pol_x);
           for (int j = 0; j < nb16; ++j)

@@ -108,6 +108,15 @@ __device__ __forceinline__ bool handoff(bool stop) {
       : "memory");
   return r != 0;
 }
+// The map whose box is a whole BN-row token stage (BN 32, 64, 128 or 256).
+template <int BN>
+__device__ __forceinline__ const CUtensorMap* full_stage_map(const GemmParams& p, bool dense) {
+  if (BN == 256) return dense ? &p.xb_d256 : &p.xb_exp256;
+  if (BN == 128) return dense ? &p.xb_d128 : &p.xb_exp128;
+  if (BN == 64) return dense ? &p.xb_d64 : &p.xb_exp64;
+  return dense ? &p.xb_d32 : &p.xb_exp32;
+}
+
 // Wait that ignores the abort flag (used to drain in-flight copies and MMAs
 // before the CTA exits); bounded by kWaitLimitNs.
 __device__ __forceinline__ bool wait_no_abort(uint64_t* bar, uint32_t parity) {

@@ -293,10 +293,8 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
     tma_prefetch_map(&p.xb_exp16);
     tma_prefetch_map(&p.xb_d64);
     tma_prefetch_map(&p.xb_d16);
-    if (BN == 256) {
-      tma_prefetch_map(&p.xb_exp256);
-      tma_prefetch_map(&p.xb_d256);
-    }
+    tma_prefetch_map(full_stage_map<BN>(p, false));
+    tma_prefetch_map(full_stage_map<BN>(p, true));
   }
   if (warp == 2) {
     tmem_alloc(tmem_holder, 512);
@@ -442,12 +440,12 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
         const int4 td = decode_tile(p, tile, nd, s_start, s_off);
         const bool dense = td.x == p.E;
         const int ng = dense ? p.kb_dense : p.kb_exp;
-        // a full 256-row stage in one box, else 64-row then 16-row boxes
-        const bool full256 = BN == 256 && td.w == 256;
-        const int nb64 = full256 ? 0 : td.w / 64;
-        const int nb16 = full256 ? 0 : (td.w - 64 * nb64 + kBoxRows - 1) / kBoxRows;
-        const uint32_t group_bytes = full256 ? 256u * 128u : nb64 * 64 * 128 + nb16 * kBoxBytes;
-        const CUtensorMap* mb256 = dense ? &p.xb_d256 : &p.xb_exp256;
+        // a full BN-row stage in one box, else 64-row then 16-row boxes
+        const bool full = td.w == BN;
+        const int nb64 = full ? 0 : td.w / 64;
+        const int nb16 = full ? 0 : (td.w - 64 * nb64 + kBoxRows - 1) / kBoxRows;
+        const uint32_t group_bytes = full ? BN * 128u : nb64 * 64 * 128 + nb16 * kBoxBytes;
+        const CUtensorMap* mbf = full_stage_map<BN>(p, dense);
         const CUtensorMap* mb64 = dense ? &p.xb_d64 : &p.xb_exp64;
         const CUtensorMap* mb16 = dense ? &p.xb_d16 : &p.xb_exp16;
         const int nst = (ng + GPS - 1) / GPS;
@@ -466,7 +464,7 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
           for (int gi = 0; gi < ngk; ++gi) {
             uint8_t* b_dst = sB + (size_t)bs * C::kBStageBytes + (size_t)gi * C::kBGroupBytes;
             const int x = 64 * (GPS * k + gi);
-            if (full256) tma_load_2d_hint(mb256, &bfull[bs], b_dst, x, td.z, pol_x);
+            if (full) tma_load_2d_hint(mbf, &bfull[bs], b_dst, x, td.z, pol_x);
             for (int r = 0; r < nb64; ++r)
               tma_load_2d_hint(mb64, &bfull[bs], b_dst + r * 64 * 128, x, td.z + 64 * r, pol_x);
             for (int r = 0; r < nb16; ++r)

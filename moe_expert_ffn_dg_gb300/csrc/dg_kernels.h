@@ -102,9 +102,14 @@ struct GemmParams {
   CUtensorMap xb_exp16;
   CUtensorMap xb_d64;
   CUtensorMap xb_d16;
-  // 256-row boxes of the same tensors: a full 256-token stage in one copy
+  // Boxes of a whole tile width (256, 128 and 32 rows) of the same tensors:
+  // a full token stage in one copy (64-row stages use the 64-row maps)
   CUtensorMap xb_exp256;
   CUtensorMap xb_d256;
+  CUtensorMap xb_exp128;
+  CUtensorMap xb_d128;
+  CUtensorMap xb_exp32;
+  CUtensorMap xb_d32;
   // Tiles, decoded in each CTA from the expert offsets: first the dense tiles
   // (ceil(T/bn) token tiles x mt_dense feature tiles), then per expert e
   // ceil(n_e/bn) token tiles x mt_exp feature tiles, feature tile fastest.

@@ -264,8 +264,12 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
   ok = ok && encode_bf16_rows(&m->gu.xb_exp16, ws + L.xe_perm, TK, H, 16);
   ok = ok && encode_bf16_rows(&m->gu.xb_d64, ws + L.xd, T, H, 64);
   ok = ok && encode_bf16_rows(&m->gu.xb_d16, ws + L.xd, T, H, 16);
-  ok = ok && encode_bf16_rows(&m->gu.xb_exp256, ws + L.xe_perm, TK, H, 256);
-  ok = ok && encode_bf16_rows(&m->gu.xb_d256, ws + L.xd, T, H, 256);
+  for (const uint32_t br : {256u, 128u, 32u}) {
+    CUtensorMap* me = br == 256 ? &m->gu.xb_exp256 : br == 128 ? &m->gu.xb_exp128 : &m->gu.xb_exp32;
+    CUtensorMap* md = br == 256 ? &m->gu.xb_d256 : br == 128 ? &m->gu.xb_d128 : &m->gu.xb_d32;
+    ok = ok && encode_bf16_rows(me, ws + L.xe_perm, TK, H, br);
+    ok = ok && encode_bf16_rows(md, ws + L.xd, T, H, br);
+  }
   // down A: [E*H, I] and [H, D] in 128-row boxes; B: act / act_d rows
   if (q4) {
     ok = ok && encode_q4_rows(&m->dn.wa_exp, weights->down.q, E * H, I, 128);
@@ -281,8 +285,12 @@ dg_status_t dg_moe_create(const dg_moe_config_t* cfg, const dg_moe_weights_t* we
   ok = ok && encode_bf16_rows(&m->dn.xb_exp16, ws + L.act, TK, I, 16);
   ok = ok && encode_bf16_rows(&m->dn.xb_d64, ws + L.act_d, T, D, 64);
   ok = ok && encode_bf16_rows(&m->dn.xb_d16, ws + L.act_d, T, D, 16);
-  ok = ok && encode_bf16_rows(&m->dn.xb_exp256, ws + L.act, TK, I, 256);
-  ok = ok && encode_bf16_rows(&m->dn.xb_d256, ws + L.act_d, T, D, 256);
+  for (const uint32_t br : {256u, 128u, 32u}) {
+    CUtensorMap* me = br == 256 ? &m->dn.xb_exp256 : br == 128 ? &m->dn.xb_exp128 : &m->dn.xb_exp32;
+    CUtensorMap* md = br == 256 ? &m->dn.xb_d256 : br == 128 ? &m->dn.xb_d128 : &m->dn.xb_d32;
+    ok = ok && encode_bf16_rows(me, ws + L.act, TK, I, br);
+    ok = ok && encode_bf16_rows(md, ws + L.act_d, T, D, br);
+  }
   if (!ok) {
     delete m;
     return DG_ERR_CUDA;
@@ -505,7 +513,8 @@ dg_status_t forward_impl(dg_moe_t* m, const void* h_in, void* h_out, int n_token
       return cuda_fail(m, "router token map", cudaErrorInvalidValue);
     gr.xb_exp64 = gr.xb_d64;
     gr.xb_exp16 = gr.xb_d16;
-    gr.xb_exp256 = gr.xb_d256 = gr.xb_d64;  // not used by the router GEMM
+    // (whole-tile maps are not used by the router GEMM)
+    gr.xb_exp256 = gr.xb_d256 = gr.xb_exp128 = gr.xb_d128 = gr.xb_exp32 = gr.xb_d32 = gr.xb_d64;
     if (err == cudaSuccess) err = launch_gemm(2, kRouterBn, gr, m->num_sms, s);
   } else if (err == cudaSuccess) {
     // small batches: the CUDA-core logit kernel (latency-bound either way,

@@ -244,12 +244,16 @@ dg_status_t dg_sc_mlp_create(const dg_sc_mlp_config_t* cfg, const dg_sc_mlp_weig
   ok = ok && encode_bf16_rows(&m->gu.xb_d64, ws + L.x, T, H, 64);
   ok = ok && encode_bf16_rows(&m->gu.xb_d16, ws + L.x, T, H, 16);
   ok = ok && encode_bf16_rows(&m->gu.xb_d256, ws + L.x, T, H, 256);
+  ok = ok && encode_bf16_rows(&m->gu.xb_d128, ws + L.x, T, H, 128);
+  ok = ok && encode_bf16_rows(&m->gu.xb_d32, ws + L.x, T, H, 32);
   // down: [H, D] in 128-row boxes over act
   if (q4) ok = ok && encode_q4_rows(&m->dn.wa_d0, weights->down.q, H, D, 128);
   else ok = ok && encode_bf16_rows(&m->dn.wa_d0, weights->down.q, H, D, 128);
   ok = ok && encode_bf16_rows(&m->dn.xb_d64, ws + L.act, T, D, 64);
   ok = ok && encode_bf16_rows(&m->dn.xb_d16, ws + L.act, T, D, 16);
   ok = ok && encode_bf16_rows(&m->dn.xb_d256, ws + L.act, T, D, 256);
+  ok = ok && encode_bf16_rows(&m->dn.xb_d128, ws + L.act, T, D, 128);
+  ok = ok && encode_bf16_rows(&m->dn.xb_d32, ws + L.act, T, D, 32);
   if (!ok) {
     delete m;
     return DG_ERR_CUDA;
@@ -259,6 +263,8 @@ dg_status_t dg_sc_mlp_create(const dg_sc_mlp_config_t* cfg, const dg_sc_mlp_weig
   m->gu.xb_exp64 = m->gu.xb_d64;
   m->gu.xb_exp16 = m->gu.xb_d16;
   m->gu.xb_exp256 = m->gu.xb_d256;
+  m->gu.xb_exp128 = m->gu.xb_d128;
+  m->gu.xb_exp32 = m->gu.xb_d32;
   m->dn.wa_exp = m->dn.wa_d0;
   m->dn.wa_d1 = m->dn.wa_d0;
   m->dn.wa_d5 = m->dn.wa_d0;
@@ -266,6 +272,8 @@ dg_status_t dg_sc_mlp_create(const dg_sc_mlp_config_t* cfg, const dg_sc_mlp_weig
   m->dn.xb_exp64 = m->dn.xb_d64;
   m->dn.xb_exp16 = m->dn.xb_d16;
   m->dn.xb_exp256 = m->dn.xb_d256;
+  m->dn.xb_exp128 = m->dn.xb_d128;
+  m->dn.xb_exp32 = m->dn.xb_d32;
   if (cudaMemset(ws + L.status, 0, sizeof(DevStatus)) != cudaSuccess ||
       cudaMemset(ws + L.zero, 0, 16) != cudaSuccess) {
     delete m;
