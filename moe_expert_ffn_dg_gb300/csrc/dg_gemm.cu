@@ -154,9 +154,9 @@ __global__ void __launch_bounds__(threads_of<MODE>(), ctas_of<MODE, BN>())
         const int kbn = dense ? p.kb_dense : p.kb_exp;
         // router: this tile's K range (split-K) and expert tile
         const int2 kr = MODE == 2 ? router_krange(p, td.y, kbn) : make_int2(0, kbn);
-        // a full BN-row token tile in one box (projections), else 64-row then
-        // 16-row boxes
-        const bool whole = MODE != 2 && td.w == BN;
+        // a full token tile of 128 or 256 rows in one box (projections), else
+        // 64-row then 16-row boxes
+        const bool whole = MODE != 2 && BN >= 128 && td.w == BN;
         const int nb64 = whole ? 0 : td.w / 64;
         const int nb16 = whole ? 0 : (td.w - 64 * nb64 + kBoxRows - 1) / kBoxRows;
         const uint32_t bytes =

@@ -440,8 +440,9 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
         const int4 td = decode_tile(p, tile, nd, s_start, s_off);
         const bool dense = td.x == p.E;
         const int ng = dense ? p.kb_dense : p.kb_exp;
-        // a full BN-row stage in one box, else 64-row then 16-row boxes
-        const bool full = td.w == BN;
+        // a full stage of 128 or 256 rows in one box (measured: faster there,
+        // slower than two 16-row boxes at 32), else 64-row then 16-row boxes
+        const bool full = BN >= 128 && td.w == BN;
         const int nb64 = full ? 0 : td.w / 64;
         const int nb16 = full ? 0 : (td.w - 64 * nb64 + kBoxRows - 1) / kBoxRows;
         const uint32_t group_bytes = full ? BN * 128u : nb64 * 64 * 128 + nb16 * kBoxBytes;

@@ -102,8 +102,9 @@ struct GemmParams {
   CUtensorMap xb_exp16;
   CUtensorMap xb_d64;
   CUtensorMap xb_d16;
-  // Boxes of a whole tile width (256, 128 and 32 rows) of the same tensors:
-  // a full token stage in one copy (64-row stages use the 64-row maps)
+  // Boxes of a whole tile width (256 and 128 rows; 32 is encoded but measured
+  // slower than two 16-row boxes) of the same tensors: a full token stage in
+  // one copy
   CUtensorMap xb_exp256;
   CUtensorMap xb_d256;
   CUtensorMap xb_exp128;
