@@ -56,6 +56,26 @@
 // TMEM is released).
 #include "dg_gemm_common.cuh"
 
+// Cycle accounting of the pipeline roles, compiled in only with
+// -DDG_Q4_TIMING=1 (off by default: it adds clock reads and atomics).
+// Slots (cycles summed over the warps that record them; [15] counts
+// stages): 0 dequant waits for its scales, 1 for a code slab, 2 for its A
+// slot (the MMAs of its previous stage), 3 dequantising and storing a stage,
+// 4 fence and arrive; 5 waiter on the accumulators, 6 on an A stage, 7 on a
+// token stage; 8 issuer at the hand-off barrier.  Read with
+// dg_q4_timing_read() (exported only in such a build).
+#ifndef DG_Q4_TIMING
+#define DG_Q4_TIMING 0
+#endif
+#if DG_Q4_TIMING
+__device__ unsigned long long g_q4_timing[16];
+#define DG_T0(v) const long long v = clock64()
+#define DG_TADD(slot, v) atomicAdd(&g_q4_timing[slot], (unsigned long long)(clock64() - (v)))
+#else
+#define DG_T0(v)
+#define DG_TADD(slot, v)
+#endif
+
 namespace dg {
 namespace {
 
@@ -503,7 +523,10 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
       const uint32_t idesc = idesc_bf16_f32(128, nb * kBoxRows);
       const int nst = (ng + GPS - 1) / GPS;
       for (int k = 0; k < nst; ++k, ++st) {
-        if (handoff(false)) {
+        DG_T0(t_ho);
+        const bool ho_stop = handoff(false);
+        if (lane == 0) DG_TADD(8, t_ho);
+        if (ho_stop) {
           stop = true;
           break;
         }
@@ -560,18 +583,24 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
         const uint32_t as = (uint32_t)team + NT * (n % C::kM);
         const uint32_t aph = (n / C::kM) & 1u;
         cnt += 1ull << (16 * team);
+        DG_T0(t_w0);
         if (k == 0 && !mbar_wait(&acc_empty[acc], (use & 1u) ^ 1u, abort_flag)) {
           ok = false;
           what = 0xffffffffu;
         }
+        if (lane == 0) DG_TADD(5, t_w0);
+        DG_T0(t_w1);
         if (ok && !mbar_wait(&afull[as], aph, abort_flag)) {
           ok = false;
           what = 0x10000u + k;
         }
+        if (lane == 0) DG_TADD(6, t_w1);
+        DG_T0(t_w2);
         if (ok && !mbar_wait(&bfull[bs], bph, abort_flag)) {
           ok = false;
           what = 0x20000u + k;
         }
+        if (lane == 0) DG_TADD(7, t_w2);
         if (++bs == NB) {
           bs = 0;
           bph ^= 1u;
@@ -606,7 +635,10 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
       const int nsl = (ng + GPSL - 1) / GPSL;
       const int ss = local & 1;
       const uint32_t sph = (uint32_t)(local >> 1) & 1u;
-      if (!mbar_wait(&sfull[ss], sph, abort_flag)) {
+      DG_T0(t_sf);
+      const bool sf_ok = mbar_wait(&sfull[ss], sph, abort_flag);
+      if (lane == 0) DG_TADD(0, t_sf);
+      if (!sf_ok) {
         if (lane == 0) report(p.status, kDevTimeout, kSiteGemmDequant, (unsigned)tile, 0xffffu);
         *abort_flag = 1;
         break;
@@ -617,7 +649,10 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
       // NVFP4: this row's e4m3 block scales, 4 per group
       const uint8_t* e4_row = sScale + (size_t)ss * 2 * slot_bytes + (size_t)row * 4 * ng;
       for (int sl = 0; sl < nsl && ok; ++sl) {
-        if (!mbar_wait(&qfull[qs], qph, abort_flag)) {
+        DG_T0(t_qf);
+        const bool qf_ok = mbar_wait(&qfull[qs], qph, abort_flag);
+        if (lane == 0) DG_TADD(1, t_qf);
+        if (!qf_ok) {
           if (lane == 0) report(p.status, kDevTimeout, kSiteGemmDequant, (unsigned)tile, (unsigned)sl);
           *abort_flag = 1;
           ok = false;
@@ -634,7 +669,12 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
           const uint32_t w = stg - (uint32_t)(C::kM * NT);
           const bool first_use = j < (uint32_t)C::kM;
           ++j;
-          if (!first_use && !mbar_wait(&sdone[w % kStageRing], (w / kStageRing) & 1u, abort_flag)) {
+          DG_T0(t_sd);
+          const bool sd_ok =
+              first_use || mbar_wait(&sdone[w % kStageRing], (w / kStageRing) & 1u, abort_flag);
+          if (lane == 0) DG_TADD(2, t_sd);
+          DG_T0(t_dq);
+          if (!sd_ok) {
             if (lane == 0)
               report(p.status, kDevTimeout, kSiteGemmDequant, (unsigned)tile, 0x10000u + k);
             *abort_flag = 1;
@@ -679,10 +719,16 @@ __global__ void __launch_bounds__(CfgQ<BN>::kThreads, 1)
               sts_u32x4(dst + (uint32_t)((ch ^ rsw) << 4), o[4 * ch], o[4 * ch + 1],
                         o[4 * ch + 2], o[4 * ch + 3]);
           }
+          if (lane == 0) DG_TADD(3, t_dq);
+          DG_T0(t_fa);
           // make the generic-proxy stores visible to the tensor core
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&afull[as]);
+          if (lane == 0) DG_TADD(4, t_fa);
+#if DG_Q4_TIMING
+          if (lane == 0) atomicAdd(&g_q4_timing[15], 1ull);
+#endif
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&qempty[qs]);
@@ -810,3 +856,15 @@ cudaError_t launch_gemm_affine(int mode, int bn, int qf, const GemmParams& p, in
 }
 
 }  // namespace dg
+
+#if DG_Q4_TIMING
+extern "C" int dg_q4_timing_read(unsigned long long* out16, int reset) {
+  if (cudaMemcpyFromSymbol(out16, g_q4_timing, 16 * sizeof(unsigned long long)) != cudaSuccess)
+    return 1;
+  if (reset) {
+    static const unsigned long long zero[16] = {};
+    if (cudaMemcpyToSymbol(g_q4_timing, zero, sizeof(zero)) != cudaSuccess) return 1;
+  }
+  return 0;
+}
+#endif
