@@ -25,6 +25,10 @@ struct RouterParams {
   int T, H, E, K;
   int router_u8;
   float eps;
+  // H^-1/2 rounded to fp32 and to fp64, computed on the host: square root
+  // and division in double are slow on this part, and every thread needs them
+  float cH;
+  double cHd;
   float* r_out;      // [T] 1/rms(h)
   float* xnorm_out;  // [T] |router input|
   float* wnorm_out;  // [E] |router row|

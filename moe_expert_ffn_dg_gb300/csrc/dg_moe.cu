@@ -463,6 +463,8 @@ dg_status_t forward_impl(dg_moe_t* m, const void* h_in, void* h_out, int n_token
   rp.router_bias = m->w.router_bias;
   rp.T = T;
   rp.H = H;
+  rp.cHd = 1.0 / sqrt((double)H);
+  rp.cH = (float)rp.cHd;
   rp.E = E;
   rp.K = K;
   rp.router_u8 = c.router_fmt == DG_FMT_AFFINE_U8_G64;

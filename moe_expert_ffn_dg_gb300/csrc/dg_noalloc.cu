@@ -155,6 +155,8 @@ extern "C" dg_status_t dg_moe_route_noalloc(const dg_moe_config_t* cfg,
   rp.router_bias = weights->router_bias;
   rp.T = n_tokens;
   rp.H = H;
+  rp.cHd = 1.0 / sqrt((double)H);
+  rp.cH = (float)rp.cHd;
   rp.E = E;
   rp.K = K;
   rp.router_u8 = u8 ? 1 : 0;

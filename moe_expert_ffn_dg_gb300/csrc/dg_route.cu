@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(256) k_router_prep_tc(const RouterParams p, in
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = p.H, nvec = H >> 3;
-  const float cH = (float)(1.0 / sqrt((double)H));
+  const float cH = p.cH;
   if ((int)blockIdx.x < nbt) {
     const int t = blockIdx.x * 8 + warp;
     if (t >= p.T) return;
@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(256) k_router_logits(const RouterParams p) {
   const int t0 = blockIdx.x * TB;
   const bool first_col = blockIdx.y == 0;
   const int nvec = H >> 3;
-  const float cH = (float)(1.0 / sqrt((double)H));
+  const float cH = p.cH;
   const int ngroups = H >> 6;
 
   // thread (expert el, slice j); its first weight runs are requested before
@@ -556,7 +556,7 @@ __global__ void __launch_bounds__(256, 3) k_router_logits_tile(const RouterParam
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int t0 = blockIdx.x * kRT, e0 = blockIdx.y * kRE;
   const bool first_col = blockIdx.y == 0;
-  const float cH = (float)(1.0 / sqrt((double)H));
+  const float cH = p.cH;
   const int nvec = H >> 3;
   pdl_trigger();
   pdl_wait();
@@ -884,7 +884,7 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
     // split-K logits: the partial sums added error-free (hi, lo), then
     // z = hi rc + (lo rc + bias) in fp32, as the unsplit epilogue does; the
     // logits are written for the record
-    const float rc = p.z_part ? p.r_out[t] * (float)(1.0 / sqrt((double)H)) : 0.f;
+    const float rc = p.z_part ? p.r_out[t] * p.cH : 0.f;
     float el[SLOTS];
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) {
@@ -1056,7 +1056,7 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
     }
     __syncthreads();
     // exact logit = dot * (1/rms) * H^-1/2 + bias
-    const double cHd = 1.0 / sqrt((double)H);
+    const double cHd = p.cHd;
     for (int i = threadIdx.x; i < kSelTokens * 256; i += blockDim.x) {
       const int w = i >> 8, c = i & 255;
       if (c < s_ncand[w]) {
