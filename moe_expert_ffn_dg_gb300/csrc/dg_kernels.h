@@ -248,9 +248,11 @@ cudaError_t launch_router_prep_tc(const RouterParams& p, cudaStream_t s);
 
 // K ranges of the router GEMM (kb = 2H / 64 K blocks): the fewest that keep
 // an accumulator to kRouterMaxAccMmas MMAs (the bound of the logits), none
-// empty.  More ranges would give more CTAs but more partial sums for the
-// selection to add, which costs more than it saves.
-constexpr int kRouterMaxAccMmas = 44;
+// empty.  Fewer MMAs an accumulator tighten the bound, so fewer tokens take
+// the exact re-check, but give more partial sums to write and add: of 44, 24
+// and 12 (four, eight and fifteen ranges at H = 2816), 24 measured fastest
+// at 1024, 2048 and 16 384 tokens.
+constexpr int kRouterMaxAccMmas = 24;
 inline int router_split(int T, int E, int kb) {
   (void)T;
   (void)E;

@@ -212,11 +212,20 @@ def test_batch2048_zipf_beta1_stress():
     assert counts.max() == wl.tokens and int((counts == 0).sum()) == wl.n_experts - wl.top_k
 
 
+def _max_acc_mmas():
+    """kRouterMaxAccMmas, read from the kernels' header."""
+    import os
+    import re
+    hdr = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                       "moe_expert_ffn_dg_gb300", "csrc", "dg_kernels.h")
+    return int(re.search(r"constexpr int kRouterMaxAccMmas = (\d+);", open(hdr).read()).group(1))
+
+
 def router_split(T, E, H):
     """K ranges of the router GEMM (two accumulators): the fewest that keep
-    44 MMAs an accumulator, none empty."""
+    at most kRouterMaxAccMmas MMAs an accumulator, none empty."""
     kb = 2 * H // 64
-    s = max(1, -(-kb // 22))
+    s = max(1, -(-kb // (2 * (_max_acc_mmas() // 4))))
     while s > 1 and (s - 1) * -(-kb // s) >= kb:
         s -= 1
     return s
