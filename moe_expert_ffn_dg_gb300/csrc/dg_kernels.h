@@ -36,6 +36,9 @@ struct RouterParams {
   float* w;          // [T, K]
   float* logits;     // [T, E] fp32 logits
   int32_t* chunk_counts;  // [nchunks, E] expert histogram per 256 tokens (zeroed)
+  // [nchunks, E, 8]: per 256-token chunk and expert, a bit per token that
+  // chose the expert (zeroed), or null
+  uint32_t* chunk_masks;
   uint16_t* xd;      // bf16 [T, H]
   // Fused attention half of the decoder layer: with attn non-null, h is the
   // layer input (the attention residual) and the block input is built as
@@ -71,6 +74,7 @@ struct ScatterParams {
   const int32_t* idx;        // [T, K]
   const float* w;            // [T, K]
   const int32_t* chunk_counts;  // [nchunks, E]
+  const uint32_t* chunk_masks;  // [nchunks, E, 8] token bits of each chunk and expert
   int T, K, E;
   int32_t* offsets;          // [E + 1]
   int32_t* perm;             // [T*K]

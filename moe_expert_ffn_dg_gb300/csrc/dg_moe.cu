@@ -24,10 +24,10 @@ const char* const kKernelNames[kNumKernels] = {
 
 
 struct Layout {
-  size_t status, counters, r, xnorm, wnorm, logits, idx, w, chunk_counts, offsets, perm,
+  size_t status, counters, r, xnorm, wnorm, logits, idx, w, chunk_counts, chunk_masks, offsets, perm,
       tok_perm, w_perm, inv, zero16, planes, flagged, zpart;
   size_t xd, xe_perm, act, act_d, y_moe, y_dense, y_perm, hmid, stage_in, stage_out;
-  size_t zero_begin, zero_end;  // counters and chunk counts, cleared per forward
+  size_t zero_begin, zero_end;  // counters, chunk counts and masks, cleared per forward
   size_t total;
 };
 
@@ -46,8 +46,9 @@ Layout make_layout(const dg_moe_config_t& c) {
   L.status = take(sizeof(DevStatus));
   L.counters = take(16 * sizeof(int));  // [0] n_refined, [1] flagged tokens
   L.chunk_counts = take(nchunks * E * 4);
+  L.chunk_masks = take(nchunks * E * (kChunkTokens / 32) * 4);
   L.zero_begin = L.counters;
-  L.zero_end = L.chunk_counts + nchunks * E * 4;
+  L.zero_end = L.chunk_masks + nchunks * E * (kChunkTokens / 32) * 4;
   L.r = take(T * 4);
   L.xnorm = take(T * 4);
   L.wnorm = take(E * 4);
@@ -476,6 +477,7 @@ dg_status_t forward_impl(dg_moe_t* m, const void* h_in, void* h_out, int n_token
   rp.w = reinterpret_cast<float*>(ws + L.w);
   rp.logits = reinterpret_cast<float*>(ws + L.logits);
   rp.chunk_counts = reinterpret_cast<int32_t*>(ws + L.chunk_counts);
+  rp.chunk_masks = reinterpret_cast<uint32_t*>(ws + L.chunk_masks);
   rp.xd = reinterpret_cast<uint16_t*>(ws + L.xd);
   // large batches: weighted expert rows summed by the combine, no
   // accumulator to clear; small ones: atomic adds into the cleared y_moe
@@ -531,6 +533,7 @@ dg_status_t forward_impl(dg_moe_t* m, const void* h_in, void* h_out, int n_token
   sp.idx = rp.idx;
   sp.w = rp.w;
   sp.chunk_counts = reinterpret_cast<const int32_t*>(ws + L.chunk_counts);
+  sp.chunk_masks = reinterpret_cast<const uint32_t*>(ws + L.chunk_masks);
   sp.T = T;
   sp.K = K;
   sp.E = E;

@@ -1128,6 +1128,10 @@ __global__ void __launch_bounds__(256) k_router_select(const RouterParams p) {
       p.idx[(size_t)t * K + rank] = e;
       p.w[(size_t)t * K + rank] = ex[s] / se * bf16_to_f32(p.pes[e]);
       atomicAdd(&p.chunk_counts[(size_t)(t / kChunkTokens) * E + e], 1);
+      if (p.chunk_masks)
+        atomicOr(&p.chunk_masks[((size_t)(t / kChunkTokens) * E + e) * (kChunkTokens / 32) +
+                                ((t % kChunkTokens) >> 5)],
+                 1u << (t & 31));
     }
     running += __popc(ms);
   }
@@ -1222,16 +1226,15 @@ __global__ void __launch_bounds__(256, 1) k_route_scatter(const ScatterParams p)
 // takes TPB consecutive tokens (one 256-token chunk holds them all) with
 // 8 / TPB warps per token.  It rebuilds from the per-chunk histograms what
 // it needs: the expert offsets (exclusive scan of the totals; block 0
-// publishes them), per expert the assignments in earlier chunks, and the
-// chunk's per-expert token bit masks.  The stable position of assignment
-// (t, j) with expert e is then offset[e] + earlier chunks' count + the
-// chunk's tokens before t that chose e (assignments sorted by expert, then
-// token).  Each token's row of h is read once; xe = bf16(h / rms(h) *
+// publishes them) and per expert the assignments in earlier chunks.  The
+// stable position of assignment (t, j) with expert e is then offset[e] +
+// earlier chunks' count + the chunk's tokens before t that chose e, counted
+// in the chunk's token bit mask of e that the selection wrote (assignments
+// sorted by expert, then token).  Each token's row of h is read once; xe = bf16(h / rms(h) *
 // w_pre_ff2) is formed once and stored at its K grouped rows.
 template <int TPB>
 __global__ void __launch_bounds__(256) k_scatter_gather(const ScatterParams sp,
                                                         const GatherParams gp) {
-  __shared__ unsigned s_mask[256][kChunkTokens / 32];  // [expert][token word]
   __shared__ int s_tmp[256];
   __shared__ int s_base[256];
   __shared__ int s_pos[TPB][16];
@@ -1242,7 +1245,6 @@ __global__ void __launch_bounds__(256) k_scatter_gather(const ScatterParams sp,
   const int t0 = blockIdx.x * TPB;
   const int chunk = t0 / kChunkTokens, c0 = chunk * kChunkTokens;
   const int nchunks = (T + kChunkTokens - 1) / kChunkTokens;
-  for (int i = tid; i < 256 * (kChunkTokens / 32); i += 256) (&s_mask[0][0])[i] = 0u;
   int tot = 0, bef = 0;
   if (tid < E) {
     for (int c = 0; c < nchunks; ++c) {
@@ -1252,18 +1254,11 @@ __global__ void __launch_bounds__(256) k_scatter_gather(const ScatterParams sp,
     }
   }
   int total;
-  const int base = block_excl_scan256(tot, s_tmp, &total);  // synchronises: masks are clear
+  const int base = block_excl_scan256(tot, s_tmp, &total);
   s_base[tid] = base + bef;
   if (blockIdx.x == 0) {
     if (tid < E) sp.offsets[tid] = base;
     if (tid == 0) sp.offsets[E] = total;
-  }
-  const int nc = min(kChunkTokens, T - c0);
-  for (int i = tid; i < nc * K; i += 256) {
-    const int tl = i / K;
-    const int e = sp.idx[(size_t)(c0 + tl) * K + (i - tl * K)];
-    if ((unsigned)e < (unsigned)E) atomicOr(&s_mask[e][tl >> 5], 1u << (tl & 31));
-    else report(sp.status, kDevBounds, kSiteScatter, (unsigned)(c0 + tl), (unsigned)e);
   }
   __syncthreads();
   if (tid < TPB * K) {
@@ -1273,13 +1268,16 @@ __global__ void __launch_bounds__(256) k_scatter_gather(const ScatterParams sp,
       int pos = 0;
       if ((unsigned)e < (unsigned)E) {
         const int tl = t - c0;
-        int rank = __popc(s_mask[e][tl >> 5] & ((1u << (tl & 31)) - 1u));
-        for (int w = 0; w < (tl >> 5); ++w) rank += __popc(s_mask[e][w]);
+        const uint32_t* m = sp.chunk_masks + ((size_t)chunk * E + e) * (kChunkTokens / 32);
+        int rank = __popc(__ldg(m + (tl >> 5)) & ((1u << (tl & 31)) - 1u));
+        for (int w = 0; w < (tl >> 5); ++w) rank += __popc(__ldg(m + w));
         pos = s_base[e] + rank;
         sp.perm[pos] = t * K + j;
         sp.tok_perm[pos] = t;
         sp.w_perm[pos] = sp.w[(size_t)t * K + j];
         if (sp.inv) sp.inv[t * K + j] = pos;
+      } else {
+        report(sp.status, kDevBounds, kSiteScatter, (unsigned)t, (unsigned)e);
       }
       s_pos[tt][j] = pos;  // an out-of-range expert was reported; its row is not read
     }
