@@ -116,53 +116,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   return mbar_wait_for(bar, parity, abort, kWaitLimitNs);
 }
 
-// Non-blocking test of a phase (never suspends the thread).
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// The same bounded wait as a tight spin on test_wait, for a warp whose wake-up
-// latency gates the tensor core (the MMA issuer's waiter).
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity,
-                                               volatile int* abort) {
-  if (mbar_test_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 256; ++i)
-      if (mbar_test_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
-
-// The same bounded wait for warps that wait long and whose latency matters
-// less (dequantising teams between their stages, epilogues between tiles,
-// producers ahead of their consumers): between polls the warp sleeps for a
-// pause that grows from 32 to max_ns, leaving the issue slots to the warps
-// that work.
-__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity,
-                                                  volatile int* abort, unsigned max_ns = 256u) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  unsigned ns = 32u;
-  while (true) {
-    __nanosleep(ns);
-    if (mbar_try_wait(bar, parity)) return true;
-    if (ns < max_ns) ns <<= 1;
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
-
 // Limit of the bounded-wait test (GemmParams::test_stall): CTA 0's epilogue
 // waits this long on a barrier nothing arrives on, then reports a timeout
 // and winds the CTA down as any wait that runs out does.

@@ -228,8 +228,6 @@ cudaError_t prepare_gemm_affine(int smem_max);
 
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s);
 cudaError_t launch_router_select(const RouterParams& p, int num_sms, cudaStream_t s);
-cudaError_t launch_route_scatter(const ScatterParams& p, cudaStream_t s);
-cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s);
 // The grouping (offsets, perm, tok_perm, w_perm, inv) and the grouped expert
 // rows in one token-major kernel.
 cudaError_t launch_scatter_gather(const ScatterParams& sp, const GatherParams& gp,

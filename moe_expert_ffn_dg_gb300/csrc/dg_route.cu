@@ -13,11 +13,11 @@
 //   the one exact arithmetic gives.  The logits kernel also writes the dense
 //   branch input xd = bf16(h / rms(h) * w_pre_ff) and zeroes the token's row
 //   of the f32 expert-sum accumulator; the select kernel also counts the
-//   per-chunk expert histogram.
-// k_route_scatter: token -> expert grouping from the per-chunk histogram,
-//   prefix sum and a stable scatter (assignments sorted by expert, then token).
-// k_gather_xe: expert input rows xe = bf16(h / rms(h) * w_pre_ff2) in
-//   grouped order, the B operand of the gate_up GEMM.
+//   per-chunk expert histogram and token bit masks.
+// k_scatter_gather: token -> expert grouping from the per-chunk histograms
+//   (prefix sum, stable positions: assignments sorted by expert, then token)
+//   and the expert input rows xe = bf16(h / rms(h) * w_pre_ff2) in grouped
+//   order, the B operand of the gate_up GEMM.
 #include <math.h>
 
 #include "dg_kernels.h"
@@ -1158,70 +1158,6 @@ __device__ int block_excl_scan256(int v, int* tmp, int* total) {
   return incl - v;
 }
 
-// One block per 256-token chunk.  Stable position of assignment (t, j) with
-// expert e: all assignments to lower experts, then to e from earlier chunks,
-// earlier warps of this chunk and earlier lanes of this warp (per-warp
-// expert masks built with shared-memory atomics).
-__global__ void __launch_bounds__(256, 1) k_route_scatter(const ScatterParams p) {
-  __shared__ int s_tmp[256];
-  __shared__ int s_base[256];
-  __shared__ unsigned s_wmask[8][256];  // per warp and expert: lanes (tokens) that chose it
-  __shared__ int s_wbase[8][256];
-  pdl_trigger();
-  pdl_wait();
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int chunk = blockIdx.x, nchunks = gridDim.x;
-  const int E = p.E, K = p.K, T = p.T;
-
-  for (int i = tid; i < 8 * 256; i += 256) (&s_wmask[0][0])[i] = 0u;
-  int tot = 0, bef = 0;
-  if (tid < E) {
-    for (int c = 0; c < nchunks; ++c) {
-      const int v = p.chunk_counts[(size_t)c * E + tid];
-      tot += v;
-      if (c < chunk) bef += v;
-    }
-  }
-  const int t = chunk * kChunkTokens + tid;
-  const bool valid = t < T;
-  int ex[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) ex[j] = (j < K && valid) ? p.idx[(size_t)t * K + j] : -1;
-  int total;
-  const int base = block_excl_scan256(tot, s_tmp, &total);  // synchronises: masks are clear
-  s_base[tid] = base + bef;
-  if (chunk == 0) {
-    if (tid < E) p.offsets[tid] = base;
-    if (tid == 0) p.offsets[E] = total;
-  }
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    if ((unsigned)ex[j] < (unsigned)E) atomicOr(&s_wmask[warp][ex[j]], 1u << lane);
-    else if (ex[j] >= 0) report(p.status, kDevBounds, kSiteScatter, (unsigned)t, (unsigned)ex[j]);
-  }
-  __syncthreads();
-  if (tid < E) {
-    int run = 0;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      s_wbase[w][tid] = run;
-      run += __popc(s_wmask[w][tid]);
-    }
-  }
-  __syncthreads();
-  const unsigned lt = (1u << lane) - 1u;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int e = ex[j];
-    if ((unsigned)e >= (unsigned)E) continue;
-    const int pos = s_base[e] + s_wbase[warp][e] + __popc(s_wmask[warp][e] & lt);
-    p.perm[pos] = t * K + j;
-    p.tok_perm[pos] = t;
-    p.w_perm[pos] = p.w[(size_t)t * K + j];
-    if (p.inv) p.inv[t * K + j] = pos;
-  }
-}
-
 // Grouping and expert rows in one pass, token-major.  A block of 256 threads
 // takes TPB consecutive tokens (one 256-token chunk holds them all) with
 // 8 / TPB warps per token.  It rebuilds from the per-chunk histograms what
@@ -1308,46 +1244,6 @@ __global__ void __launch_bounds__(256) k_scatter_gather(const ScatterParams sp,
   }
 }
 
-// Warp per grouped row; loads of four vectors per round.
-__global__ void __launch_bounds__(256) k_gather_xe(const GatherParams p) {
-  pdl_trigger();
-  pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int nwarps = (gridDim.x * blockDim.x) >> 5;
-  const int nvec = p.H >> 3;
-  const uint4* wv = reinterpret_cast<const uint4*>(p.w_pre_ff2);
-  for (int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < p.TK; row += nwarps) {
-    const int t = p.tok_perm[row];
-    const float r = p.r[t];
-    const uint4* hrow = reinterpret_cast<const uint4*>(p.h + (size_t)t * p.H);
-    uint4* orow = reinterpret_cast<uint4*>(p.xe_perm + (size_t)row * p.H);
-    for (int v0 = lane; v0 < nvec; v0 += 128) {
-      uint4 rh[4], rw[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int v = v0 + 32 * u;
-        if (v < nvec) {
-          rh[u] = __ldg(hrow + v);
-          rw[u] = __ldg(wv + v);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int v = v0 + 32 * u;
-        if (v >= nvec) break;
-        float f[8], w[8];
-        unpack8(rh[u], f);
-        unpack8(rw[u], w);
-        uint4 o;
-        o.x = pack2_bf16(f[0] * r * w[0], f[1] * r * w[1]);
-        o.y = pack2_bf16(f[2] * r * w[2], f[3] * r * w[3]);
-        o.z = pack2_bf16(f[4] * r * w[4], f[5] * r * w[5]);
-        o.w = pack2_bf16(f[6] * r * w[6], f[7] * r * w[7]);
-        orow[v] = o;
-      }
-    }
-  }
-}
 
 template <int TB>
 size_t router_smem(int H) {
@@ -1418,26 +1314,13 @@ cudaError_t launch_router_select(const RouterParams& p, int num_sms, cudaStream_
                      : launch_select_slots<false, 8>(p, num_sms, s);
 }
 
-cudaError_t launch_route_scatter(const ScatterParams& p, cudaStream_t s) {
-  const int grid = (p.T + kChunkTokens - 1) / kChunkTokens;
-  return launch_pdl(k_route_scatter, dim3(grid), dim3(256), 0, s, p);
-}
-
 cudaError_t launch_scatter_gather(const ScatterParams& sp, const GatherParams& gp,
                                   cudaStream_t s) {
   // small batches: two tokens a block (four warps each) for enough blocks;
-  // large ones: eight (a warp each), so the per-block rebuild is shared
+  // large ones: eight (a warp each)
   if (sp.T < kRouterTcMinTokens)
     return launch_pdl(k_scatter_gather<2>, dim3((sp.T + 1) / 2), dim3(256), 0, s, sp, gp);
   return launch_pdl(k_scatter_gather<8>, dim3((sp.T + 7) / 8), dim3(256), 0, s, sp, gp);
-}
-
-cudaError_t launch_gather(const GatherParams& p, int num_sms, cudaStream_t s) {
-  const int rows_per_block = 8;
-  int grid = (p.TK + rows_per_block - 1) / rows_per_block;
-  grid = grid < num_sms * 8 ? grid : num_sms * 8;
-  if (grid < 1) grid = 1;
-  return launch_pdl(k_gather_xe, dim3(grid), dim3(256), 0, s, p);
 }
 
 }  // namespace dg
