@@ -9,7 +9,7 @@ step are 12x the L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload canvas256|canvas256_q4|canvas256_q4d8|batch2048_zipf|stack30_q4|
-                              sc_canvas256|sc_canvas256_q4]
+                              sc_canvas256|sc_canvas256_q4|sc_canvas256_q8]
 
 Prints one JSON line.  ``--impl reference`` times the CPU oracle (the only
 reference there is: the pages hold no runnable implementation) on the host
@@ -774,7 +774,8 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["canvas256", "canvas256_q4", "canvas256_q4d8", "canvas256_fp4",
                              "batch2048_zipf",
-                             "stack30_q4", "sc_canvas256", "sc_canvas256_q4"])
+                             "stack30_q4", "sc_canvas256", "sc_canvas256_q4",
+                             "sc_canvas256_q8"])
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -317,7 +317,8 @@ typedef struct {
   int hidden;         /* H, multiple of 128 */
   int inter;          /* gate/up rows, multiple of 64 */
   int max_tokens;     /* largest n_tokens of a forward */
-  dg_format_t fmt;    /* gate, up, down: DG_FMT_BF16 or DG_FMT_AFFINE_U4_G64 */
+  dg_format_t fmt;    /* gate, up, down: DG_FMT_BF16, DG_FMT_AFFINE_U4_G64 or
+                         DG_FMT_AFFINE_U8_G64 (q8); quantised: H and inter <= 2944 */
   float rms_eps;      /* 0 means 1e-6 */
   unsigned flags;     /* must be 0 */
 } dg_sc_mlp_config_t;

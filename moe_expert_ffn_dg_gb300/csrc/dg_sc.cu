@@ -158,9 +158,9 @@ dg_status_t sc_check_config(const dg_sc_mlp_config_t* c) {
   if (c->hidden % 128 || c->inter % 64 || c->hidden > 8 * 8 * kScThreads)
     return DG_ERR_UNSUPPORTED;
   if (c->max_tokens > (1 << 20)) return DG_ERR_UNSUPPORTED;
-  if (c->fmt != DG_FMT_BF16 && c->fmt != DG_FMT_AFFINE_U4_G64) return DG_ERR_UNSUPPORTED;
-  if (c->fmt == DG_FMT_AFFINE_U4_G64 && (c->hidden > 2944 || c->inter > 2944))
+  if (c->fmt != DG_FMT_BF16 && c->fmt != DG_FMT_AFFINE_U4_G64 && c->fmt != DG_FMT_AFFINE_U8_G64)
     return DG_ERR_UNSUPPORTED;
+  if (c->fmt != DG_FMT_BF16 && (c->hidden > 2944 || c->inter > 2944)) return DG_ERR_UNSUPPORTED;
   return DG_OK;
 }
 
@@ -173,7 +173,8 @@ struct dg_sc_mlp {
   ScLayout L;
   int num_sms;
   size_t smem_optin;
-  bool q4;
+  bool q4;    // group-64 affine weights (the quantised GEMM)
+  int qbits;  // their code width: 4 or 8
   GemmParams gu, dn;
   dg_event_t* prof = nullptr;
 };
@@ -210,7 +211,8 @@ dg_status_t dg_sc_mlp_create(const dg_sc_mlp_config_t* cfg, const dg_sc_mlp_weig
   m->w = *weights;
   m->ws = static_cast<uint8_t*>(workspace);
   m->L = L;
-  m->q4 = cfg->fmt == DG_FMT_AFFINE_U4_G64;
+  m->q4 = cfg->fmt != DG_FMT_BF16;
+  m->qbits = cfg->fmt == DG_FMT_AFFINE_U8_G64 ? 8 : 4;
   int dev = 0, optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -226,11 +228,12 @@ dg_status_t dg_sc_mlp_create(const dg_sc_mlp_config_t* cfg, const dg_sc_mlp_weig
   const uint64_t H = cfg->hidden, D = cfg->inter, T = cfg->max_tokens;
   uint8_t* ws = m->ws;
   const bool q4 = m->q4;
+  const int qb = m->qbits;
   bool ok = true;
   // gate_up: the dense pair (4-D interleaving view when up lies above gate)
   if (q4) {
-    ok = ok && encode_q4_rows(&m->gu.wa_d0, weights->gate.q, D, H, 16);
-    ok = ok && encode_q4_rows(&m->gu.wa_d1, weights->up.q, D, H, 16);
+    ok = ok && encode_q_rows(&m->gu.wa_d0, weights->gate.q, D, H, 16, qb);
+    ok = ok && encode_q_rows(&m->gu.wa_d1, weights->up.q, D, H, 16, qb);
   } else {
     ok = ok && encode_bf16_rows(&m->gu.wa_d0, weights->gate.q, D, H, 16);
     ok = ok && encode_bf16_rows(&m->gu.wa_d1, weights->up.q, D, H, 16);
@@ -238,7 +241,7 @@ dg_status_t dg_sc_mlp_create(const dg_sc_mlp_config_t* cfg, const dg_sc_mlp_weig
   {
     const uintptr_t g = (uintptr_t)weights->gate.q, u = (uintptr_t)weights->up.q;
     m->gu.dense_5d = u > g && ((u - g) % 16) == 0 && (u - g) < (1ull << 40) &&
-                     encode_gate_up(&m->gu.wa_d5, weights->gate.q, H, D, u - g, 4, 1, 0, q4 ? 4 : 0);
+                     encode_gate_up(&m->gu.wa_d5, weights->gate.q, H, D, u - g, 4, 1, 0, q4 ? qb : 0);
     if (!m->gu.dense_5d) m->gu.wa_d5 = m->gu.wa_d0;
   }
   ok = ok && encode_bf16_rows(&m->gu.xb_d64, ws + L.x, T, H, 64);
@@ -247,7 +250,7 @@ dg_status_t dg_sc_mlp_create(const dg_sc_mlp_config_t* cfg, const dg_sc_mlp_weig
   ok = ok && encode_bf16_rows(&m->gu.xb_d128, ws + L.x, T, H, 128);
   ok = ok && encode_bf16_rows(&m->gu.xb_d32, ws + L.x, T, H, 32);
   // down: [H, D] in 128-row boxes over act
-  if (q4) ok = ok && encode_q4_rows(&m->dn.wa_d0, weights->down.q, H, D, 128);
+  if (q4) ok = ok && encode_q_rows(&m->dn.wa_d0, weights->down.q, H, D, 128, qb);
   else ok = ok && encode_bf16_rows(&m->dn.wa_d0, weights->down.q, H, D, 128);
   ok = ok && encode_bf16_rows(&m->dn.xb_d64, ws + L.act, T, D, 64);
   ok = ok && encode_bf16_rows(&m->dn.xb_d16, ws + L.act, T, D, 16);
@@ -350,11 +353,11 @@ dg_status_t dg_sc_mlp_forward(dg_sc_mlp_t* m, const void* embeds, const void* si
                        : pick_bn(T);
   gu.bn = dn.bn = bn;
   if (err == cudaSuccess)
-    err = m->q4 ? launch_gemm_affine(0, bn, 4, gu, m->num_sms, s)
+    err = m->q4 ? launch_gemm_affine(0, bn, m->qbits, gu, m->num_sms, s)
                 : launch_gemm(0, bn, gu, m->num_sms, s);
   mark(2);
   if (err == cudaSuccess)
-    err = m->q4 ? launch_gemm_affine(1, bn, 4, dn, m->num_sms, s)
+    err = m->q4 ? launch_gemm_affine(1, bn, m->qbits, dn, m->num_sms, s)
                 : launch_gemm(1, bn, dn, m->num_sms, s);
   mark(3);
   if (err == cudaSuccess)

@@ -127,6 +127,8 @@ SC_WORKLOADS = {
                              weight_std=0.02, router_std=0.02),
     "sc_canvas256_q4": Workload("sc_canvas256_q4", 256, 2816, 1, 1, 704, 2112, seed=5,
                                 weight_std=0.02, router_std=0.02, quant=(4, 4, 8)),
+    "sc_canvas256_q8": Workload("sc_canvas256_q8", 256, 2816, 1, 1, 704, 2112, seed=5,
+                                weight_std=0.02, router_std=0.02, quant=(8, 8, 8)),
 }
 
 

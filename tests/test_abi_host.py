@@ -110,7 +110,11 @@ def _sc_cfg(**kw):
 
 def test_sc_mlp_workspace_and_create_validation(lib):
     assert B.dg_sc_mlp_workspace_size(_sc_cfg()) > 256 * 2816 * 4
-    for bad in (dict(hidden=100), dict(inter=100), dict(fmt=2), dict(flags=1)):
+    # bf16, 4-bit and 8-bit (q8) group-64 affine weights; NVFP4 is not an SC format
+    for fmt in (B.DG_FMT_AFFINE_U4_G64, B.DG_FMT_AFFINE_U8_G64):
+        assert B.dg_sc_mlp_workspace_size(_sc_cfg(fmt=fmt)) > 256 * 2816 * 4
+    for bad in (dict(hidden=100), dict(inter=100), dict(fmt=B.DG_FMT_NVFP4_G16), dict(flags=1),
+                dict(fmt=B.DG_FMT_AFFINE_U8_G64, hidden=3072)):
         with pytest.raises(B.DgError):
             B.dg_sc_mlp_workspace_size(_sc_cfg(**bad))
     w = B.dg_sc_mlp_weights_t()

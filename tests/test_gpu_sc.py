@@ -64,6 +64,14 @@ def test_sc_tiny_q4():
     _run(wl, mi.make_sc_inputs(wl, randvec=True, quantise=True), ref_bf16_weights=True)
 
 
+@pytest.mark.parametrize("T", [32, 1, 300])
+def test_sc_tiny_q8(T):
+    """8-bit group-64 affine gate/up/down (the q8 format the pages give the
+    self-conditioning MLP beside 4-bit)."""
+    wl = mi.get_workload("sc_tiny", quant=(8, 8, 8), tokens=T)
+    _run(wl, mi.make_sc_inputs(wl, randvec=True, quantise=True), ref_bf16_weights=True)
+
+
 def test_sc_zero_signal_gives_the_normed_embeddings():
     import moe_expert_ffn_dg_gb300 as pkg
     wl = mi.get_workload("sc_tiny")
@@ -93,3 +101,8 @@ def test_sc_canvas256_bf16():
 def test_sc_canvas256_q4_exact_decode():
     wl = mi.get_workload("sc_canvas256_q4")
     print("sc_canvas256_q4", _run(wl, mi.make_sc_inputs(wl, randvec=True)))
+
+
+def test_sc_canvas256_q8_exact_decode():
+    wl = mi.get_workload("sc_canvas256_q8")
+    print("sc_canvas256_q8", _run(wl, mi.make_sc_inputs(wl, randvec=True)))
