@@ -376,6 +376,21 @@ def test_quantised_block_equals_dequant_then_bf16_block():
     np.testing.assert_allclose(rq["out"], rd["out"], rtol=1e-12, atol=1e-12)
 
 
+@pytest.mark.parametrize("bits", [4, 8])
+def test_quantised_sc_mlp_equals_the_mlp_on_hand_decoded_weights(bits):
+    # the self-conditioning MLP on 4- and 8-bit (q8) affine weights is the
+    # same MLP on the weights decoded by hand
+    wl = mi.get_workload("sc_tiny", quant=(bits, bits, 8))
+    pq = mi.make_sc_inputs(wl, randvec=True, quantise=True)
+    assert all(pq[n]["bits"] == bits for n in ("gate", "up", "down"))
+    pd = dict(pq)
+    for n in ("gate", "up", "down"):
+        pd[n] = _dequant_by_hand(pq[n])
+    e, sg = pq["embeds"][:5], pq["signal"][:5]
+    np.testing.assert_allclose(o.sc_mlp_forward(e, sg, pq), o.sc_mlp_forward(e, sg, pd),
+                               rtol=1e-12, atol=1e-12)
+
+
 def test_bf16_decoded_weights_are_the_rounded_exact_decode():
     # the bf16_weights variant: exact decode by hand, then round to nearest
     # even bf16 through the input module's independent rounding (the decode
